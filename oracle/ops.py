@@ -1,0 +1,223 @@
+"""Oracle primitives (float64, NCHW) — test infrastructure only.
+
+Each function restates one operation of the pages in plain numpy; the
+docstring names the passage it follows. Inputs may be any numeric dtype
+(f16 weights, f32 streams); everything is promoted to float64 first.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+_F = np.float64
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=_F)
+
+
+def silu(v):
+    """SiLU, v / (1 + e^-v).
+
+    ``vae.rs``, ``fn silu`` and ``qi21_vae.rs``, ``qv_rmsn`` (its flags-2 branch).
+    """
+    v = _f64(v)
+    with np.errstate(over="ignore"):
+        return v / (1.0 + np.exp(-v))
+
+
+def upsample2x(x):
+    """Nearest-neighbour 2x: dst[c, Y, X] = src[c, Y//2, X//2].
+
+    ``vae.rs``, ``fn upsample2x``. ``x``: [c][h][w] -> [c][2h][2w].
+    """
+    x = _f64(x)
+    return np.repeat(np.repeat(x, 2, axis=1), 2, axis=2)
+
+
+def conv2d(x, w, b=None, upsample: bool = False, pad: str = "zero"):
+    """2-D convolution, stride 1, padding k//2 (cross-correlation, PyTorch order).
+
+    y[o, Y, X] = b[o] + sum_{c, ky, kx} w[o, c, ky, kx] * xt[c, Y+ky-r, X+kx-r],
+    r = k//2, where xt is ``x`` (or ``upsample2x(x)`` when ``upsample``) and
+    reads outside the grid are 0 (``pad="zero"``) or the nearest edge pixel
+    (``pad="replicate"``, a clamp on the upsampled grid).
+
+    ``vae.rs``, ``Conv2d::apply`` (zero padding, pad = k/2, bias added per
+    output channel) and ``VaeDecoder::decode`` (upsample, then conv);
+    replicate padding from ``s2v_vae.rs``'s causal-replicate conv, read for 2-D.
+
+    ``x``: [cin][h][w]; ``w``: [cout][cin][k][k]; returns [cout][H][W].
+    Each tap is one channel contraction (a matmul) over a shifted view.
+    """
+    x = upsample2x(x) if upsample else _f64(x)
+    w = _f64(w)
+    cout, cin, k, k2 = w.shape
+    assert k == k2 and x.shape[0] == cin, (w.shape, x.shape)
+    _, H, W = x.shape
+    r = k // 2
+    mode = {"zero": "constant", "replicate": "edge"}[pad]
+    xp = np.pad(x, ((0, 0), (r, r), (r, r)), mode=mode)
+    y = np.zeros((cout, H * W), _F)
+    for ky in range(k):
+        for kx in range(k):
+            tap = xp[:, ky:ky + H, kx:kx + W].reshape(cin, H * W)
+            y += w[:, :, ky, kx] @ tap
+    if b is not None:
+        y += _f64(b)[:, None]
+    return y.reshape(cout, H, W)
+
+
+def conv2d_at(x, w, b, ys, xs, upsample: bool = False, pad: str = "zero"):
+    """``conv2d`` evaluated only at output pixels (ys[i], xs[i]).
+
+    The same definition as ``conv2d``, one output pixel at a time, so that
+    very large convs can be checked on a sample. ``x`` may be any array
+    indexable as [c][y][x] (e.g. a transposed view of an NHWC tensor); only
+    the receptive fields of the sampled pixels are read.
+    Returns [len(ys)][cout].
+    """
+    w = _f64(w)
+    cout, cin, k, _ = w.shape
+    r = k // 2
+    h_in, w_in = x.shape[1], x.shape[2]
+    H, W = (2 * h_in, 2 * w_in) if upsample else (h_in, w_in)
+    ys = np.asarray(ys, np.int64)
+    xs = np.asarray(xs, np.int64)
+    out = np.zeros((len(ys), cout), _F)
+    if b is not None:
+        out += _f64(b)[None, :]
+    for ky in range(k):
+        for kx in range(k):
+            Y = ys + ky - r
+            X = xs + kx - r
+            if pad == "replicate":
+                Y = np.clip(Y, 0, H - 1)
+                X = np.clip(X, 0, W - 1)
+                inside = np.ones(len(ys), bool)
+            else:
+                inside = (Y >= 0) & (Y < H) & (X >= 0) & (X < W)
+            Yc = np.clip(Y, 0, H - 1)
+            Xc = np.clip(X, 0, W - 1)
+            if upsample:
+                Yc, Xc = Yc // 2, Xc // 2
+            vals = np.stack([_f64(x[:, int(a), int(c)]) for a, c in zip(Yc, Xc)])  # [n][cin]
+            vals[~inside] = 0.0
+            out += vals @ w[:, :, ky, kx].T
+    return out
+
+
+def group_norm(x, groups: int, gamma, beta, eps: float = 1e-6, bias_in=None):
+    """GroupNorm over ``groups`` groups of consecutive channels.
+
+    For group g (channels g*C/G .. (g+1)*C/G - 1, all pixels): mean mu and the
+    biased variance var (divided by n), then
+    y = (v - mu) / sqrt(var + eps) * gamma[c] + beta[c], with v = x + bias_in[c].
+
+    ``vae.rs``, ``GroupNorm::apply`` (f64 statistics, eps inside the root);
+    the bias on read follows ``s2v_vae.rs``'s ``s2v_gn_part``/``s2v_gn_apply``.
+    ``x``: [c][...spatial]; returns the same shape.
+    """
+    v = _f64(x)
+    c = v.shape[0]
+    assert c % groups == 0
+    if bias_in is not None:
+        v = v + _f64(bias_in).reshape((c,) + (1,) * (v.ndim - 1))
+    per = c // groups
+    out = np.empty_like(v)
+    g_ = _f64(gamma).reshape((c,) + (1,) * (v.ndim - 1))
+    b_ = _f64(beta).reshape((c,) + (1,) * (v.ndim - 1))
+    for g in range(groups):
+        s = v[g * per:(g + 1) * per]
+        mu = s.mean()
+        var = ((s - mu) ** 2).mean()
+        out[g * per:(g + 1) * per] = (s - mu) / np.sqrt(var + eps) * g_[g * per:(g + 1) * per] \
+            + b_[g * per:(g + 1) * per]
+    return out
+
+
+def rms_norm(x, gamma, bias_in=None, c_real=None):
+    """Per-pixel RMS_norm over the channels (the Wan ``RMS_norm``).
+
+    v = x + bias_in[c]; y = v * sqrt(C) / max(||v||_2, 1e-12) * gamma[c],
+    the norm taken over the C real channels of one pixel.
+
+    ``qi21_vae.rs``, the ``qv_rmsn`` kernel and its module doc.
+    ``x``: [c][...spatial]; returns the same shape.
+    """
+    v = _f64(x)
+    c = v.shape[0]
+    if bias_in is not None:
+        v = v + _f64(bias_in).reshape((c,) + (1,) * (v.ndim - 1))
+    C = c if c_real is None else c_real
+    nrm = np.sqrt((v * v).sum(axis=0))
+    inv = np.sqrt(float(C)) / np.maximum(nrm, 1e-12)
+    return v * inv[None] * _f64(gamma).reshape((c,) + (1,) * (v.ndim - 1))
+
+
+def dupup(src, out_dim: int, ft: int = 1):
+    """The DupUp3D shortcut of an up block, as a tensor on the 2x grid.
+
+    d[o, 2y+sy, 2x+sx] = src[j // repeats, y, x] with
+    j = o*factor + (ft-1)*4 + 2*sy + sx, factor = 4*ft and
+    repeats = out_dim*factor / in_dim (required to divide).
+
+    ``qi21_vae.rs``, ``DUPUP_SRC`` (``qv_dupup``) and its uniform set-up in
+    ``run_blocks``. ``src``: [in_dim][h][w] -> [out_dim][2h][2w].
+    """
+    s = _f64(src)
+    cin, h, w = s.shape
+    factor = 4 * ft
+    assert (out_dim * factor) % cin == 0
+    repeats = out_dim * factor // cin
+    d = np.empty((out_dim, 2 * h, 2 * w), _F)
+    for sy in range(2):
+        for sx in range(2):
+            for o in range(out_dim):
+                j = o * factor + (ft - 1) * 4 + 2 * sy + sx
+                d[o, sy::2, sx::2] = s[j // repeats]
+    return d
+
+
+def linear_tokens(t, conv):
+    """A 1x1 conv on token-major rows: t [m][cin] -> t @ W^T + b, [m][cout].
+
+    ``vae.rs``, ``AttnBlock::proj`` (weight rows are output channels).
+    """
+    w = _f64(conv.w).reshape(conv.w.shape[0], conv.w.shape[1])
+    return _f64(t) @ w.T + _f64(conv.b)[None, :]
+
+
+def attention(x, attn, family: str, groups: int = 32, eps: float = 1e-6,
+              chunk: int = 1024):
+    """Single-head spatial self-attention of the mid block, with its residual.
+
+    n = GroupNorm(x) (FLUX family) or RMS_norm(x)*gamma (Qwen family), no SiLU;
+    token-major q, k, v = n W^T + b; A = softmax_row(q k^T / sqrt(C)) with the
+    row maximum subtracted before exp; o = A v; y = x + (o W_o^T + b_o).
+
+    ``vae.rs``, ``AttnBlock::apply`` / ``AttnBlock::finish`` and
+    ``qi21_vae.rs``, ``fn attention`` (the RMS variant; there the v bias is
+    added after P.V, identical in exact arithmetic because rows of A sum to 1).
+    ``x``: [c][h][w]; returns [c][h][w]. Query rows are taken ``chunk`` at a time.
+    """
+    x = _f64(x)
+    c, h, w = x.shape
+    m = h * w
+    if family == "gn":
+        n = group_norm(x, groups, attn.norm.gamma, attn.norm.beta, eps)
+    else:
+        n = rms_norm(x, attn.norm.gamma)
+    t = n.reshape(c, m).T
+    q = linear_tokens(t, attn.q)
+    k = linear_tokens(t, attn.k)
+    v = linear_tokens(t, attn.v)
+    scale = 1.0 / np.sqrt(float(c))
+    o = np.empty((m, c), _F)
+    for r0 in range(0, m, chunk):
+        s = (q[r0:r0 + chunk] @ k.T) * scale
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=1, keepdims=True)
+        o[r0:r0 + chunk] = p @ v
+    y = linear_tokens(o, attn.o)
+    return x + y.T.reshape(c, h, w)

@@ -1,0 +1,701 @@
+// NHWC implicit-GEMM convolution (3x3 or 1x1, stride 1) on sm_103a tensor cores.
+//
+// What it computes ("vae.rs" Conv2d::apply; "qi21_vae.rs" conv_s and the
+// module doc's implicit-GEMM recipe): GEMM with M = output pixels,
+// N = cout, K = taps * cin in (tap, channel) order, f16 inputs, f32
+// accumulation in tensor memory, and a fused epilogue
+//   y = SiLU?(oscale * acc + bias + residual [+ DupUp(src)])  -> f32 | f16 | NCHW f32.
+//
+// How (a GB300 design, not the pages' wgpu one):
+//  - M tiles are R rows x Wt columns of a "virtual grid" (R*Wt <= 128). For a
+//    plain conv the virtual grid is the output grid. For the nearest-2x fold
+//    it is the SOURCE grid, taken once per output parity class (q, p): output
+//    (2v+q, 2u+p) reads, for tap (ky, kx), source (v + dy, u + dx) with
+//    dy = floor((q+ky-1)/2), dx = floor((p+kx-1)/2). So every tap of every
+//    tile is a dense rectangular box of the f16 input and the whole gather
+//    is a 4-D TMA tile load; zero padding comes from TMA's out-of-bounds fill.
+//  - Replicate padding clamps source coordinates per pixel, which a box
+//    cannot express; those launches use 128 gather threads instead (one A row
+//    each, 16-byte loads, stores into the 128B-swizzled layout).
+//  - B (weights [cout][taps][cin]) is a 3-D TMA tile load per (tap, chunk).
+//  - One elected thread issues tcgen05.mma (M=128, N=BN, K=16 steps) into one
+//    of two TMEM accumulators; four epilogue warps drain the other
+//    (tcgen05.ld), so the epilogue of tile i overlaps the MMAs of tile i+1.
+//  - Persistent CTAs (one per SM) walk the tile list with a fixed stride; an
+//    S-stage mbarrier ring pipelines TMA against the MMAs.
+//  - Each output element's value depends only on its own receptive field and
+//    the K order, never on the tile it falls in, so banded decodes are
+//    bit-identical to whole-frame ones.
+//  - Every wait is bounded (mbar_wait); on a timeout the CTA drains its own
+//    TMA copies and MMAs, frees TMEM and returns with the status recorded.
+#include <algorithm>
+#include <cstdio>
+
+#include "vae_conv.h"
+
+namespace vae {
+
+namespace {
+
+constexpr int kBK = 64;                // channels per K chunk (one 128-byte swizzle row)
+constexpr int kBM = 128;               // M tile (UMMA M)
+constexpr int kABytes = kBM * kBK * 2; // 16 KB
+constexpr int kMaxStages = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kGatherWarp0 = 6;
+constexpr int kMaxSmem = 232448;       // 227 KB opt-in per CTA
+
+struct ConvParams {
+    int n, hv, wv;        // images, virtual grid rows/cols (= input grid)
+    int cin, cout, taps;  // taps: 9 or 1
+    int up, rep;          // nearest-2x fold, replicate padding
+    int H, W;             // output grid
+    int R, Wt;            // tile rows, tile cols on the virtual grid
+    int tiles_x, tiles_y, npar;
+    int n_tiles, BN, acc_stride;
+    int kchunks, total_tiles, stages;
+    uint32_t a_tx;        // bytes one A box delivers
+    const __half* x;      // gather source
+    const float* bias;
+    const float* residual;
+    void* y;
+    float oscale;
+    int silu, out_f16, vec_ok;
+    // NCHW output of kept rows (conv_out): rows [keep_lo, keep_hi) land at
+    // destination row (Y - keep_lo + dst_row0) of planes `plane` floats apart.
+    int out_nchw, keep_lo, keep_hi, dst_row0;
+    long long plane;
+    // DupUp add (the RMS-family up conv): src f32 [n][hv][wv][dup_cin].
+    const float* dup_src;
+    int dup_cin, dup_factor, dup_repeats, dup_ftoff;
+    DevStatus* status;
+    unsigned long long timeout_ns;
+};
+
+struct TileInfo {
+    int img, par, v0, u0, n0;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const ConvParams& p, int t) {
+    TileInfo ti;
+    const int nt = t % p.n_tiles;
+    int r = t / p.n_tiles;
+    const int tx = r % p.tiles_x;
+    r /= p.tiles_x;
+    ti.par = r % p.npar;
+    r /= p.npar;
+    const int ty = r % p.tiles_y;
+    ti.img = r / p.tiles_y;
+    ti.v0 = ty * p.R;
+    ti.u0 = tx * p.Wt;
+    ti.n0 = nt * p.BN;
+    return ti;
+}
+
+// Source offset of tap `tap` for parity class `par` (see the file comment).
+__device__ __forceinline__ void tap_offset(const ConvParams& p, int tap, int par, int& dy, int& dx) {
+    if (p.taps == 1) {
+        dy = 0;
+        dx = 0;
+        return;
+    }
+    const int ky = tap / 3, kx = tap % 3;
+    if (p.up) {
+        const int q = par >> 1, pp = par & 1;
+        dy = (q + ky + 1) / 2 - 1;
+        dx = (pp + kx + 1) / 2 - 1;
+    } else {
+        dy = ky - 1;
+        dx = kx - 1;
+    }
+}
+
+struct Smem {
+    uint8_t* a;          // stages x 16 KB
+    uint8_t* b;          // stages x BN*128 B
+    uint64_t* full;      // [stages]
+    uint64_t* empty;     // [stages]
+    uint64_t* accf;      // [2]
+    uint64_t* acce;      // [2]
+    uint64_t* drain;     // [1]
+    uint32_t* tmem_slot;
+    int* abort_flag;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
+    Smem s;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    s.a = base;
+    s.b = base + p.stages * kABytes;
+    uint8_t* tail = s.b + p.stages * p.BN * 128;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
+    s.full = bars;
+    s.empty = bars + kMaxStages;
+    s.accf = bars + 2 * kMaxStages;
+    s.acce = s.accf + 2;
+    s.drain = s.acce + 2;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
+    return s;
+}
+
+// Waits on a barrier during the final drain: bounded, but not cut short by
+// the abort flag (the point is to let in-flight async work land).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const ConvParams& p) {
+    int never = 0;
+    (void)mbar_wait(bar, parity, &never, p.timeout_ns, p.status, kWhereDrain);
+}
+
+// ───────────────────────────── roles ─────────────────────────────
+
+template <bool kGather>
+__device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensorMap* mapA,
+                              const CUtensorMap* mapB) {
+    const uint64_t pol_w = policy_evict_last();
+    const uint64_t pol_a = policy_evict_normal();
+    const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * 128u;
+    const uint32_t tx = b_bytes + (kGather ? 0u : p.a_tx);
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, arm_par = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p, t);
+        for (int tap = 0; tap < p.taps && ok; ++tap) {
+            int dy, dx;
+            tap_offset(p, tap, ti.par, dy, dx);
+            for (int kc = 0; kc < p.kchunks; ++kc) {
+                const uint32_t fb = smem_u32(&s.full[stage]);
+                if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, s.abort_flag, p.timeout_ns,
+                               p.status, kWhereProducerEmpty)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(fb, tx);
+                armed |= 1u << stage;
+                arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
+                if (!kGather)
+                    tma_load_4d(smem_u32(s.a + stage * kABytes), mapA, fb, kc * kBK, ti.u0 + dx,
+                                ti.v0 + dy, ti.img, pol_a);
+                tma_load_3d(smem_u32(s.b + stage * p.BN * 128), mapB, fb, kc * kBK, tap, ti.n0, pol_w);
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+    // Let every copy this thread started land before the CTA can exit.
+    for (int st = 0; st < p.stages; ++st)
+        if (armed & (1u << st)) drain_wait(smem_u32(&s.full[st]), (arm_par >> st) & 1u, p);
+}
+
+// One thread per A row: gathers the row's 64-channel slice for each
+// (tap, chunk) with clamped (replicate) or zero-filled (zero) borders.
+__device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p, t);
+        const int rr = gt / p.Wt, cc = gt % p.Wt;
+        const int v = ti.v0 + rr, u = ti.u0 + cc;
+        const bool rowvalid = gt < p.R * p.Wt && v < p.hv && u < p.wv;
+        for (int tap = 0; tap < p.taps && ok; ++tap) {
+            int dy, dx;
+            tap_offset(p, tap, ti.par, dy, dx);
+            int sy = v + dy, sx = u + dx;
+            bool inb;
+            if (p.rep) {
+                sy = min(max(sy, 0), p.hv - 1);
+                sx = min(max(sx, 0), p.wv - 1);
+                inb = rowvalid;
+            } else {
+                inb = rowvalid && sy >= 0 && sy < p.hv && sx >= 0 && sx < p.wv;
+            }
+            const __half* src =
+                p.x + ((static_cast<long long>(ti.img) * p.hv + (inb ? sy : 0)) * p.wv + (inb ? sx : 0)) *
+                          p.cin;
+            for (int kc = 0; kc < p.kchunks; ++kc) {
+                if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, s.abort_flag, p.timeout_ns,
+                               p.status, kWhereGatherEmpty)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* dst = s.a + stage * kABytes;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int c = kc * kBK + j * 8;
+                    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+                    if (inb && c < p.cin) val = __ldg(reinterpret_cast<const uint4*>(src + c));
+                    *reinterpret_cast<uint4*>(dst + sw128_off(static_cast<uint32_t>(gt), j)) = val;
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&s.full[stage]));
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    }
+}
+
+__device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base) {
+    const uint32_t idesc = idesc_f16_f32(kBM, p.BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int accbuf = 0;
+    uint32_t accphase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(smem_u32(&s.acce[accbuf]), accphase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
+                       kWhereMmaAccEmpty))
+            break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
+        int kit = 0;
+        for (int tap = 0; tap < p.taps && ok; ++tap) {
+            for (int kc = 0; kc < p.kchunks; ++kc) {
+                if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                               kWhereMmaFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int nk = min(4, (p.cin - kc * kBK) / 16);
+                const uint64_t ad = sw128_kmajor_desc(smem_u32(s.a + stage * kABytes));
+                const uint64_t bd = sw128_kmajor_desc(smem_u32(s.b + stage * p.BN * 128));
+                for (int k = 0; k < nk; ++k)
+                    umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                             (kit | k) != 0 ? 1u : 0u);
+                umma_commit(smem_u32(&s.empty[stage]));
+                ++kit;
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&s.accf[accbuf]));
+        accbuf ^= 1;
+        if (accbuf == 0) accphase ^= 1u;
+    }
+    // Every MMA this thread issued must finish before TMEM and SMEM go away.
+    umma_commit(smem_u32(s.drain));
+    drain_wait(smem_u32(s.drain), 0u, p);
+}
+
+__device__ __forceinline__ void store_chunk(const ConvParams& p, long long pix, int o0, float (&v)[16],
+                                            int Y, int X, int img) {
+    if (p.out_nchw) {
+        if (Y < p.keep_lo || Y >= p.keep_hi) return;
+        float* y = static_cast<float*>(p.y);
+        const long long rowoff = static_cast<long long>(Y - p.keep_lo + p.dst_row0) * p.W + X;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int o = o0 + i;
+            if (o < p.cout) y[(static_cast<long long>(img) * p.cout + o) * p.plane + rowoff] = v[i];
+        }
+        return;
+    }
+    const bool full = p.vec_ok && (o0 + 16 <= p.cout);
+    if (p.out_f16) {
+        __half* y = static_cast<__half*>(p.y) + pix * p.cout + o0;
+        if (full) {
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                __half2 t = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+                h[i] = *reinterpret_cast<uint32_t*>(&t);
+            }
+            reinterpret_cast<uint4*>(y)[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            reinterpret_cast<uint4*>(y)[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (o0 + i < p.cout) y[i] = __float2half_rn(v[i]);
+        }
+    } else {
+        float* y = static_cast<float*>(p.y) + pix * p.cout + o0;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                reinterpret_cast<float4*>(y)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (o0 + i < p.cout) y[i] = v[i];
+        }
+    }
+}
+
+__device__ __forceinline__ void epilogue_chunk(const ConvParams& p, const TileInfo& ti, const uint32_t (&r)[16],
+                                               int o0, int v, int u, int q, int pp, int Y, int X,
+                                               long long pix) {
+    float val[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) val[i] = __uint_as_float(r[i]) * p.oscale;
+    const bool full = p.vec_ok && (o0 + 16 <= p.cout);
+    if (p.bias != nullptr) {
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 b = __ldg(reinterpret_cast<const float4*>(p.bias + o0) + i);
+                val[4 * i] += b.x;
+                val[4 * i + 1] += b.y;
+                val[4 * i + 2] += b.z;
+                val[4 * i + 3] += b.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (o0 + i < p.cout) val[i] += __ldg(p.bias + o0 + i);
+        }
+    }
+    if (p.residual != nullptr) {
+        const float* rs = p.residual + pix * p.cout + o0;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 b = reinterpret_cast<const float4*>(rs)[i];
+                val[4 * i] += b.x;
+                val[4 * i + 1] += b.y;
+                val[4 * i + 2] += b.z;
+                val[4 * i + 3] += b.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (o0 + i < p.cout) val[i] += rs[i];
+        }
+    }
+    if (p.dup_src != nullptr) {
+        const float* ds =
+            p.dup_src + ((static_cast<long long>(ti.img) * p.hv + v) * p.wv + u) * p.dup_cin;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int o = o0 + i;
+            if (o < p.cout) {
+                const int jj = o * p.dup_factor + p.dup_ftoff + 2 * q + pp;
+                val[i] += __ldg(ds + jj / p.dup_repeats);
+            }
+        }
+    }
+    if (p.silu) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) val[i] = silu_f(val[i]);
+    }
+    store_chunk(p, pix, o0, val, Y, X, ti.img);
+}
+
+__device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane) {
+    const int row = ew * 32 + lane;
+    int accbuf = 0;
+    uint32_t accphase = 0;
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p, t);
+        if (!mbar_wait(smem_u32(&s.accf[accbuf]), accphase, s.abort_flag, p.timeout_ns, p.status,
+                       kWhereEpiAccFull))
+            break;
+        tc_fence_after();
+        const int rr = row / p.Wt, cc = row % p.Wt;
+        const int v = ti.v0 + rr, u = ti.u0 + cc;
+        const bool valid = row < p.R * p.Wt && v < p.hv && u < p.wv;
+        const int q = ti.par >> 1, pp = ti.par & 1;
+        const int Y = p.up ? 2 * v + q : v;
+        const int X = p.up ? 2 * u + pp : u;
+        const long long pix = (static_cast<long long>(ti.img) * p.H + Y) * p.W + X;
+        const uint32_t tbase =
+            tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
+        for (int j = 0; j < p.BN; j += 16) {
+            uint32_t r[16];
+            __syncwarp();
+            tmem_ld16(tbase + static_cast<uint32_t>(j), r);
+            tmem_ld_wait();
+            const int o0 = ti.n0 + j;
+            if (valid && o0 < p.cout) epilogue_chunk(p, ti, r, o0, v, u, q, pp, Y, X, pix);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s.acce[accbuf]));
+        accbuf ^= 1;
+        if (accbuf == 0) accphase ^= 1u;
+    }
+}
+
+template <bool kGather>
+__global__ void __launch_bounds__(kGather ? 320 : 192, 1)
+    conv_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                const ConvParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem s = carve(smem_raw, p);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        *s.abort_flag = 0;
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(smem_u32(&s.full[i]), kGather ? 129u : 1u);
+            mbar_init(smem_u32(&s.empty[i]), 1u);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&s.accf[i]), 1u);
+            mbar_init(smem_u32(&s.acce[i]), static_cast<uint32_t>(kEpiWarps * 32));
+        }
+        mbar_init(smem_u32(s.drain), 1u);
+        fence_mbar_init();
+    }
+    const uint32_t tmem_cols = p.acc_stride * 2 <= 32 ? 32u
+                               : p.acc_stride * 2 <= 64 ? 64u
+                               : p.acc_stride * 2 <= 128 ? 128u
+                               : p.acc_stride * 2 <= 256 ? 256u
+                                                          : 512u;
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(s.tmem_slot), tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        if (!kGather) tma_prefetch_desc(&mapA);
+        tma_prefetch_desc(&mapB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s.tmem_slot;
+
+    if (warp < kEpiWarps) {
+        role_epilogue(p, s, tmem_base, warp, lane);
+    } else if (warp == kProducerWarp) {
+        if (lane == 0) role_producer<kGather>(p, s, &mapA, &mapB);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) role_mma(p, s, tmem_base);
+    } else if (kGather && warp >= kGatherWarp0) {
+        role_gather(p, s, (warp - kGatherWarp0) * 32 + lane);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, tmem_cols);
+    }
+}
+
+int choose_bn(int cout) {
+    const int c16 = (cout + 15) / 16 * 16;
+    if (c16 <= 256) return c16;
+    int best = 256, best_cost = (c16 + 255) / 256 * 256;
+    for (int bn = 256; bn >= 64; bn -= 16) {
+        const int cost = (c16 + bn - 1) / bn * bn;
+        if (cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+template <bool kGather>
+int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, size_t smem, int grid,
+           cudaStream_t stream) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    VAE_CUDA_CHECK(cudaGetDevice(&dev));
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        VAE_CUDA_CHECK(
+            cudaFuncSetAttribute(conv_kernel<kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+        attr_set[dev] = true;
+    }
+    conv_kernel<kGather><<<grid, kGather ? 320 : 192, smem, stream>>>(ma, mb, p);
+    VAE_CUDA_CHECK(cudaGetLastError());
+    return VAE_OK;
+}
+
+}  // namespace
+
+int conv_validate(const ConvArgs& a) {
+    if (a.x == nullptr || a.w == nullptr || a.y == nullptr)
+        return set_error(VAE_ERR_ARG, "conv: x, w and y must be non-NULL");
+    if (a.taps != 1 && a.taps != 9) return set_error(VAE_ERR_ARG, "conv: taps must be 1 or 9");
+    if (a.n < 1 || a.h_in < 1 || a.w_in < 1)
+        return set_error(VAE_ERR_SHAPE, "conv: n=%d h=%d w=%d must be >= 1", a.n, a.h_in, a.w_in);
+    if (a.cin < 16 || a.cin % 16 != 0 || a.cin > 8192)
+        return set_error(VAE_ERR_SHAPE, "conv: cin=%d must be a multiple of 16 in [16, 8192]", a.cin);
+    if (a.cout < 1 || a.cout > 8192) return set_error(VAE_ERR_SHAPE, "conv: cout=%d out of [1, 8192]", a.cout);
+    if (a.taps == 1 && (a.up || a.rep)) return set_error(VAE_ERR_ARG, "conv1x1: no upsample/replicate");
+    if (!aligned16(a.x) || !aligned16(a.w))
+        return set_error(VAE_ERR_ALIGN, "conv: x and w must be 16-byte aligned");
+    const long long H = a.up ? 2LL * a.h_in : a.h_in, W = a.up ? 2LL * a.w_in : a.w_in;
+    if (static_cast<long long>(a.n) * H * W >= (1LL << 31) || static_cast<long long>(a.w_in) >= (1LL << 31))
+        return set_error(VAE_ERR_SHAPE, "conv: too many output pixels");
+    if (a.out_nchw && (a.out_f16 || a.residual != nullptr))
+        return set_error(VAE_ERR_ARG, "conv: NCHW output is f32 without residual");
+    if (a.dup_src != nullptr) {
+        if (!a.up || a.dup_cin < 1 || a.dup_repeats < 1 || a.dup_factor < 1)
+            return set_error(VAE_ERR_ARG, "conv: DupUp needs the upsample fold and a valid shuffle");
+        const long long jmax = static_cast<long long>(a.cout - 1) * a.dup_factor + a.dup_ftoff + 3;
+        if (jmax / a.dup_repeats >= a.dup_cin)
+            return set_error(VAE_ERR_SHAPE, "conv: DupUp reads past the source channels");
+    }
+    return VAE_OK;
+}
+
+int conv_run(const ConvArgs& a, cudaStream_t stream) {
+    int rc = conv_validate(a);
+    if (rc != VAE_OK) return rc;
+    rc = check_device();
+    if (rc != VAE_OK) return rc;
+    DevStatus* st = device_status_ptr();
+    if (st == nullptr) return VAE_ERR_CUDA;
+    const int nsm = sm_count();
+    if (nsm <= 0) return set_error(VAE_ERR_CUDA, "conv: no SM count");
+
+    ConvParams p{};
+    p.n = a.n;
+    p.hv = a.h_in;
+    p.wv = a.w_in;
+    p.cin = a.cin;
+    p.cout = a.cout;
+    p.taps = a.taps;
+    p.up = a.up ? 1 : 0;
+    p.rep = a.rep ? 1 : 0;
+    p.H = p.up ? 2 * a.h_in : a.h_in;
+    p.W = p.up ? 2 * a.w_in : a.w_in;
+    if (p.wv >= kBM) {
+        p.Wt = kBM;
+        p.R = 1;
+    } else {
+        p.Wt = p.wv;
+        p.R = kBM / p.wv;
+    }
+    p.tiles_x = (p.wv + p.Wt - 1) / p.Wt;
+    p.tiles_y = (p.hv + p.R - 1) / p.R;
+    p.npar = p.up ? 4 : 1;
+    p.BN = choose_bn(a.cout);
+    p.n_tiles = (a.cout + p.BN - 1) / p.BN;
+    p.acc_stride = (p.BN + 31) / 32 * 32;
+    p.kchunks = (a.cin + kBK - 1) / kBK;
+    const long long m_tiles = static_cast<long long>(p.n) * p.tiles_y * p.npar * p.tiles_x;
+    const long long total = m_tiles * p.n_tiles;
+    if (total >= (1LL << 31)) return set_error(VAE_ERR_SHAPE, "conv: too many tiles");
+    p.total_tiles = static_cast<int>(total);
+    const int stage_bytes = kABytes + p.BN * 128;
+    p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - 256) / stage_bytes);
+    p.a_tx = static_cast<uint32_t>(128 * p.Wt * p.R);
+    p.x = static_cast<const __half*>(a.x);
+    p.bias = a.bias;
+    p.residual = a.residual;
+    p.y = a.y;
+    p.oscale = a.oscale;
+    p.silu = a.silu ? 1 : 0;
+    p.out_f16 = a.out_f16 ? 1 : 0;
+    p.vec_ok = (a.cout % 16 == 0) && aligned16(a.y) && (a.residual == nullptr || aligned16(a.residual)) &&
+               (a.bias == nullptr || aligned16(a.bias));
+    p.out_nchw = a.out_nchw ? 1 : 0;
+    p.keep_lo = a.keep_lo;
+    p.keep_hi = a.keep_hi;
+    p.dst_row0 = a.dst_row0;
+    p.plane = a.plane;
+    if (p.out_nchw && p.keep_hi <= p.keep_lo) {
+        p.keep_lo = 0;
+        p.keep_hi = p.H;
+        p.dst_row0 = 0;
+        p.plane = static_cast<long long>(p.H) * p.W;
+    }
+    p.dup_src = a.dup_src;
+    p.dup_cin = a.dup_cin;
+    p.dup_factor = a.dup_factor;
+    p.dup_repeats = a.dup_repeats;
+    p.dup_ftoff = a.dup_ftoff;
+    p.status = st;
+    p.timeout_ns = wait_timeout_ns();
+
+    CUtensorMap ma{}, mb{};
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(a.taps),
+                                  static_cast<uint64_t>(a.cout)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(a.taps) * a.cin * 2};
+        const uint32_t box[3] = {static_cast<uint32_t>(kBK), 1u, static_cast<uint32_t>(p.BN)};
+        rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != VAE_OK) return rc;
+    }
+    bool gather = p.rep != 0;
+    if (!gather) {
+        const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(p.wv),
+                                  static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n)};
+        const uint64_t strides[3] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(p.wv) * a.cin * 2,
+                                     static_cast<uint64_t>(p.hv) * p.wv * a.cin * 2};
+        const uint32_t box[4] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(p.Wt),
+                                 static_cast<uint32_t>(p.R), 1u};
+        if (encode_tiled(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.x, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B) != VAE_OK) {
+            clear_error();
+            gather = true;  // shapes TMA cannot describe: gather threads build the A tiles
+        }
+    }
+    const size_t smem = 1024 + static_cast<size_t>(p.stages) * stage_bytes + 256;
+    const int grid = static_cast<int>(std::min<long long>(total, nsm));
+    return gather ? launch<true>(p, ma, mb, smem, grid, stream) : launch<false>(p, ma, mb, smem, grid, stream);
+}
+
+}  // namespace vae
+
+using namespace vae;
+
+extern "C" {
+
+int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin, const void* w_dev,
+                     const float* bias_dev, const float* residual_dev, void* y_dev, int cout, float oscale,
+                     unsigned flags, vae_stream_t stream) {
+    clear_error();
+    if (flags & ~static_cast<unsigned>(VAE_UPSAMPLE2X | VAE_PAD_REPLICATE | VAE_EPI_SILU | VAE_OUT_F16))
+        return set_error(VAE_ERR_ARG, "vae_conv3x3_nhwc: unknown flag bits 0x%x", flags);
+    ConvArgs a{};
+    a.x = x_dev;
+    a.n = n;
+    a.h_in = h_in;
+    a.w_in = w_in;
+    a.cin = cin;
+    a.w = w_dev;
+    a.cout = cout;
+    a.taps = 9;
+    a.bias = bias_dev;
+    a.residual = residual_dev;
+    a.y = y_dev;
+    a.oscale = oscale;
+    a.up = (flags & VAE_UPSAMPLE2X) != 0;
+    a.rep = (flags & VAE_PAD_REPLICATE) != 0;
+    a.silu = (flags & VAE_EPI_SILU) != 0;
+    a.out_f16 = (flags & VAE_OUT_F16) != 0;
+    return conv_run(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int vae_conv1x1(const void* x_dev, int m, int cin, const void* w_dev, const float* bias_dev,
+                const float* residual_dev, void* y_dev, int cout, float oscale, unsigned flags,
+                vae_stream_t stream) {
+    clear_error();
+    if (flags & ~static_cast<unsigned>(VAE_EPI_SILU | VAE_OUT_F16))
+        return set_error(VAE_ERR_ARG, "vae_conv1x1: only VAE_EPI_SILU and VAE_OUT_F16 apply (0x%x)", flags);
+    ConvArgs a{};
+    a.x = x_dev;
+    a.n = 1;
+    a.h_in = 1;
+    a.w_in = m;
+    a.cin = cin;
+    a.w = w_dev;
+    a.cout = cout;
+    a.taps = 1;
+    a.bias = bias_dev;
+    a.residual = residual_dev;
+    a.y = y_dev;
+    a.oscale = oscale;
+    a.silu = (flags & VAE_EPI_SILU) != 0;
+    a.out_f16 = (flags & VAE_OUT_F16) != 0;
+    return conv_run(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,36 @@
+// Internal interface of the implicit-GEMM conv kernel, shared by the public
+// conv entry points, the mid attention and the decoder driver.
+#pragma once
+
+#include "vae_common.cuh"
+
+namespace vae {
+
+struct ConvArgs {
+    const void* x = nullptr;     // f16 NHWC [n][h_in][w_in][cin]
+    int n = 1, h_in = 0, w_in = 0, cin = 0;
+    const void* w = nullptr;     // f16 [cout][taps][cin]
+    int cout = 0;
+    int taps = 9;                // 9 (3x3) or 1 (1x1)
+    const float* bias = nullptr;
+    const float* residual = nullptr;  // f32 NHWC [n][H][W][cout]; may alias y
+    void* y = nullptr;
+    float oscale = 1.0f;
+    bool up = false, rep = false, silu = false, out_f16 = false;
+    // NCHW f32 output of output rows [keep_lo, keep_hi) at destination row
+    // (Y - keep_lo + dst_row0), channel planes `plane` floats apart.
+    // keep_hi <= keep_lo means all rows of an [n][cout][H][W] tensor.
+    bool out_nchw = false;
+    int keep_lo = 0, keep_hi = 0, dst_row0 = 0;
+    long long plane = 0;
+    // DupUp3D add of the up conv: src f32 NHWC [n][h_in][w_in][dup_cin];
+    // output channel o of parity (q, p) adds
+    // src[..., (o*dup_factor + dup_ftoff + 2q + p) / dup_repeats].
+    const float* dup_src = nullptr;
+    int dup_cin = 0, dup_factor = 0, dup_repeats = 0, dup_ftoff = 0;
+};
+
+int conv_validate(const ConvArgs& a);
+int conv_run(const ConvArgs& a, cudaStream_t stream);
+
+}  // namespace vae

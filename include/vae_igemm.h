@@ -1,0 +1,283 @@
+/*
+ * vae_igemm.h — C ABI of the GB300 (sm_103a) image-VAE decoder hot path.
+ *
+ * The operations restate the image-VAE decoders of the cortiq-engine pages:
+ * "qi21_vae.rs" (the resident Qwen-Image-2.1 decoder: NHWC implicit-GEMM
+ * 3x3 convs with the nearest-2x upsample folded into the A-tile gather,
+ * the qv_rmsn RMS_norm, the qv_dupup DupUp3D shortcut, the band planner) and
+ * "vae.rs" (the FLUX-class AutoencoderKL decoder: Conv2d::apply,
+ * GroupNorm::apply, AttnBlock::apply, VaeDecoder::decode), with replicate
+ * padding from "s2v_vae.rs".
+ *
+ * Conventions for every entry point below:
+ *  - Pointers named *_dev are CUDA device memory owned by the caller. The
+ *    library never frees or keeps them past the call (the decoder handle owns
+ *    only its own packed weights).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream). No call synchronises the stream except vae_sync_status and
+ *    vae_decode_host.
+ *  - Return value: VAE_OK (0) or a negative vae_status. Every shape, flag and
+ *    alignment is validated before anything is enqueued: on an error nothing
+ *    was launched and outputs are untouched. vae_last_error() gives the text.
+ *  - f16 tensors are IEEE binary16 (passed as void* / uint16_t bits); f32 is
+ *    IEEE binary32. "NHWC" = [n][h][w][c], c contiguous.
+ *  - Device-side waits are bounded (vae_set_wait_timeout_ns). A wait that
+ *    runs out makes the kernel record VAE_ERR_DEVICE_TIMEOUT in the device
+ *    status word and return; vae_sync_status() reports it.
+ *  - There is no CPU fallback: without a usable sm_103a GPU every compute
+ *    call returns VAE_ERR_CUDA.
+ */
+#ifndef VAE_IGEMM_H
+#define VAE_IGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* vae_stream_t;
+
+typedef enum {
+    VAE_OK = 0,
+    VAE_ERR_ARG = -1,            /* NULL where a pointer is required, bad flag, bad enum */
+    VAE_ERR_SHAPE = -2,          /* unsupported or inconsistent sizes */
+    VAE_ERR_ALIGN = -3,          /* a pointer is not 16-byte aligned */
+    VAE_ERR_NOMEM = -4,          /* workspace too small / host allocation failed */
+    VAE_ERR_CUDA = -5,           /* a CUDA runtime/driver call failed (text in vae_last_error) */
+    VAE_ERR_DEVICE_TIMEOUT = -6, /* a bounded device wait ran out */
+    VAE_ERR_UNSUPPORTED = -7     /* no sm_103a device */
+} vae_status;
+
+/* Conv flags. */
+enum {
+    VAE_UPSAMPLE2X = 1,     /* nearest-2x of the input folded into the gather: output is 2h x 2w */
+    VAE_PAD_REPLICATE = 2,  /* out-of-grid reads take the nearest edge pixel (default: zero) */
+    VAE_EPI_SILU = 16,      /* SiLU v/(1+e^-v) applied last in the epilogue */
+    VAE_OUT_F16 = 32        /* store the output as f16 (default f32) */
+};
+
+/* Library version string and the compute capability it was built for. */
+const char* vae_version(void);
+
+/* Thread-local text of the last error returned on this thread ("" if none). */
+const char* vae_last_error(void);
+
+/* Synchronises `stream`, reads and clears the device status word of the
+ * current device. Returns VAE_OK or VAE_ERR_DEVICE_TIMEOUT (a kernel gave up a
+ * bounded wait since the last call) or VAE_ERR_CUDA. */
+int vae_sync_status(vae_stream_t stream);
+
+/* Upper bound, in nanoseconds of %globaltimer, on any single device-side wait
+ * of later launches from this process (default 4e9). 0 restores the default. */
+int vae_set_wait_timeout_ns(unsigned long long ns);
+
+/* Failure-detection self test: launches one CTA that waits (bounded by
+ * timeout_ns) on an mbarrier phase nothing completes, then returns. The
+ * kernel records VAE_ERR_DEVICE_TIMEOUT; this call synchronises and returns
+ * what vae_sync_status reports (VAE_ERR_DEVICE_TIMEOUT when the path works).
+ * No fault, trap or hang is involved. */
+int vae_selftest_wait_timeout(unsigned long long timeout_ns, vae_stream_t stream);
+
+/*
+ * 3x3 convolution, stride 1, padding 1, as an implicit GEMM on tcgen05.
+ *   y[p, o] = SiLU?( oscale * sum_{tap, c} xt[p + d_tap, c] * w[o, tap, c]
+ *                    + bias[o] + residual[p, o] )
+ * where xt is x, or nearest-2x(x) with VAE_UPSAMPLE2X, and reads outside the
+ * (upsampled) grid are 0 or, with VAE_PAD_REPLICATE, the nearest edge pixel.
+ * ("vae.rs" Conv2d::apply; "qi21_vae.rs" conv_s and the module doc's
+ * implicit-GEMM recipe; "s2v_vae.rs" replicate padding.)
+ *
+ *   x_dev     f16 NHWC [n][h_in][w_in][cin], 16-byte aligned.
+ *   w_dev     f16 [cout][3][3][cin] (tap-major: K index = (ky*3+kx)*cin + c).
+ *   bias_dev  f32 [cout] or NULL (no bias).
+ *   residual_dev  f32 NHWC [n][H][W][cout] or NULL; may equal y_dev (in place).
+ *   y_dev     NHWC [n][H][W][cout], f32, or f16 with VAE_OUT_F16;
+ *             H = h_in, W = w_in, or 2*h_in, 2*w_in with VAE_UPSAMPLE2X.
+ *   oscale    multiplies the f32 accumulator (the undo of a 2^-g input guard).
+ * Requirements: n, h_in, w_in >= 1; cin % 16 == 0, 16 <= cin <= 8192;
+ * 1 <= cout <= 8192; x_dev, w_dev 16-byte aligned. Outputs of any cout are
+ * supported (vector stores when cout % 16 == 0).
+ */
+int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin,
+                     const void* w_dev, const float* bias_dev, const float* residual_dev,
+                     void* y_dev, int cout, float oscale, unsigned flags, vae_stream_t stream);
+
+/*
+ * 1x1 convolution = plain GEMM over m pixels, the same kernel with one tap.
+ *   y[p, o] = SiLU?( oscale * sum_c x[p, c] * w[o, c] + bias[o] + residual[p, o] )
+ * ("qi21_vae.rs" conv mode 0: post_quant, the guarded shortcut, attention
+ * q/k/v/proj; "vae.rs" AttnBlock::proj.)
+ *   x_dev f16 [m][cin]; w_dev f16 [cout][cin]; bias_dev f32 [cout] or NULL;
+ *   residual_dev f32 [m][cout] or NULL (may equal y_dev); y_dev [m][cout]
+ *   f32 or f16 (VAE_OUT_F16). Flags: VAE_EPI_SILU, VAE_OUT_F16 only.
+ * Requirements as vae_conv3x3_nhwc; m >= 1.
+ */
+int vae_conv1x1(const void* x_dev, int m, int cin, const void* w_dev,
+                const float* bias_dev, const float* residual_dev, void* y_dev, int cout,
+                float oscale, unsigned flags, vae_stream_t stream);
+
+/*
+ * Per-pixel RMS_norm (+ bias on read, optional SiLU) -> f16:
+ *   v = x[p, :] + bias_in;  y[p, c] = SiLU?( v[c] * sqrt(C) / max(||v||_2, 1e-12) * gamma[c] ) * out_scale
+ * ("qi21_vae.rs" qv_rmsn.)
+ *   x_dev f32 [m][c]; bias_in_dev f32 [c] or NULL; gamma_dev f32 [c];
+ *   y_dev f16 [m][c]. Requirements: m >= 1, c % 4 == 0, 4 <= c <= 16384;
+ *   pointers 16-byte aligned.
+ */
+int vae_rmsnorm_silu(const float* x_dev, int m, int c, const float* bias_in_dev,
+                     const float* gamma_dev, int silu, float out_scale, void* y_dev,
+                     vae_stream_t stream);
+
+/*
+ * GroupNorm(groups) over each image (+ bias on read, optional SiLU) -> f16:
+ *   v = x + bias_in; per (image, group g of c/groups consecutive channels):
+ *   mean mu and biased variance var over hw * c/groups values;
+ *   y = SiLU?( (v - mu) / sqrt(var + eps) * gamma[c] + beta[c] ) * out_scale
+ * ("vae.rs" GroupNorm::apply; "s2v_vae.rs" s2v_gn_part / s2v_gn_fin /
+ * s2v_gn_apply.) Statistics: per-chunk (count, mean, M2) partials in f32
+ * merged with Chan's formula.
+ *   x_dev f32 NHWC [n][hw][c]; gamma/beta f32 [c]; bias_in f32 [c] or NULL;
+ *   y_dev f16 [n][hw][c]; workspace_dev of at least
+ *   vae_groupnorm_workspace_bytes(n, hw, c, groups) bytes, 16-byte aligned,
+ *   contents ignored on entry.
+ * Requirements: c % groups == 0, c % 4 == 0, 4 <= c <= 16384, 1 <= groups <= 1024.
+ */
+size_t vae_groupnorm_workspace_bytes(int n, int hw, int c, int groups);
+int vae_groupnorm_silu(const float* x_dev, int n, int hw, int c, int groups, float eps,
+                       const float* bias_in_dev, const float* gamma_dev, const float* beta_dev,
+                       int silu, float out_scale, void* y_dev,
+                       void* workspace_dev, size_t workspace_bytes, vae_stream_t stream);
+
+/*
+ * f32 -> f16 cast of the raw residual stream with its range guard:
+ *   y[i] = (x[i] + bias[i % c]) * scale            (scale normally 2^-g)
+ * ("qi21_vae.rs" qv_cast and the guard() doc.)
+ *   x_dev f32 [count]; bias_dev f32 [c] or NULL; y_dev f16 [count];
+ *   count % c == 0, c % 4 == 0, pointers 16-byte aligned.
+ */
+int vae_cast_f16(const float* x_dev, size_t count, int c, const float* bias_dev,
+                 float scale, void* y_dev, vae_stream_t stream);
+
+/* Mid self-attention norm kinds. */
+enum { VAE_NORM_GROUP = 0, VAE_NORM_RMS = 1 };
+
+/*
+ * Single-head spatial self-attention of the decoder's mid block, in place on
+ * the f32 residual stream:
+ *   n = GroupNorm(x) or RMS_norm(x)*gamma (no SiLU); q,k,v = n W^T + b (f16);
+ *   o = softmax(q k^T / sqrt(c)) v; x += o W_o^T + b_o.
+ * ("vae.rs" AttnBlock::apply / finish; "qi21_vae.rs" attention.) The
+ * q k^T -> softmax -> P.V part is one fused tcgen05 kernel (no score matrix
+ * in memory).
+ *   x_dev f32 [m][c] (tokens = pixels of one image); w*_dev f16 [c][c]
+ *   (row = output channel); b*_dev f32 [c]; norm_beta_dev ignored for RMS.
+ *   workspace_dev >= vae_mid_attention_workspace_bytes(m, c, groups).
+ * Requirements: c % 64 == 0, 64 <= c <= 2048, m >= 1.
+ */
+size_t vae_mid_attention_workspace_bytes(int m, int c, int groups);
+int vae_mid_attention(float* x_dev, int m, int c, int norm_kind, int groups, float eps,
+                      const float* norm_gamma_dev, const float* norm_beta_dev,
+                      const void* wq_dev, const float* bq_dev, const void* wk_dev, const float* bk_dev,
+                      const void* wv_dev, const float* bv_dev, const void* wo_dev, const float* bo_dev,
+                      void* workspace_dev, size_t workspace_bytes, vae_stream_t stream);
+
+/* ───────────────────────────── whole decoder ───────────────────────────── */
+
+/* Host-side description of a decoder, mirroring "vae.rs" VaeChainArgs and
+ * its Vae*Ref structs. All pointers are HOST memory read only during
+ * vae_decoder_create (which copies and re-lays the weights on the device). */
+typedef struct {
+    const uint16_t* w;  /* f16 bits, OIHW [cout][cin][k][k]; NULL = this conv is absent */
+    const float* b;     /* f32 [cout] */
+    int cout, cin, k;   /* k = 1 or 3 */
+} vae_conv_desc;
+
+typedef struct {
+    const float* gamma; /* f32 [c] */
+    const float* beta;  /* f32 [c]; GroupNorm only (NULL for RMS_norm) */
+} vae_norm_desc;
+
+typedef struct {
+    vae_norm_desc norm1;
+    vae_conv_desc conv1;
+    vae_norm_desc norm2;
+    vae_conv_desc conv2;
+    vae_conv_desc shortcut; /* 1x1 when cin != cout; w = NULL otherwise */
+} vae_resnet_desc;
+
+typedef struct {
+    vae_norm_desc norm;
+    vae_conv_desc q, k, v, o; /* 1x1, c -> c */
+} vae_attn_desc;
+
+typedef struct {
+    const vae_resnet_desc* resnets;
+    int n_resnets;
+    vae_conv_desc up;  /* 3x3 conv after nearest-2x; w = NULL: no upsample */
+    int in_dim, out_dim;
+    int ft;            /* DupUp temporal factor (1 for images) */
+} vae_up_desc;
+
+enum { VAE_FAMILY_GN = 0, VAE_FAMILY_RMS = 1 };
+
+typedef struct {
+    int family;            /* VAE_FAMILY_GN (FLUX-class) or VAE_FAMILY_RMS (Qwen/Wan-style) */
+    int latent_channels;
+    float scaling, shift;  /* GN family: z/scaling + shift before conv_in */
+    int groups;            /* GroupNorm groups (GN family) */
+    float eps;             /* GroupNorm eps */
+    int dupup;             /* RMS family: add the DupUp shortcut after each up conv */
+    vae_conv_desc post_quant; /* RMS family 1x1 before conv_in; w = NULL: none */
+    vae_conv_desc conv_in;
+    vae_resnet_desc mid_res1;
+    vae_attn_desc mid_attn;
+    vae_resnet_desc mid_res2;
+    const vae_up_desc* ups;
+    int n_ups;
+    vae_norm_desc norm_out;
+    vae_conv_desc conv_out;
+} vae_decoder_desc;
+
+typedef struct vae_decoder* vae_decoder_t;
+
+/* Validates `desc`, copies every weight to the current device in the
+ * kernels' layouts and returns a handle. */
+int vae_decoder_create(const vae_decoder_desc* desc, vae_decoder_t* out);
+int vae_decoder_destroy(vae_decoder_t dec);
+
+typedef struct {
+    int band_from;   /* RMS family: up blocks >= band_from run in horizontal bands */
+    int nbands;      /* number of equal kept-row bands (0 or 1 with band_rows 0: whole frame) */
+    int band_rows;   /* alternative to nbands: at most this many kept rows per band */
+    int guard_log2;  /* f16 range guard g of the raw-stream casts (default 8 when < 0) */
+    unsigned flags;  /* reserved, 0 */
+} vae_decode_opts;
+
+/* Device workspace (bytes) vae_decode needs for an h0 x w0 latent. */
+int vae_decode_workspace(vae_decoder_t dec, int h0, int w0, const vae_decode_opts* opts,
+                         size_t* bytes);
+
+/*
+ * Decode one latent frame ("qi21_vae.rs" decode, "vae.rs" VaeDecoder::decode).
+ *   z_dev   f32 NCHW [latent_channels][h0][w0] (device)
+ *   out_dev f32 NCHW [nch][h0 << ups][w0 << ups] (device), nch = conv_out cout
+ *   opts    NULL = whole frame, guard 8.
+ * A banded decode writes the same kept rows bit for bit as the whole-frame one.
+ */
+int vae_decode(vae_decoder_t dec, const float* z_dev, int h0, int w0, float* out_dev,
+               const vae_decode_opts* opts, void* workspace_dev, size_t workspace_bytes,
+               vae_stream_t stream);
+
+/* As vae_decode with HOST z and out: copies z in, decodes, copies out and
+ * synchronises `stream` (the end-to-end call). */
+int vae_decode_host(vae_decoder_t dec, const float* z_host, int h0, int w0, float* out_host,
+                    const vae_decode_opts* opts, void* workspace_dev, size_t workspace_bytes,
+                    vae_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VAE_IGEMM_H */

@@ -1,0 +1,36 @@
+"""Helpers of the GPU parity tests: device transfer, tolerances, sentinels."""
+import numpy as np
+
+# Per conv, from the hot path's stated target: max|d| / max|ref| <= 2e-3,
+# the oracle run on the same f16-rounded inputs and weights.
+CONV_TOL = 2e-3
+# f16 outputs of the norms: one rounding to f16 (relative 2^-11 ~ 4.9e-4 of
+# each element) plus f32 statistics; bounded well inside 1e-3 of max|ref|.
+NORM_TOL = 1e-3
+
+
+def torch_mod():
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("these tests need a CUDA device (GB300, sm_103a)")
+    return torch
+
+
+def to_dev(a, dtype=None):
+    torch = torch_mod()
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def rel_err(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def sentinel_like(shape, dtype):
+    """A CUDA tensor filled with NaN, so unwritten outputs are caught."""
+    torch = torch_mod()
+    return torch.full(shape, float("nan"), dtype=dtype, device="cuda")

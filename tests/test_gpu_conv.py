@@ -1,0 +1,162 @@
+"""GPU parity of the implicit-GEMM conv (through the C ABI) against the oracle.
+
+Element by element on small and ragged shapes (several M and N tiles, a
+ragged tail, K chunks shorter than 64 channels, every padding/upsample
+combination, every epilogue variant), and on sampled pixels at the
+full 1024^2 stage sizes in the launch configuration the bench times.
+Outputs start as NaN so an unwritten element fails.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import implicit_gemm_convolution_vae_gb300 as vg
+from gpu_common import CONV_TOL, rel_err, sentinel_like, to_dev, torch_mod
+from vae_inputs import conv_case, f16_normal, stream_normal
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(case, upsample=False, replicate=False, silu=False, out_f16=False, residual=None, oscale=1.0):
+    torch = torch_mod()
+    x = to_dev(case["x"])
+    w = to_dev(vg.pack_conv3x3(case["w"]))
+    b = to_dev(case["b"])
+    n, h, wd, _ = case["x"].shape
+    cout = case["w"].shape[0]
+    H, W = (2 * h, 2 * wd) if upsample else (h, wd)
+    out = sentinel_like((n, H, W, cout), torch.float16 if out_f16 else torch.float32)
+    res = None if residual is None else to_dev(residual)
+    vg.conv3x3_nhwc(x, w, b, residual=res, out=out, oscale=oscale, upsample=upsample, replicate=replicate,
+                    silu=silu, out_f16=out_f16)
+    vg.sync_status()
+    return out.float().cpu().numpy()
+
+
+def _ref(case, upsample=False, replicate=False, silu=False, residual=None):
+    outs = []
+    for i in range(case["x"].shape[0]):
+        xc = np.moveaxis(case["x"][i].astype(np.float64), -1, 0)
+        y = oracle.conv2d(xc, case["w"], case["b"], upsample=upsample, pad="replicate" if replicate else "zero")
+        y = np.moveaxis(y, 0, -1)
+        if residual is not None:
+            y = y + residual[i]
+        if silu:
+            y = oracle.silu(y)
+        outs.append(y)
+    return np.stack(outs)
+
+
+@pytest.mark.parametrize("variant", ["zero", "upsample", "replicate", "upsample_replicate"])
+def test_single_conv_config(variant):
+    """The 32x32x64 -> 64 conv (and its 16x16 -> 32x32 upsample fold), seed 0."""
+    up = variant.startswith("upsample")
+    rep = variant.endswith("replicate")
+    h = 16 if up else 32
+    case = conv_case(seed=0, h=h, w=h, cin=64, cout=64, name=f"cfg1.{'up' if up else 'plain'}")
+    got = _run(case, upsample=up, replicate=rep)
+    ref = _ref(case, upsample=up, replicate=rep)
+    assert not np.isnan(got).any()
+    assert rel_err(got, ref) <= CONV_TOL
+
+
+SHAPES = [
+    # n, h, w, cin, cout
+    (1, 1, 1, 16, 16),
+    (1, 2, 3, 16, 48),
+    (1, 3, 7, 48, 16),
+    (2, 7, 33, 16, 144),
+    (1, 33, 7, 144, 16),
+    (1, 5, 200, 32, 64),
+    (1, 3, 256, 64, 3),
+    (1, 4, 130, 144, 288),
+    (1, 9, 40, 80, 320),
+]
+
+
+@pytest.mark.parametrize("n,h,w,cin,cout", SHAPES)
+@pytest.mark.parametrize("up,rep", [(False, False), (True, False), (False, True), (True, True)])
+def test_conv_shapes(n, h, w, cin, cout, up, rep):
+    case = conv_case(seed=1, n=n, h=h, w=w, cin=cin, cout=cout, name=f"shape.{n}.{h}.{w}.{cin}.{cout}")
+    got = _run(case, upsample=up, replicate=rep)
+    ref = _ref(case, upsample=up, replicate=rep)
+    assert not np.isnan(got).any()
+    assert rel_err(got, ref) <= CONV_TOL
+
+
+@pytest.mark.parametrize("silu,out_f16,with_res", [(True, False, False), (False, True, False),
+                                                   (False, False, True), (True, True, True)])
+def test_conv_epilogue(silu, out_f16, with_res):
+    case = conv_case(seed=2, h=12, w=150, cin=48, cout=96, name="epi")
+    res = stream_normal(2, "epi.res", (1, 12, 150, 96)) if with_res else None
+    got = _run(case, silu=silu, out_f16=out_f16, residual=res, oscale=1.0)
+    ref = _ref(case, silu=silu, residual=res)
+    tol = CONV_TOL + (1e-3 if out_f16 else 0.0)
+    assert not np.isnan(got).any()
+    assert rel_err(got, ref) <= tol
+
+
+def test_conv_in_place_residual_and_oscale():
+    """y = oscale*acc + b + y (the stream update x += conv(..)), with a 2^8 guard undo."""
+    torch = torch_mod()
+    case = conv_case(seed=3, h=8, w=64, cin=32, cout=32, name="inplace")
+    xs = (case["x"].astype(np.float32) * 2.0 ** -8).astype(np.float16)
+    stream = stream_normal(3, "inplace.s", (1, 8, 64, 32))
+    y = to_dev(stream.copy())
+    vg.conv3x3_nhwc(to_dev(xs), to_dev(vg.pack_conv3x3(case["w"])), to_dev(case["b"]), residual=y, out=y,
+                    oscale=256.0)
+    vg.sync_status()
+    xc = np.moveaxis(xs[0].astype(np.float64), -1, 0) * 256.0
+    ref = np.moveaxis(oracle.conv2d(xc, case["w"], case["b"]), 0, -1)[None] + stream
+    assert rel_err(y.cpu().numpy(), ref) <= CONV_TOL
+
+
+@pytest.mark.parametrize("m,cin,cout", [(1, 16, 16), (100, 16, 16), (1000, 512, 256), (333, 1152, 1152),
+                                        (4096, 144, 3)])
+def test_conv1x1(m, cin, cout):
+    torch = torch_mod()
+    x = f16_normal(4, f"c11.x.{m}", (m, cin), 1.0)
+    w = f16_normal(4, f"c11.w.{cin}", (cout, cin, 1, 1), (1.0 / cin) ** 0.5)
+    b = stream_normal(4, f"c11.b.{cout}", (cout,)) * 0.1
+    out = sentinel_like((m, cout), torch.float32)
+    vg.conv1x1(to_dev(x), to_dev(vg.pack_conv1x1(w)), to_dev(b.astype(np.float32)), out=out)
+    vg.sync_status()
+    ref = x.astype(np.float64) @ w[:, :, 0, 0].astype(np.float64).T + b
+    got = out.cpu().numpy()
+    assert not np.isnan(got).any()
+    assert rel_err(got, ref) <= CONV_TOL
+
+
+def _sample_points(H, W, n, seed):
+    rng = np.random.default_rng(seed)
+    ys = list(rng.integers(0, H, n))
+    xs = list(rng.integers(0, W, n))
+    for y in (0, 1, H // 2, H - 2, H - 1):
+        for x in (0, 1, 127, 128, W // 2, W - 129, W - 128, W - 1):
+            ys.append(y)
+            xs.append(x)
+    return np.array(ys), np.array(xs)
+
+
+@pytest.mark.parametrize("stage", ["b3_resnet_1024", "b2_upconv_512_to_1024"])
+def test_full_size_stage_sampled(stage):
+    """The 1024^2 stages: 144->144 3x3 at 1024^2, and the 288->144 up conv 512^2 -> 1024^2."""
+    torch = torch_mod()
+    if stage == "b3_resnet_1024":
+        h = w = 1024
+        cin, cout, up = 144, 144, False
+    else:
+        h = w = 512
+        cin, cout, up = 288, 144, True
+    x = f16_normal(5, f"full.{stage}.x", (1, h, w, cin), 1.0)
+    wt = f16_normal(5, f"full.{stage}.w", (cout, cin, 3, 3), (2.0 / (9 * cin)) ** 0.5)
+    b = (stream_normal(5, f"full.{stage}.b", (cout,)) * 0.1).astype(np.float32)
+    H, W = (2 * h, 2 * w) if up else (h, w)
+    out = sentinel_like((1, H, W, cout), torch.float32)
+    vg.conv3x3_nhwc(to_dev(x), to_dev(vg.pack_conv3x3(wt)), to_dev(b), out=out, upsample=up)
+    vg.sync_status()
+    assert not torch.isnan(out).any().item()
+    ys, xs = _sample_points(H, W, 400, 6)
+    got = out[0, torch.from_numpy(ys).cuda(), torch.from_numpy(xs).cuda()].cpu().numpy()
+    ref = oracle.conv2d_at(np.moveaxis(x[0], -1, 0), wt, b, ys, xs, upsample=up)
+    assert rel_err(got, ref) <= CONV_TOL

@@ -105,6 +105,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Warp-uniform outcome of a per-lane wait: a warp that runs tcgen05.ld/st
+// (.sync.aligned) must never split on an abort, so every lane takes the
+// same branch.
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
 // TMA: tiled tensor loads into shared memory, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2, uint64_t policy) {

@@ -398,8 +398,8 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
     uint32_t accphase = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
         const TileInfo ti = decode_tile(p, t);
-        if (!mbar_wait(smem_u32(&s.accf[accbuf]), accphase, s.abort_flag, p.timeout_ns, p.status,
-                       kWhereEpiAccFull))
+        if (!warp_all(mbar_wait(smem_u32(&s.accf[accbuf]), accphase, s.abort_flag, p.timeout_ns, p.status,
+                                kWhereEpiAccFull)))
             break;
         tc_fence_after();
         const int rr = row / p.Wt, cc = row % p.Wt;
@@ -524,7 +524,8 @@ int conv_validate(const ConvArgs& a) {
         return set_error(VAE_ERR_SHAPE, "conv: n=%d h=%d w=%d must be >= 1", a.n, a.h_in, a.w_in);
     if (a.cin < 16 || a.cin % 16 != 0 || a.cin > 8192)
         return set_error(VAE_ERR_SHAPE, "conv: cin=%d must be a multiple of 16 in [16, 8192]", a.cin);
-    if (a.cout < 1 || a.cout > 8192) return set_error(VAE_ERR_SHAPE, "conv: cout=%d out of [1, 8192]", a.cout);
+    if (a.cout < 1 || a.cout > (1 << 20))
+        return set_error(VAE_ERR_SHAPE, "conv: cout=%d out of [1, 2^20]", a.cout);
     if (a.taps == 1 && (a.up || a.rep)) return set_error(VAE_ERR_ARG, "conv1x1: no upsample/replicate");
     if (!aligned16(a.x) || !aligned16(a.w))
         return set_error(VAE_ERR_ALIGN, "conv: x and w must be 16-byte aligned");

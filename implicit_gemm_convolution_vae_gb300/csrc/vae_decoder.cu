@@ -1,0 +1,670 @@
+// The whole decoder on one GPU: handle creation (weights copied to the
+// device in the kernels' layouts), workspace sizing and the decode driver
+// with exact-halo horizontal bands.
+//
+// Follows "vae.rs" VaeDecoder::decode (FLUX-class GroupNorm family) and
+// "qi21_vae.rs" decode / run_blocks / output_rows / plan_band (Qwen/Wan RMS
+// family with DupUp and bands). Per stage:
+//   ResNet: norm1+SiLU -> f16, conv1 (+bias) -> f32, norm2+SiLU -> f16,
+//           conv2 (+bias +skip, in the epilogue) -> stream; the 1x1 shortcut
+//           reads the raw stream cast to f16 with the 2^-g guard and undoes
+//           it with oscale = 2^g.
+//   Up conv: raw stream cast with the guard, 3x3 conv with the nearest-2x
+//           fold, + bias (+ the DupUp shortcut of the block input) in the
+//           epilogue.
+//   Output: norm_out+SiLU -> f16, conv_out writes NCHW f32 kept rows directly.
+// Banded decoding runs the head and blocks < band_from on the whole frame,
+// then each band from the saved stream rows its plan needs; every kernel is
+// row-local with a per-pixel result independent of tiling, so kept rows are
+// bit-identical to the whole-frame decode.
+//
+// The driver runs twice over the same code: a dry run records the size of
+// every logical buffer, a real run launches. The workspace layout therefore
+// always matches what the launches use.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "vae_attn.h"
+#include "vae_conv.h"
+#include "vae_norm.h"
+
+namespace vae {
+
+struct DConv {
+    __half* w = nullptr;  // [cout][k][k][cin]
+    float* b = nullptr;
+    int cout = 0, cin = 0, k = 0;
+    bool present() const { return w != nullptr; }
+};
+struct DNorm {
+    float* gamma = nullptr;
+    float* beta = nullptr;
+    int c = 0;
+};
+struct DRes {
+    DNorm n1, n2;
+    DConv c1, c2, sc;
+};
+struct DAttn {
+    DNorm n;
+    DConv q, k, v, o;
+};
+struct DUp {
+    std::vector<DRes> res;
+    DConv up;
+    int in_dim = 0, out_dim = 0, ft = 1;
+};
+
+}  // namespace vae
+
+struct vae_decoder {
+    int family = 0, zc = 0, groups = 32, dupup = 0, device = 0;
+    float scaling = 1.f, shift = 0.f, eps = 1e-6f;
+    vae::DConv pq, conv_in, conv_out;
+    vae::DRes mid1, mid2;
+    vae::DAttn attn;
+    std::vector<vae::DUp> ups;
+    vae::DNorm norm_out;
+    std::vector<void*> allocs;
+};
+
+namespace vae {
+
+namespace {
+
+// ───────────────────────────── handle creation ─────────────────────────────
+
+struct Uploader {
+    vae_decoder* d;
+    int rc = VAE_OK;
+
+    template <typename T>
+    T* put(const void* host, size_t bytes) {
+        if (rc != VAE_OK) return nullptr;
+        void* p = nullptr;
+        cudaError_t e = cudaMalloc(&p, std::max<size_t>(bytes, 16));
+        if (e != cudaSuccess) {
+            rc = set_error(VAE_ERR_NOMEM, "decoder_create: cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+            return nullptr;
+        }
+        d->allocs.push_back(p);
+        e = cudaMemcpy(p, host, bytes, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            rc = set_error(VAE_ERR_CUDA, "decoder_create: cudaMemcpy: %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        return static_cast<T*>(p);
+    }
+
+    DConv conv(const vae_conv_desc& c, const char* what, bool required = true) {
+        DConv o;
+        if (rc != VAE_OK) return o;
+        if (c.w == nullptr) {
+            if (required) rc = set_error(VAE_ERR_ARG, "decoder_create: %s has no weights", what);
+            return o;
+        }
+        if ((c.k != 1 && c.k != 3) || c.cout < 1 || c.cin < 16 || c.cin % 16 != 0 || c.b == nullptr) {
+            rc = set_error(VAE_ERR_SHAPE, "decoder_create: %s k=%d cout=%d cin=%d (cin %% 16 == 0 needed)", what,
+                           c.k, c.cout, c.cin);
+            return o;
+        }
+        const int kk = c.k * c.k;
+        std::vector<uint16_t> packed(static_cast<size_t>(c.cout) * kk * c.cin);
+        for (int o_ = 0; o_ < c.cout; ++o_)
+            for (int ci = 0; ci < c.cin; ++ci)
+                for (int t = 0; t < kk; ++t)
+                    packed[(static_cast<size_t>(o_) * kk + t) * c.cin + ci] =
+                        c.w[(static_cast<size_t>(o_) * c.cin + ci) * kk + t];
+        o.w = put<__half>(packed.data(), packed.size() * 2);
+        o.b = put<float>(c.b, static_cast<size_t>(c.cout) * 4);
+        o.cout = c.cout;
+        o.cin = c.cin;
+        o.k = c.k;
+        return o;
+    }
+
+    DNorm norm(const vae_norm_desc& n, int c, bool need_beta, const char* what) {
+        DNorm o;
+        if (rc != VAE_OK) return o;
+        if (n.gamma == nullptr || (need_beta && n.beta == nullptr)) {
+            rc = set_error(VAE_ERR_ARG, "decoder_create: %s norm parameters missing", what);
+            return o;
+        }
+        o.gamma = put<float>(n.gamma, static_cast<size_t>(c) * 4);
+        if (need_beta) o.beta = put<float>(n.beta, static_cast<size_t>(c) * 4);
+        o.c = c;
+        return o;
+    }
+
+    DRes res(const vae_resnet_desc& r, int cin, bool gn, const char* what) {
+        DRes o;
+        o.c1 = conv(r.conv1, what);
+        o.c2 = conv(r.conv2, what);
+        o.sc = conv(r.shortcut, what, false);
+        if (rc != VAE_OK) return o;
+        const int cout = o.c1.cout;
+        if (o.c1.k != 3 || o.c2.k != 3 || o.c1.cin != cin || o.c2.cin != cout || o.c2.cout != cout) {
+            rc = set_error(VAE_ERR_SHAPE, "decoder_create: %s conv shapes do not chain (cin %d)", what, cin);
+            return o;
+        }
+        if (o.sc.present() ? (o.sc.k != 1 || o.sc.cin != cin || o.sc.cout != cout) : (cin != cout)) {
+            rc = set_error(VAE_ERR_SHAPE, "decoder_create: %s needs a 1x1 shortcut %d->%d", what, cin, cout);
+            return o;
+        }
+        o.n1 = norm(r.norm1, cin, gn, what);
+        o.n2 = norm(r.norm2, cout, gn, what);
+        return o;
+    }
+};
+
+// ───────────────────────────── decode driver ─────────────────────────────
+
+struct Rows {
+    int lo, hi;
+    int n() const { return hi - lo; }
+};
+Rows grow(Rows r, int k, int h) { return Rows{std::max(r.lo - k, 0), std::min(r.hi + k, h)}; }
+Rows half_rows(Rows r) { return Rows{r.lo / 2, (r.hi + 1) / 2}; }
+
+enum Buf { kS0, kS1, kS2, kB0, kB1, kB2, kH, kSC, kXN, kZ, kATT, kGN, kZIN, kOUT, kNBuf };
+
+struct Band {
+    Rows input;
+    std::vector<Rows> feed;
+    Rows keep;
+};
+
+// The first of the three stream buffers that is neither `a` nor `b`.
+inline int other(int a, int b) {
+    for (int i = 0; i < 3; ++i)
+        if (i != a && i != b) return i;
+    return -1;
+}
+
+struct Exec {
+    const vae_decoder* d;
+    bool dry;
+    cudaStream_t st;
+    uint8_t* base = nullptr;
+    size_t need[kNBuf] = {};
+    size_t off[kNBuf] = {};
+    float guard = 256.f;
+
+    void* buf(int id, size_t bytes) {
+        if (dry) {
+            need[id] = std::max(need[id], bytes);
+            return reinterpret_cast<void*>(static_cast<uintptr_t>(1) << 20);
+        }
+        return base + off[id];
+    }
+    float* f32(int id, size_t count) { return static_cast<float*>(buf(id, count * 4)); }
+    __half* f16(int id, size_t count) { return static_cast<__half*>(buf(id, count * 2)); }
+
+    int conv(const ConvArgs& a) { return dry ? conv_validate(a) : conv_run(a, st); }
+
+    // norm (+SiLU) of stream `x` [hw][c] -> f16 `y`.
+    int norm(const float* x, long long hw, int c, const DNorm& n, bool silu, __half* y) {
+        if (d->family == VAE_FAMILY_GN) {
+            GnPlan gp;
+            int rc = gn_plan(1, static_cast<int>(hw), c, d->groups, &gp);
+            if (rc != VAE_OK) return rc;
+            void* ws = buf(kGN, gp.bytes);
+            return dry ? VAE_OK
+                       : gn_run(x, 1, static_cast<int>(hw), c, d->groups, d->eps, nullptr, n.gamma, n.beta,
+                                silu ? 1 : 0, 1.f, y, ws, gp.bytes, st);
+        }
+        return dry ? VAE_OK : rms_run(x, hw, c, nullptr, n.gamma, silu ? 1 : 0, 1.f, y, st);
+    }
+
+    int cast(const float* x, size_t count, int c, float scale, __half* y) {
+        return dry ? VAE_OK : cast_run(x, count, c, nullptr, scale, y, st);
+    }
+
+    static ConvArgs c3(const void* x, int h, int w, const DConv& cv, void* y) {
+        ConvArgs a{};
+        a.x = x;
+        a.n = 1;
+        a.h_in = h;
+        a.w_in = w;
+        a.cin = cv.cin;
+        a.w = cv.w;
+        a.cout = cv.cout;
+        a.taps = cv.k * cv.k;
+        a.bias = cv.b;
+        a.y = y;
+        return a;
+    }
+
+    // One ResNet on stream `x` (rows h x w, channels r.c1.cin) -> stream `y`
+    // (may equal x when the channel count does not change).
+    int resnet(const DRes& r, float* x, float* y, int h, int w) {
+        const long long hw = static_cast<long long>(h) * w;
+        const int cin = r.c1.cin, cout = r.c1.cout;
+        __half* xn = f16(kXN, hw * std::max(cin, cout));
+        float* hb = f32(kH, hw * cout);
+        const float* skip = x;
+        int rc;
+        if (r.sc.present()) {
+            float* s = f32(kSC, hw * cout);
+            if ((rc = cast(x, hw * cin, cin, 1.f / guard, xn)) != VAE_OK) return rc;
+            ConvArgs a = c3(xn, h, w, r.sc, s);
+            a.oscale = guard;
+            if ((rc = conv(a)) != VAE_OK) return rc;
+            skip = s;
+        }
+        if ((rc = norm(x, hw, cin, r.n1, true, xn)) != VAE_OK) return rc;
+        if ((rc = conv(c3(xn, h, w, r.c1, hb))) != VAE_OK) return rc;
+        if ((rc = norm(hb, hw, cout, r.n2, true, xn)) != VAE_OK) return rc;
+        ConvArgs a = c3(xn, h, w, r.c2, y);
+        a.residual = skip;
+        return conv(a);
+    }
+
+    // Up blocks [b0, b1) on a stream held in one of three buffers
+    // `bufs` (rows `cur` of the first block's level; buffer row 0 = cur.lo).
+    // `feed(i)` = the rows block i feeds to its up conv (nullptr: all).
+    int blocks(int b0, int b1, const int bufs[3], int* cur_buf, Rows* cur, int w0,
+               const std::vector<Rows>* feed, int* ch) {
+        int rc;
+        for (int i = b0; i < b1; ++i) {
+            const DUp& u = d->ups[i];
+            int lvl = 0;
+            for (int k = 0; k < i; ++k) lvl += d->ups[k].up.present() ? 1 : 0;
+            const int w = w0 << lvl;
+            const int h = cur->n();
+            const long long hw = static_cast<long long>(h) * w;
+            const bool keep_input = u.up.present() && d->dupup;
+            const int in_b = *cur_buf;
+            const int avoid = keep_input ? in_b : -1;
+            int s_b = in_b;
+            for (size_t r = 0; r < u.res.size(); ++r) {
+                const DRes& rs = u.res[r];
+                const bool fresh = rs.c1.cin != rs.c1.cout || (r == 0 && keep_input);
+                const int out_b = fresh ? other(s_b, avoid) : s_b;
+                float* xin = f32(bufs[s_b], hw * rs.c1.cin);
+                float* xout = f32(bufs[out_b], hw * rs.c1.cout);
+                if ((rc = resnet(rs, xin, xout, h, w)) != VAE_OK) return rc;
+                s_b = out_b;
+                *ch = rs.c1.cout;
+            }
+            if (!u.up.present()) {
+                *cur_buf = s_b;
+                continue;
+            }
+            const Rows f = feed ? (*feed)[i] : *cur;
+            if (f.lo < cur->lo || f.hi > cur->hi || f.n() <= 0)
+                return set_error(VAE_ERR_SHAPE, "decode: band feed rows [%d,%d) outside [%d,%d)", f.lo, f.hi, cur->lo,
+                                 cur->hi);
+            const long long skip_px = static_cast<long long>(f.lo - cur->lo) * w;
+            const long long fhw = static_cast<long long>(f.n()) * w;
+            const int out_b = other(s_b, avoid);
+            float* xs = f32(bufs[s_b], hw * (*ch));
+            __half* xn = f16(kXN, hw * (*ch));
+            if ((rc = cast(xs + (dry ? 0 : skip_px * (*ch)), fhw * (*ch), *ch, 1.f / guard, xn)) != VAE_OK) return rc;
+            float* y = f32(bufs[out_b], fhw * 4 * u.up.cout);
+            ConvArgs a = c3(xn, f.n(), w, u.up, y);
+            a.up = true;
+            a.oscale = guard;
+            if (d->dupup) {
+                const float* src = f32(bufs[in_b], hw * u.in_dim);
+                a.dup_src = src + (dry ? 0 : skip_px * u.in_dim);
+                a.dup_cin = u.in_dim;
+                a.dup_factor = 4 * u.ft;
+                a.dup_repeats = u.out_dim * 4 * u.ft / u.in_dim;
+                a.dup_ftoff = (u.ft - 1) * 4;
+            }
+            if ((rc = conv(a)) != VAE_OK) return rc;
+            *cur_buf = out_b;
+            *cur = Rows{2 * f.lo, 2 * f.hi};
+            *ch = u.up.cout;
+        }
+        return VAE_OK;
+    }
+
+    // norm_out + SiLU -> conv_out on stream rows `cur` (width w); kept rows
+    // `keep` go to `out` [nch][hf][w].
+    int output(const float* x, Rows cur, int w, int ch, Rows keep, float* out, int hf) {
+        const long long hw = static_cast<long long>(cur.n()) * w;
+        __half* xn = f16(kXN, hw * ch);
+        int rc = norm(x, hw, ch, d->norm_out, true, xn);
+        if (rc != VAE_OK) return rc;
+        ConvArgs a = c3(xn, cur.n(), w, d->conv_out, out);
+        a.out_nchw = true;
+        a.keep_lo = keep.lo - cur.lo;
+        a.keep_hi = keep.hi - cur.lo;
+        a.dst_row0 = keep.lo;
+        a.plane = static_cast<long long>(hf) * w;
+        return conv(a);
+    }
+};
+
+int levels_total(const vae_decoder* d) {
+    int l = 0;
+    for (const DUp& u : d->ups) l += u.up.present() ? 1 : 0;
+    return l;
+}
+
+std::vector<Band> plan_bands(const vae_decoder* d, int s, int h0, int nbands) {
+    const int nb = static_cast<int>(d->ups.size());
+    std::vector<int> lvl(nb);
+    int l = 0;
+    for (int i = 0; i < nb; ++i) {
+        lvl[i] = l;
+        l += d->ups[i].up.present() ? 1 : 0;
+    }
+    const int lf = l;
+    std::vector<int> hs(lf + 1);
+    for (int k = 0; k <= lf; ++k) hs[k] = h0 << k;
+    const int hf = hs[lf];
+    const int k = (hf + nbands - 1) / nbands;
+    std::vector<Band> out;
+    for (int j = 0; j * k < hf; ++j) {
+        Band b;
+        b.keep = Rows{j * k, std::min((j + 1) * k, hf)};
+        b.feed.assign(nb, Rows{0, 0});
+        Rows e = grow(b.keep, d->conv_out.k / 2, hs[lf]);
+        for (int i = nb - 1; i >= s; --i) {
+            const DUp& u = d->ups[i];
+            if (u.up.present()) {
+                Rows a = half_rows(grow(e, u.up.k / 2, hs[lvl[i] + 1]));
+                b.feed[i] = a;
+                e = a;
+            }
+            int convs = 0;
+            for (const DRes& r : u.res) convs += r.c1.k / 2 + r.c2.k / 2;
+            e = grow(e, convs, hs[lvl[i]]);
+        }
+        b.input = e;
+        out.push_back(b);
+    }
+    return out;
+}
+
+// The whole decode, dry or real. `z` NCHW f32 (device), `out` NCHW f32.
+int run_decode(Exec& X, int h0, int w0, const vae_decode_opts* opts, const float* z, float* out) {
+    const vae_decoder* d = X.d;
+    const int nb = static_cast<int>(d->ups.size());
+    const int lf = levels_total(d);
+    const int hf = h0 << lf, wf = w0 << lf;
+    const long long hw0 = static_cast<long long>(h0) * w0;
+    int rc;
+    X.guard = std::ldexp(1.0f, opts ? (opts->guard_log2 < 0 ? 8 : std::min(opts->guard_log2, 14)) : 8);
+    int nbands = 1;
+    if (opts && opts->band_rows > 0) nbands = (hf + opts->band_rows - 1) / opts->band_rows;
+    if (opts && opts->nbands > 1) nbands = opts->nbands;
+    int s = nb;
+    if (nbands > 1) {
+        if (d->family != VAE_FAMILY_RMS)
+            return set_error(VAE_ERR_UNSUPPORTED,
+                             "decode: bands need per-pixel norms (RMS family); GroupNorm statistics are frame-global");
+        s = std::min(std::max(opts->band_from, 0), nb);
+        if (nbands > hf) nbands = hf;
+    }
+    // head: latent -> f16 NHWC -> (post_quant) -> conv_in -> mid
+    const int s_bufs[3] = {kS0, kS1, kS2};
+    __half* zl = X.f16(kZ, hw0 * d->zc);
+    if (!X.dry) {
+        const float mul = d->family == VAE_FAMILY_GN ? 1.f / d->scaling : 1.f;
+        const float add = d->family == VAE_FAMILY_GN ? d->shift : 0.f;
+        if ((rc = latent_run(z, d->zc, hw0, mul, add, zl, X.st)) != VAE_OK) return rc;
+    }
+    const void* cin_src = zl;
+    if (d->pq.present()) {
+        __half* xq = X.f16(kXN, hw0 * d->pq.cout);
+        ConvArgs a = Exec::c3(zl, h0, w0, d->pq, xq);
+        a.out_f16 = true;
+        if ((rc = X.conv(a)) != VAE_OK) return rc;
+        cin_src = xq;
+    }
+    int cur_buf = 0;
+    int ch = d->conv_in.cout;
+    float* x = X.f32(kS0, hw0 * ch);
+    if ((rc = X.conv(Exec::c3(cin_src, h0, w0, d->conv_in, x))) != VAE_OK) return rc;
+    for (int part = 0; part < 3; ++part) {
+        if (part == 1) {
+            size_t ab = 0;
+            const int kind = d->family == VAE_FAMILY_GN ? VAE_NORM_GROUP : VAE_NORM_RMS;
+            if ((rc = attn_workspace_bytes(static_cast<int>(hw0), ch, d->groups, kind, &ab)) != VAE_OK) return rc;
+            void* aws = X.buf(kATT, ab);
+            float* xa = X.f32(s_bufs[cur_buf], hw0 * ch);
+            if (!X.dry &&
+                (rc = attn_run(xa, static_cast<int>(hw0), ch, kind, d->groups, d->eps, d->attn.n.gamma,
+                               d->attn.n.beta, d->attn.q.w, d->attn.q.b, d->attn.k.w, d->attn.k.b, d->attn.v.w,
+                               d->attn.v.b, d->attn.o.w, d->attn.o.b, aws, ab, X.st)) != VAE_OK)
+                return rc;
+            continue;
+        }
+        const DRes& r = part == 0 ? d->mid1 : d->mid2;
+        const int out_b = r.c1.cin != r.c1.cout ? other(cur_buf, -1) : cur_buf;
+        float* xin = X.f32(s_bufs[cur_buf], hw0 * r.c1.cin);
+        float* xout = X.f32(s_bufs[out_b], hw0 * r.c1.cout);
+        if ((rc = X.resnet(r, xin, xout, h0, w0)) != VAE_OK) return rc;
+        cur_buf = out_b;
+        ch = r.c1.cout;
+    }
+    // whole-frame up blocks [0, s)
+    Rows cur{0, h0};
+    if ((rc = X.blocks(0, s, s_bufs, &cur_buf, &cur, w0, nullptr, &ch)) != VAE_OK) return rc;
+    int ls = 0;
+    for (int i = 0; i < s; ++i) ls += d->ups[i].up.present() ? 1 : 0;
+    const int ws_ = w0 << ls;
+    if (s == nb) {
+        const float* xs = X.f32(s_bufs[cur_buf], static_cast<size_t>(cur.n()) * ws_ * ch);
+        return X.output(xs, cur, wf, ch, Rows{0, hf}, out, hf);
+    }
+    // bands over blocks [s, nb) from the saved level-s stream
+    const float* saved = X.f32(s_bufs[cur_buf], static_cast<size_t>(cur.n()) * ws_ * ch);
+    const int b_bufs[3] = {kB0, kB1, kB2};
+    const std::vector<Band> bands = plan_bands(d, s, h0, nbands);
+    for (const Band& bd : bands) {
+        const size_t row_floats = static_cast<size_t>(ws_) * ch;
+        float* xb = X.f32(kB0, bd.input.n() * row_floats);
+        if (!X.dry)
+            VAE_CUDA_CHECK(cudaMemcpyAsync(xb, saved + bd.input.lo * row_floats,
+                                           bd.input.n() * row_floats * sizeof(float), cudaMemcpyDeviceToDevice,
+                                           X.st));
+        int bcur = 0, bch = ch;
+        Rows r = bd.input;
+        if ((rc = X.blocks(s, nb, b_bufs, &bcur, &r, w0, &bd.feed, &bch)) != VAE_OK) return rc;
+        const float* xo = X.f32(b_bufs[bcur], static_cast<size_t>(r.n()) * wf * bch);
+        if ((rc = X.output(xo, r, wf, bch, bd.keep, out, hf)) != VAE_OK) return rc;
+    }
+    return VAE_OK;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+int plan_workspace(const vae_decoder* d, int h0, int w0, const vae_decode_opts* opts, Exec* X) {
+    if (h0 < 1 || w0 < 1) return set_error(VAE_ERR_SHAPE, "decode: latent %dx%d", h0, w0);
+    const int lf = levels_total(d);
+    if ((static_cast<long long>(h0) << lf) > (1 << 20) || (static_cast<long long>(w0) << lf) > (1 << 20))
+        return set_error(VAE_ERR_SHAPE, "decode: frame too large");
+    X->dry = true;
+    const long long nz = static_cast<long long>(d->zc) * h0 * w0;
+    const long long nout = static_cast<long long>(d->conv_out.cout) * (static_cast<long long>(h0) << lf) * (w0 << lf);
+    int rc = run_decode(*X, h0, w0, opts, reinterpret_cast<const float*>(1 << 20), reinterpret_cast<float*>(1 << 20));
+    if (rc != VAE_OK) return rc;
+    X->need[kZIN] = nz * 4;
+    X->need[kOUT] = nout * 4;
+    size_t off = 0;
+    for (int i = 0; i < kNBuf; ++i) {
+        X->off[i] = off;
+        off = align256(off + X->need[i]);
+    }
+    return VAE_OK;
+}
+
+size_t total_bytes(const Exec& X) {
+    size_t off = 0;
+    for (int i = 0; i < kNBuf; ++i) off = align256(off + X.need[i]);
+    return off;
+}
+
+}  // namespace
+
+}  // namespace vae
+
+using namespace vae;
+
+extern "C" {
+
+int vae_decoder_create(const vae_decoder_desc* desc, vae_decoder_t* out) {
+    clear_error();
+    if (desc == nullptr || out == nullptr) return set_error(VAE_ERR_ARG, "decoder_create: NULL argument");
+    *out = nullptr;
+    if (desc->family != VAE_FAMILY_GN && desc->family != VAE_FAMILY_RMS)
+        return set_error(VAE_ERR_ARG, "decoder_create: family %d", desc->family);
+    if (desc->n_ups < 1 || desc->ups == nullptr) return set_error(VAE_ERR_ARG, "decoder_create: no up blocks");
+    int rc = check_device();
+    if (rc != VAE_OK) return rc;
+    const bool gn = desc->family == VAE_FAMILY_GN;
+    if (gn && (desc->groups < 1 || desc->scaling == 0.f))
+        return set_error(VAE_ERR_ARG, "decoder_create: GroupNorm family needs groups >= 1 and scaling != 0");
+    vae_decoder* d = new (std::nothrow) vae_decoder();
+    if (d == nullptr) return set_error(VAE_ERR_NOMEM, "decoder_create: host allocation");
+    VAE_CUDA_CHECK(cudaGetDevice(&d->device));
+    d->family = desc->family;
+    d->zc = desc->latent_channels;
+    d->groups = gn ? desc->groups : 32;
+    d->eps = desc->eps;
+    d->scaling = desc->scaling;
+    d->shift = desc->shift;
+    d->dupup = (!gn && desc->dupup) ? 1 : 0;
+    Uploader U{d};
+    d->pq = U.conv(desc->post_quant, "post_quant", false);
+    d->conv_in = U.conv(desc->conv_in, "conv_in");
+    const int zc_in = d->pq.present() ? d->pq.cout : d->zc;
+    if (U.rc == VAE_OK && d->pq.present() && (d->pq.k != 1 || d->pq.cin != d->zc))
+        U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: post_quant must be 1x1 from the latent channels");
+    if (U.rc == VAE_OK && (d->conv_in.k != 3 || d->conv_in.cin != zc_in))
+        U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: conv_in must be 3x3 from %d channels", zc_in);
+    int ch = d->conv_in.cout;
+    d->mid1 = U.res(desc->mid_res1, ch, gn, "mid_res1");
+    if (U.rc == VAE_OK) ch = d->mid1.c1.cout;
+    d->attn.n = U.norm(desc->mid_attn.norm, ch, gn, "mid_attn");
+    d->attn.q = U.conv(desc->mid_attn.q, "attn.q");
+    d->attn.k = U.conv(desc->mid_attn.k, "attn.k");
+    d->attn.v = U.conv(desc->mid_attn.v, "attn.v");
+    d->attn.o = U.conv(desc->mid_attn.o, "attn.o");
+    if (U.rc == VAE_OK) {
+        for (const DConv* c : {&d->attn.q, &d->attn.k, &d->attn.v, &d->attn.o})
+            if (c->k != 1 || c->cin != ch || c->cout != ch)
+                U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: attention projections must be 1x1 %d->%d", ch, ch);
+    }
+    d->mid2 = U.res(desc->mid_res2, ch, gn, "mid_res2");
+    if (U.rc == VAE_OK) ch = d->mid2.c1.cout;
+    for (int i = 0; i < desc->n_ups && U.rc == VAE_OK; ++i) {
+        const vae_up_desc& ud = desc->ups[i];
+        DUp u;
+        u.in_dim = ud.in_dim;
+        u.out_dim = ud.out_dim;
+        u.ft = ud.ft < 1 ? 1 : ud.ft;
+        if (ud.n_resnets < 0 || (ud.n_resnets > 0 && ud.resnets == nullptr)) {
+            U.rc = set_error(VAE_ERR_ARG, "decoder_create: up block %d resnets", i);
+            break;
+        }
+        const int block_in = ch;
+        for (int r = 0; r < ud.n_resnets && U.rc == VAE_OK; ++r) {
+            u.res.push_back(U.res(ud.resnets[r], ch, gn, "up block resnet"));
+            if (U.rc == VAE_OK) ch = u.res.back().c1.cout;
+        }
+        u.up = U.conv(ud.up, "up conv", false);
+        if (U.rc == VAE_OK && u.up.present()) {
+            if (u.up.k != 3 || u.up.cin != ch)
+                U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: up conv of block %d must be 3x3 from %d", i, ch);
+            if (d->dupup) {
+                if (u.in_dim != block_in || u.out_dim != u.up.cout || (u.out_dim * 4 * u.ft) % u.in_dim != 0)
+                    U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: DupUp of block %d: in %d out %d ft %d", i,
+                                     u.in_dim, u.out_dim, u.ft);
+            }
+            ch = u.up.cout;
+        }
+        d->ups.push_back(std::move(u));
+    }
+    d->norm_out = U.norm(desc->norm_out, ch, gn, "norm_out");
+    d->conv_out = U.conv(desc->conv_out, "conv_out");
+    if (U.rc == VAE_OK && (d->conv_out.k != 3 || d->conv_out.cin != ch))
+        U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: conv_out must be 3x3 from %d", ch);
+    if (U.rc == VAE_OK && gn && ch % d->groups != 0)
+        U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: %d channels not divisible by %d groups", ch, d->groups);
+    if (U.rc != VAE_OK) {
+        const int keep = U.rc;
+        std::string msg = vae_last_error();
+        vae_decoder_destroy(d);
+        return set_error(keep, "%s", msg.c_str());
+    }
+    *out = d;
+    return VAE_OK;
+}
+
+int vae_decoder_destroy(vae_decoder_t dec) {
+    if (dec == nullptr) return VAE_OK;
+    for (void* p : dec->allocs) cudaFree(p);
+    delete dec;
+    return VAE_OK;
+}
+
+int vae_decode_workspace(vae_decoder_t dec, int h0, int w0, const vae_decode_opts* opts, size_t* bytes) {
+    clear_error();
+    if (dec == nullptr || bytes == nullptr) return set_error(VAE_ERR_ARG, "decode_workspace: NULL argument");
+    Exec X{dec, true, nullptr};
+    int rc = plan_workspace(dec, h0, w0, opts, &X);
+    if (rc != VAE_OK) return rc;
+    *bytes = total_bytes(X);
+    return VAE_OK;
+}
+
+static int decode_impl(vae_decoder_t dec, const float* z, int h0, int w0, float* out, const vae_decode_opts* opts,
+                       void* ws, size_t ws_bytes, cudaStream_t st, bool host) {
+    if (dec == nullptr || z == nullptr || out == nullptr || ws == nullptr)
+        return set_error(VAE_ERR_ARG, "decode: NULL argument");
+    if (opts != nullptr && opts->flags != 0) return set_error(VAE_ERR_ARG, "decode: opts.flags must be 0");
+    int rc = check_device();
+    if (rc != VAE_OK) return rc;
+    Exec X{dec, true, st};
+    rc = plan_workspace(dec, h0, w0, opts, &X);
+    if (rc != VAE_OK) return rc;
+    const size_t need = total_bytes(X);
+    if (ws_bytes < need) return set_error(VAE_ERR_NOMEM, "decode: workspace %zu < %zu bytes", ws_bytes, need);
+    if (!aligned16(ws)) return set_error(VAE_ERR_ALIGN, "decode: workspace must be 16-byte aligned");
+    X.dry = false;
+    X.base = static_cast<uint8_t*>(ws);
+    const int lf = levels_total(dec);
+    const size_t zbytes = static_cast<size_t>(dec->zc) * h0 * w0 * 4;
+    const size_t obytes = static_cast<size_t>(dec->conv_out.cout) * (static_cast<size_t>(h0) << lf) * (w0 << lf) * 4;
+    const float* zd = z;
+    float* od = out;
+    if (host) {
+        float* zs = reinterpret_cast<float*>(X.base + X.off[kZIN]);
+        VAE_CUDA_CHECK(cudaMemcpyAsync(zs, z, zbytes, cudaMemcpyHostToDevice, st));
+        zd = zs;
+        od = reinterpret_cast<float*>(X.base + X.off[kOUT]);
+    }
+    rc = run_decode(X, h0, w0, opts, zd, od);
+    if (rc != VAE_OK) return rc;
+    if (host) {
+        VAE_CUDA_CHECK(cudaMemcpyAsync(out, od, obytes, cudaMemcpyDeviceToHost, st));
+        return vae_sync_status(reinterpret_cast<vae_stream_t>(st));
+    }
+    return VAE_OK;
+}
+
+int vae_decode(vae_decoder_t dec, const float* z_dev, int h0, int w0, float* out_dev, const vae_decode_opts* opts,
+               void* workspace_dev, size_t workspace_bytes, vae_stream_t stream) {
+    clear_error();
+    return decode_impl(dec, z_dev, h0, w0, out_dev, opts, workspace_dev, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+int vae_decode_host(vae_decoder_t dec, const float* z_host, int h0, int w0, float* out_host,
+                    const vae_decode_opts* opts, void* workspace_dev, size_t workspace_bytes, vae_stream_t stream) {
+    clear_error();
+    return decode_impl(dec, z_host, h0, w0, out_host, opts, workspace_dev, workspace_bytes,
+                       reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+}  // extern "C"

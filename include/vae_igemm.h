@@ -97,7 +97,7 @@ int vae_selftest_wait_timeout(unsigned long long timeout_ns, vae_stream_t stream
  *             H = h_in, W = w_in, or 2*h_in, 2*w_in with VAE_UPSAMPLE2X.
  *   oscale    multiplies the f32 accumulator (the undo of a 2^-g input guard).
  * Requirements: n, h_in, w_in >= 1; cin % 16 == 0, 16 <= cin <= 8192;
- * 1 <= cout <= 8192; x_dev, w_dev 16-byte aligned. Outputs of any cout are
+ * 1 <= cout <= 2^20; x_dev, w_dev 16-byte aligned. Outputs of any cout are
  * supported (vector stores when cout % 16 == 0).
  */
 int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin,
@@ -142,7 +142,7 @@ int vae_rmsnorm_silu(const float* x_dev, int m, int c, const float* bias_in_dev,
  *   y_dev f16 [n][hw][c]; workspace_dev of at least
  *   vae_groupnorm_workspace_bytes(n, hw, c, groups) bytes, 16-byte aligned,
  *   contents ignored on entry.
- * Requirements: c % groups == 0, c % 4 == 0, 4 <= c <= 16384, 1 <= groups <= 1024.
+ * Requirements: c % groups == 0, c % 4 == 0, 4 <= c <= 4096, 1 <= groups <= 1024.
  */
 size_t vae_groupnorm_workspace_bytes(int n, int hw, int c, int groups);
 int vae_groupnorm_silu(const float* x_dev, int n, int hw, int c, int groups, float eps,
@@ -174,7 +174,7 @@ enum { VAE_NORM_GROUP = 0, VAE_NORM_RMS = 1 };
  *   x_dev f32 [m][c] (tokens = pixels of one image); w*_dev f16 [c][c]
  *   (row = output channel); b*_dev f32 [c]; norm_beta_dev ignored for RMS.
  *   workspace_dev >= vae_mid_attention_workspace_bytes(m, c, groups).
- * Requirements: c % 64 == 0, 64 <= c <= 2048, m >= 1.
+ * Requirements: c % 16 == 0, 16 <= c <= 2048, m >= 1.
  */
 size_t vae_mid_attention_workspace_bytes(int m, int c, int groups);
 int vae_mid_attention(float* x_dev, int m, int c, int norm_kind, int groups, float eps,

@@ -34,3 +34,18 @@ def sentinel_like(shape, dtype):
     """A CUDA tensor filled with NaN, so unwritten outputs are caught."""
     torch = torch_mod()
     return torch.full(shape, float("nan"), dtype=dtype, device="cuda")
+
+
+def u8(y):
+    """RGB in about [-1, 1] -> u8 levels: round(clamp((y+1)/2, 0, 1) * 255)."""
+    return np.round(np.clip((np.asarray(y, np.float64) + 1.0) / 2.0, 0.0, 1.0) * 255.0)
+
+
+def psnr_u8(got, ref):
+    mse = float(np.mean((u8(got) - u8(ref)) ** 2))
+    return float("inf") if mse == 0 else 10.0 * np.log10(255.0 ** 2 / mse)
+
+
+def saturated_fraction(ref):
+    r = np.asarray(ref)
+    return float(np.mean((r <= -1.0) | (r >= 1.0)))

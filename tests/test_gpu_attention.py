@@ -1,0 +1,72 @@
+"""GPU parity of the mid attention (norm, projections, fused QK^T-softmax-PV
+kernel, output projection) against the oracle, on the attention's
+contribution y - x. Tolerance 5e-3 of max|ref|: the GPU rounds xn, q, k, v,
+the unnormalised P and o to f16 (relative 2^-11 each) and accumulates in
+f32; those roundings stay near 1e-3 of the output scale."""
+import numpy as np
+import pytest
+
+import oracle
+import implicit_gemm_convolution_vae_gb300 as vg
+from gpu_common import rel_err, to_dev, torch_mod
+from vae_inputs import Attn, Conv, Norm, bias_vec, conv_weight, rng_for, stream_normal
+
+pytestmark = pytest.mark.gpu
+
+ATTN_TOL = 5e-3
+
+
+def _attn(seed, c, family):
+    def lin(nm):
+        return Conv(w=conv_weight(seed, f"at.{nm}.{c}", c, c, 1), b=bias_vec(seed, f"at.{nm}.b.{c}", c))
+    g = rng_for(seed, f"at.n.{c}")
+    norm = Norm(gamma=g.uniform(0.5, 1.5, c).astype(np.float32),
+                beta=(g.standard_normal(c) * 0.1).astype(np.float32) if family == "gn" else None)
+    return Attn(norm=norm, q=lin("q"), k=lin("k"), v=lin("v"), o=lin("o"))
+
+
+def run_gpu(x, a, family, groups=32):
+    torch = torch_mod()
+    xd = to_dev(x.copy())
+    w = lambda cv: to_dev(vg.pack_conv1x1(cv.w))
+    vg.mid_attention(xd, vg.NORM_GROUP if family == "gn" else vg.NORM_RMS, to_dev(a.norm.gamma),
+                     to_dev(a.norm.beta) if a.norm.beta is not None else None,
+                     w(a.q), to_dev(a.q.b), w(a.k), to_dev(a.k.b), w(a.v), to_dev(a.v.b), w(a.o), to_dev(a.o.b),
+                     groups=groups)
+    vg.sync_status()
+    return xd.cpu().numpy()
+
+
+@pytest.mark.parametrize("m,c,family", [(1, 64, "rms"), (5, 32, "gn"), (33, 48, "rms"), (7, 128, "gn"), (200, 192, "rms"), (1024, 512, "gn"),
+                                        (1000, 640, "rms"), (2500, 1152, "rms"), (300, 2048, "rms")])
+def test_mid_attention(m, c, family):
+    x = stream_normal(20, f"attn.x.{m}.{c}", (m, c))
+    a = _attn(20, c, family)
+    got = run_gpu(x, a, family)
+    ref = oracle.attention(x.T.reshape(c, m, 1), a, family, groups=32).reshape(c, m).T
+    assert np.isfinite(got).all()
+    assert rel_err(got - x, ref - x) <= ATTN_TOL
+
+
+def test_mid_attention_full_size_qwen_mid():
+    """m = 128 x 128 latent tokens, c = 1152: the 1024^2 decoder's mid block."""
+    m, c = 16384, 1152
+    x = stream_normal(21, "attn.full.x", (m, c)) * 2.0
+    a = _attn(21, c, "rms")
+    got = run_gpu(x, a, "rms")
+    ref = oracle.attention(x.T.reshape(c, 128, 128), a, "rms").reshape(c, m).T
+    assert rel_err(got - x, ref - x) <= ATTN_TOL
+
+
+def test_peaked_softmax_rescales():
+    """Scores that grow block after block force the lazy O rescale path."""
+    m, c = 1024, 128
+    x = stream_normal(22, "attn.peak.x", (m, c))
+    x = x + np.linspace(0, 40, m, dtype=np.float32)[:, None] * x[:, :1]
+    a = _attn(22, c, "rms")
+    a.q = Conv(w=(a.q.w.astype(np.float32) * 4).astype(np.float16), b=a.q.b)
+    got = run_gpu(x, a, "rms")
+    ref = oracle.attention(x.T.reshape(c, m, 1), a, "rms").reshape(c, m).T
+    # Logits here reach the hundreds, so the f16 rounding of q and k moves them by
+    # up to |s| * 2^-10 and the sharply peaked softmax passes that on: 1e-2.
+    assert rel_err(got - x, ref - x) <= 1e-2

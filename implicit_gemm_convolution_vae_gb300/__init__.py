@@ -69,6 +69,7 @@ SIGNATURES = {
     "vae_decode_workspace": ([_P, _I, _I, _P, ctypes.POINTER(_SZ)], _I),
     "vae_decode": ([_P, _P, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "vae_decode_host": ([_P, _P, _I, _I, _P, _P, _P, _SZ, _P], _I),
+    "vae_decode_profile": ([_P, _P, _I, ctypes.POINTER(_I)], _I),
 }
 
 
@@ -307,6 +308,15 @@ class _DecoderDesc(ctypes.Structure):
                 ("conv_out", _ConvDesc)]
 
 
+DECODE_PROFILE = 1
+STAGE_NAMES = {0: "conv3x3", 1: "conv1x1", 2: "norm", 3: "cast", 4: "attention", 5: "layout", 6: "copy"}
+
+
+class StageRecord(ctypes.Structure):
+    _fields_ = [("kind", _I), ("launches", _I), ("h", _I), ("w", _I), ("cin", _I), ("cout", _I),
+                ("flops", ctypes.c_double), ("bytes", ctypes.c_double), ("ms", ctypes.c_float)]
+
+
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("band_from", _I), ("nbands", _I), ("band_rows", _I), ("guard_log2", _I),
                 ("flags", ctypes.c_uint)]
@@ -383,8 +393,19 @@ class Decoder:
                            self._conv(r.shortcut))
 
     @staticmethod
-    def opts(band_from: int = 0, nbands: int = 0, band_rows: int = 0, guard_log2: int = 8) -> DecodeOpts:
-        return DecodeOpts(band_from, nbands, band_rows, guard_log2, 0)
+    def opts(band_from: int = 0, nbands: int = 0, band_rows: int = 0, guard_log2: int = 8,
+             profile: bool = False) -> DecodeOpts:
+        return DecodeOpts(band_from, nbands, band_rows, guard_log2, DECODE_PROFILE if profile else 0)
+
+    def profile(self):
+        """Stage records of the most recent profiled decode, as dicts (synchronises)."""
+        n = _I()
+        _check(lib().vae_decode_profile(self._h, None, 0, ctypes.byref(n)))
+        arr = (StageRecord * max(1, n.value))()
+        _check(lib().vae_decode_profile(self._h, ctypes.cast(arr, _P), n.value, ctypes.byref(n)))
+        return [{"kind": STAGE_NAMES.get(r.kind, r.kind), "launches": r.launches, "h": r.h, "w": r.w,
+                 "cin": r.cin, "cout": r.cout, "flops": r.flops, "bytes": r.bytes, "ms": r.ms}
+                for r in arr[:n.value]]
 
     def workspace_bytes(self, h0: int, w0: int, opts: Optional[DecodeOpts] = None) -> int:
         n = _SZ()

@@ -70,6 +70,10 @@ struct vae_decoder {
     std::vector<vae::DUp> ups;
     vae::DNorm norm_out;
     std::vector<void*> allocs;
+    // profiling of the most recent VAE_DECODE_PROFILE decode
+    std::vector<cudaEvent_t> events;
+    std::vector<vae_stage_record> recs;
+    std::vector<int> rec_ev;  // first event index of each record (start, start + 1 = end)
 };
 
 namespace vae {
@@ -193,6 +197,36 @@ struct Exec {
     size_t need[kNBuf] = {};
     size_t off[kNBuf] = {};
     float guard = 256.f;
+    vae_decoder* prof = nullptr;  // non-null: record events around stages
+
+    // Starts a profiled stage; returns its record index (or -1).
+    int begin(int kind, int launches, int h, int w, int cin, int cout, double flops, double bytes) {
+        if (dry || prof == nullptr) return -1;
+        const int i = static_cast<int>(prof->recs.size());
+        const size_t ev = prof->rec_ev.size() * 2;
+        while (prof->events.size() < ev + 2) {
+            cudaEvent_t e;
+            if (cudaEventCreate(&e) != cudaSuccess) return -1;
+            prof->events.push_back(e);
+        }
+        vae_stage_record r{};
+        r.kind = kind;
+        r.launches = launches;
+        r.h = h;
+        r.w = w;
+        r.cin = cin;
+        r.cout = cout;
+        r.flops = flops;
+        r.bytes = bytes;
+        prof->recs.push_back(r);
+        prof->rec_ev.push_back(static_cast<int>(ev));
+        cudaEventRecord(prof->events[ev], st);
+        return i;
+    }
+    void end(int i) {
+        if (i < 0) return;
+        cudaEventRecord(prof->events[prof->rec_ev[i] + 1], st);
+    }
 
     void* buf(int id, size_t bytes) {
         if (dry) {
@@ -204,7 +238,15 @@ struct Exec {
     float* f32(int id, size_t count) { return static_cast<float*>(buf(id, count * 4)); }
     __half* f16(int id, size_t count) { return static_cast<__half*>(buf(id, count * 2)); }
 
-    int conv(const ConvArgs& a) { return dry ? conv_validate(a) : conv_run(a, st); }
+    int conv(const ConvArgs& a) {
+        if (dry) return conv_validate(a);
+        const int H = a.up ? 2 * a.h_in : a.h_in, W = a.up ? 2 * a.w_in : a.w_in;
+        const double flops = 2.0 * a.n * H * W * static_cast<double>(a.cout) * a.taps * a.cin;
+        const int i = begin(a.taps == 9 ? VAE_STAGE_CONV3X3 : VAE_STAGE_CONV1X1, 1, H, W, a.cin, a.cout, flops, 0.0);
+        const int rc = conv_run(a, st);
+        end(i);
+        return rc;
+    }
 
     // norm (+SiLU) of stream `x` [hw][c] -> f16 `y`.
     int norm(const float* x, long long hw, int c, const DNorm& n, bool silu, __half* y) {
@@ -213,15 +255,26 @@ struct Exec {
             int rc = gn_plan(1, static_cast<int>(hw), c, d->groups, &gp);
             if (rc != VAE_OK) return rc;
             void* ws = buf(kGN, gp.bytes);
-            return dry ? VAE_OK
-                       : gn_run(x, 1, static_cast<int>(hw), c, d->groups, d->eps, nullptr, n.gamma, n.beta,
-                                silu ? 1 : 0, 1.f, y, ws, gp.bytes, st);
+            if (dry) return VAE_OK;
+            const int i = begin(VAE_STAGE_NORM, 3, static_cast<int>(hw), 1, c, c, 0.0, static_cast<double>(hw) * c * 10.0);
+            rc = gn_run(x, 1, static_cast<int>(hw), c, d->groups, d->eps, nullptr, n.gamma, n.beta, silu ? 1 : 0,
+                        1.f, y, ws, gp.bytes, st);
+            end(i);
+            return rc;
         }
-        return dry ? VAE_OK : rms_run(x, hw, c, nullptr, n.gamma, silu ? 1 : 0, 1.f, y, st);
+        if (dry) return VAE_OK;
+        const int i = begin(VAE_STAGE_NORM, 1, static_cast<int>(hw), 1, c, c, 0.0, static_cast<double>(hw) * c * 6.0);
+        const int rc = rms_run(x, hw, c, nullptr, n.gamma, silu ? 1 : 0, 1.f, y, st);
+        end(i);
+        return rc;
     }
 
     int cast(const float* x, size_t count, int c, float scale, __half* y) {
-        return dry ? VAE_OK : cast_run(x, count, c, nullptr, scale, y, st);
+        if (dry) return VAE_OK;
+        const int i = begin(VAE_STAGE_CAST, 1, static_cast<int>(count / c), 1, c, c, 0.0, count * 6.0);
+        const int rc = cast_run(x, count, c, nullptr, scale, y, st);
+        end(i);
+        return rc;
     }
 
     static ConvArgs c3(const void* x, int h, int w, const DConv& cv, void* y) {
@@ -410,7 +463,10 @@ int run_decode(Exec& X, int h0, int w0, const vae_decode_opts* opts, const float
     if (!X.dry) {
         const float mul = d->family == VAE_FAMILY_GN ? 1.f / d->scaling : 1.f;
         const float add = d->family == VAE_FAMILY_GN ? d->shift : 0.f;
-        if ((rc = latent_run(z, d->zc, hw0, mul, add, zl, X.st)) != VAE_OK) return rc;
+        const int i = X.begin(VAE_STAGE_LAYOUT, 1, h0, w0, d->zc, d->zc, 0.0, hw0 * d->zc * 6.0);
+        rc = latent_run(z, d->zc, hw0, mul, add, zl, X.st);
+        X.end(i);
+        if (rc != VAE_OK) return rc;
     }
     const void* cin_src = zl;
     if (d->pq.present()) {
@@ -431,11 +487,16 @@ int run_decode(Exec& X, int h0, int w0, const vae_decode_opts* opts, const float
             if ((rc = attn_workspace_bytes(static_cast<int>(hw0), ch, d->groups, kind, &ab)) != VAE_OK) return rc;
             void* aws = X.buf(kATT, ab);
             float* xa = X.f32(s_bufs[cur_buf], hw0 * ch);
-            if (!X.dry &&
-                (rc = attn_run(xa, static_cast<int>(hw0), ch, kind, d->groups, d->eps, d->attn.n.gamma,
-                               d->attn.n.beta, d->attn.q.w, d->attn.q.b, d->attn.k.w, d->attn.k.b, d->attn.v.w,
-                               d->attn.v.b, d->attn.o.w, d->attn.o.b, aws, ab, X.st)) != VAE_OK)
-                return rc;
+            if (!X.dry) {
+                const double m = static_cast<double>(hw0);
+                const int i = X.begin(VAE_STAGE_ATTENTION, (kind == VAE_NORM_GROUP ? 3 : 1) + 5 + (hw0 % 8 ? 1 : 0),
+                                      h0, w0, ch, ch, 4.0 * m * m * ch + 4.0 * 2.0 * m * ch * ch, 0.0);
+                rc = attn_run(xa, static_cast<int>(hw0), ch, kind, d->groups, d->eps, d->attn.n.gamma,
+                              d->attn.n.beta, d->attn.q.w, d->attn.q.b, d->attn.k.w, d->attn.k.b, d->attn.v.w,
+                              d->attn.v.b, d->attn.o.w, d->attn.o.b, aws, ab, X.st);
+                X.end(i);
+                if (rc != VAE_OK) return rc;
+            }
             continue;
         }
         const DRes& r = part == 0 ? d->mid1 : d->mid2;
@@ -463,10 +524,14 @@ int run_decode(Exec& X, int h0, int w0, const vae_decode_opts* opts, const float
     for (const Band& bd : bands) {
         const size_t row_floats = static_cast<size_t>(ws_) * ch;
         float* xb = X.f32(kB0, bd.input.n() * row_floats);
-        if (!X.dry)
+        if (!X.dry) {
+            const int i = X.begin(VAE_STAGE_COPY, 1, bd.input.n(), ws_, ch, ch, 0.0,
+                                  2.0 * bd.input.n() * row_floats * sizeof(float));
             VAE_CUDA_CHECK(cudaMemcpyAsync(xb, saved + bd.input.lo * row_floats,
                                            bd.input.n() * row_floats * sizeof(float), cudaMemcpyDeviceToDevice,
                                            X.st));
+            X.end(i);
+        }
         int bcur = 0, bch = ch;
         Rows r = bd.input;
         if ((rc = X.blocks(s, nb, b_bufs, &bcur, &r, w0, &bd.feed, &bch)) != VAE_OK) return rc;
@@ -603,8 +668,29 @@ int vae_decoder_create(const vae_decoder_desc* desc, vae_decoder_t* out) {
 
 int vae_decoder_destroy(vae_decoder_t dec) {
     if (dec == nullptr) return VAE_OK;
+    for (cudaEvent_t e : dec->events) cudaEventDestroy(e);
     for (void* p : dec->allocs) cudaFree(p);
     delete dec;
+    return VAE_OK;
+}
+
+int vae_decode_profile(vae_decoder_t dec, vae_stage_record* recs, int max_recs, int* n_recs) {
+    clear_error();
+    if (dec == nullptr || n_recs == nullptr || (recs == nullptr && max_recs > 0))
+        return set_error(VAE_ERR_ARG, "decode_profile: NULL argument");
+    *n_recs = static_cast<int>(dec->recs.size());
+    if (dec->recs.empty()) return VAE_OK;
+    VAE_CUDA_CHECK(cudaEventSynchronize(dec->events[dec->rec_ev.back() + 1]));
+    for (size_t i = 0; i < dec->recs.size(); ++i) {
+        float ms = 0.f;
+        VAE_CUDA_CHECK(cudaEventElapsedTime(&ms, dec->events[dec->rec_ev[i]], dec->events[dec->rec_ev[i] + 1]));
+        dec->recs[i].ms = ms;
+        if (static_cast<int>(i) < max_recs) recs[i] = dec->recs[i];
+    }
+    if (max_recs > 0) {  // a read that copies records also clears them
+        dec->recs.clear();
+        dec->rec_ev.clear();
+    }
     return VAE_OK;
 }
 
@@ -622,7 +708,8 @@ static int decode_impl(vae_decoder_t dec, const float* z, int h0, int w0, float*
                        void* ws, size_t ws_bytes, cudaStream_t st, bool host) {
     if (dec == nullptr || z == nullptr || out == nullptr || ws == nullptr)
         return set_error(VAE_ERR_ARG, "decode: NULL argument");
-    if (opts != nullptr && opts->flags != 0) return set_error(VAE_ERR_ARG, "decode: opts.flags must be 0");
+    if (opts != nullptr && (opts->flags & ~static_cast<unsigned>(VAE_DECODE_PROFILE)) != 0)
+        return set_error(VAE_ERR_ARG, "decode: unknown opts.flags 0x%x", opts->flags);
     int rc = check_device();
     if (rc != VAE_OK) return rc;
     Exec X{dec, true, st};
@@ -633,6 +720,7 @@ static int decode_impl(vae_decoder_t dec, const float* z, int h0, int w0, float*
     if (!aligned16(ws)) return set_error(VAE_ERR_ALIGN, "decode: workspace must be 16-byte aligned");
     X.dry = false;
     X.base = static_cast<uint8_t*>(ws);
+    if (opts != nullptr && (opts->flags & VAE_DECODE_PROFILE)) X.prof = dec;
     const int lf = levels_total(dec);
     const size_t zbytes = static_cast<size_t>(dec->zc) * h0 * w0 * 4;
     const size_t obytes = static_cast<size_t>(dec->conv_out.cout) * (static_cast<size_t>(h0) << lf) * (w0 << lf) * 4;

@@ -252,8 +252,44 @@ typedef struct {
     int nbands;      /* number of equal kept-row bands (0 or 1 with band_rows 0: whole frame) */
     int band_rows;   /* alternative to nbands: at most this many kept rows per band */
     int guard_log2;  /* f16 range guard g of the raw-stream casts (default 8 when < 0) */
-    unsigned flags;  /* reserved, 0 */
+    unsigned flags;  /* 0, or VAE_DECODE_PROFILE */
 } vae_decode_opts;
+
+/* vae_decode_opts.flags: record CUDA events around every stage of this
+ * decode (read back with vae_decode_profile). */
+enum { VAE_DECODE_PROFILE = 1 };
+
+/* Stage kinds of a profiled decode. */
+enum {
+    VAE_STAGE_CONV3X3 = 0,   /* one implicit-GEMM 3x3 conv launch (incl. up convs) */
+    VAE_STAGE_CONV1X1 = 1,   /* one 1x1 conv launch (post_quant, shortcut) */
+    VAE_STAGE_NORM = 2,      /* RMS_norm (1 launch) or GroupNorm (3 launches) */
+    VAE_STAGE_CAST = 3,      /* guarded f32 -> f16 cast of the raw stream */
+    VAE_STAGE_ATTENTION = 4, /* the whole mid attention (norm, projections, fused core) */
+    VAE_STAGE_LAYOUT = 5,    /* latent NCHW f32 -> NHWC f16 */
+    VAE_STAGE_COPY = 6       /* band input rows copied from the saved stream */
+};
+
+/* One stage of a profiled decode. `flops` are the algorithmic FLOPs
+ * (2*M*N*K with real channels, upsample convs counted on the output grid;
+ * attention 4*m^2*c plus 2*m*c^2 per projection); `bytes` the algorithmic
+ * HBM bytes of bandwidth-bound stages (0 for convs). */
+typedef struct {
+    int kind;
+    int launches;
+    int h, w;       /* output grid of the stage */
+    int cin, cout;  /* channels */
+    double flops;
+    double bytes;
+    float ms;       /* device time between the stage's start and end events */
+} vae_stage_record;
+
+/* Records accumulate over every decode run with VAE_DECODE_PROFILE on this
+ * handle. This call synchronises on their events and sets *n_recs to how many
+ * there are; with max_recs > 0 it copies up to max_recs of them (in launch
+ * order) and then clears them all (max_recs = 0 only counts). Not thread-safe
+ * per handle. */
+int vae_decode_profile(vae_decoder_t dec, vae_stage_record* recs, int max_recs, int* n_recs);
 
 /* Device workspace (bytes) vae_decode needs for an h0 x w0 latent. */
 int vae_decode_workspace(vae_decoder_t dec, int h0, int w0, const vae_decode_opts* opts,

@@ -565,8 +565,12 @@ using namespace vae;
 extern "C" {
 
 size_t vae_mid_attention_workspace_bytes(int m, int c, int groups) {
+    // Enough for either norm kind; channel counts GroupNorm cannot split into
+    // `groups` still get the RMS_norm size.
     size_t b = 0;
-    if (attn_workspace_bytes(m, c, groups, VAE_NORM_GROUP, &b) != VAE_OK) return 0;
+    if (attn_workspace_bytes(m, c, groups, VAE_NORM_GROUP, &b) == VAE_OK) return b;
+    clear_error();
+    if (attn_workspace_bytes(m, c, groups, VAE_NORM_RMS, &b) != VAE_OK) return 0;
     return b;
 }
 

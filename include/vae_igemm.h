@@ -173,7 +173,8 @@ enum { VAE_NORM_GROUP = 0, VAE_NORM_RMS = 1 };
  * in memory).
  *   x_dev f32 [m][c] (tokens = pixels of one image); w*_dev f16 [c][c]
  *   (row = output channel); b*_dev f32 [c]; norm_beta_dev ignored for RMS.
- *   workspace_dev >= vae_mid_attention_workspace_bytes(m, c, groups).
+ *   workspace_dev >= vae_mid_attention_workspace_bytes(m, c, groups) (which
+ *   sizes for GroupNorm when c % groups == 0, else for RMS_norm).
  * Requirements: c % 16 == 0, 16 <= c <= 2048, m >= 1.
  */
 size_t vae_mid_attention_workspace_bytes(int m, int c, int groups);

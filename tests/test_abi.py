@@ -72,6 +72,7 @@ def test_norms_reject_bad_shapes(L):
 
 def test_attention_and_decoder_reject_bad_arguments(L):
     assert L.vae_mid_attention_workspace_bytes(1024, 100, 32) == 0
+    assert L.vae_mid_attention_workspace_bytes(1024, 48, 32) > 0
     assert L.vae_mid_attention_workspace_bytes(1024, 48, 16) > 0
     assert L.vae_mid_attention_workspace_bytes(1024, 512, 32) > 0
     assert L.vae_mid_attention(FAKE, 16, 100, 1, 32, 1e-6, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,

@@ -61,6 +61,7 @@ SIGNATURES = {
     "vae_rmsnorm_silu": ([_P, _I, _I, _P, _P, _I, _F, _P, _P], _I),
     "vae_groupnorm_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "vae_groupnorm_silu": ([_P, _I, _I, _I, _I, _F, _P, _P, _P, _I, _F, _P, _P, _SZ, _P], _I),
+    "vae_groupnorm_silu_static": ([_P, _I, _I, _I, _I, _F, _P, _P, _P, _I, _F, _P, _P], _I),
     "vae_cast_f16": ([_P, _SZ, _I, _P, _F, _P, _P], _I),
     "vae_mid_attention_workspace_bytes": ([_I, _I, _I], _SZ),
     "vae_mid_attention": ([_P, _I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P], _I),

@@ -3,6 +3,7 @@
 // f32->f16 cast of the raw stream, and the latent's NCHW f32 -> NHWC f16
 // layout. All read f32 with 128-bit loads and write f16 with 64-bit stores.
 #include <algorithm>
+#include <mutex>
 
 #include "vae_norm.h"
 
@@ -363,11 +364,64 @@ int latent_run(const float* z, int c, long long hw, float mul, float add, void* 
     return VAE_OK;
 }
 
+// Scratch of vae_groupnorm_silu_static: a fixed array in device memory that
+// every GPU loading this library holds until the process exits. Host code
+// must not pass the symbol itself to a kernel (on the host it only names a
+// stand-in); gn_static_scratch() looks its device address up once per device.
+constexpr size_t kGnStaticFloats = 131072;  // 512 KB
+static __device__ __align__(256) float g_gn_static_scratch[kGnStaticFloats];
+
+static float* gn_static_scratch() {
+    static std::mutex mu;
+    static float* ptr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        set_error(VAE_ERR_CUDA, "groupnorm_static: cudaGetDevice: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    if (dev < 0 || dev >= 64) {
+        set_error(VAE_ERR_UNSUPPORTED, "groupnorm_static: device index %d", dev);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_gn_static_scratch);
+        if (e != cudaSuccess) {
+            set_error(VAE_ERR_CUDA, "groupnorm_static: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        ptr[dev] = static_cast<float*>(p);
+    }
+    return ptr[dev];
+}
+
 }  // namespace vae
 
 using namespace vae;
 
 extern "C" {
+
+int vae_groupnorm_silu_static(const float* x_dev, int n, int hw, int c, int groups, float eps,
+                              const float* bias_in_dev, const float* gamma_dev, const float* beta_dev, int silu,
+                              float out_scale, void* y_dev, vae_stream_t stream) {
+    clear_error();
+    GnPlan plan;
+    int rc = gn_plan(n, hw, c, groups, &plan);
+    if (rc != VAE_OK) return rc;
+    if (plan.bytes > kGnStaticFloats * sizeof(float))
+        return set_error(VAE_ERR_NOMEM,
+                         "groupnorm_static: n=%d hw=%d groups=%d needs %zu bytes of scratch, more than the fixed "
+                         "%zu bytes; use vae_groupnorm_silu with a workspace",
+                         n, hw, groups, plan.bytes, kGnStaticFloats * sizeof(float));
+    rc = check_device();
+    if (rc != VAE_OK) return rc;
+    float* ws = gn_static_scratch();
+    if (ws == nullptr) return VAE_ERR_CUDA;
+    return gn_run(x_dev, n, hw, c, groups, eps, bias_in_dev, gamma_dev, beta_dev, silu, out_scale, y_dev, ws,
+                  kGnStaticFloats * sizeof(float), reinterpret_cast<cudaStream_t>(stream));
+}
 
 int vae_rmsnorm_silu(const float* x_dev, int m, int c, const float* bias_in_dev, const float* gamma_dev, int silu,
                      float out_scale, void* y_dev, vae_stream_t stream) {

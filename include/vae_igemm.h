@@ -151,6 +151,34 @@ int vae_groupnorm_silu(const float* x_dev, int n, int hw, int c, int groups, flo
                        void* workspace_dev, size_t workspace_bytes, vae_stream_t stream);
 
 /*
+ * GroupNorm exactly as vae_groupnorm_silu, for callers that cannot allocate
+ * device memory. The pages have no counterpart to this entry point.
+ *
+ * Some callers have no way to hand this library a workspace: an inference
+ * engine's plugin whose only memory is what the engine planned ahead of time,
+ * or a serving loop that must never call cudaMalloc because an allocation can
+ * synchronise the whole device and stall every stream in flight. This variant
+ * needs no workspace and allocates nothing: its partial statistics live in a
+ * fixed 512 KB array of device memory that the library defines at file scope;
+ * every GPU that loads the library holds that array until the process exits.
+ *
+ * Limit: calls whose statistics need more than 512 KB of scratch (see
+ * vae_groupnorm_workspace_bytes; every call with groups <= 32 and n <= 416
+ * fits) return VAE_ERR_NOMEM without launching anything.
+ * Set-up: the first call on each device looks the array's device address up
+ * (with that device current); make that first call before any stream capture.
+ * Sharing: all calls use the same array and it keeps the last call's
+ * contents (each call overwrites every entry it reads, so nothing needs to
+ * start at zero). Calls that may overlap on the GPU (different streams, or
+ * different host threads) race on the array and must be serialised by the
+ * caller.
+ * Arguments, layouts, requirements and errors otherwise as vae_groupnorm_silu.
+ */
+int vae_groupnorm_silu_static(const float* x_dev, int n, int hw, int c, int groups, float eps,
+                              const float* bias_in_dev, const float* gamma_dev, const float* beta_dev,
+                              int silu, float out_scale, void* y_dev, vae_stream_t stream);
+
+/*
  * f32 -> f16 cast of the raw residual stream with its range guard:
  *   y[i] = (x[i] + bias[i % c]) * scale            (scale normally 2^-g)
  * ("qi21_vae.rs" qv_cast and the guard() doc.)

@@ -40,7 +40,16 @@ namespace {
 constexpr int kBK = 64;                // channels per K chunk (one 128-byte swizzle row)
 constexpr int kBM = 128;               // M tile (UMMA M)
 constexpr int kABytes = kBM * kBK * 2; // 16 KB
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;       // B (or shared A+B) ring slots
+constexpr int kMaxAStages = 4;       // A halo ring slots (halo mode)
+constexpr int kHaloRows = 130;       // one output row segment of 128 pixels + a pixel each side
+constexpr int kHaloBytes = 17408;    // 130 rows x 128 B, rounded up to 1024 B
+constexpr int kTail = 512;           // barriers, TMEM slot and abort flag
+
+// Kernel variants: A tile per tap by TMA; A tile per tap by gather threads
+// (replicate padding); one A "halo" box per (ky, chunk) shared by the three
+// kx taps through descriptor start offsets of whole 128-byte rows.
+constexpr int kModeTma = 0, kModeGather = 1, kModeHalo = 2;
 constexpr int kEpiWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -56,6 +65,7 @@ struct ConvParams {
     int tiles_x, tiles_y, npar;
     int n_tiles, BN, acc_stride;
     int kchunks, total_tiles, stages;
+    int halo, a_stages;   // halo mode: A ring of a_stages halo boxes; B ring of `stages`
     uint32_t a_tx;        // bytes one A box delivers
     const __half* x;      // gather source
     const float* bias;
@@ -113,10 +123,12 @@ __device__ __forceinline__ void tap_offset(const ConvParams& p, int tap, int par
 }
 
 struct Smem {
-    uint8_t* a;          // stages x 16 KB
+    uint8_t* a;          // stages x 16 KB, or (halo mode) a_stages x kHaloBytes
     uint8_t* b;          // stages x BN*128 B
     uint64_t* full;      // [stages]
     uint64_t* empty;     // [stages]
+    uint64_t* afull;     // [a_stages] (halo mode)
+    uint64_t* aempty;    // [a_stages] (halo mode)
     uint64_t* accf;      // [2]
     uint64_t* acce;      // [2]
     uint64_t* drain;     // [1]
@@ -128,12 +140,14 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
     Smem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.a = base;
-    s.b = base + p.stages * kABytes;
+    s.b = base + (p.halo ? p.a_stages * kHaloBytes : p.stages * kABytes);
     uint8_t* tail = s.b + p.stages * p.BN * 128;
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
     s.full = bars;
     s.empty = bars + kMaxStages;
-    s.accf = bars + 2 * kMaxStages;
+    s.afull = bars + 2 * kMaxStages;
+    s.aempty = s.afull + kMaxAStages;
+    s.accf = s.aempty + kMaxAStages;
     s.acce = s.accf + 2;
     s.drain = s.acce + 2;
     s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
@@ -150,39 +164,77 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 // ───────────────────────────── roles ─────────────────────────────
 
-template <bool kGather>
+template <int kMode>
 __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensorMap* mapA,
                               const CUtensorMap* mapB) {
     const uint64_t pol_w = policy_evict_last();
     const uint64_t pol_a = policy_evict_normal();
     const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * 128u;
-    const uint32_t tx = b_bytes + (kGather ? 0u : p.a_tx);
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t armed = 0, arm_par = 0;
+    int stage = 0, astage = 0;
+    uint32_t phase = 0, aphase = 0;
+    uint32_t armed = 0, arm_par = 0, aarmed = 0, aarm_par = 0;
     bool ok = true;
+    // Arms the next B-ring slot for `tx` bytes; returns its barrier, or 0 on abort.
+    auto next_b = [&](uint32_t tx, uint32_t* slot) -> uint32_t {
+        if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
+                       kWhereProducerEmpty)) {
+            ok = false;
+            return 0u;
+        }
+        const uint32_t fb = smem_u32(&s.full[stage]);
+        mbar_arrive_expect_tx(fb, tx);
+        armed |= 1u << stage;
+        arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
+        *slot = static_cast<uint32_t>(stage);
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        return fb;
+    };
     for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile(p, t);
-        for (int tap = 0; tap < p.taps && ok; ++tap) {
-            int dy, dx;
-            tap_offset(p, tap, ti.par, dy, dx);
-            for (int kc = 0; kc < p.kchunks; ++kc) {
-                const uint32_t fb = smem_u32(&s.full[stage]);
-                if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, s.abort_flag, p.timeout_ns,
-                               p.status, kWhereProducerEmpty)) {
-                    ok = false;
-                    break;
+        if (kMode == kModeHalo) {
+            const int q = ti.par >> 1, pp = ti.par & 1;
+            const int dxmin = (p.up && pp == 1) ? 0 : -1;
+            for (int ky = 0; ky < 3 && ok; ++ky) {
+                const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                    if (!mbar_wait(smem_u32(&s.aempty[astage]), aphase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
+                                   kWhereProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t afb = smem_u32(&s.afull[astage]);
+                    mbar_arrive_expect_tx(afb, p.a_tx);
+                    aarmed |= 1u << astage;
+                    aarm_par = (aarm_par & ~(1u << astage)) | (aphase << astage);
+                    tma_load_4d(smem_u32(s.a + astage * kHaloBytes), mapA, afb, kc * kBK, ti.u0 + dxmin, ti.v0 + dy,
+                                ti.img, pol_a);
+                    if (++astage == p.a_stages) {
+                        astage = 0;
+                        aphase ^= 1u;
+                    }
+                    for (int kx = 0; kx < 3; ++kx) {
+                        uint32_t slot;
+                        const uint32_t fb = next_b(b_bytes, &slot);
+                        if (!ok) break;
+                        tma_load_3d(smem_u32(s.b + slot * p.BN * 128), mapB, fb, kc * kBK, ky * 3 + kx, ti.n0, pol_w);
+                    }
                 }
-                mbar_arrive_expect_tx(fb, tx);
-                armed |= 1u << stage;
-                arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
-                if (!kGather)
-                    tma_load_4d(smem_u32(s.a + stage * kABytes), mapA, fb, kc * kBK, ti.u0 + dx,
-                                ti.v0 + dy, ti.img, pol_a);
-                tma_load_3d(smem_u32(s.b + stage * p.BN * 128), mapB, fb, kc * kBK, tap, ti.n0, pol_w);
-                if (++stage == p.stages) {
-                    stage = 0;
-                    phase ^= 1u;
+            }
+        } else {
+            for (int tap = 0; tap < p.taps && ok; ++tap) {
+                int dy, dx;
+                tap_offset(p, tap, ti.par, dy, dx);
+                for (int kc = 0; kc < p.kchunks; ++kc) {
+                    uint32_t slot;
+                    const uint32_t fb = next_b(b_bytes + (kMode == kModeGather ? 0u : p.a_tx), &slot);
+                    if (!ok) break;
+                    if (kMode == kModeTma)
+                        tma_load_4d(smem_u32(s.a + slot * kABytes), mapA, fb, kc * kBK, ti.u0 + dx, ti.v0 + dy,
+                                    ti.img, pol_a);
+                    tma_load_3d(smem_u32(s.b + slot * p.BN * 128), mapB, fb, kc * kBK, tap, ti.n0, pol_w);
                 }
             }
         }
@@ -190,6 +242,9 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
     // Let every copy this thread started land before the CTA can exit.
     for (int st = 0; st < p.stages; ++st)
         if (armed & (1u << st)) drain_wait(smem_u32(&s.full[st]), (arm_par >> st) & 1u, p);
+    if (kMode == kModeHalo)
+        for (int st = 0; st < p.a_stages; ++st)
+            if (aarmed & (1u << st)) drain_wait(smem_u32(&s.afull[st]), (aarm_par >> st) & 1u, p);
 }
 
 // One thread per A row: gathers the row's 64-channel slice for each
@@ -245,11 +300,30 @@ __device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
 
 __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base) {
     const uint32_t idesc = idesc_f16_f32(kBM, p.BN);
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, astage = 0;
+    uint32_t phase = 0, aphase = 0;
     int accbuf = 0;
     uint32_t accphase = 0;
     bool ok = true;
+    // Issues the MMAs of one B-ring slot against the A tile at `a_addr`.
+    auto mma_slot = [&](uint32_t d, bool halo_a, uint32_t a_addr, int nk, int& kit) {
+        if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status, kWhereMmaFull)) {
+            ok = false;
+            return;
+        }
+        tc_fence_after();
+        const uint64_t ad = sw128_kmajor_desc(halo_a ? a_addr : smem_u32(s.a + stage * kABytes));
+        const uint64_t bd = sw128_kmajor_desc(smem_u32(s.b + stage * p.BN * 128));
+        for (int k = 0; k < nk; ++k)
+            umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                     (kit | k) != 0 ? 1u : 0u);
+        umma_commit(smem_u32(&s.empty[stage]));
+        ++kit;
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    };
     for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         if (!mbar_wait(smem_u32(&s.acce[accbuf]), accphase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
                        kWhereMmaAccEmpty))
@@ -257,27 +331,34 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
         int kit = 0;
-        for (int tap = 0; tap < p.taps && ok; ++tap) {
-            for (int kc = 0; kc < p.kchunks; ++kc) {
-                if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
-                               kWhereMmaFull)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const int nk = min(4, (p.cin - kc * kBK) / 16);
-                const uint64_t ad = sw128_kmajor_desc(smem_u32(s.a + stage * kABytes));
-                const uint64_t bd = sw128_kmajor_desc(smem_u32(s.b + stage * p.BN * 128));
-                for (int k = 0; k < nk; ++k)
-                    umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                             (kit | k) != 0 ? 1u : 0u);
-                umma_commit(smem_u32(&s.empty[stage]));
-                ++kit;
-                if (++stage == p.stages) {
-                    stage = 0;
-                    phase ^= 1u;
+        if (p.halo) {
+            const int pp = decode_tile(p, t).par & 1;
+            const int dxmin = (p.up && pp == 1) ? 0 : -1;
+            for (int ky = 0; ky < 3 && ok; ++ky) {
+                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                    if (!mbar_wait(smem_u32(&s.afull[astage]), aphase, s.abort_flag, p.timeout_ns, p.status,
+                                   kWhereMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t abase = smem_u32(s.a + astage * kHaloBytes);
+                    const int nk = min(4, (p.cin - kc * kBK) / 16);
+                    for (int kx = 0; kx < 3 && ok; ++kx) {
+                        const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
+                        // a whole-row offset: the tensor core swizzles on absolute address bits
+                        mma_slot(d, true, abase + static_cast<uint32_t>((dx - dxmin) * 128), nk, kit);
+                    }
+                    if (!ok) break;
+                    umma_commit(smem_u32(&s.aempty[astage]));
+                    if (++astage == p.a_stages) {
+                        astage = 0;
+                        aphase ^= 1u;
+                    }
                 }
             }
+        } else {
+            for (int tap = 0; tap < p.taps && ok; ++tap)
+                for (int kc = 0; kc < p.kchunks && ok; ++kc) mma_slot(d, false, 0u, min(4, (p.cin - kc * kBK) / 16), kit);
         }
         if (!ok) break;
         umma_commit(smem_u32(&s.accf[accbuf]));
@@ -426,8 +507,8 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
     }
 }
 
-template <bool kGather>
-__global__ void __launch_bounds__(kGather ? 320 : 192, 1)
+template <int kMode>
+__global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     conv_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const ConvParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -438,9 +519,14 @@ __global__ void __launch_bounds__(kGather ? 320 : 192, 1)
     if (threadIdx.x == 0) {
         *s.abort_flag = 0;
         for (int i = 0; i < p.stages; ++i) {
-            mbar_init(smem_u32(&s.full[i]), kGather ? 129u : 1u);
+            mbar_init(smem_u32(&s.full[i]), kMode == kModeGather ? 129u : 1u);
             mbar_init(smem_u32(&s.empty[i]), 1u);
         }
+        if (kMode == kModeHalo)
+            for (int i = 0; i < p.a_stages; ++i) {
+                mbar_init(smem_u32(&s.afull[i]), 1u);
+                mbar_init(smem_u32(&s.aempty[i]), 1u);
+            }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s.accf[i]), 1u);
             mbar_init(smem_u32(&s.acce[i]), static_cast<uint32_t>(kEpiWarps * 32));
@@ -458,7 +544,7 @@ __global__ void __launch_bounds__(kGather ? 320 : 192, 1)
         tmem_relinquish();
     }
     if (warp == kProducerWarp && lane == 0) {
-        if (!kGather) tma_prefetch_desc(&mapA);
+        if (kMode != kModeGather) tma_prefetch_desc(&mapA);
         tma_prefetch_desc(&mapB);
     }
     tc_fence_before();
@@ -469,10 +555,10 @@ __global__ void __launch_bounds__(kGather ? 320 : 192, 1)
     if (warp < kEpiWarps) {
         role_epilogue(p, s, tmem_base, warp, lane);
     } else if (warp == kProducerWarp) {
-        if (lane == 0) role_producer<kGather>(p, s, &mapA, &mapB);
+        if (lane == 0) role_producer<kMode>(p, s, &mapA, &mapB);
     } else if (warp == kMmaWarp) {
         if (lane == 0) role_mma(p, s, tmem_base);
-    } else if (kGather && warp >= kGatherWarp0) {
+    } else if (kMode == kModeGather && warp >= kGatherWarp0) {
         role_gather(p, s, (warp - kGatherWarp0) * 32 + lane);
     }
     tc_fence_before();
@@ -498,7 +584,7 @@ int choose_bn(int cout) {
     return best;
 }
 
-template <bool kGather>
+template <int kMode>
 int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, size_t smem, int grid,
            cudaStream_t stream) {
     static bool attr_set[64] = {false};
@@ -506,10 +592,10 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, si
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
         VAE_CUDA_CHECK(
-            cudaFuncSetAttribute(conv_kernel<kGather>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+            cudaFuncSetAttribute(conv_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set[dev] = true;
     }
-    conv_kernel<kGather><<<grid, kGather ? 320 : 192, smem, stream>>>(ma, mb, p);
+    conv_kernel<kMode><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, p);
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -584,7 +670,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     if (total >= (1LL << 31)) return set_error(VAE_ERR_SHAPE, "conv: too many tiles");
     p.total_tiles = static_cast<int>(total);
     const int stage_bytes = kABytes + p.BN * 128;
-    p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - 256) / stage_bytes);
+    p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail) / stage_bytes);
     p.a_tx = static_cast<uint32_t>(128 * p.Wt * p.R);
     p.x = static_cast<const __half*>(a.x);
     p.bias = a.bias;
@@ -624,8 +710,28 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                           CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != VAE_OK) return rc;
     }
-    bool gather = p.rep != 0;
-    if (!gather) {
+    int mode = p.rep ? kModeGather : kModeTma;
+    // The halo box saves L2 traffic but its row-shifted descriptors cost shared-
+    // memory read bandwidth; measured on GB300 it wins only for narrow inputs.
+    if (mode == kModeTma && !a.no_halo && a.taps == 9 && p.R == 1 && p.Wt == kBM && a.cin <= 192) {
+        // one 130-pixel halo box per (ky, chunk), shared by the three kx taps
+        const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(p.wv),
+                                  static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n)};
+        const uint64_t strides[3] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(p.wv) * a.cin * 2,
+                                     static_cast<uint64_t>(p.hv) * p.wv * a.cin * 2};
+        const uint32_t box[4] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kHaloRows), 1u, 1u};
+        if (encode_tiled(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.x, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B) == VAE_OK) {
+            mode = kModeHalo;
+            p.halo = 1;
+            p.a_stages = 3;
+            p.a_tx = static_cast<uint32_t>(kHaloRows * 128);
+            p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail - p.a_stages * kHaloBytes) / (p.BN * 128));
+        } else {
+            clear_error();
+        }
+    }
+    if (mode == kModeTma) {
         const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(p.wv),
                                   static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n)};
         const uint64_t strides[3] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(p.wv) * a.cin * 2,
@@ -635,12 +741,17 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         if (encode_tiled(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.x, dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_128B) != VAE_OK) {
             clear_error();
-            gather = true;  // shapes TMA cannot describe: gather threads build the A tiles
+            mode = kModeGather;  // shapes TMA cannot describe: gather threads build the A tiles
         }
     }
-    const size_t smem = 1024 + static_cast<size_t>(p.stages) * stage_bytes + 256;
+    const size_t smem = mode == kModeHalo
+                            ? 1024 + static_cast<size_t>(p.a_stages) * kHaloBytes +
+                                  static_cast<size_t>(p.stages) * p.BN * 128 + kTail
+                            : 1024 + static_cast<size_t>(p.stages) * stage_bytes + kTail;
     const int grid = static_cast<int>(std::min<long long>(total, nsm));
-    return gather ? launch<true>(p, ma, mb, smem, grid, stream) : launch<false>(p, ma, mb, smem, grid, stream);
+    if (mode == kModeHalo) return launch<kModeHalo>(p, ma, mb, smem, grid, stream);
+    if (mode == kModeGather) return launch<kModeGather>(p, ma, mb, smem, grid, stream);
+    return launch<kModeTma>(p, ma, mb, smem, grid, stream);
 }
 
 }  // namespace vae

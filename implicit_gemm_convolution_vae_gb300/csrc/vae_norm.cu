@@ -63,6 +63,57 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
     }
 }
 
+// The same RMS_norm with the pixel held in registers: G lanes per pixel, one
+// pixel per lane group (no grid-stride loop, so every group's loads are in
+// flight at once), each lane loading its <= kRmsV float4s before any use;
+// x is read from memory once. Used when c/4 <= kRmsV * 32.
+constexpr int kRmsV = 9;
+
+template <int G>
+__global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const float* __restrict__ x, long long m, int c,
+                                                          const float* __restrict__ bias,
+                                                          const float* __restrict__ gamma, int silu,
+                                                          float out_scale, __half* __restrict__ y) {
+    const int c4 = c / 4;
+    const int lane = threadIdx.x % G;
+    const long long pix = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / G;
+    const bool live = pix < m;
+    const float4* xr = reinterpret_cast<const float4*>(x + (live ? pix : 0) * c);
+    float4 v[kRmsV];
+#pragma unroll
+    for (int k = 0; k < kRmsV; ++k) {
+        const int i = lane + k * G;
+        v[k] = (live && i < c4) ? __ldg(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRmsV; ++k) {
+        const int i = lane + k * G;
+        if (bias != nullptr && i < c4) {
+            const float4 b = __ldg(reinterpret_cast<const float4*>(bias) + i);
+            v[k].x += b.x; v[k].y += b.y; v[k].z += b.z; v[k].w += b.w;
+        }
+        ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    }
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, G);
+    if (!live) return;
+    const float inv = sqrtf(static_cast<float>(c)) / fmaxf(sqrtf(ss), 1e-12f);
+    uint2* yr = reinterpret_cast<uint2*>(y + pix * c);
+#pragma unroll
+    for (int k = 0; k < kRmsV; ++k) {
+        const int i = lane + k * G;
+        if (i >= c4) continue;
+        const float4 g = __ldg(reinterpret_cast<const float4*>(gamma) + i);
+        float o[4] = {v[k].x * inv * g.x, v[k].y * inv * g.y, v[k].z * inv * g.z, v[k].w * inv * g.w};
+        if (silu) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[e] = silu_f(o[e]);
+        }
+        yr[i] = pack4_f16(o[0] * out_scale, o[1] * out_scale, o[2] * out_scale, o[3] * out_scale);
+    }
+}
+
 // ───────────────────────────── GroupNorm ─────────────────────────────
 // "vae.rs" GroupNorm::apply and "s2v_vae.rs" s2v_gn_part / s2v_gn_fin /
 // s2v_gn_apply. Pass 1: block (chunk, image) reduces its rows; thread t
@@ -332,7 +383,20 @@ int rms_run(const float* x, long long m, int c, const float* bias, const float* 
     if (rc != VAE_OK) return rc;
     const int c4 = c / 4;
     __half* yh = static_cast<__half*>(y);
-    if (c4 >= 128) {
+    if (c4 <= kRmsV * 32) {
+        const int G = c4 <= kRmsV * 4 ? 4 : c4 <= kRmsV * 8 ? 8 : c4 <= kRmsV * 16 ? 16 : 32;
+        const long long blocks = (m * G + 255) / 256;
+        if (blocks > 0x7fffffffLL) return set_error(VAE_ERR_SHAPE, "rmsnorm: m=%lld too large", m);
+        const int grid = static_cast<int>(blocks);
+        if (G == 4)
+            rmsnorm_reg_kernel<4><<<grid, 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+        else if (G == 8)
+            rmsnorm_reg_kernel<8><<<grid, 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+        else if (G == 16)
+            rmsnorm_reg_kernel<16><<<grid, 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+        else
+            rmsnorm_reg_kernel<32><<<grid, 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+    } else if (c4 >= 128) {
         rmsnorm_kernel<32><<<grid_for(m * 32, 256), 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
     } else if (c4 >= 32) {
         rmsnorm_kernel<16><<<grid_for(m * 16, 256), 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);

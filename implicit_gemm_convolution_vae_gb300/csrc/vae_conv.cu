@@ -30,6 +30,7 @@
 //    TMA copies and MMAs, frees TMEM and returns with the status recorded.
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 
 #include "vae_conv.h"
 
@@ -66,6 +67,9 @@ struct ConvParams {
     int n_tiles, BN, acc_stride;
     int kchunks, total_tiles, stages;
     int halo, a_stages;   // halo mode: A ring of a_stages halo boxes; B ring of `stages`
+    int ks;               // K chunks per pipeline stage (1 or 2; per-tap A path only)
+    int pair;             // CTA-pair kernel: each CTA holds BN/2 rows of B (b_rows)
+    int b_rows, typ_tiles, pair_tiles;
     uint32_t a_tx;        // bytes one A box delivers
     const __half* x;      // gather source
     const float* bias;
@@ -140,8 +144,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
     Smem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.a = base;
-    s.b = base + (p.halo ? p.a_stages * kHaloBytes : p.stages * kABytes);
-    uint8_t* tail = s.b + p.stages * p.BN * 128;
+    s.b = base + (p.halo ? p.a_stages * kHaloBytes : p.stages * p.ks * kABytes);
+    uint8_t* tail = s.b + p.stages * p.ks * p.b_rows * 128;
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
     s.full = bars;
     s.empty = bars + kMaxStages;
@@ -227,14 +231,20 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
             for (int tap = 0; tap < p.taps && ok; ++tap) {
                 int dy, dx;
                 tap_offset(p, tap, ti.par, dy, dx);
-                for (int kc = 0; kc < p.kchunks; ++kc) {
+                for (int kc = 0; kc < p.kchunks; kc += p.ks) {
+                    // one stage = up to ks consecutive 64-channel chunks of this tap
+                    const int nck = min(p.ks, p.kchunks - kc);
                     uint32_t slot;
-                    const uint32_t fb = next_b(b_bytes + (kMode == kModeGather ? 0u : p.a_tx), &slot);
+                    const uint32_t fb =
+                        next_b(static_cast<uint32_t>(nck) * (b_bytes + (kMode == kModeGather ? 0u : p.a_tx)), &slot);
                     if (!ok) break;
-                    if (kMode == kModeTma)
-                        tma_load_4d(smem_u32(s.a + slot * kABytes), mapA, fb, kc * kBK, ti.u0 + dx, ti.v0 + dy,
-                                    ti.img, pol_a);
-                    tma_load_3d(smem_u32(s.b + slot * p.BN * 128), mapB, fb, kc * kBK, tap, ti.n0, pol_w);
+                    for (int h = 0; h < nck; ++h) {
+                        if (kMode == kModeTma)
+                            tma_load_4d(smem_u32(s.a + (slot * p.ks + h) * kABytes), mapA, fb, (kc + h) * kBK,
+                                        ti.u0 + dx, ti.v0 + dy, ti.img, pol_a);
+                        tma_load_3d(smem_u32(s.b + (slot * p.ks + h) * p.BN * 128), mapB, fb, (kc + h) * kBK, tap,
+                                    ti.n0, pol_w);
+                    }
                 }
             }
         }
@@ -305,18 +315,22 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
     int accbuf = 0;
     uint32_t accphase = 0;
     bool ok = true;
-    // Issues the MMAs of one B-ring slot against the A tile at `a_addr`.
-    auto mma_slot = [&](uint32_t d, bool halo_a, uint32_t a_addr, int nk, int& kit) {
+    // Issues the MMAs of one B-ring slot: chunk kc0 (and the next ones of the
+    // slot, per-tap path) against the A tile at `a_addr` (halo) or in the slot.
+    auto mma_slot = [&](uint32_t d, bool halo_a, uint32_t a_addr, int kc0, int nck, int& kit) {
         if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status, kWhereMmaFull)) {
             ok = false;
             return;
         }
         tc_fence_after();
-        const uint64_t ad = sw128_kmajor_desc(halo_a ? a_addr : smem_u32(s.a + stage * kABytes));
-        const uint64_t bd = sw128_kmajor_desc(smem_u32(s.b + stage * p.BN * 128));
-        for (int k = 0; k < nk; ++k)
-            umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                     (kit | k) != 0 ? 1u : 0u);
+        for (int h = 0; h < nck; ++h) {
+            const int nk = min(4, (p.cin - (kc0 + h) * kBK) / 16);
+            const uint64_t ad = sw128_kmajor_desc(halo_a ? a_addr : smem_u32(s.a + (stage * p.ks + h) * kABytes));
+            const uint64_t bd = sw128_kmajor_desc(smem_u32(s.b + (stage * p.ks + h) * p.BN * 128));
+            for (int k = 0; k < nk; ++k)
+                umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                         (kit | h | k) != 0 ? 1u : 0u);
+        }
         umma_commit(smem_u32(&s.empty[stage]));
         ++kit;
         if (++stage == p.stages) {
@@ -342,11 +356,10 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
                         break;
                     }
                     const uint32_t abase = smem_u32(s.a + astage * kHaloBytes);
-                    const int nk = min(4, (p.cin - kc * kBK) / 16);
                     for (int kx = 0; kx < 3 && ok; ++kx) {
                         const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
                         // a whole-row offset: the tensor core swizzles on absolute address bits
-                        mma_slot(d, true, abase + static_cast<uint32_t>((dx - dxmin) * 128), nk, kit);
+                        mma_slot(d, true, abase + static_cast<uint32_t>((dx - dxmin) * 128), kc, 1, kit);
                     }
                     if (!ok) break;
                     umma_commit(smem_u32(&s.aempty[astage]));
@@ -358,7 +371,7 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
             }
         } else {
             for (int tap = 0; tap < p.taps && ok; ++tap)
-                for (int kc = 0; kc < p.kchunks && ok; ++kc) mma_slot(d, false, 0u, min(4, (p.cin - kc * kBK) / 16), kit);
+                for (int kc = 0; kc < p.kchunks && ok; kc += p.ks) mma_slot(d, false, 0u, kc, min(p.ks, p.kchunks - kc), kit);
         }
         if (!ok) break;
         umma_commit(smem_u32(&s.accf[accbuf]));
@@ -570,9 +583,306 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     }
 }
 
+
+// ───────────────────────────── CTA-pair kernel ─────────────────────────────
+// A cluster of two CTAs computes a 256 x BN tile with tcgen05.mma.cta_group::2:
+// each CTA holds its own 128-row A tile and half (BN/2 rows) of B at the same
+// shared-memory offsets and its own 128 x BN accumulator in TMEM. Both CTAs'
+// TMA copies complete on the EVEN CTA's full barrier, whose single arrival
+// (by the even producer) expects the bytes of both. The even CTA's MMA thread
+// commits with multicast to the empty / accumulator barriers of both CTAs;
+// both epilogues arrive on the even CTA's accumulator-empty barrier. The odd
+// CTA learns its copies landed from its empty barriers (the MMAs that read
+// them completed). Halves the weight traffic and the shared-memory operand
+// reads per SM.
+
+__device__ __forceinline__ TileInfo decode_pair_tile(const ConvParams& p, int t, int rank) {
+    TileInfo ti;
+    const int nt = t % p.n_tiles;
+    int r = t / p.n_tiles;
+    const int tx = r % p.tiles_x;
+    r /= p.tiles_x;
+    ti.par = r % p.npar;
+    r /= p.npar;
+    const int typ = r % p.typ_tiles;
+    ti.img = r / p.typ_tiles;
+    ti.v0 = (2 * typ + rank) * p.R;  // same column block and parity, rows 2*typ and 2*typ+1
+    ti.u0 = tx * p.Wt;
+    ti.n0 = nt * p.BN;
+    return ti;
+}
+
+template <int kMode>
+__device__ void pair_producer(const ConvParams& p, const Smem& s, const CUtensorMap* mapA,
+                              const CUtensorMap* mapB, int rank) {
+    const uint64_t pol_w = policy_evict_last();
+    const uint64_t pol_a = policy_evict_normal();
+    const uint32_t b_bytes = static_cast<uint32_t>(p.b_rows) * 128u;
+    const int boff = rank * p.b_rows;
+    int stage = 0, astage = 0;
+    uint32_t phase = 0, aphase = 0, armed = 0, arm_par = 0, aarmed = 0, aarm_par = 0;
+    bool ok = true;
+    // Waits for a free B slot; the even CTA arms its (shared) full barrier for
+    // the bytes of both CTAs. Returns the full barrier's cluster address.
+    auto next_b = [&](uint32_t tx, uint32_t* slot) -> uint32_t {
+        if (!mbar_wait_cluster(smem_u32(&s.empty[stage]), phase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
+                               kWhereProducerEmpty)) {
+            ok = false;
+            return 0u;
+        }
+        const uint32_t fb = smem_u32(&s.full[stage]);
+        if (rank == 0) mbar_arrive_expect_tx(fb, 2u * tx);
+        armed |= 1u << stage;
+        arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
+        *slot = static_cast<uint32_t>(stage);
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        return mapa_shared(fb, 0u);
+    };
+    for (int t = blockIdx.x >> 1; t < p.pair_tiles && ok; t += gridDim.x >> 1) {
+        const TileInfo ti = decode_pair_tile(p, t, rank);
+        if (kMode == kModeHalo) {
+            const int q = ti.par >> 1, pp = ti.par & 1;
+            const int dxmin = (p.up && pp == 1) ? 0 : -1;
+            for (int ky = 0; ky < 3 && ok; ++ky) {
+                const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                    if (!mbar_wait_cluster(smem_u32(&s.aempty[astage]), aphase ^ 1u, s.abort_flag, p.timeout_ns,
+                                           p.status, kWhereProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t afb = smem_u32(&s.afull[astage]);
+                    if (rank == 0) mbar_arrive_expect_tx(afb, 2u * p.a_tx);
+                    aarmed |= 1u << astage;
+                    aarm_par = (aarm_par & ~(1u << astage)) | (aphase << astage);
+                    tma_load_4d_pair(smem_u32(s.a + astage * kHaloBytes), mapA, mapa_shared(afb, 0u), kc * kBK,
+                                     ti.u0 + dxmin, ti.v0 + dy, ti.img, pol_a);
+                    if (++astage == p.a_stages) {
+                        astage = 0;
+                        aphase ^= 1u;
+                    }
+                    for (int kx = 0; kx < 3; ++kx) {
+                        uint32_t slot;
+                        const uint32_t fb = next_b(b_bytes, &slot);
+                        if (!ok) break;
+                        tma_load_3d_pair(smem_u32(s.b + slot * p.b_rows * 128), mapB, fb, kc * kBK, ky * 3 + kx,
+                                         ti.n0 + boff, pol_w);
+                    }
+                }
+            }
+        } else {
+            for (int tap = 0; tap < p.taps && ok; ++tap) {
+                int dy, dx;
+                tap_offset(p, tap, ti.par, dy, dx);
+                for (int kc = 0; kc < p.kchunks; ++kc) {
+                    uint32_t slot;
+                    const uint32_t fb = next_b(b_bytes + p.a_tx, &slot);
+                    if (!ok) break;
+                    tma_load_4d_pair(smem_u32(s.a + slot * kABytes), mapA, fb, kc * kBK, ti.u0 + dx, ti.v0 + dy,
+                                     ti.img, pol_a);
+                    tma_load_3d_pair(smem_u32(s.b + slot * p.b_rows * 128), mapB, fb, kc * kBK, tap, ti.n0 + boff,
+                                     pol_w);
+                }
+            }
+        }
+    }
+    // Let every copy this CTA started land before it can exit: the even CTA
+    // sees them on its full barriers; the odd CTA on its empty barriers (the
+    // MMAs that read a slot complete only after that slot's copies landed).
+    for (int st = 0; st < p.stages; ++st)
+        if (armed & (1u << st))
+            drain_wait(smem_u32(rank == 0 ? &s.full[st] : &s.empty[st]), (arm_par >> st) & 1u, p);
+    if (kMode == kModeHalo)
+        for (int st = 0; st < p.a_stages; ++st)
+            if (aarmed & (1u << st))
+                drain_wait(smem_u32(rank == 0 ? &s.afull[st] : &s.aempty[st]), (aarm_par >> st) & 1u, p);
+}
+
+// Even CTA: one thread issues the pair MMAs (M = 256).
+__device__ void pair_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base) {
+    const uint32_t idesc = idesc_f16_f32(2 * kBM, p.BN);
+    int stage = 0, astage = 0;
+    uint32_t phase = 0, aphase = 0;
+    int accbuf = 0;
+    uint32_t accphase = 0;
+    bool ok = true;
+    auto mma_slot = [&](uint32_t d, bool halo_a, uint32_t a_addr, int nk, int& kit) {
+        if (!mbar_wait_cluster(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                               kWhereMmaFull)) {
+            ok = false;
+            return;
+        }
+        tc_fence_after();
+        const uint64_t ad = sw128_kmajor_desc(halo_a ? a_addr : smem_u32(s.a + stage * kABytes));
+        const uint64_t bd = sw128_kmajor_desc(smem_u32(s.b + stage * p.b_rows * 128));
+        for (int k = 0; k < nk; ++k)
+            umma_f16_pair(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                          (kit | k) != 0 ? 1u : 0u);
+        umma_commit_pair(smem_u32(&s.empty[stage]));
+        ++kit;
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    };
+    for (int t = blockIdx.x >> 1; t < p.pair_tiles && ok; t += gridDim.x >> 1) {
+        if (!mbar_wait_cluster(smem_u32(&s.acce[accbuf]), accphase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
+                               kWhereMmaAccEmpty))
+            break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
+        int kit = 0;
+        if (p.halo) {
+            const int pp = decode_pair_tile(p, t, 0).par & 1;
+            const int dxmin = (p.up && pp == 1) ? 0 : -1;
+            for (int ky = 0; ky < 3 && ok; ++ky)
+                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                    if (!mbar_wait_cluster(smem_u32(&s.afull[astage]), aphase, s.abort_flag, p.timeout_ns, p.status,
+                                           kWhereMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t abase = smem_u32(s.a + astage * kHaloBytes);
+                    const int nk = min(4, (p.cin - kc * kBK) / 16);
+                    for (int kx = 0; kx < 3 && ok; ++kx) {
+                        const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
+                        mma_slot(d, true, abase + static_cast<uint32_t>((dx - dxmin) * 128), nk, kit);
+                    }
+                    if (!ok) break;
+                    umma_commit_pair(smem_u32(&s.aempty[astage]));
+                    if (++astage == p.a_stages) {
+                        astage = 0;
+                        aphase ^= 1u;
+                    }
+                }
+        } else {
+            for (int tap = 0; tap < p.taps && ok; ++tap)
+                for (int kc = 0; kc < p.kchunks && ok; ++kc)
+                    mma_slot(d, false, 0u, min(4, (p.cin - kc * kBK) / 16), kit);
+        }
+        if (!ok) break;
+        umma_commit_pair(smem_u32(&s.accf[accbuf]));
+        accbuf ^= 1;
+        if (accbuf == 0) accphase ^= 1u;
+    }
+    umma_commit_pair(smem_u32(s.drain));
+    drain_wait(smem_u32(s.drain), 0u, p);
+}
+
+__device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane, int rank) {
+    const int row = ew * 32 + lane;
+    int accbuf = 0;
+    uint32_t accphase = 0;
+    for (int t = blockIdx.x >> 1; t < p.pair_tiles; t += gridDim.x >> 1) {
+        const TileInfo ti = decode_pair_tile(p, t, rank);
+        if (!warp_all(mbar_wait_cluster(smem_u32(&s.accf[accbuf]), accphase, s.abort_flag, p.timeout_ns, p.status,
+                                        kWhereEpiAccFull)))
+            break;
+        tc_fence_after();
+        const int rr = row / p.Wt, cc = row % p.Wt;
+        const int v = ti.v0 + rr, u = ti.u0 + cc;
+        const bool valid = row < p.R * p.Wt && v < p.hv && u < p.wv && ti.img < p.n;
+        const int q = ti.par >> 1, pp = ti.par & 1;
+        const int Y = p.up ? 2 * v + q : v;
+        const int X = p.up ? 2 * u + pp : u;
+        const long long pix = (static_cast<long long>(ti.img) * p.H + Y) * p.W + X;
+        const uint32_t tbase =
+            tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
+        for (int j = 0; j < p.BN; j += 16) {
+            uint32_t r[16];
+            __syncwarp();
+            tmem_ld16(tbase + static_cast<uint32_t>(j), r);
+            tmem_ld_wait();
+            const int o0 = ti.n0 + j;
+            if (valid && o0 < p.cout) epilogue_chunk(p, ti, r, o0, v, u, q, pp, Y, X, pix);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&s.acce[accbuf]), 0u));
+        accbuf ^= 1;
+        if (accbuf == 0) accphase ^= 1u;
+    }
+}
+
+template <int kMode>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    conv_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                     const ConvParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem s = carve(smem_raw, p);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int rank = static_cast<int>(cluster_ctarank());
+    if (threadIdx.x == 0) {
+        *s.abort_flag = 0;
+        const uint32_t fullc = 1u;  // the even producer's arrive; both CTAs' bytes as transactions
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(smem_u32(&s.full[i]), fullc);
+            mbar_init(smem_u32(&s.empty[i]), 1u);
+        }
+        if (kMode == kModeHalo)
+            for (int i = 0; i < p.a_stages; ++i) {
+                mbar_init(smem_u32(&s.afull[i]), fullc);
+                mbar_init(smem_u32(&s.aempty[i]), 1u);
+            }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&s.accf[i]), 1u);
+            mbar_init(smem_u32(&s.acce[i]), static_cast<uint32_t>(2 * kEpiWarps));
+        }
+        mbar_init(smem_u32(s.drain), 1u);
+        fence_mbar_init();
+    }
+    const uint32_t tmem_cols = p.acc_stride * 2 <= 32 ? 32u
+                               : p.acc_stride * 2 <= 64 ? 64u
+                               : p.acc_stride * 2 <= 128 ? 128u
+                               : p.acc_stride * 2 <= 256 ? 256u
+                                                          : 512u;
+    if (warp == kMmaWarp) {
+        tmem_alloc_pair(smem_u32(s.tmem_slot), tmem_cols);
+        tmem_relinquish_pair();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&mapA);
+        tma_prefetch_desc(&mapB);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers and TMEM exist before any remote arrive or pair MMA
+    tc_fence_after();
+    const uint32_t tmem_base = *s.tmem_slot;
+
+    if (warp < kEpiWarps) {
+        pair_epilogue(p, s, tmem_base, warp, lane, rank);
+    } else if (warp == kProducerWarp) {
+        if (lane == 0) pair_producer<kMode>(p, s, &mapA, &mapB, rank);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0 && rank == 0) pair_mma(p, s, tmem_base);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the even CTA's MMAs into both TMEMs are done; no remote arrives remain
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, tmem_cols);
+    }
+}
+
+bool cta_pair_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("VAE_CONV_CTA_PAIR");
+        return e != nullptr && e[0] == '1';
+    }();
+    return on;
+}
+
 int choose_bn(int cout) {
     const int c16 = (cout + 15) / 16 * 16;
     if (c16 <= 256) return c16;
+    if (c16 >= 1024) return 256;  // widest MMA; measured faster at 1152 despite a ragged last tile
     int best = 256, best_cost = (c16 + 255) / 256 * 256;
     for (int bn = 256; bn >= 64; bn -= 16) {
         const int cost = (c16 + bn - 1) / bn * bn;
@@ -582,6 +892,22 @@ int choose_bn(int cout) {
         }
     }
     return best;
+}
+
+template <int kMode>
+int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, size_t smem, int grid,
+                cudaStream_t stream) {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    VAE_CUDA_CHECK(cudaGetDevice(&dev));
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        VAE_CUDA_CHECK(
+            cudaFuncSetAttribute(conv_pair_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+        attr_set[dev] = true;
+    }
+    conv_pair_kernel<kMode><<<grid, 192, smem, stream>>>(ma, mb, p);
+    VAE_CUDA_CHECK(cudaGetLastError());
+    return VAE_OK;
 }
 
 template <int kMode>
@@ -662,6 +988,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.tiles_y = (p.hv + p.R - 1) / p.R;
     p.npar = p.up ? 4 : 1;
     p.BN = choose_bn(a.cout);
+    p.b_rows = p.BN;
     p.n_tiles = (a.cout + p.BN - 1) / p.BN;
     p.acc_stride = (p.BN + 31) / 32 * 32;
     p.kchunks = (a.cin + kBK - 1) / kBK;
@@ -669,7 +996,11 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     const long long total = m_tiles * p.n_tiles;
     if (total >= (1LL << 31)) return set_error(VAE_ERR_SHAPE, "conv: too many tiles");
     p.total_tiles = static_cast<int>(total);
-    const int stage_bytes = kABytes + p.BN * 128;
+    // Two K chunks per stage halve the per-stage barrier/commit overhead of the
+    // MMA thread (measured +10-21 % on the wide convs) when two such stages fit.
+    p.ks = 1;
+    if (!a.rep && p.kchunks >= 2 && 2 * 2 * (kABytes + p.BN * 128) <= kMaxSmem - 1024 - kTail) p.ks = 2;
+    const int stage_bytes = p.ks * (kABytes + p.BN * 128);
     p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail) / stage_bytes);
     p.a_tx = static_cast<uint32_t>(128 * p.Wt * p.R);
     p.x = static_cast<const __half*>(a.x);
@@ -724,6 +1055,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                          CU_TENSOR_MAP_SWIZZLE_128B) == VAE_OK) {
             mode = kModeHalo;
             p.halo = 1;
+            p.ks = 1;
             p.a_stages = 3;
             p.a_tx = static_cast<uint32_t>(kHaloRows * 128);
             p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail - p.a_stages * kHaloBytes) / (p.BN * 128));
@@ -742,13 +1074,49 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                          CU_TENSOR_MAP_SWIZZLE_128B) != VAE_OK) {
             clear_error();
             mode = kModeGather;  // shapes TMA cannot describe: gather threads build the A tiles
+            p.ks = 1;
+            p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail) / (kABytes + p.BN * 128));
         }
+    }
+    const int grid = static_cast<int>(std::min<long long>(total, nsm));
+    // CTA pairs (cta_group::2) are correct and tested but measured 3-6 % slower
+    // than single CTAs on GB300 at every decoder shape, so they run only when
+    // requested (VAE_CONV_CTA_PAIR=1 in the environment).
+    if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2) {
+        // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
+        p.pair = 1;
+        p.ks = 1;
+        p.b_rows = p.BN / 2;
+        p.typ_tiles = (p.tiles_y + 1) / 2;
+        const long long pt = static_cast<long long>(p.n) * p.typ_tiles * p.npar * p.tiles_x * p.n_tiles;
+        if (pt >= (1LL << 31)) return set_error(VAE_ERR_SHAPE, "conv: too many tiles");
+        p.pair_tiles = static_cast<int>(pt);
+        const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(a.taps),
+                                  static_cast<uint64_t>(a.cout)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(a.taps) * a.cin * 2};
+        const uint32_t box[3] = {static_cast<uint32_t>(kBK), 1u, static_cast<uint32_t>(p.b_rows)};
+        rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != VAE_OK) return rc;
+        size_t smem;
+        if (mode == kModeHalo) {
+            p.a_stages = 4;
+            p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail - p.a_stages * kHaloBytes) / (p.b_rows * 128));
+            smem = 1024 + static_cast<size_t>(p.a_stages) * kHaloBytes + static_cast<size_t>(p.stages) * p.b_rows * 128 +
+                   kTail;
+        } else {
+            const int sb = kABytes + p.b_rows * 128;
+            p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail) / sb);
+            smem = 1024 + static_cast<size_t>(p.stages) * sb + kTail;
+        }
+        const int pgrid = 2 * static_cast<int>(std::min<long long>(pt, nsm / 2));
+        return mode == kModeHalo ? launch_pair<kModeHalo>(p, ma, mb, smem, pgrid, stream)
+                                 : launch_pair<kModeTma>(p, ma, mb, smem, pgrid, stream);
     }
     const size_t smem = mode == kModeHalo
                             ? 1024 + static_cast<size_t>(p.a_stages) * kHaloBytes +
                                   static_cast<size_t>(p.stages) * p.BN * 128 + kTail
-                            : 1024 + static_cast<size_t>(p.stages) * stage_bytes + kTail;
-    const int grid = static_cast<int>(std::min<long long>(total, nsm));
+                            : 1024 + static_cast<size_t>(p.stages) * p.ks * (kABytes + p.BN * 128) + kTail;
     if (mode == kModeHalo) return launch<kModeHalo>(p, ma, mb, smem, grid, stream);
     if (mode == kModeGather) return launch<kModeGather>(p, ma, mb, smem, grid, stream);
     return launch<kModeTma>(p, ma, mb, smem, grid, stream);

@@ -18,6 +18,7 @@ struct ConvArgs {
     float oscale = 1.0f;
     bool up = false, rep = false, silu = false, out_f16 = false;
     bool no_halo = false;        // force the per-tap A path (tests and sweeps)
+    bool no_pair = false;        // force the single-CTA kernel
     // NCHW f32 output of output rows [keep_lo, keep_hi) at destination row
     // (Y - keep_lo + dst_row0), channel planes `plane` floats apart.
     // keep_hi <= keep_lo means all rows of an [n][cout][H][W] tensor.

@@ -310,6 +310,7 @@ class _DecoderDesc(ctypes.Structure):
 
 
 DECODE_PROFILE = 1
+DECODE_NO_FUSION = 2
 STAGE_NAMES = {0: "conv3x3", 1: "conv1x1", 2: "norm", 3: "cast", 4: "attention", 5: "layout", 6: "copy"}
 
 
@@ -395,8 +396,9 @@ class Decoder:
 
     @staticmethod
     def opts(band_from: int = 0, nbands: int = 0, band_rows: int = 0, guard_log2: int = 8,
-             profile: bool = False) -> DecodeOpts:
-        return DecodeOpts(band_from, nbands, band_rows, guard_log2, DECODE_PROFILE if profile else 0)
+             profile: bool = False, fuse: bool = True) -> DecodeOpts:
+        return DecodeOpts(band_from, nbands, band_rows, guard_log2,
+                          (DECODE_PROFILE if profile else 0) | (0 if fuse else DECODE_NO_FUSION))
 
     def profile(self):
         """Stage records of the most recent profiled decode, as dicts (synchronises)."""

@@ -32,8 +32,8 @@ namespace vae {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStageBytes = 48 * 1024;
-constexpr int kStages = 3;
+constexpr int kStageBytes = 64 * 1024;  // QK: two (Q, K) 64-channel chunk pairs; PV: one 64-key V^T half
+constexpr int kStages = 2;
 constexpr int kPBytes = 32 * 1024;  // 128 x 128 f16: two 64-key SW128 atoms
 constexpr uint32_t kSCol = 384;
 constexpr uint32_t kTmemCols = 512;
@@ -105,19 +105,23 @@ __device__ void attn_producer(const AttnParams& p, const ASmem& s, const CUtenso
             phase ^= 1u;
         }
     };
+    // Chunks cc and cc+1 (when it exists) of Q and of K block j in one stage.
     auto load_qk = [&](int j, int cc) {
         if (!ok) return;
         if (!wait_(&s.empty[stage], phase ^ 1u, s, p)) {
             ok = false;
             return;
         }
+        const int nck = min(2, p.nchunk_c - cc);
         const uint32_t fb = smem_u32(&s.full[stage]);
-        mbar_arrive_expect_tx(fb, 32768u);
+        mbar_arrive_expect_tx(fb, 32768u * static_cast<uint32_t>(nck));
         armed |= 1u << stage;
         arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
         uint8_t* st = s.ring + stage * kStageBytes;
-        tma_load_2d(smem_u32(st), mq, fb, cc * 64, q0, pol);
-        tma_load_2d(smem_u32(st + 16384), mk, fb, cc * 64, j * 128, pol);
+        for (int h = 0; h < nck; ++h) {
+            tma_load_2d(smem_u32(st + h * 32768), mq, fb, (cc + h) * 64, q0, pol);
+            tma_load_2d(smem_u32(st + h * 32768 + 16384), mk, fb, (cc + h) * 64, j * 128, pol);
+        }
         next();
     };
     auto load_v = [&](int j, int half) {
@@ -136,10 +140,10 @@ __device__ void attn_producer(const AttnParams& p, const ASmem& s, const CUtenso
                         pol);
         next();
     };
-    for (int cc = 0; cc < p.nchunk_c; ++cc) load_qk(0, cc);
+    for (int cc = 0; cc < p.nchunk_c; cc += 2) load_qk(0, cc);
     for (int j = 0; j < p.nkb && ok; ++j) {
         if (j + 1 < p.nkb)
-            for (int cc = 0; cc < p.nchunk_c; ++cc) load_qk(j + 1, cc);
+            for (int cc = 0; cc < p.nchunk_c; cc += 2) load_qk(j + 1, cc);
         load_v(j, 0);
         load_v(j, 1);
     }
@@ -164,17 +168,20 @@ __device__ void attn_mma(const AttnParams& p, const ASmem& s, uint32_t tmem) {
         }
     };
     auto issue_qk = [&]() {
-        for (int cc = 0; cc < p.nchunk_c && ok; ++cc) {
+        for (int cc = 0; cc < p.nchunk_c && ok; cc += 2) {
             if (!wait_(&s.full[stage], phase, s, p)) {
                 ok = false;
                 return;
             }
             tc_fence_after();
             uint8_t* st = s.ring + stage * kStageBytes;
-            const uint64_t ad = sw128_kmajor_desc(smem_u32(st));
-            const uint64_t bd = sw128_kmajor_desc(smem_u32(st + 16384));
-            for (int k = 0; k < 4; ++k)
-                umma_f16(tmem + kSCol, ad + 2 * k, bd + 2 * k, id_s, (cc | k) != 0 ? 1u : 0u);
+            const int nck = min(2, p.nchunk_c - cc);
+            for (int h = 0; h < nck; ++h) {
+                const uint64_t ad = sw128_kmajor_desc(smem_u32(st + h * 32768));
+                const uint64_t bd = sw128_kmajor_desc(smem_u32(st + h * 32768 + 16384));
+                for (int k = 0; k < 4; ++k)
+                    umma_f16(tmem + kSCol, ad + 2 * k, bd + 2 * k, id_s, (cc | h | k) != 0 ? 1u : 0u);
+            }
             umma_commit(smem_u32(&s.empty[stage]));
             next();
         }

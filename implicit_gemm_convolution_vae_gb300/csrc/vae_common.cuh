@@ -353,7 +353,10 @@ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t j) {
     return r * 128u + ((j ^ (r & 7u)) << 4);
 }
 
-__device__ __forceinline__ float silu_f(float v) { return v / (1.0f + __expf(-v)); }
+// SiLU v / (1 + e^-v) with the fast (approximate, <= 2 ulp) division: every
+// kernel of the library uses this one form, so fused and standalone norms agree
+// bit for bit; its error is far below the f16 rounding of every output it feeds.
+__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // ───────────────────────────── host helpers ─────────────────────────────
 

@@ -33,6 +33,7 @@
 #include <cstdlib>
 
 #include "vae_conv.h"
+#include "vae_rms.cuh"
 
 namespace vae {
 
@@ -84,6 +85,11 @@ struct ConvParams {
     // DupUp add (the RMS-family up conv): src f32 [n][hv][wv][dup_cin].
     const float* dup_src;
     int dup_cin, dup_factor, dup_repeats, dup_ftoff;
+    // Fused RMS_norm of the output pixel (cout <= kRmsMaxC, one N tile): f16
+    // SiLU?(y * sqrt(C) / max(||y||, 1e-12) * gamma) into rms_out [pixels][cout].
+    const float* rms_gamma;
+    __half* rms_out;
+    int rms_silu;
     DevStatus* status;
     unsigned long long timeout_ns;
 };
@@ -427,10 +433,10 @@ __device__ __forceinline__ void store_chunk(const ConvParams& p, long long pix, 
     }
 }
 
-__device__ __forceinline__ void epilogue_chunk(const ConvParams& p, const TileInfo& ti, const uint32_t (&r)[16],
-                                               int o0, int v, int u, int q, int pp, int Y, int X,
-                                               long long pix) {
-    float val[16];
+// The epilogue value of 16 output channels o0.. of one pixel: oscale * acc +
+// bias + residual + DupUp, then SiLU (channels >= cout are left unspecified).
+__device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInfo& ti, const uint32_t (&r)[16],
+                                              int o0, int v, int u, int q, int pp, long long pix, float (&val)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) val[i] = __uint_as_float(r[i]) * p.oscale;
     const bool full = p.vec_ok && (o0 + 16 <= p.cout);
@@ -483,7 +489,80 @@ __device__ __forceinline__ void epilogue_chunk(const ConvParams& p, const TileIn
 #pragma unroll
         for (int i = 0; i < 16; ++i) val[i] = silu_f(val[i]);
     }
+}
+
+__device__ __forceinline__ void epilogue_chunk(const ConvParams& p, const TileInfo& ti, const uint32_t (&r)[16],
+                                               int o0, int v, int u, int q, int pp, int Y, int X,
+                                               long long pix) {
+    float val[16];
+    compute_chunk(p, ti, r, o0, v, u, q, pp, pix, val);
     store_chunk(p, pix, o0, val, Y, X, ti.img);
+}
+
+constexpr int kRmsMaxC = 144;  // fused RMS_norm keeps one pixel's channels in registers
+
+// Whole-row epilogue with a fused RMS_norm: all cout (<= 144) channels of the
+// pixel stay in registers, the f32 output is stored if requested, and the
+// normalised f16 row is written with the standalone kernel's exact arithmetic
+// order (vae_rms.cuh), so fused and unfused decodes agree bit for bit.
+__device__ __forceinline__ void epilogue_rms_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, bool valid,
+                                                 int v, int u, int q, int pp, int Y, int X, long long pix) {
+    float row[kRmsMaxC];
+#pragma unroll
+    for (int c = 0; c < kRmsMaxC / 16; ++c) {
+        if (c * 16 < p.BN) {  // warp-uniform
+            uint32_t r[16];
+            __syncwarp();
+            tmem_ld16(tbase + static_cast<uint32_t>(c * 16), r);
+            tmem_ld_wait();
+            float val[16];
+            compute_chunk(p, ti, r, c * 16, v, u, q, pp, pix, val);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) row[c * 16 + i] = val[i];
+            if (valid && p.y != nullptr) store_chunk(p, pix, c * 16, val, Y, X, ti.img);
+        }
+    }
+    if (!valid) return;
+    constexpr int G = rms_lanes(kRmsMaxC);  // 4: the standalone kernel's lanes for c <= 144
+    const int c4 = p.cout / 4;
+    float part[G];
+#pragma unroll
+    for (int l = 0; l < G; ++l) {
+        part[l] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kRmsMaxC / (4 * G); ++k) {
+            const int i = l + k * G;
+            if (i < c4) part[l] = rms_acc4(part[l], row[4 * i], row[4 * i + 1], row[4 * i + 2], row[4 * i + 3]);
+        }
+    }
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1)
+#pragma unroll
+        for (int l = 0; l < off; ++l) part[l] = __fadd_rn(part[l], part[l + off]);
+    const float inv = rms_inv(part[0], p.cout);
+    __half* dst = p.rms_out + pix * p.cout;
+#pragma unroll
+    for (int c = 0; c < kRmsMaxC / 16; ++c) {
+        if (c * 16 >= p.cout) break;
+        uint32_t h[8];
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+            const int o = c * 16 + 4 * i4;
+            const float4 g = __ldg(reinterpret_cast<const float4*>(p.rms_gamma + o));
+            float a[4] = {rms_apply(row[o], inv, g.x), rms_apply(row[o + 1], inv, g.y),
+                          rms_apply(row[o + 2], inv, g.z), rms_apply(row[o + 3], inv, g.w)};
+            if (p.rms_silu) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a[e] = silu_f(a[e]);
+            }
+            __half2 t0 = __floats2half2_rn(a[0], a[1]);
+            __half2 t1 = __floats2half2_rn(a[2], a[3]);
+            h[2 * i4] = *reinterpret_cast<uint32_t*>(&t0);
+            h[2 * i4 + 1] = *reinterpret_cast<uint32_t*>(&t1);
+        }
+        reinterpret_cast<uint4*>(dst + c * 16)[0] = make_uint4(h[0], h[1], h[2], h[3]);
+        reinterpret_cast<uint4*>(dst + c * 16)[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    }
 }
 
 __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane) {
@@ -505,13 +584,17 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         const long long pix = (static_cast<long long>(ti.img) * p.H + Y) * p.W + X;
         const uint32_t tbase =
             tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
-        for (int j = 0; j < p.BN; j += 16) {
-            uint32_t r[16];
-            __syncwarp();
-            tmem_ld16(tbase + static_cast<uint32_t>(j), r);
-            tmem_ld_wait();
-            const int o0 = ti.n0 + j;
-            if (valid && o0 < p.cout) epilogue_chunk(p, ti, r, o0, v, u, q, pp, Y, X, pix);
+        if (p.rms_out != nullptr) {
+            epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
+        } else {
+            for (int j = 0; j < p.BN; j += 16) {
+                uint32_t r[16];
+                __syncwarp();
+                tmem_ld16(tbase + static_cast<uint32_t>(j), r);
+                tmem_ld_wait();
+                const int o0 = ti.n0 + j;
+                if (valid && o0 < p.cout) epilogue_chunk(p, ti, r, o0, v, u, q, pp, Y, X, pix);
+            }
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&s.acce[accbuf]));
@@ -791,13 +874,17 @@ __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         const long long pix = (static_cast<long long>(ti.img) * p.H + Y) * p.W + X;
         const uint32_t tbase =
             tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
-        for (int j = 0; j < p.BN; j += 16) {
-            uint32_t r[16];
-            __syncwarp();
-            tmem_ld16(tbase + static_cast<uint32_t>(j), r);
-            tmem_ld_wait();
-            const int o0 = ti.n0 + j;
-            if (valid && o0 < p.cout) epilogue_chunk(p, ti, r, o0, v, u, q, pp, Y, X, pix);
+        if (p.rms_out != nullptr) {
+            epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
+        } else {
+            for (int j = 0; j < p.BN; j += 16) {
+                uint32_t r[16];
+                __syncwarp();
+                tmem_ld16(tbase + static_cast<uint32_t>(j), r);
+                tmem_ld_wait();
+                const int o0 = ti.n0 + j;
+                if (valid && o0 < p.cout) epilogue_chunk(p, ti, r, o0, v, u, q, pp, Y, X, pix);
+            }
         }
         tc_fence_before();
         __syncwarp();
@@ -929,8 +1016,8 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, si
 }  // namespace
 
 int conv_validate(const ConvArgs& a) {
-    if (a.x == nullptr || a.w == nullptr || a.y == nullptr)
-        return set_error(VAE_ERR_ARG, "conv: x, w and y must be non-NULL");
+    if (a.x == nullptr || a.w == nullptr)
+        return set_error(VAE_ERR_ARG, "conv: x and w must be non-NULL");
     if (a.taps != 1 && a.taps != 9) return set_error(VAE_ERR_ARG, "conv: taps must be 1 or 9");
     if (a.n < 1 || a.h_in < 1 || a.w_in < 1)
         return set_error(VAE_ERR_SHAPE, "conv: n=%d h=%d w=%d must be >= 1", a.n, a.h_in, a.w_in);
@@ -946,6 +1033,14 @@ int conv_validate(const ConvArgs& a) {
         return set_error(VAE_ERR_SHAPE, "conv: too many output pixels");
     if (a.out_nchw && (a.out_f16 || a.residual != nullptr))
         return set_error(VAE_ERR_ARG, "conv: NCHW output is f32 without residual");
+    if (a.rms_out != nullptr) {
+        if (a.rms_gamma == nullptr || !aligned16(a.rms_gamma) || a.cout > 144 || a.cout % 16 != 0 || a.out_nchw ||
+            a.out_f16 || a.silu)
+            return set_error(VAE_ERR_ARG, "conv: the fused RMS_norm needs gamma, cout %% 16 == 0, cout <= 144, f32 y");
+        if (!aligned16(a.rms_out)) return set_error(VAE_ERR_ALIGN, "conv: rms_out must be 16-byte aligned");
+    } else if (a.y == nullptr) {
+        return set_error(VAE_ERR_ARG, "conv: y must be non-NULL");
+    }
     if (a.dup_src != nullptr) {
         if (!a.up || a.dup_cin < 1 || a.dup_repeats < 1 || a.dup_factor < 1)
             return set_error(VAE_ERR_ARG, "conv: DupUp needs the upsample fold and a valid shuffle");
@@ -1010,7 +1105,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.oscale = a.oscale;
     p.silu = a.silu ? 1 : 0;
     p.out_f16 = a.out_f16 ? 1 : 0;
-    p.vec_ok = (a.cout % 16 == 0) && aligned16(a.y) && (a.residual == nullptr || aligned16(a.residual)) &&
+    p.vec_ok = (a.cout % 16 == 0) && (a.y == nullptr || aligned16(a.y)) && (a.residual == nullptr || aligned16(a.residual)) &&
                (a.bias == nullptr || aligned16(a.bias));
     p.out_nchw = a.out_nchw ? 1 : 0;
     p.keep_lo = a.keep_lo;
@@ -1028,6 +1123,9 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.dup_factor = a.dup_factor;
     p.dup_repeats = a.dup_repeats;
     p.dup_ftoff = a.dup_ftoff;
+    p.rms_gamma = a.rms_gamma;
+    p.rms_out = static_cast<__half*>(a.rms_out);
+    p.rms_silu = a.rms_silu ? 1 : 0;
     p.status = st;
     p.timeout_ns = wait_timeout_ns();
 

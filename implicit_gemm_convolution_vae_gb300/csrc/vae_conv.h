@@ -30,6 +30,11 @@ struct ConvArgs {
     // src[..., (o*dup_factor + dup_ftoff + 2q + p) / dup_repeats].
     const float* dup_src = nullptr;
     int dup_cin = 0, dup_factor = 0, dup_repeats = 0, dup_ftoff = 0;
+    // Fused RMS_norm (+SiLU) of each output pixel into rms_out, f16
+    // [n][H][W][cout] (cout % 16 == 0, cout <= 144); y (f32) may then be NULL.
+    const float* rms_gamma = nullptr;
+    void* rms_out = nullptr;
+    bool rms_silu = false;
 };
 
 int conv_validate(const ConvArgs& a);

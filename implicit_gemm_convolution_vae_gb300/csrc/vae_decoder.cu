@@ -174,7 +174,7 @@ struct Rows {
 Rows grow(Rows r, int k, int h) { return Rows{std::max(r.lo - k, 0), std::min(r.hi + k, h)}; }
 Rows half_rows(Rows r) { return Rows{r.lo / 2, (r.hi + 1) / 2}; }
 
-enum Buf { kS0, kS1, kS2, kB0, kB1, kB2, kH, kSC, kXN, kZ, kATT, kGN, kZIN, kOUT, kNBuf };
+enum Buf { kS0, kS1, kS2, kB0, kB1, kB2, kH, kSC, kXN, kXN2, kZ, kATT, kGN, kZIN, kOUT, kNBuf };
 
 struct Band {
     Rows input;
@@ -198,6 +198,15 @@ struct Exec {
     size_t off[kNBuf] = {};
     float guard = 256.f;
     vae_decoder* prof = nullptr;  // non-null: record events around stages
+    bool no_fuse = false;         // VAE_DECODE_NO_FUSION
+    // RMS_norm rides in the epilogue of a ResNet's first conv (whose f32 output
+    // only feeds that norm) when its CTA holds all of a pixel's channels (one N
+    // tile of <= 144). Measured on GB300: a win there (no f32 write, no norm
+    // pass); for convs that also store the stream and read a residual, keeping
+    // the whole row in registers costs more than the separate norm saves.
+    bool fusable(int cout) const {
+        return !no_fuse && d->family == VAE_FAMILY_RMS && cout <= 144 && cout % 16 == 0;
+    }
 
     // Starts a profiled stage; returns its record index (or -1).
     int begin(int kind, int launches, int h, int w, int cin, int cout, double flops, double bytes) {
@@ -297,10 +306,9 @@ struct Exec {
     int resnet(const DRes& r, float* x, float* y, int h, int w) {
         const long long hw = static_cast<long long>(h) * w;
         const int cin = r.c1.cin, cout = r.c1.cout;
-        __half* xn = f16(kXN, hw * std::max(cin, cout));
-        float* hb = f32(kH, hw * cout);
-        const float* skip = x;
         int rc;
+        const float* skip = x;
+        __half* xn = f16(kXN, hw * std::max(cin, cout));
         if (r.sc.present()) {
             float* s = f32(kSC, hw * cout);
             if ((rc = cast(x, hw * cin, cin, 1.f / guard, xn)) != VAE_OK) return rc;
@@ -310,9 +318,21 @@ struct Exec {
             skip = s;
         }
         if ((rc = norm(x, hw, cin, r.n1, true, xn)) != VAE_OK) return rc;
-        if ((rc = conv(c3(xn, h, w, r.c1, hb))) != VAE_OK) return rc;
-        if ((rc = norm(hb, hw, cout, r.n2, true, xn)) != VAE_OK) return rc;
-        ConvArgs a = c3(xn, h, w, r.c2, y);
+        __half* xmid = f16(kXN2, hw * std::max(cin, cout));
+        ConvArgs a1 = c3(xn, h, w, r.c1, nullptr);
+        if (fusable(cout)) {
+            // conv1's output feeds only norm2: the epilogue writes norm2(h), no f32 h
+            a1.rms_out = xmid;
+            a1.rms_gamma = r.n2.gamma;
+            a1.rms_silu = true;
+            if ((rc = conv(a1)) != VAE_OK) return rc;
+        } else {
+            float* hb = f32(kH, hw * cout);
+            a1.y = hb;
+            if ((rc = conv(a1)) != VAE_OK) return rc;
+            if ((rc = norm(hb, hw, cout, r.n2, true, xmid)) != VAE_OK) return rc;
+        }
+        ConvArgs a = c3(xmid, h, w, r.c2, y);
         a.residual = skip;
         return conv(a);
     }
@@ -446,6 +466,7 @@ int run_decode(Exec& X, int h0, int w0, const vae_decode_opts* opts, const float
     const long long hw0 = static_cast<long long>(h0) * w0;
     int rc;
     X.guard = std::ldexp(1.0f, opts ? (opts->guard_log2 < 0 ? 8 : std::min(opts->guard_log2, 14)) : 8);
+    X.no_fuse = opts != nullptr && (opts->flags & VAE_DECODE_NO_FUSION) != 0;
     int nbands = 1;
     if (opts && opts->band_rows > 0) nbands = (hf + opts->band_rows - 1) / opts->band_rows;
     if (opts && opts->nbands > 1) nbands = opts->nbands;
@@ -555,6 +576,7 @@ int plan_workspace(const vae_decoder* d, int h0, int w0, const vae_decode_opts* 
     if (rc != VAE_OK) return rc;
     X->need[kZIN] = nz * 4;
     X->need[kOUT] = nout * 4;
+    X->need[kXN2] = std::max(X->need[kXN], X->need[kXN2]);
     size_t off = 0;
     for (int i = 0; i < kNBuf; ++i) {
         X->off[i] = off;
@@ -708,7 +730,7 @@ static int decode_impl(vae_decoder_t dec, const float* z, int h0, int w0, float*
                        void* ws, size_t ws_bytes, cudaStream_t st, bool host) {
     if (dec == nullptr || z == nullptr || out == nullptr || ws == nullptr)
         return set_error(VAE_ERR_ARG, "decode: NULL argument");
-    if (opts != nullptr && (opts->flags & ~static_cast<unsigned>(VAE_DECODE_PROFILE)) != 0)
+    if (opts != nullptr && (opts->flags & ~static_cast<unsigned>(VAE_DECODE_PROFILE | VAE_DECODE_NO_FUSION)) != 0)
         return set_error(VAE_ERR_ARG, "decode: unknown opts.flags 0x%x", opts->flags);
     int rc = check_device();
     if (rc != VAE_OK) return rc;

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "vae_norm.h"
+#include "vae_rms.cuh"
 
 namespace vae {
 
@@ -93,24 +94,26 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const float* __restric
             const float4 b = __ldg(reinterpret_cast<const float4*>(bias) + i);
             v[k].x += b.x; v[k].y += b.y; v[k].z += b.z; v[k].w += b.w;
         }
-        ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+        if (i < c4) ss = rms_acc4(ss, v[k].x, v[k].y, v[k].z, v[k].w);
     }
 #pragma unroll
-    for (int off = G / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off, G);
+    for (int off = G / 2; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off, G));
     if (!live) return;
-    const float inv = sqrtf(static_cast<float>(c)) / fmaxf(sqrtf(ss), 1e-12f);
+    const float inv = rms_inv(ss, c);
     uint2* yr = reinterpret_cast<uint2*>(y + pix * c);
 #pragma unroll
     for (int k = 0; k < kRmsV; ++k) {
         const int i = lane + k * G;
         if (i >= c4) continue;
         const float4 g = __ldg(reinterpret_cast<const float4*>(gamma) + i);
-        float o[4] = {v[k].x * inv * g.x, v[k].y * inv * g.y, v[k].z * inv * g.z, v[k].w * inv * g.w};
+        float o[4] = {rms_apply(v[k].x, inv, g.x), rms_apply(v[k].y, inv, g.y), rms_apply(v[k].z, inv, g.z),
+                      rms_apply(v[k].w, inv, g.w)};
         if (silu) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[e] = silu_f(o[e]);
         }
-        yr[i] = pack4_f16(o[0] * out_scale, o[1] * out_scale, o[2] * out_scale, o[3] * out_scale);
+        yr[i] = pack4_f16(__fmul_rn(o[0], out_scale), __fmul_rn(o[1], out_scale), __fmul_rn(o[2], out_scale),
+                          __fmul_rn(o[3], out_scale));
     }
 }
 
@@ -384,7 +387,7 @@ int rms_run(const float* x, long long m, int c, const float* bias, const float* 
     const int c4 = c / 4;
     __half* yh = static_cast<__half*>(y);
     if (c4 <= kRmsV * 32) {
-        const int G = c4 <= kRmsV * 4 ? 4 : c4 <= kRmsV * 8 ? 8 : c4 <= kRmsV * 16 ? 16 : 32;
+        const int G = rms_lanes(c);
         const long long blocks = (m * G + 255) / 256;
         if (blocks > 0x7fffffffLL) return set_error(VAE_ERR_SHAPE, "rmsnorm: m=%lld too large", m);
         const int grid = static_cast<int>(blocks);

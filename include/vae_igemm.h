@@ -281,12 +281,18 @@ typedef struct {
     int nbands;      /* number of equal kept-row bands (0 or 1 with band_rows 0: whole frame) */
     int band_rows;   /* alternative to nbands: at most this many kept rows per band */
     int guard_log2;  /* f16 range guard g of the raw-stream casts (default 8 when < 0) */
-    unsigned flags;  /* 0, or VAE_DECODE_PROFILE */
+    unsigned flags;  /* 0, or VAE_DECODE_PROFILE | VAE_DECODE_NO_FUSION */
 } vae_decode_opts;
 
 /* vae_decode_opts.flags: record CUDA events around every stage of this
  * decode (read back with vae_decode_profile). */
-enum { VAE_DECODE_PROFILE = 1 };
+enum {
+    VAE_DECODE_PROFILE = 1,
+    /* Run every RMS_norm as its own kernel instead of in the epilogue of a
+     * ResNet's first conv (done where one CTA holds all <= 144 channels of a
+     * pixel). Same bits either way; for tests and measurements. */
+    VAE_DECODE_NO_FUSION = 2
+};
 
 /* Stage kinds of a profiled decode. */
 enum {

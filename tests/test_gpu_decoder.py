@@ -138,6 +138,19 @@ def test_host_buffer_decode_matches_device_decode():
     assert torch.equal(oh, dev_out.cpu())
 
 
+@pytest.mark.parametrize("widths,nres,hw", [((64, 32, 32, 16), 2, (12, 10)), ((1152, 576, 288, 144), 3, (16, 16))])
+def test_fused_norms_are_bit_identical_to_separate_norms(widths, nres, hw):
+    """RMS_norm fused into the producing conv's epilogue gives the same bits as
+    the standalone RMS_norm kernel (one shared evaluation order)."""
+    torch = torch_mod()
+    dec = qwen_decoder(seed=7, widths=widths, nres=nres)
+    z = latent_channel_stats(7, 16, *hw)
+    fused, D = gpu_decode(dec, z)
+    plain = D.decode(to_dev(z), opts=vg.Decoder.opts(fuse=False))
+    vg.sync_status()
+    assert torch.equal(fused, plain)
+
+
 def test_gn_family_rejects_bands():
     dec = flux_decoder(seed=1, block_out=(32, 32, 32, 32), layers_per_block=1)
     D = vg.Decoder(dec)

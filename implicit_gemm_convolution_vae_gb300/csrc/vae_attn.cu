@@ -14,9 +14,13 @@
 //    shared memory in the K-major 128B-swizzled layout;
 //  - O[:, chunk] += P V_j^T[chunk] accumulates in TMEM columns [0, dv) (dv <=
 //    384, so c = 1152 takes three chunks and recomputes S per chunk);
-//  - the MMA issue order QK(j+1) before PV(j), a double-buffered P and one
-//    S buffer let the softmax of block j overlap the tensor-core work of
-//    blocks j+1 (QK) and j-1 (PV);
+//  - the MMA issue order QK(j+1) before PV(j) and one S buffer let the
+//    softmax of block j overlap the tensor-core work of blocks j+1 (QK) and
+//    j-1 (PV); one P buffer is enough, because PV(j-1) finishes while the
+//    softmax of block j is still taking its row maxima, and the 32 KB saved
+//    buys a third 64 KB slot of the Q/K/V ring: a key block streams about
+//    twice the ring's capacity of Q and K, so the bytes in flight, not the
+//    tensor cores, set the pace;
 //  - the epilogue writes O / l + b_v as f16 (the v bias is added after P.V,
 //    exact because the rows of the softmax sum to one).
 // No score matrix is ever written to memory. Every wait is bounded.
@@ -33,8 +37,9 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kStageBytes = 64 * 1024;  // QK: two (Q, K) 64-channel chunk pairs; PV: one 64-key V^T half
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kPBytes = 32 * 1024;  // 128 x 128 f16: two 64-key SW128 atoms
+static_assert(1024 + kStages * kStageBytes + kPBytes + 256 <= 232448, "attention shared memory over 227 KB");
 constexpr uint32_t kSCol = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxDv = 384;
@@ -71,7 +76,7 @@ __device__ __forceinline__ ASmem carve_attn(uint8_t* raw) {
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.ring = base;
     s.p = base + kStages * kStageBytes;
-    uint64_t* b = reinterpret_cast<uint64_t*>(s.p + 2 * kPBytes);
+    uint64_t* b = reinterpret_cast<uint64_t*>(s.p + kPBytes);
     s.full = b;
     s.empty = b + kStages;
     s.s_full = b + 2 * kStages;
@@ -188,7 +193,7 @@ __device__ void attn_mma(const AttnParams& p, const ASmem& s, uint32_t tmem) {
         if (ok) umma_commit(smem_u32(s.s_full));
     };
     auto issue_pv = [&](int j) {
-        uint8_t* pb = s.p + (j & 1) * kPBytes;
+        uint8_t* pb = s.p;
         for (int half = 0; half < 2 && ok; ++half) {
             if (!wait_(&s.full[stage], phase, s, p)) {
                 ok = false;
@@ -267,15 +272,12 @@ __device__ void attn_softmax(const AttnParams& p, const ASmem& s, uint32_t tmem,
             m_run = mx;
             resc = true;
         }
-        if (j >= 2 && !wwait_(&s.pv_done[j & 1], static_cast<uint32_t>(((j - 2) >> 1) & 1), s, p)) {
+        // P and the O accumulator are free once PV(j-1) is done.
+        if (j >= 1 && !wwait_(&s.pv_done[(j - 1) & 1], static_cast<uint32_t>(((j - 1) >> 1) & 1), s, p)) {
             ok = false;
             break;
         }
         if (__any_sync(0xffffffffu, resc)) {
-            if (!wwait_(&s.pv_done[(j - 1) & 1], static_cast<uint32_t>(((j - 1) >> 1) & 1), s, p)) {
-                ok = false;
-                break;
-            }
             tc_fence_after();
             for (int col = 0; col < p.dv; col += 16) {
                 uint32_t rr[16];
@@ -290,7 +292,7 @@ __device__ void attn_softmax(const AttnParams& p, const ASmem& s, uint32_t tmem,
         }
         l *= alpha;
         float sum = 0.f;
-        uint8_t* pb = s.p + (j & 1) * kPBytes;
+        uint8_t* pb = s.p;
 #pragma unroll
         for (int g = 0; g < 16; ++g) {
             uint32_t h[4];
@@ -469,7 +471,7 @@ int attn_core_run(const __half* q, const __half* k, const __half* vt, int m, int
         rc = encode_tiled(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, vt, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != VAE_OK) return rc;
     }
-    const size_t smem = 1024 + kStages * kStageBytes + 2 * kPBytes + 256;
+    const size_t smem = 1024 + kStages * kStageBytes + kPBytes + 256;
     static bool attr_set[64] = {false};
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));

@@ -67,7 +67,8 @@ struct ConvParams {
     int tiles_x, tiles_y, npar;
     int n_tiles, BN, acc_stride;
     int kchunks, total_tiles, stages;
-    int halo, a_stages;   // halo mode: A ring of a_stages halo boxes; B ring of `stages`
+    int halo, a_stages;   // halo mode: a_stages halo boxes; B ring of `stages` x ks taps
+                          // (ks == 3: box slot i belongs to stage i, one barrier pair)
     int ks;               // K chunks per pipeline stage (1 or 2; per-tap A path only)
     int pair;             // CTA-pair kernel: each CTA holds BN/2 rows of B (b_rows)
     int b_rows, typ_tiles, pair_tiles;
@@ -78,6 +79,8 @@ struct ConvParams {
     void* y;
     float oscale;
     int silu, out_f16, vec_ok;
+    int res_prefetch;     // L2-prefetch each tile's residual span (one row, all channels)
+    int v8_ok;            // f32 y / residual rows 32-byte aligned: 32-byte accesses
     // NCHW output of kept rows (conv_out): rows [keep_lo, keep_hi) land at
     // destination row (Y - keep_lo + dst_row0) of planes `plane` floats apart.
     int out_nchw, keep_lo, keep_hi, dst_row0;
@@ -204,7 +207,31 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
     };
     for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile(p, t);
-        if (kMode == kModeHalo) {
+        if (p.res_prefetch) {
+            // The tile's residual rows, one contiguous span, are pulled into L2 now
+            // so the epilogue (a mainloop later) reads them at L2 latency.
+            const int npx = min(p.Wt, p.wv - ti.u0);
+            const long long pix0 = (static_cast<long long>(ti.img) * p.H + ti.v0) * p.W + ti.u0;
+            prefetch_l2_bulk(p.residual + pix0 * p.cout, static_cast<uint32_t>(npx * p.cout * 4));
+        }
+        if (kMode == kModeHalo && p.ks == 3) {
+            // one stage = the halo box of (ky, chunk) and the three kx taps' weights
+            const int q = ti.par >> 1, pp = ti.par & 1;
+            const int dxmin = (p.up && pp == 1) ? 0 : -1;
+            for (int ky = 0; ky < 3 && ok; ++ky) {
+                const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                    uint32_t slot;
+                    const uint32_t fb = next_b(p.a_tx + 3u * b_bytes, &slot);
+                    if (!ok) break;
+                    tma_load_4d(smem_u32(s.a + slot * kHaloBytes), mapA, fb, kc * kBK, ti.u0 + dxmin, ti.v0 + dy,
+                                ti.img, pol_a);
+                    for (int kx = 0; kx < 3; ++kx)
+                        tma_load_3d(smem_u32(s.b + (slot * 3 + kx) * p.BN * 128), mapB, fb, kc * kBK, ky * 3 + kx,
+                                    ti.n0, pol_w);
+                }
+            }
+        } else if (kMode == kModeHalo) {
             const int q = ti.par >> 1, pp = ti.par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             for (int ky = 0; ky < 3 && ok; ++ky) {
@@ -351,7 +378,48 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
         int kit = 0;
-        if (p.halo) {
+        if (p.halo && p.ks == 3) {
+            const int pp = decode_tile(p, t).par & 1;
+            const int dxmin = (p.up && pp == 1) ? 0 : -1;
+            for (int ky = 0; ky < 3 && ok; ++ky) {
+                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                    if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                                   kWhereMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // All MMAs of the stage go out back to back: the tensor core's
+                    // issue queue then covers this thread's barrier work.
+                    const int nk = min(4, (p.cin - kc * kBK) / 16);
+                    const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
+                    const uint32_t bbase = smem_u32(s.b + stage * 3 * p.BN * 128);
+#pragma unroll
+                    for (int kx = 0; kx < 3; ++kx) {
+                        const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
+                        // a whole-row offset: the tensor core swizzles on absolute address bits
+                        const uint64_t ad = sw128_kmajor_desc(abase + static_cast<uint32_t>((dx - dxmin) * 128));
+                        const uint64_t bd = sw128_kmajor_desc(bbase + static_cast<uint32_t>(kx * p.BN * 128));
+                        if (nk == 4) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                                         (kit | kx | k) != 0 ? 1u : 0u);
+                        } else {
+                            for (int k = 0; k < nk; ++k)
+                                umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                                         (kit | kx | k) != 0 ? 1u : 0u);
+                        }
+                    }
+                    umma_commit(smem_u32(&s.empty[stage]));
+                    ++kit;
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        } else if (p.halo) {
             const int pp = decode_tile(p, t).par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             for (int ky = 0; ky < 3 && ok; ++ky) {
@@ -421,7 +489,10 @@ __device__ __forceinline__ void store_chunk(const ConvParams& p, long long pix, 
         }
     } else {
         float* y = static_cast<float*>(p.y) + pix * p.cout + o0;
-        if (full) {
+        if (full && p.v8_ok) {
+            st_v8_f32(y, v);
+            st_v8_f32(y + 8, v + 8);
+        } else if (full) {
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 reinterpret_cast<float4*>(y)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
@@ -435,8 +506,10 @@ __device__ __forceinline__ void store_chunk(const ConvParams& p, long long pix, 
 
 // The epilogue value of 16 output channels o0.. of one pixel: oscale * acc +
 // bias + residual + DupUp, then SiLU (channels >= cout are left unspecified).
+// `pre_res`, when given, holds the chunk's 16 residual values already loaded.
 __device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInfo& ti, const uint32_t (&r)[16],
-                                              int o0, int v, int u, int q, int pp, long long pix, float (&val)[16]) {
+                                              int o0, int v, int u, int q, int pp, long long pix, float (&val)[16],
+                                              const float* pre_res = nullptr) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) val[i] = __uint_as_float(r[i]) * p.oscale;
     const bool full = p.vec_ok && (o0 + 16 <= p.cout);
@@ -456,9 +529,18 @@ __device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInf
                 if (o0 + i < p.cout) val[i] += __ldg(p.bias + o0 + i);
         }
     }
-    if (p.residual != nullptr) {
+    if (pre_res != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) val[i] += pre_res[i];
+    } else if (p.residual != nullptr) {
         const float* rs = p.residual + pix * p.cout + o0;
-        if (full) {
+        if (full && p.v8_ok) {
+            float r8[16];
+            ld_v8_f32(rs, r8);
+            ld_v8_f32(rs + 8, r8 + 8);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) val[i] += r8[i];
+        } else if (full) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float4 b = reinterpret_cast<const float4*>(rs)[i];
@@ -565,6 +647,59 @@ __device__ __forceinline__ void epilogue_rms_row(const ConvParams& p, const Tile
     }
 }
 
+// Epilogue of one accumulator row (pixel) without a fused norm. kPipe: the
+// register-hungry pipelined residual path (off in the 320-thread gather kernel).
+template <bool kPipe>
+__device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, bool valid,
+                                                   int v, int u, int q, int pp, int Y, int X, long long pix) {
+    if (kPipe && p.residual != nullptr && p.v8_ok && !p.out_nchw) {
+        // Residual loads run two chunks ahead of their use (a three-slot
+        // register ring), so three are in flight instead of one.
+        const int nch = p.BN / 16;
+        float r0[16], r1[16], r2[16];
+        auto ld = [&](int c, float* rr) {
+            if (valid && c < nch && ti.n0 + c * 16 < p.cout) {
+                const float* rs = p.residual + pix * p.cout + ti.n0 + c * 16;
+                ld_v8_f32(rs, rr);
+                ld_v8_f32(rs + 8, rr + 8);
+            }
+        };
+        auto step = [&](int c, const float* rr) {
+            if (c >= nch) return;  // warp-uniform
+            uint32_t acc[16];
+            __syncwarp();
+            tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
+            tmem_ld_wait();
+            const int o0 = ti.n0 + c * 16;
+            if (valid && o0 < p.cout) {
+                float val[16];
+                compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, rr);
+                store_chunk(p, pix, o0, val, Y, X, ti.img);
+            }
+        };
+        ld(0, r0);
+        ld(1, r1);
+        for (int c = 0; c < nch; c += 3) {
+            ld(c + 2, r2);
+            step(c, r0);
+            ld(c + 3, r0);
+            step(c + 1, r1);
+            ld(c + 4, r1);
+            step(c + 2, r2);
+        }
+        return;
+    }
+    for (int j = 0; j < p.BN; j += 16) {
+        uint32_t r[16];
+        __syncwarp();
+        tmem_ld16(tbase + static_cast<uint32_t>(j), r);
+        tmem_ld_wait();
+        const int o0 = ti.n0 + j;
+        if (valid && o0 < p.cout) epilogue_chunk(p, ti, r, o0, v, u, q, pp, Y, X, pix);
+    }
+}
+
+template <int kMode>
 __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane) {
     const int row = ew * 32 + lane;
     int accbuf = 0;
@@ -587,14 +722,7 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         if (p.rms_out != nullptr) {
             epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         } else {
-            for (int j = 0; j < p.BN; j += 16) {
-                uint32_t r[16];
-                __syncwarp();
-                tmem_ld16(tbase + static_cast<uint32_t>(j), r);
-                tmem_ld_wait();
-                const int o0 = ti.n0 + j;
-                if (valid && o0 < p.cout) epilogue_chunk(p, ti, r, o0, v, u, q, pp, Y, X, pix);
-            }
+            epilogue_plain_row<kMode != kModeGather>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&s.acce[accbuf]));
@@ -618,7 +746,7 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
             mbar_init(smem_u32(&s.full[i]), kMode == kModeGather ? 129u : 1u);
             mbar_init(smem_u32(&s.empty[i]), 1u);
         }
-        if (kMode == kModeHalo)
+        if (kMode == kModeHalo && p.ks != 3)  // the separate halo-box ring
             for (int i = 0; i < p.a_stages; ++i) {
                 mbar_init(smem_u32(&s.afull[i]), 1u);
                 mbar_init(smem_u32(&s.aempty[i]), 1u);
@@ -649,7 +777,7 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     const uint32_t tmem_base = *s.tmem_slot;
 
     if (warp < kEpiWarps) {
-        role_epilogue(p, s, tmem_base, warp, lane);
+        role_epilogue<kMode>(p, s, tmem_base, warp, lane);
     } else if (warp == kProducerWarp) {
         if (lane == 0) role_producer<kMode>(p, s, &mapA, &mapB);
     } else if (warp == kMmaWarp) {
@@ -877,14 +1005,7 @@ __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         if (p.rms_out != nullptr) {
             epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         } else {
-            for (int j = 0; j < p.BN; j += 16) {
-                uint32_t r[16];
-                __syncwarp();
-                tmem_ld16(tbase + static_cast<uint32_t>(j), r);
-                tmem_ld_wait();
-                const int o0 = ti.n0 + j;
-                if (valid && o0 < p.cout) epilogue_chunk(p, ti, r, o0, v, u, q, pp, Y, X, pix);
-            }
+            epilogue_plain_row<true>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         }
         tc_fence_before();
         __syncwarp();
@@ -1107,6 +1228,12 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.out_f16 = a.out_f16 ? 1 : 0;
     p.vec_ok = (a.cout % 16 == 0) && (a.y == nullptr || aligned16(a.y)) && (a.residual == nullptr || aligned16(a.residual)) &&
                (a.bias == nullptr || aligned16(a.bias));
+    p.v8_ok = p.vec_ok && (a.y == nullptr || (reinterpret_cast<uintptr_t>(a.y) & 31) == 0) &&
+              (a.residual == nullptr || (reinterpret_cast<uintptr_t>(a.residual) & 31) == 0) ? 1 : 0;
+    p.res_prefetch = (p.residual != nullptr && p.vec_ok && p.R == 1 && !p.up && p.n_tiles == 1 &&
+                      static_cast<long long>(p.Wt) * a.cout * 4 < (1LL << 31))
+                         ? 1
+                         : 0;
     p.out_nchw = a.out_nchw ? 1 : 0;
     p.keep_lo = a.keep_lo;
     p.keep_hi = a.keep_hi;
@@ -1153,10 +1280,20 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                          CU_TENSOR_MAP_SWIZZLE_128B) == VAE_OK) {
             mode = kModeHalo;
             p.halo = 1;
-            p.ks = 1;
-            p.a_stages = 3;
             p.a_tx = static_cast<uint32_t>(kHaloRows * 128);
-            p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail - p.a_stages * kHaloBytes) / (p.BN * 128));
+            // Preferred: a stage holds the halo box and all three kx taps (12
+            // MMAs per 64-channel chunk) when three such stages fit; else one
+            // tap per stage with a separate ring of halo boxes.
+            const int st3 = (kMaxSmem - 1024 - kTail) / (kHaloBytes + 3 * p.BN * 128);
+            if (st3 >= 3) {
+                p.ks = 3;
+                p.stages = std::min(kMaxStages, st3);
+                p.a_stages = p.stages;
+            } else {
+                p.ks = 1;
+                p.a_stages = 3;
+                p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail - p.a_stages * kHaloBytes) / (p.BN * 128));
+            }
         } else {
             clear_error();
         }
@@ -1213,7 +1350,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     }
     const size_t smem = mode == kModeHalo
                             ? 1024 + static_cast<size_t>(p.a_stages) * kHaloBytes +
-                                  static_cast<size_t>(p.stages) * p.BN * 128 + kTail
+                                  static_cast<size_t>(p.stages) * p.ks * p.BN * 128 + kTail
                             : 1024 + static_cast<size_t>(p.stages) * p.ks * (kABytes + p.BN * 128) + kTail;
     if (mode == kModeHalo) return launch<kModeHalo>(p, ma, mb, smem, grid, stream);
     if (mode == kModeGather) return launch<kModeGather>(p, ma, mb, smem, grid, stream);

@@ -1087,8 +1087,25 @@ bool cta_pair_enabled() {
     return on;
 }
 
-int choose_bn(int cout) {
+// N tile width. halo3: the tile can use three-tap halo stages, which need
+// BN <= 144 for three stages to fit; measured on GB300 they beat the widest
+// per-tap tiles (BN = 256) by 1.3-1.7x at 288, 576 and 1152 output channels
+// and tie at 192 and 768, while BN = 256 stays ahead when cout is a multiple of
+// 256 (256, 512, 1024).
+int choose_bn(int cout, bool halo3) {
     const int c16 = (cout + 15) / 16 * 16;
+    if (halo3 && c16 % 256 != 0) {
+        if (c16 <= 144) return c16;
+        int best = 144, best_cost = (c16 + 143) / 144 * 144;
+        for (int bn = 144; bn >= 64; bn -= 16) {
+            const int cost = (c16 + bn - 1) / bn * bn;
+            if (cost < best_cost) {
+                best = bn;
+                best_cost = cost;
+            }
+        }
+        return best;
+    }
     if (c16 <= 256) return c16;
     if (c16 >= 1024) return 256;  // widest MMA; measured faster at 1152 despite a ragged last tile
     int best = 256, best_cost = (c16 + 255) / 256 * 256;
@@ -1203,7 +1220,10 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.tiles_x = (p.wv + p.Wt - 1) / p.Wt;
     p.tiles_y = (p.hv + p.R - 1) / p.R;
     p.npar = p.up ? 4 : 1;
-    p.BN = choose_bn(a.cout);
+    // Geometry that allows a halo box: a tile is 128 pixels of one row, 3x3 taps,
+    // zero padding (the TMA box fills out-of-range pixels with zeros).
+    const bool halo_geom = !p.rep && !a.no_halo && a.taps == 9 && p.R == 1 && p.Wt == kBM;
+    p.BN = choose_bn(a.cout, halo_geom);
     p.b_rows = p.BN;
     p.n_tiles = (a.cout + p.BN - 1) / p.BN;
     p.acc_stride = (p.BN + 31) / 32 * 32;
@@ -1267,9 +1287,11 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         if (rc != VAE_OK) return rc;
     }
     int mode = p.rep ? kModeGather : kModeTma;
-    // The halo box saves L2 traffic but its row-shifted descriptors cost shared-
-    // memory read bandwidth; measured on GB300 it wins only for narrow inputs.
-    if (mode == kModeTma && !a.no_halo && a.taps == 9 && p.R == 1 && p.Wt == kBM && a.cin <= 192) {
+    // Halo stages: three-tap stages whenever three fit (any cin); otherwise one
+    // tap per stage, which measured faster than per-tap A tiles only for
+    // narrow inputs (cin <= 192).
+    const int st3 = (kMaxSmem - 1024 - kTail) / (kHaloBytes + 3 * p.BN * 128);
+    if (mode == kModeTma && halo_geom && (st3 >= 3 || a.cin <= 192)) {
         // one 130-pixel halo box per (ky, chunk), shared by the three kx taps
         const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(p.wv),
                                   static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n)};
@@ -1284,7 +1306,6 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
             // Preferred: a stage holds the halo box and all three kx taps (12
             // MMAs per 64-channel chunk) when three such stages fit; else one
             // tap per stage with a separate ring of halo boxes.
-            const int st3 = (kMaxSmem - 1024 - kTail) / (kHaloBytes + 3 * p.BN * 128);
             if (st3 >= 3) {
                 p.ks = 3;
                 p.stages = std::min(kMaxStages, st3);

@@ -80,6 +80,9 @@ struct ConvParams {
     float oscale;
     int silu, out_f16, vec_ok;
     int res_prefetch;     // L2-prefetch each tile's residual span (one row, all channels)
+    int dup_prefetch;     // L2-prefetch each tile's DupUp source span (one source row)
+    int dup_step;         // DupUp: source channel = dup_base[2q+p] + dup_step * o (1 or 2), or 0
+    int dup_base[4];
     int v8_ok;            // f32 y / residual rows 32-byte aligned: 32-byte accesses
     // NCHW output of kept rows (conv_out): rows [keep_lo, keep_hi) land at
     // destination row (Y - keep_lo + dst_row0) of planes `plane` floats apart.
@@ -213,6 +216,11 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
             const int npx = min(p.Wt, p.wv - ti.u0);
             const long long pix0 = (static_cast<long long>(ti.img) * p.H + ti.v0) * p.W + ti.u0;
             prefetch_l2_bulk(p.residual + pix0 * p.cout, static_cast<uint32_t>(npx * p.cout * 4));
+        }
+        if (p.dup_prefetch) {  // likewise the DupUp source pixels of the tile (source grid)
+            const int npx = min(p.Wt, p.wv - ti.u0);
+            const long long pix0 = (static_cast<long long>(ti.img) * p.hv + ti.v0) * p.wv + ti.u0;
+            prefetch_l2_bulk(p.dup_src + pix0 * p.dup_cin, static_cast<uint32_t>(npx * p.dup_cin * 4));
         }
         if (kMode == kModeHalo && p.ks == 3) {
             // one stage = the halo box of (ky, chunk) and the three kx taps' weights
@@ -555,7 +563,19 @@ __device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInf
                 if (o0 + i < p.cout) val[i] += rs[i];
         }
     }
-    if (p.dup_src != nullptr) {
+    if (p.dup_src != nullptr && full && p.dup_step != 0) {
+        // Division-free form: the 16 source channels are base + step * o, step
+        // 1 or 2, so the loads have constant offsets and all go out at once.
+        const float* ds = p.dup_src + ((static_cast<long long>(ti.img) * p.hv + v) * p.wv + u) * p.dup_cin +
+                          static_cast<long long>(o0) * p.dup_step + p.dup_base[2 * q + pp];
+        if (p.dup_step == 2) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) val[i] += __ldg(ds + 2 * i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) val[i] += __ldg(ds + i);
+        }
+    } else if (p.dup_src != nullptr) {
         const float* ds =
             p.dup_src + ((static_cast<long long>(ti.img) * p.hv + v) * p.wv + u) * p.dup_cin;
 #pragma unroll
@@ -1270,6 +1290,16 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.dup_factor = a.dup_factor;
     p.dup_repeats = a.dup_repeats;
     p.dup_ftoff = a.dup_ftoff;
+    // (o*F + off)/R = o*(F/R) + off/R exactly when R divides F.
+    p.dup_step = 0;
+    if (a.dup_src != nullptr && a.dup_factor % a.dup_repeats == 0 && a.dup_factor / a.dup_repeats <= 2) {
+        p.dup_step = a.dup_factor / a.dup_repeats;
+        for (int c = 0; c < 4; ++c) p.dup_base[c] = (a.dup_ftoff + c) / a.dup_repeats;
+    }
+    p.dup_prefetch = (a.dup_src != nullptr && p.R == 1 && a.dup_cin % 4 == 0 && aligned16(a.dup_src) &&
+                      static_cast<long long>(p.Wt) * a.dup_cin * 4 < (1LL << 31))
+                         ? 1
+                         : 0;
     p.rms_gamma = a.rms_gamma;
     p.rms_out = static_cast<__half*>(a.rms_out);
     p.rms_silu = a.rms_silu ? 1 : 0;

@@ -311,6 +311,7 @@ class _DecoderDesc(ctypes.Structure):
 
 DECODE_PROFILE = 1
 DECODE_NO_FUSION = 2
+DECODE_FUSE_NORM = 4
 STAGE_NAMES = {0: "conv3x3", 1: "conv1x1", 2: "norm", 3: "cast", 4: "attention", 5: "layout", 6: "copy"}
 
 
@@ -396,9 +397,9 @@ class Decoder:
 
     @staticmethod
     def opts(band_from: int = 0, nbands: int = 0, band_rows: int = 0, guard_log2: int = 8,
-             profile: bool = False, fuse: bool = True) -> DecodeOpts:
+             profile: bool = False, fuse: bool = False) -> DecodeOpts:
         return DecodeOpts(band_from, nbands, band_rows, guard_log2,
-                          (DECODE_PROFILE if profile else 0) | (0 if fuse else DECODE_NO_FUSION))
+                          (DECODE_PROFILE if profile else 0) | (DECODE_FUSE_NORM if fuse else 0))
 
     def profile(self):
         """Stage records of the most recent profiled decode, as dicts (synchronises)."""

@@ -198,14 +198,14 @@ struct Exec {
     size_t off[kNBuf] = {};
     float guard = 256.f;
     vae_decoder* prof = nullptr;  // non-null: record events around stages
-    bool no_fuse = false;         // VAE_DECODE_NO_FUSION
+    bool fuse = false;            // VAE_DECODE_FUSE_NORM without VAE_DECODE_NO_FUSION
     // RMS_norm rides in the epilogue of a ResNet's first conv (whose f32 output
     // only feeds that norm) when its CTA holds all of a pixel's channels (one N
     // tile of <= 144). Measured on GB300: a win there (no f32 write, no norm
     // pass); for convs that also store the stream and read a residual, keeping
     // the whole row in registers costs more than the separate norm saves.
     bool fusable(int cout) const {
-        return !no_fuse && d->family == VAE_FAMILY_RMS && cout <= 144 && cout % 16 == 0;
+        return fuse && d->family == VAE_FAMILY_RMS && cout <= 144 && cout % 16 == 0;
     }
 
     // Starts a profiled stage; returns its record index (or -1).
@@ -466,7 +466,7 @@ int run_decode(Exec& X, int h0, int w0, const vae_decode_opts* opts, const float
     const long long hw0 = static_cast<long long>(h0) * w0;
     int rc;
     X.guard = std::ldexp(1.0f, opts ? (opts->guard_log2 < 0 ? 8 : std::min(opts->guard_log2, 14)) : 8);
-    X.no_fuse = opts != nullptr && (opts->flags & VAE_DECODE_NO_FUSION) != 0;
+    X.fuse = opts != nullptr && (opts->flags & VAE_DECODE_FUSE_NORM) != 0 && (opts->flags & VAE_DECODE_NO_FUSION) == 0;
     int nbands = 1;
     if (opts && opts->band_rows > 0) nbands = (hf + opts->band_rows - 1) / opts->band_rows;
     if (opts && opts->nbands > 1) nbands = opts->nbands;
@@ -730,7 +730,8 @@ static int decode_impl(vae_decoder_t dec, const float* z, int h0, int w0, float*
                        void* ws, size_t ws_bytes, cudaStream_t st, bool host) {
     if (dec == nullptr || z == nullptr || out == nullptr || ws == nullptr)
         return set_error(VAE_ERR_ARG, "decode: NULL argument");
-    if (opts != nullptr && (opts->flags & ~static_cast<unsigned>(VAE_DECODE_PROFILE | VAE_DECODE_NO_FUSION)) != 0)
+    if (opts != nullptr &&
+        (opts->flags & ~static_cast<unsigned>(VAE_DECODE_PROFILE | VAE_DECODE_NO_FUSION | VAE_DECODE_FUSE_NORM)) != 0)
         return set_error(VAE_ERR_ARG, "decode: unknown opts.flags 0x%x", opts->flags);
     int rc = check_device();
     if (rc != VAE_OK) return rc;

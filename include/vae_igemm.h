@@ -281,17 +281,23 @@ typedef struct {
     int nbands;      /* number of equal kept-row bands (0 or 1 with band_rows 0: whole frame) */
     int band_rows;   /* alternative to nbands: at most this many kept rows per band */
     int guard_log2;  /* f16 range guard g of the raw-stream casts (default 8 when < 0) */
-    unsigned flags;  /* 0, or VAE_DECODE_PROFILE | VAE_DECODE_NO_FUSION */
+    unsigned flags;  /* 0, or VAE_DECODE_PROFILE | VAE_DECODE_FUSE_NORM | VAE_DECODE_NO_FUSION */
 } vae_decode_opts;
 
 /* vae_decode_opts.flags: record CUDA events around every stage of this
  * decode (read back with vae_decode_profile). */
 enum {
     VAE_DECODE_PROFILE = 1,
-    /* Run every RMS_norm as its own kernel instead of in the epilogue of a
-     * ResNet's first conv (done where one CTA holds all <= 144 channels of a
-     * pixel). Same bits either way; for tests and measurements. */
-    VAE_DECODE_NO_FUSION = 2
+    /* Run every RMS_norm as its own kernel (the default); overrides
+     * VAE_DECODE_FUSE_NORM. */
+    VAE_DECODE_NO_FUSION = 2,
+    /* Compute a ResNet's second RMS_norm (+SiLU) in the epilogue of its first
+     * conv where one CTA holds all <= 144 channels of a pixel, instead of
+     * writing the f32 conv output and normalising it in a separate kernel.
+     * Same bits either way. Off by default: on GB300 the per-pixel norm
+     * epilogue takes longer than the conv mainloop it overlaps, and the pair
+     * (conv + separate RMS_norm) measured faster. */
+    VAE_DECODE_FUSE_NORM = 4
 };
 
 /* Stage kinds of a profiled decode. */

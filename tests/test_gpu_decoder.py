@@ -145,8 +145,8 @@ def test_fused_norms_are_bit_identical_to_separate_norms(widths, nres, hw):
     torch = torch_mod()
     dec = qwen_decoder(seed=7, widths=widths, nres=nres)
     z = latent_channel_stats(7, 16, *hw)
-    fused, D = gpu_decode(dec, z)
-    plain = D.decode(to_dev(z), opts=vg.Decoder.opts(fuse=False))
+    fused, D = gpu_decode(dec, z, opts=vg.Decoder.opts(fuse=True))
+    plain = D.decode(to_dev(z))
     vg.sync_status()
     assert torch.equal(fused, plain)
 

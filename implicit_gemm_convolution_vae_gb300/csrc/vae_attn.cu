@@ -1,29 +1,32 @@
 // Mid-block single-head spatial self-attention ("vae.rs" AttnBlock::apply /
 // finish; "qi21_vae.rs" attention): norm -> q, k, v^T projections (the
-// implicit-GEMM kernel with one tap) -> one fused tcgen05 kernel computing
-// o = softmax(q k^T / sqrt(c)) v + b_v -> output projection added onto the
-// stream by the conv epilogue's residual path.
+// implicit-GEMM kernel with one tap) -> o = softmax(q k^T / sqrt(c)) v + b_v
+// by two tcgen05 kernels -> output projection added onto the stream by the
+// conv epilogue's residual path.
 //
-// The fused kernel (one CTA per (128-query tile, value-channel chunk)):
-//  - S = Q K_j^T for key block j (128 keys) accumulates in TMEM columns
-//    [384, 512) from 64-channel chunks of Q and K streamed by TMA;
-//  - four softmax warps (one query row per thread) read S with tcgen05.ld,
-//    mask keys >= m, keep a running max m and sum l (online softmax; O is
-//    rescaled in TMEM only when the max grows by more than 2^8, so the
-//    unnormalised P = 2^(s - m) stays <= 256 in f16), and write P (f16) to
-//    shared memory in the K-major 128B-swizzled layout;
-//  - O[:, chunk] += P V_j^T[chunk] accumulates in TMEM columns [0, dv) (dv <=
-//    384, so c = 1152 takes three chunks and recomputes S per chunk);
-//  - the MMA issue order QK(j+1) before PV(j) and one S buffer let the
-//    softmax of block j overlap the tensor-core work of blocks j+1 (QK) and
-//    j-1 (PV); one P buffer is enough, because PV(j-1) finishes while the
-//    softmax of block j is still taking its row maxima, and the 32 KB saved
-//    buys a third 64 KB slot of the Q/K/V ring: a key block streams about
-//    twice the ring's capacity of Q and K, so the bytes in flight, not the
-//    tensor cores, set the pace;
-//  - the epilogue writes O / l + b_v as f16 (the v bias is added after P.V,
-//    exact because the rows of the softmax sum to one).
-// No score matrix is ever written to memory. Every wait is bounded.
+// Scores kernel (one CTA per 128-query tile): S = Q K_j^T for key block j
+// (128 keys) accumulates in one of two TMEM buffers from 64-channel chunks of
+// Q and K streamed by TMA; four softmax warps (one query row per thread) read
+// S with tcgen05.ld, mask keys >= m and keep a running max m and sum l (online
+// softmax, rescaling only when the max grows by more than 2^8, so the
+// unnormalised P = 2^(s - m) stays <= 256 in f16). They write P (f16) to a
+// row-major workspace, the factor alpha_j each row's O must be scaled by before
+// block j is added (1 when its max did not move), one "some row rescaled" flag
+// per warp and block, and the final l.
+//
+// PV kernel (one CTA per (query tile, value-channel chunk of <= 384)): O +=
+// P_j V_j^T in TMEM from TMA-streamed 64-key halves of P and V^T; on a flagged
+// block the four row warps scale O by alpha_j after PV(j-1) and before PV(j).
+// The epilogue writes O / l + b_v as f16 (the v bias is added after P.V, exact
+// because the rows of the softmax sum to one).
+//
+// S is computed once however many value chunks c needs (the O accumulator of
+// c = 1152 columns cannot live in one SM's 512 TMEM columns, so a fused kernel
+// had to recompute S per chunk, doubling the tensor work), at the price of
+// writing P (2 bytes per score) once and reading it once per chunk. The
+// arithmetic (S, the softmax, P, the rescale sequence, the P.V order) is the
+// same as the fused kernel's, so the output is too. Query tiles run in groups
+// whose P fits a 2 GiB workspace. Every wait is bounded.
 #include <algorithm>
 #include <cmath>
 
@@ -36,18 +39,36 @@ namespace vae {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStageBytes = 64 * 1024;  // QK: two (Q, K) 64-channel chunk pairs; PV: one 64-key V^T half
+constexpr int kStageBytes = 64 * 1024;  // scores: two (Q, K) 64-channel chunk pairs; PV: a 64-key P half + V^T half
 constexpr int kStages = 3;
-constexpr int kPBytes = 32 * 1024;  // 128 x 128 f16: two 64-key SW128 atoms
-static_assert(1024 + kStages * kStageBytes + kPBytes + 256 <= 232448, "attention shared memory over 227 KB");
-constexpr uint32_t kSCol = 384;
+static_assert(1024 + kStages * kStageBytes + 256 <= 232448, "attention shared memory over 227 KB");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxDv = 384;
+constexpr int kMaxFlagWords = 256;                   // key blocks <= 8192, i.e. m <= 2^20
+constexpr size_t kMaxPBytes = size_t(2) << 30;       // P of one group of query tiles
+constexpr int kPHalfBytes = 128 * 64 * 2;            // 128 query rows x 64 keys
 
-struct AttnParams {
-    int m, c, dv, ndv, nkb, nchunk_c;
-    int vbox_rows, vboxes;
+struct ScoreParams {
+    int m, nkb, nchunk_c;
+    int q_tile0;   // first query tile of this group
+    int kcols;     // P row length (nkb * 128)
+    int grows;     // rows of the group buffers (tiles * 128)
     float scale_log2;
+    __half* p;        // [grows][kcols]
+    float* alpha;     // [nkb][grows]
+    float* lsum;      // [grows]
+    uint32_t* flags;  // [tiles][nkb][4]
+    DevStatus* status;
+    unsigned long long timeout_ns;
+};
+
+struct PvParams {
+    int m, c, dv, ndv, nkb;
+    int q_tile0, grows;
+    int vbox_rows, vboxes;
+    const float* alpha;
+    const float* lsum;
+    const uint32_t* flags;
     const float* bv;
     __half* out;
     DevStatus* status;
@@ -63,10 +84,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+__device__ __forceinline__ void st_v8_b32(void* dst, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 struct ASmem {
     uint8_t* ring;
-    uint8_t* p;
-    uint64_t *full, *empty, *s_full, *s_free, *p_full, *pv_done, *drain;
+    uint64_t *full, *empty;    // [kStages]
+    uint64_t *s_full, *s_free;  // [2] (scores)
+    uint64_t* resc_ready;       // (PV) MMAs up to PV(j-1) done before a flagged block j
+    uint64_t* scaled;           // (PV) O scaled by alpha_j
+    uint64_t* final;            // (PV) every PV done
+    uint64_t* drain;
     uint32_t* tmem_slot;
     int* abort_flag;
 };
@@ -75,187 +106,142 @@ __device__ __forceinline__ ASmem carve_attn(uint8_t* raw) {
     ASmem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.ring = base;
-    s.p = base + kStages * kStageBytes;
-    uint64_t* b = reinterpret_cast<uint64_t*>(s.p + kPBytes);
+    uint64_t* b = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes);
     s.full = b;
     s.empty = b + kStages;
     s.s_full = b + 2 * kStages;
-    s.s_free = s.s_full + 1;
-    s.p_full = s.s_free + 1;   // [2]
-    s.pv_done = s.p_full + 2;  // [2]
-    s.drain = s.pv_done + 2;
+    s.s_free = s.s_full + 2;
+    s.resc_ready = s.s_free + 2;
+    s.scaled = s.resc_ready + 1;
+    s.final = s.scaled + 1;
+    s.drain = s.final + 1;
     s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
     s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
     return s;
 }
 
-__device__ __forceinline__ bool wait_(uint64_t* bar, uint32_t parity, const ASmem& s, const AttnParams& p) {
-    return mbar_wait(smem_u32(bar), parity, s.abort_flag, p.timeout_ns, p.status, kWhereAttn);
+__device__ __forceinline__ bool wait_(uint64_t* bar, uint32_t parity, const ASmem& s, DevStatus* st,
+                                      unsigned long long timeout) {
+    return mbar_wait(smem_u32(bar), parity, s.abort_flag, timeout, st, kWhereAttn);
 }
 
 // The same wait taken by a whole warp, with a warp-uniform result.
-__device__ __forceinline__ bool wwait_(uint64_t* bar, uint32_t parity, const ASmem& s, const AttnParams& p) {
-    return warp_all(wait_(bar, parity, s, p));
+__device__ __forceinline__ bool wwait_(uint64_t* bar, uint32_t parity, const ASmem& s, DevStatus* st,
+                                       unsigned long long timeout) {
+    return warp_all(wait_(bar, parity, s, st, timeout));
 }
 
-__device__ void attn_producer(const AttnParams& p, const ASmem& s, const CUtensorMap* mq, const CUtensorMap* mk,
-                              const CUtensorMap* mv, int q0, int d0) {
-    const uint64_t pol = policy_evict_normal();
+// Ring bookkeeping shared by the producers and MMA threads.
+struct Ring {
     int stage = 0;
     uint32_t phase = 0, armed = 0, arm_par = 0;
-    bool ok = true;
-    auto next = [&]() {
+    __device__ __forceinline__ void next() {
         if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
         }
-    };
-    // Chunks cc and cc+1 (when it exists) of Q and of K block j in one stage.
-    auto load_qk = [&](int j, int cc) {
-        if (!ok) return;
-        if (!wait_(&s.empty[stage], phase ^ 1u, s, p)) {
-            ok = false;
-            return;
-        }
-        const int nck = min(2, p.nchunk_c - cc);
-        const uint32_t fb = smem_u32(&s.full[stage]);
-        mbar_arrive_expect_tx(fb, 32768u * static_cast<uint32_t>(nck));
-        armed |= 1u << stage;
-        arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
-        uint8_t* st = s.ring + stage * kStageBytes;
-        for (int h = 0; h < nck; ++h) {
-            tma_load_2d(smem_u32(st + h * 32768), mq, fb, (cc + h) * 64, q0, pol);
-            tma_load_2d(smem_u32(st + h * 32768 + 16384), mk, fb, (cc + h) * 64, j * 128, pol);
-        }
-        next();
-    };
-    auto load_v = [&](int j, int half) {
-        if (!ok) return;
-        if (!wait_(&s.empty[stage], phase ^ 1u, s, p)) {
-            ok = false;
-            return;
-        }
-        const uint32_t fb = smem_u32(&s.full[stage]);
-        mbar_arrive_expect_tx(fb, static_cast<uint32_t>(p.vboxes * p.vbox_rows * 128));
-        armed |= 1u << stage;
-        arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
-        uint8_t* st = s.ring + stage * kStageBytes;
-        for (int b = 0; b < p.vboxes; ++b)
-            tma_load_2d(smem_u32(st + b * p.vbox_rows * 128), mv, fb, j * 128 + half * 64, d0 + b * p.vbox_rows,
-                        pol);
-        next();
-    };
-    for (int cc = 0; cc < p.nchunk_c; cc += 2) load_qk(0, cc);
-    for (int j = 0; j < p.nkb && ok; ++j) {
-        if (j + 1 < p.nkb)
-            for (int cc = 0; cc < p.nchunk_c; cc += 2) load_qk(j + 1, cc);
-        load_v(j, 0);
-        load_v(j, 1);
     }
+    __device__ __forceinline__ void arm() {
+        armed |= 1u << stage;
+        arm_par = (arm_par & ~(1u << stage)) | (phase << stage);
+    }
+    // Lets every copy this thread started land before the CTA can exit.
+    __device__ __forceinline__ void drain(const ASmem& s, DevStatus* st, unsigned long long timeout) const {
+        int never = 0;
+        for (int i = 0; i < kStages; ++i)
+            if (armed & (1u << i))
+                (void)mbar_wait(smem_u32(&s.full[i]), (arm_par >> i) & 1u, &never, timeout, st, kWhereDrain);
+    }
+};
+
+__device__ __forceinline__ void mma_drain(const ASmem& s, DevStatus* st, unsigned long long timeout) {
+    umma_commit(smem_u32(s.drain));
     int never = 0;
-    for (int st = 0; st < kStages; ++st)
-        if (armed & (1u << st))
-            (void)mbar_wait(smem_u32(&s.full[st]), (arm_par >> st) & 1u, &never, p.timeout_ns, p.status, kWhereDrain);
+    (void)mbar_wait(smem_u32(s.drain), 0u, &never, timeout, st, kWhereDrain);
 }
 
-__device__ void attn_mma(const AttnParams& p, const ASmem& s, uint32_t tmem) {
-    const uint32_t id_s = idesc_f16_f32(128, 128);
-    const int nsplit = p.dv > 256 ? 2 : 1;
-    const int ns = p.dv / nsplit;
-    const uint32_t id_o = idesc_f16_f32(128, ns);
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    auto next = [&]() {
-        if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-        }
-    };
-    auto issue_qk = [&]() {
-        for (int cc = 0; cc < p.nchunk_c && ok; cc += 2) {
-            if (!wait_(&s.full[stage], phase, s, p)) {
-                ok = false;
+// ───────────────────────────── scores kernel ─────────────────────────────
+
+__device__ void scores_producer(const ScoreParams& p, const ASmem& s, const CUtensorMap* mq, const CUtensorMap* mk,
+                                int q0) {
+    const uint64_t pol = policy_evict_normal();
+    Ring r;
+    for (int j = 0; j < p.nkb; ++j)
+        for (int cc = 0; cc < p.nchunk_c; cc += 2) {
+            if (!wait_(&s.empty[r.stage], r.phase ^ 1u, s, p.status, p.timeout_ns)) {
+                r.drain(s, p.status, p.timeout_ns);
                 return;
             }
+            const int nck = min(2, p.nchunk_c - cc);
+            const uint32_t fb = smem_u32(&s.full[r.stage]);
+            mbar_arrive_expect_tx(fb, 32768u * static_cast<uint32_t>(nck));
+            r.arm();
+            uint8_t* st = s.ring + r.stage * kStageBytes;
+            for (int h = 0; h < nck; ++h) {
+                tma_load_2d(smem_u32(st + h * 32768), mq, fb, (cc + h) * 64, q0, pol);
+                tma_load_2d(smem_u32(st + h * 32768 + 16384), mk, fb, (cc + h) * 64, j * 128, pol);
+            }
+            r.next();
+        }
+    r.drain(s, p.status, p.timeout_ns);
+}
+
+__device__ void scores_mma(const ScoreParams& p, const ASmem& s, uint32_t tmem) {
+    const uint32_t id_s = idesc_f16_f32(128, 128);
+    Ring r;
+    bool ok = true;
+    for (int j = 0; j < p.nkb && ok; ++j) {
+        const int b = j & 1;
+        if (j >= 2) {  // the softmax has read S(j - 2) out of this buffer
+            if (!wait_(&s.s_free[b], static_cast<uint32_t>(((j - 2) >> 1) & 1), s, p.status, p.timeout_ns)) break;
             tc_fence_after();
-            uint8_t* st = s.ring + stage * kStageBytes;
+        }
+        for (int cc = 0; cc < p.nchunk_c; cc += 2) {
+            if (!wait_(&s.full[r.stage], r.phase, s, p.status, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint8_t* st = s.ring + r.stage * kStageBytes;
             const int nck = min(2, p.nchunk_c - cc);
             for (int h = 0; h < nck; ++h) {
                 const uint64_t ad = sw128_kmajor_desc(smem_u32(st + h * 32768));
                 const uint64_t bd = sw128_kmajor_desc(smem_u32(st + h * 32768 + 16384));
+#pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    umma_f16(tmem + kSCol, ad + 2 * k, bd + 2 * k, id_s, (cc | h | k) != 0 ? 1u : 0u);
+                    umma_f16(tmem + static_cast<uint32_t>(b * 128), ad + 2 * k, bd + 2 * k, id_s,
+                             (cc | h | k) != 0 ? 1u : 0u);
             }
-            umma_commit(smem_u32(&s.empty[stage]));
-            next();
+            umma_commit(smem_u32(&s.empty[r.stage]));
+            r.next();
         }
-        if (ok) umma_commit(smem_u32(s.s_full));
-    };
-    auto issue_pv = [&](int j) {
-        uint8_t* pb = s.p;
-        for (int half = 0; half < 2 && ok; ++half) {
-            if (!wait_(&s.full[stage], phase, s, p)) {
-                ok = false;
-                return;
-            }
-            tc_fence_after();
-            uint8_t* st = s.ring + stage * kStageBytes;
-            const uint64_t ad = sw128_kmajor_desc(smem_u32(pb + half * 16384));
-            for (int k = 0; k < 4; ++k)
-                for (int sp = 0; sp < nsplit; ++sp) {
-                    const uint64_t bd = sw128_kmajor_desc(smem_u32(st + sp * ns * 128));
-                    umma_f16(tmem + static_cast<uint32_t>(sp * ns), ad + 2 * k, bd + 2 * k, id_o,
-                             (j | half | k) != 0 ? 1u : 0u);
-                }
-            umma_commit(smem_u32(&s.empty[stage]));
-            next();
-        }
-        if (ok) umma_commit(smem_u32(&s.pv_done[j & 1]));
-    };
-    issue_qk();
-    for (int j = 0; j < p.nkb && ok; ++j) {
-        if (j + 1 < p.nkb) {
-            if (!wait_(s.s_free, static_cast<uint32_t>(j & 1), s, p)) break;
-            tc_fence_after();
-            issue_qk();
-        }
-        if (!ok) break;
-        if (!wait_(&s.p_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), s, p)) break;
-        tc_fence_after();
-        issue_pv(j);
+        if (ok) umma_commit(smem_u32(&s.s_full[b]));
     }
-    umma_commit(smem_u32(s.drain));
-    int never = 0;
-    (void)mbar_wait(smem_u32(s.drain), 0u, &never, p.timeout_ns, p.status, kWhereDrain);
+    mma_drain(s, p.status, p.timeout_ns);
 }
 
-__device__ void attn_softmax(const AttnParams& p, const ASmem& s, uint32_t tmem, int warp, int lane, int q0,
-                             int d0) {
+__device__ void scores_softmax(const ScoreParams& p, const ASmem& s, uint32_t tmem, int warp, int lane, int tl) {
     const int r = warp * 32 + lane;
+    const int row = tl * 128 + r;  // row of the group buffers
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_off + kSCol;
-    const uint32_t tO = tmem + lane_off;
+    __half* prow = p.p + static_cast<size_t>(row) * p.kcols;
     float m_run = -INFINITY, l = 0.f;
-    bool ok = true;
     for (int j = 0; j < p.nkb; ++j) {
-        if (!wwait_(s.s_full, static_cast<uint32_t>(j & 1), s, p)) {
-            ok = false;
-            break;
-        }
+        const int b = j & 1;
+        if (!wwait_(&s.s_full[b], static_cast<uint32_t>((j >> 1) & 1), s, p.status, p.timeout_ns)) return;
         tc_fence_after();
         float sv[128];
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
             uint32_t rr[16];
             __syncwarp();
-            tmem_ld16(tS + g * 16, rr);
+            tmem_ld16(tmem + lane_off + static_cast<uint32_t>(b * 128 + g * 16), rr);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) sv[g * 16 + i] = __uint_as_float(rr[i]);
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(s.s_free));
+        mbar_arrive(smem_u32(&s.s_free[b]));
         const int nvalid = min(128, p.m - j * 128);
         float mx = -INFINITY;
 #pragma unroll
@@ -272,52 +258,180 @@ __device__ void attn_softmax(const AttnParams& p, const ASmem& s, uint32_t tmem,
             m_run = mx;
             resc = true;
         }
-        // P and the O accumulator are free once PV(j-1) is done.
-        if (j >= 1 && !wwait_(&s.pv_done[(j - 1) & 1], static_cast<uint32_t>(((j - 1) >> 1) & 1), s, p)) {
-            ok = false;
-            break;
-        }
-        if (__any_sync(0xffffffffu, resc)) {
-            tc_fence_after();
-            for (int col = 0; col < p.dv; col += 16) {
-                uint32_t rr[16];
-                __syncwarp();
-                tmem_ld16(tO + col, rr);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-                tmem_st16(tO + col, rr);
-            }
-            tmem_st_wait();
+        const bool any = __any_sync(0xffffffffu, resc);
+        if (j >= 1) {
+            p.alpha[static_cast<size_t>(j) * p.grows + row] = alpha;
+            if (lane == 0) p.flags[(static_cast<size_t>(tl) * p.nkb + j) * 4 + warp] = any ? 1u : 0u;
         }
         l *= alpha;
         float sum = 0.f;
-        uint8_t* pb = s.p;
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {
-            uint32_t h[4];
+        for (int g = 0; g < 8; ++g) {
+            uint32_t h[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float a = exp2f(sv[g * 8 + 2 * i] - m_run);
-                const float b = exp2f(sv[g * 8 + 2 * i + 1] - m_run);
-                sum += a + b;
-                __half2 t = __floats2half2_rn(a, b);
+            for (int i = 0; i < 8; ++i) {
+                const float a = exp2f(sv[g * 16 + 2 * i] - m_run);
+                const float c = exp2f(sv[g * 16 + 2 * i + 1] - m_run);
+                sum += a + c;
+                __half2 t = __floats2half2_rn(a, c);
                 h[i] = *reinterpret_cast<uint32_t*>(&t);
             }
-            *reinterpret_cast<uint4*>(pb + (g >> 3) * 16384 + sw128_off(static_cast<uint32_t>(r), g & 7)) =
-                make_uint4(h[0], h[1], h[2], h[3]);
+            st_v8_b32(prow + j * 128 + g * 16, h);
         }
         l += sum;
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&s.p_full[j & 1]));
     }
-    if (!ok) return;
-    const int jl = p.nkb - 1;
-    if (!wwait_(&s.pv_done[jl & 1], static_cast<uint32_t>((jl >> 1) & 1), s, p)) return;
+    p.lsum[row] = l;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_scores_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                       const ScoreParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const ASmem s = carve_attn(smem_raw);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int tl = blockIdx.x;
+    const int q0 = (p.q_tile0 + tl) * 128;
+    if (threadIdx.x == 0) {
+        *s.abort_flag = 0;
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(&s.full[i]), 1u);
+            mbar_init(smem_u32(&s.empty[i]), 1u);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&s.s_full[i]), 1u);
+            mbar_init(smem_u32(&s.s_free[i]), 128u);
+        }
+        mbar_init(smem_u32(s.drain), 1u);
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(s.tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&mq);
+        tma_prefetch_desc(&mk);
+    }
+    tc_fence_before();
+    __syncthreads();
     tc_fence_after();
-    const float inv = 1.f / l;
-    const int q = q0 + r;
+    const uint32_t tmem = *s.tmem_slot;
+    if (warp < 4) {
+        scores_softmax(p, s, tmem, warp, lane, tl);
+    } else if (warp == 4) {
+        if (lane == 0) scores_producer(p, s, &mq, &mk, q0);
+    } else {
+        if (lane == 0) scores_mma(p, s, tmem);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ───────────────────────────── PV kernel ─────────────────────────────
+
+__device__ __forceinline__ bool flagged(const uint32_t* fl, int j) { return (fl[j >> 5] >> (j & 31)) & 1u; }
+
+__device__ void pv_producer(const PvParams& p, const ASmem& s, const CUtensorMap* mp, const CUtensorMap* mv, int tl,
+                            int d0) {
+    const uint64_t pol = policy_evict_normal();
+    const uint32_t tx = static_cast<uint32_t>(kPHalfBytes + p.vboxes * p.vbox_rows * 128);
+    Ring r;
+    for (int j = 0; j < p.nkb; ++j)
+        for (int half = 0; half < 2; ++half) {
+            if (!wait_(&s.empty[r.stage], r.phase ^ 1u, s, p.status, p.timeout_ns)) {
+                r.drain(s, p.status, p.timeout_ns);
+                return;
+            }
+            const uint32_t fb = smem_u32(&s.full[r.stage]);
+            mbar_arrive_expect_tx(fb, tx);
+            r.arm();
+            uint8_t* st = s.ring + r.stage * kStageBytes;
+            const int key0 = j * 128 + half * 64;
+            tma_load_2d(smem_u32(st), mp, fb, key0, tl * 128, pol);
+            for (int b = 0; b < p.vboxes; ++b)
+                tma_load_2d(smem_u32(st + kPHalfBytes + b * p.vbox_rows * 128), mv, fb, key0, d0 + b * p.vbox_rows,
+                            pol);
+            r.next();
+        }
+    r.drain(s, p.status, p.timeout_ns);
+}
+
+__device__ void pv_mma(const PvParams& p, const ASmem& s, uint32_t tmem, const uint32_t* fl) {
+    const int nsplit = p.dv > 256 ? 2 : 1;
+    const int ns = p.dv / nsplit;
+    const uint32_t id_o = idesc_f16_f32(128, ns);
+    Ring r;
+    uint32_t ev = 0;
+    bool ok = true;
+    for (int j = 0; j < p.nkb && ok; ++j) {
+        if (j >= 1 && flagged(fl, j)) {
+            // The row warps scale O by alpha_j once PV(j - 1) is done; both
+            // sides count these events in the same order.
+            umma_commit(smem_u32(s.resc_ready));
+            if (!wait_(s.scaled, ev & 1u, s, p.status, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            ++ev;
+            tc_fence_after();
+        }
+        for (int half = 0; half < 2; ++half) {
+            if (!wait_(&s.full[r.stage], r.phase, s, p.status, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint8_t* st = s.ring + r.stage * kStageBytes;
+            const uint64_t ad = sw128_kmajor_desc(smem_u32(st));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                for (int sp = 0; sp < nsplit; ++sp) {
+                    const uint64_t bd = sw128_kmajor_desc(smem_u32(st + kPHalfBytes + sp * ns * 128));
+                    umma_f16(tmem + static_cast<uint32_t>(sp * ns), ad + 2 * k, bd + 2 * k, id_o,
+                             (j | half | k) != 0 ? 1u : 0u);
+                }
+            umma_commit(smem_u32(&s.empty[r.stage]));
+            r.next();
+        }
+    }
+    if (ok) umma_commit(smem_u32(s.final));
+    mma_drain(s, p.status, p.timeout_ns);
+}
+
+__device__ void pv_rows(const PvParams& p, const ASmem& s, uint32_t tmem, const uint32_t* fl, int warp, int lane,
+                        int tl, int d0) {
+    const int r = warp * 32 + lane;
+    const int row = tl * 128 + r;
+    const uint32_t tO = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    uint32_t ev = 0;
+    for (int j = 1; j < p.nkb; ++j) {
+        if (!flagged(fl, j)) continue;
+        if (!wwait_(s.resc_ready, ev & 1u, s, p.status, p.timeout_ns)) return;
+        ++ev;
+        tc_fence_after();
+        const float alpha = p.alpha[static_cast<size_t>(j) * p.grows + row];
+        for (int col = 0; col < p.dv; col += 16) {
+            uint32_t rr[16];
+            __syncwarp();
+            tmem_ld16(tO + col, rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st16(tO + col, rr);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(s.scaled));
+    }
+    if (!wwait_(s.final, 0u, s, p.status, p.timeout_ns)) return;
+    tc_fence_after();
+    const float inv = 1.f / p.lsum[row];
+    const int q = (p.q_tile0 + tl) * 128 + r;
     for (int col = 0; col < p.dv; col += 16) {
         uint32_t rr[16];
         __syncwarp();
@@ -344,25 +458,24 @@ __device__ void attn_softmax(const AttnParams& p, const ASmem& s, uint32_t tmem,
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                const __grid_constant__ CUtensorMap mv, const AttnParams p) {
+    attn_pv_kernel(const __grid_constant__ CUtensorMap mp, const __grid_constant__ CUtensorMap mv, const PvParams p) {
     extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t fl[kMaxFlagWords];
     const ASmem s = carve_attn(smem_raw);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int q0 = (blockIdx.x / p.ndv) * 128;
+    const int tl = blockIdx.x / p.ndv;
     const int d0 = (blockIdx.x % p.ndv) * p.dv;
+    const int nwords = (p.nkb + 31) / 32;
+    for (int i = threadIdx.x; i < nwords; i += blockDim.x) fl[i] = 0u;
     if (threadIdx.x == 0) {
         *s.abort_flag = 0;
         for (int i = 0; i < kStages; ++i) {
             mbar_init(smem_u32(&s.full[i]), 1u);
             mbar_init(smem_u32(&s.empty[i]), 1u);
         }
-        mbar_init(smem_u32(s.s_full), 1u);
-        mbar_init(smem_u32(s.s_free), 128u);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&s.p_full[i]), 128u);
-            mbar_init(smem_u32(&s.pv_done[i]), 1u);
-        }
+        mbar_init(smem_u32(s.resc_ready), 1u);
+        mbar_init(smem_u32(s.scaled), 128u);
+        mbar_init(smem_u32(s.final), 1u);
         mbar_init(smem_u32(s.drain), 1u);
         fence_mbar_init();
     }
@@ -371,20 +484,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (warp == 4 && lane == 0) {
-        tma_prefetch_desc(&mq);
-        tma_prefetch_desc(&mk);
+        tma_prefetch_desc(&mp);
         tma_prefetch_desc(&mv);
+    }
+    __syncthreads();
+    // The tile's "some row rescaled at block j" flags, one bit per key block.
+    for (int j = 1 + threadIdx.x; j < p.nkb; j += blockDim.x) {
+        const uint4 f = *reinterpret_cast<const uint4*>(p.flags + (static_cast<size_t>(tl) * p.nkb + j) * 4);
+        if ((f.x | f.y | f.z | f.w) != 0u) atomicOr(&fl[j >> 5], 1u << (j & 31));
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s.tmem_slot;
     if (warp < 4) {
-        attn_softmax(p, s, tmem, warp, lane, q0, d0);
+        pv_rows(p, s, tmem, fl, warp, lane, tl, d0);
     } else if (warp == 4) {
-        if (lane == 0) attn_producer(p, s, &mq, &mk, &mv, q0, d0);
+        if (lane == 0) pv_producer(p, s, &mp, &mv, tl, d0);
     } else {
-        if (lane == 0) attn_mma(p, s, tmem);
+        if (lane == 0) pv_mma(p, s, tmem, fl);
     }
     tc_fence_before();
     __syncthreads();
@@ -397,14 +515,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 struct AttnLayout {
     int m_pad, ndv, dv;
-    size_t xn, q, k, vt, o, gn, total;
+    int qtiles, nkb, group;  // query tiles, key blocks, query tiles per scores/PV launch pair
+    size_t xn, q, k, vt, o, gn, p, alpha, lsum, flags, total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 int attn_layout(int m, int c, int groups, int norm_kind, AttnLayout* L) {
-    if (m < 1 || c < 16 || c % 16 != 0 || c > 2048)
-        return set_error(VAE_ERR_SHAPE, "mid_attention: m=%d c=%d (need c %% 16 == 0, 16 <= c <= 2048)", m, c);
+    if (m < 1 || m > kMaxFlagWords * 32 * 128 || c < 16 || c % 16 != 0 || c > 2048)
+        return set_error(VAE_ERR_SHAPE, "mid_attention: m=%d c=%d (need 1 <= m <= 2^20, c %% 16 == 0, 16 <= c <= 2048)",
+                         m, c);
+    L->qtiles = (m + 127) / 128;
+    L->nkb = L->qtiles;
+    {
+        const size_t row_block = static_cast<size_t>(128) * L->nkb * 128 * 2;  // P of one query tile
+        L->group = static_cast<int>(std::min<size_t>(L->qtiles, std::max<size_t>(1, kMaxPBytes / row_block)));
+    }
     L->m_pad = (m + 7) / 8 * 8;
     const int nchunk = (c + kMaxDv - 1) / kMaxDv;
     L->dv = ((c + nchunk - 1) / nchunk + 31) / 32 * 32;
@@ -427,34 +553,60 @@ int attn_layout(int m, int c, int groups, int norm_kind, AttnLayout* L) {
         if (rc != VAE_OK) return rc;
         off = align256(off + gp.bytes);
     }
+    const size_t grows = static_cast<size_t>(L->group) * 128;
+    L->p = off;
+    off = align256(off + grows * L->nkb * 128 * 2);
+    L->alpha = off;
+    off = align256(off + static_cast<size_t>(L->nkb) * grows * 4);
+    L->lsum = off;
+    off = align256(off + grows * 4);
+    L->flags = off;
+    off = align256(off + static_cast<size_t>(L->group) * L->nkb * 4 * 4);
     L->total = off;
     return VAE_OK;
 }
 
 }  // namespace
 
-int attn_core_run(const __half* q, const __half* k, const __half* vt, int m, int m_pad, int c, const float* bv,
-                  __half* out, cudaStream_t stream) {
+// o = softmax(q k^T / sqrt(c)) v + b_v (f16 [m][c]) with the scratch of L in ws.
+static int attn_core_run(const __half* q, const __half* k, const __half* vt, int m, int m_pad, int c, const float* bv,
+                         __half* out, const AttnLayout& L, uint8_t* ws, cudaStream_t stream) {
     int rc = check_device();
     if (rc != VAE_OK) return rc;
     DevStatus* st = device_status_ptr();
     if (st == nullptr) return VAE_ERR_CUDA;
-    AttnParams p{};
-    p.m = m;
-    p.c = c;
-    const int nchunk = (c + kMaxDv - 1) / kMaxDv;
-    p.dv = ((c + nchunk - 1) / nchunk + 31) / 32 * 32;
-    p.ndv = (c + p.dv - 1) / p.dv;
-    p.nkb = (m + 127) / 128;
-    p.nchunk_c = (c + 63) / 64;  // a partial last chunk reads TMA zero fill
-    p.vboxes = p.dv > 256 ? 2 : 1;
-    p.vbox_rows = p.dv / p.vboxes;
-    p.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c)));
-    p.bv = bv;
-    p.out = out;
-    p.status = st;
-    p.timeout_ns = wait_timeout_ns();
-    CUtensorMap mq{}, mk{}, mv{};
+    const int grows = L.group * 128;
+    const int kcols = L.nkb * 128;
+    ScoreParams sp{};
+    sp.m = m;
+    sp.nkb = L.nkb;
+    sp.nchunk_c = (c + 63) / 64;  // a partial last chunk reads TMA zero fill
+    sp.kcols = kcols;
+    sp.grows = grows;
+    sp.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(c)));
+    sp.p = reinterpret_cast<__half*>(ws + L.p);
+    sp.alpha = reinterpret_cast<float*>(ws + L.alpha);
+    sp.lsum = reinterpret_cast<float*>(ws + L.lsum);
+    sp.flags = reinterpret_cast<uint32_t*>(ws + L.flags);
+    sp.status = st;
+    sp.timeout_ns = wait_timeout_ns();
+    PvParams pp{};
+    pp.m = m;
+    pp.c = c;
+    pp.dv = L.dv;
+    pp.ndv = L.ndv;
+    pp.nkb = L.nkb;
+    pp.grows = grows;
+    pp.vboxes = L.dv > 256 ? 2 : 1;
+    pp.vbox_rows = L.dv / pp.vboxes;
+    pp.alpha = sp.alpha;
+    pp.lsum = sp.lsum;
+    pp.flags = sp.flags;
+    pp.bv = bv;
+    pp.out = out;
+    pp.status = st;
+    pp.timeout_ns = sp.timeout_ns;
+    CUtensorMap mq{}, mk{}, mp{}, mv{};
     {
         const uint64_t dims[2] = {static_cast<uint64_t>(c), static_cast<uint64_t>(m)};
         const uint64_t strides[1] = {static_cast<uint64_t>(c) * 2};
@@ -465,24 +617,40 @@ int attn_core_run(const __half* q, const __half* k, const __half* vt, int m, int
         if (rc != VAE_OK) return rc;
     }
     {
+        const uint64_t dims[2] = {static_cast<uint64_t>(kcols), static_cast<uint64_t>(grows)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(kcols) * 2};
+        const uint32_t box[2] = {64u, 128u};
+        rc = encode_tiled(&mp, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, sp.p, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != VAE_OK) return rc;
+    }
+    {
         const uint64_t dims[2] = {static_cast<uint64_t>(m_pad), static_cast<uint64_t>(c)};
         const uint64_t strides[1] = {static_cast<uint64_t>(m_pad) * 2};
-        const uint32_t box[2] = {64u, static_cast<uint32_t>(p.vbox_rows)};
+        const uint32_t box[2] = {64u, static_cast<uint32_t>(pp.vbox_rows)};
         rc = encode_tiled(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, vt, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != VAE_OK) return rc;
     }
-    const size_t smem = 1024 + kStages * kStageBytes + kPBytes + 256;
+    const size_t smem = 1024 + kStages * kStageBytes + 256;
     static bool attr_set[64] = {false};
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        VAE_CUDA_CHECK(cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        VAE_CUDA_CHECK(cudaFuncSetAttribute(attn_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(smem)));
+        VAE_CUDA_CHECK(cudaFuncSetAttribute(attn_pv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(smem)));
         attr_set[dev] = true;
     }
-    const long long grid = static_cast<long long>((m + 127) / 128) * p.ndv;
-    attn_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(mq, mk, mv, p);
-    VAE_CUDA_CHECK(cudaGetLastError());
+    for (int t0 = 0; t0 < L.qtiles; t0 += L.group) {
+        const int nt = std::min(L.group, L.qtiles - t0);
+        sp.q_tile0 = t0;
+        pp.q_tile0 = t0;
+        attn_scores_kernel<<<static_cast<unsigned>(nt), kThreads, smem, stream>>>(mq, mk, sp);
+        VAE_CUDA_CHECK(cudaGetLastError());
+        attn_pv_kernel<<<static_cast<unsigned>(nt * L.ndv), kThreads, smem, stream>>>(mp, mv, pp);
+        VAE_CUDA_CHECK(cudaGetLastError());
+    }
     return VAE_OK;
 }
 
@@ -550,7 +718,7 @@ int attn_run(float* x, int m, int c, int norm_kind, int groups, float eps, const
     a.bias = nullptr;
     a.y = vt;
     if ((rc = conv_run(a, stream)) != VAE_OK) return rc;
-    if ((rc = attn_core_run(q, k, vt, m, L.m_pad, c, bv, o, stream)) != VAE_OK) return rc;
+    if ((rc = attn_core_run(q, k, vt, m, L.m_pad, c, bv, o, L, w8, stream)) != VAE_OK) return rc;
     // x += o W_o^T + b_o
     ConvArgs pr{};
     pr.taps = 1;

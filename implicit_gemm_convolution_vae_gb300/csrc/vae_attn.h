@@ -9,7 +9,5 @@ int attn_workspace_bytes(int m, int c, int groups, int norm_kind, size_t* bytes)
 int attn_run(float* x, int m, int c, int norm_kind, int groups, float eps, const float* gamma, const float* beta,
              const void* wq, const float* bq, const void* wk, const float* bk, const void* wv, const float* bv,
              const void* wo, const float* bo, void* ws, size_t ws_bytes, cudaStream_t stream);
-int attn_core_run(const __half* q, const __half* k, const __half* vt, int m, int m_pad, int c, const float* bv,
-                  __half* out, cudaStream_t stream);
 
 }  // namespace vae

@@ -37,14 +37,14 @@ composition of pinned parts: parity unpinned against any outside
 implementation (no trained weights or third-party decoder exist here).
 """
 from .ops import (conv2d, conv2d_at, upsample2x, silu, group_norm, rms_norm, dupup,
-                  attention, linear_tokens)
+                  attention, attention_rows, linear_tokens)
 from .decoder import (resnet, up_block, decode_gn, decode_rms, decode, Rows, grow, half,
                       levels, plan_band, plan_bands, decode_rms_banded, head_rms,
                       run_blocks_window, output_rows_window)
 
 __all__ = [
     "conv2d", "conv2d_at", "upsample2x", "silu", "group_norm", "rms_norm", "dupup",
-    "attention", "linear_tokens", "resnet", "up_block", "decode_gn", "decode_rms", "decode",
+    "attention", "attention_rows", "linear_tokens", "resnet", "up_block", "decode_gn", "decode_rms", "decode",
     "Rows", "grow", "half", "levels", "plan_band", "plan_bands", "decode_rms_banded",
     "head_rms", "run_blocks_window", "output_rows_window",
 ]

@@ -221,3 +221,31 @@ def attention(x, attn, family: str, groups: int = 32, eps: float = 1e-6,
         o[r0:r0 + chunk] = p @ v
     y = linear_tokens(o, attn.o)
     return x + y.T.reshape(c, h, w)
+
+
+def attention_rows(x, attn, family: str, rows, groups: int = 32, eps: float = 1e-6):
+    """``attention`` evaluated only at the query tokens ``rows`` (all keys).
+
+    Same definition as ``attention`` (``vae.rs``, ``AttnBlock::apply`` /
+    ``finish``; ``qi21_vae.rs``, ``fn attention``); for sampling outputs of
+    token counts whose full score matrix is too large to form here.
+    ``x``: [c][h][w]; returns [len(rows)][c] (token-major rows of the output).
+    """
+    x = _f64(x)
+    c, h, w = x.shape
+    m = h * w
+    rows = np.asarray(rows, dtype=np.int64)
+    if family == "gn":
+        n = group_norm(x, groups, attn.norm.gamma, attn.norm.beta, eps)
+    else:
+        n = rms_norm(x, attn.norm.gamma)
+    t = n.reshape(c, m).T
+    q = linear_tokens(t[rows], attn.q)
+    k = linear_tokens(t, attn.k)
+    v = linear_tokens(t, attn.v)
+    s = (q @ k.T) / np.sqrt(float(c))
+    s = s - s.max(axis=1, keepdims=True)
+    p = np.exp(s)
+    p = p / p.sum(axis=1, keepdims=True)
+    y = linear_tokens(p @ v, attn.o)
+    return x.reshape(c, m).T[rows] + y

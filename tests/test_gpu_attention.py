@@ -58,10 +58,12 @@ def test_mid_attention_full_size_qwen_mid():
     assert rel_err(got - x, ref - x) <= ATTN_TOL
 
 
-def test_peaked_softmax_rescales():
-    """Scores that grow block after block force the lazy O rescale path."""
-    m, c = 1024, 128
-    x = stream_normal(22, "attn.peak.x", (m, c))
+@pytest.mark.parametrize("c", [128, 512, 1152])
+def test_peaked_softmax_rescales(c):
+    """Scores that grow block after block force the lazy O rescale path (with
+    one, two and three value-channel chunks sharing the rescale flags)."""
+    m = 1024
+    x = stream_normal(22, f"attn.peak.x.{c}", (m, c))
     x = x + np.linspace(0, 40, m, dtype=np.float32)[:, None] * x[:, :1]
     a = _attn(22, c, "rms")
     a.q = Conv(w=(a.q.w.astype(np.float32) * 4).astype(np.float16), b=a.q.b)
@@ -70,3 +72,18 @@ def test_peaked_softmax_rescales():
     # Logits here reach the hundreds, so the f16 rounding of q and k moves them by
     # up to |s| * 2^-10 and the sharply peaked softmax passes that on: 1e-2.
     assert rel_err(got - x, ref - x) <= 1e-2
+
+
+def test_mid_attention_two_query_groups():
+    """m = 33000 tokens (258 query tiles, the last one 104 rows): the
+    probabilities of all query tiles exceed the 2 GiB workspace cap, so the
+    tiles run as two groups (254 + 4); outputs sampled per row (first and last
+    rows of both groups and of the ragged last tile)."""
+    m, c = 33000, 64
+    x = stream_normal(23, "attn.groups.x", (m, c))
+    a = _attn(23, c, "rms")
+    got = run_gpu(x, a, "rms")
+    rows = [0, 1, 127, 128, 254 * 128 - 1, 254 * 128, 254 * 128 + 5, 257 * 128, m - 1]
+    ref = oracle.attention_rows(x.T.reshape(c, m, 1), a, "rms", rows)
+    assert np.isfinite(got).all()
+    assert rel_err(got[rows] - x[rows], ref - x[rows]) <= ATTN_TOL

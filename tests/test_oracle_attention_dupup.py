@@ -2,7 +2,8 @@
 
 Attention: a single token attends to itself (o = v); identical keys give a
 uniform softmax (o = mean of v); a per-query constant added to every score
-(a key bias) changes nothing; and a brute-force per-row loop on a tiny case.
+(a key bias) changes nothing; a brute-force per-row loop on a tiny case; and
+the row-sampled form agrees with the whole-matrix form on every sampled row.
 DupUp: a brute-force loop over the printed index formula, and the mass
 invariant (each source channel feeds ``repeats`` outputs per source pixel).
 """
@@ -62,6 +63,18 @@ def test_score_shift_invariance():
     a.k = Conv(w=a.k.w, b=a.k.b + rng.standard_normal(c) * 3.0)  # adds q_i.delta to row i
     y2 = oracle.attention(x, a, "gn", groups=4)
     np.testing.assert_allclose(y1, y2, rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("family", ["gn", "rms"])
+def test_attention_rows_matches_whole_attention(family):
+    rng = np.random.default_rng(25)
+    c, h, w = 8, 5, 7
+    a = _attn(rng, c, family)
+    x = rng.standard_normal((c, h, w)) * 2.0
+    whole = oracle.attention(x, a, family, groups=4, chunk=4).reshape(c, -1).T
+    rows = [0, 3, 17, 34, 20]
+    got = oracle.attention_rows(x, a, family, rows, groups=4)
+    np.testing.assert_allclose(got, whole[rows], rtol=1e-12, atol=1e-12)
 
 
 def test_attention_brute_force_rows():

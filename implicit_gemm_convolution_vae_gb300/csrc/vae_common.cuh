@@ -359,6 +359,18 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// The same for a K-major tile whose rows are 32 bytes (16 f16 of K) with
+// the 32-byte swizzle: 8-row groups 256 B apart, swizzle code 6.
+__device__ __forceinline__ uint64_t sw32_kmajor_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);     // start address
+    d |= static_cast<uint64_t>(16u >> 4) << 16;               // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(256u >> 4) << 32;              // stride byte offset
+    d |= static_cast<uint64_t>(1u) << 46;                     // descriptor version (fixed 0b001)
+    d |= static_cast<uint64_t>(6u) << 61;                     // swizzle: 32 B
+    return d;
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16: A, B f16, D f32, both
 // K-major, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {

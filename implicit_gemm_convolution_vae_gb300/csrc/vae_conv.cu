@@ -47,6 +47,8 @@ constexpr int kMaxAStages = 4;       // A halo ring slots (halo mode)
 constexpr int kHaloRows = 130;       // one output row segment of 128 pixels + a pixel each side
 constexpr int kHaloBytes = 17408;    // 130 rows x 128 B, rounded up to 1024 B
 constexpr int kTail = 512;           // barriers, TMEM slot and abort flag
+constexpr int kRemAStride = 4352;    // one 16-channel halo box (130 rows x 32 B), rounded up to 256 B
+constexpr uint32_t kRemABytes = kHaloRows * 32;
 
 // Kernel variants: A tile per tap by TMA; A tile per tap by gather threads
 // (replicate padding); one A "halo" box per (ky, chunk) shared by the three
@@ -67,6 +69,8 @@ struct ConvParams {
     int tiles_x, tiles_y, npar;
     int n_tiles, BN, acc_stride;
     int kchunks, total_tiles, stages;
+    int rem16, kfull;     // three-tap halo stages with cin % 64 == 16: kfull 64-channel chunks, then one
+                          // stage of 16-channel boxes (32-byte swizzle) for all three ky and nine taps
     int halo, a_stages;   // halo mode: a_stages halo boxes; B ring of `stages` x ks taps
                           // (ks == 3: box slot i belongs to stage i, one barrier pair)
     int ks;               // K chunks per pipeline stage (1 or 2; per-tap A path only)
@@ -182,7 +186,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 template <int kMode>
 __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensorMap* mapA,
-                              const CUtensorMap* mapB) {
+                              const CUtensorMap* mapB, const CUtensorMap* mapA16, const CUtensorMap* mapB16) {
     const uint64_t pol_w = policy_evict_last();
     const uint64_t pol_a = policy_evict_normal();
     const uint32_t b_bytes = static_cast<uint32_t>(p.BN) * 128u;
@@ -226,9 +230,10 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
             // one stage = the halo box of (ky, chunk) and the three kx taps' weights
             const int q = ti.par >> 1, pp = ti.par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
+            const int kc_end = p.rem16 ? p.kfull : p.kchunks;
             for (int ky = 0; ky < 3 && ok; ++ky) {
                 const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
-                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                for (int kc = 0; kc < kc_end && ok; ++kc) {
                     uint32_t slot;
                     const uint32_t fb = next_b(p.a_tx + 3u * b_bytes, &slot);
                     if (!ok) break;
@@ -237,6 +242,21 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
                     for (int kx = 0; kx < 3; ++kx)
                         tma_load_3d(smem_u32(s.b + (slot * 3 + kx) * p.BN * 128), mapB, fb, kc * kBK, ky * 3 + kx,
                                     ti.n0, pol_w);
+                }
+            }
+            if (p.rem16 && ok) {
+                // the last 16 channels of all three ky and nine taps in one stage
+                uint32_t slot;
+                const uint32_t fb = next_b(3u * kRemABytes + 9u * static_cast<uint32_t>(p.BN) * 32u, &slot);
+                if (ok) {
+                    for (int ky = 0; ky < 3; ++ky) {
+                        const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                        tma_load_4d(smem_u32(s.a + slot * kHaloBytes + ky * kRemAStride), mapA16, fb, p.kfull * kBK,
+                                    ti.u0 + dxmin, ti.v0 + dy, ti.img, pol_a);
+                    }
+                    for (int tap = 0; tap < 9; ++tap)
+                        tma_load_3d(smem_u32(s.b + slot * 3 * p.BN * 128 + tap * p.BN * 32), mapB16, fb, p.kfull * kBK,
+                                    tap, ti.n0, pol_w);
                 }
             }
         } else if (kMode == kModeHalo) {
@@ -389,8 +409,9 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
         if (p.halo && p.ks == 3) {
             const int pp = decode_tile(p, t).par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
+            const int kc_end = p.rem16 ? p.kfull : p.kchunks;
             for (int ky = 0; ky < 3 && ok; ++ky) {
-                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                for (int kc = 0; kc < kc_end && ok; ++kc) {
                     if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
                                    kWhereMmaFull)) {
                         ok = false;
@@ -419,6 +440,34 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
                                          (kit | kx | k) != 0 ? 1u : 0u);
                         }
                     }
+                    umma_commit(smem_u32(&s.empty[stage]));
+                    ++kit;
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (p.rem16 && ok) {
+                if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                               kWhereMmaFull)) {
+                    ok = false;
+                } else {
+                    tc_fence_after();
+                    // one K = 16 step per tap; the 64-channel chunks came first, so always accumulate
+                    const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
+                    const uint32_t bbase = smem_u32(s.b + stage * 3 * p.BN * 128);
+#pragma unroll
+                    for (int ky = 0; ky < 3; ++ky)
+#pragma unroll
+                        for (int kx = 0; kx < 3; ++kx) {
+                            const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
+                            const uint64_t ad = sw32_kmajor_desc(abase + static_cast<uint32_t>(ky * kRemAStride) +
+                                                                 static_cast<uint32_t>((dx - dxmin) * 32));
+                            const uint64_t bd =
+                                sw32_kmajor_desc(bbase + static_cast<uint32_t>((ky * 3 + kx) * p.BN * 32));
+                            umma_f16(d, ad, bd, idesc, 1u);
+                        }
                     umma_commit(smem_u32(&s.empty[stage]));
                     ++kit;
                     if (++stage == p.stages) {
@@ -754,6 +803,7 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
 template <int kMode>
 __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     conv_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                const __grid_constant__ CUtensorMap mapA16, const __grid_constant__ CUtensorMap mapB16,
                 const ConvParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve(smem_raw, p);
@@ -790,6 +840,10 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     if (warp == kProducerWarp && lane == 0) {
         if (kMode != kModeGather) tma_prefetch_desc(&mapA);
         tma_prefetch_desc(&mapB);
+        if (p.rem16) {
+            tma_prefetch_desc(&mapA16);
+            tma_prefetch_desc(&mapB16);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -799,7 +853,7 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     if (warp < kEpiWarps) {
         role_epilogue<kMode>(p, s, tmem_base, warp, lane);
     } else if (warp == kProducerWarp) {
-        if (lane == 0) role_producer<kMode>(p, s, &mapA, &mapB);
+        if (lane == 0) role_producer<kMode>(p, s, &mapA, &mapB, &mapA16, &mapB16);
     } else if (warp == kMmaWarp) {
         if (lane == 0) role_mma(p, s, tmem_base);
     } else if (kMode == kModeGather && warp >= kGatherWarp0) {
@@ -874,7 +928,35 @@ __device__ void pair_producer(const ConvParams& p, const Smem& s, const CUtensor
     };
     for (int t = blockIdx.x >> 1; t < p.pair_tiles && ok; t += gridDim.x >> 1) {
         const TileInfo ti = decode_pair_tile(p, t, rank);
-        if (kMode == kModeHalo) {
+        if (p.res_prefetch && ti.v0 < p.hv) {
+            const int npx = min(p.Wt, p.wv - ti.u0);
+            const long long pix0 = (static_cast<long long>(ti.img) * p.H + ti.v0) * p.W + ti.u0;
+            prefetch_l2_bulk(p.residual + pix0 * p.cout, static_cast<uint32_t>(npx * p.cout * 4));
+        }
+        if (p.dup_prefetch && ti.v0 < p.hv) {
+            const int npx = min(p.Wt, p.wv - ti.u0);
+            const long long pix0 = (static_cast<long long>(ti.img) * p.hv + ti.v0) * p.wv + ti.u0;
+            prefetch_l2_bulk(p.dup_src + pix0 * p.dup_cin, static_cast<uint32_t>(npx * p.dup_cin * 4));
+        }
+        if (kMode == kModeHalo && p.ks == 3) {
+            // one stage = this CTA's halo box of (ky, chunk) and its half of the
+            // three kx taps' weights
+            const int q = ti.par >> 1, pp = ti.par & 1;
+            const int dxmin = (p.up && pp == 1) ? 0 : -1;
+            for (int ky = 0; ky < 3 && ok; ++ky) {
+                const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                    uint32_t slot;
+                    const uint32_t fb = next_b(p.a_tx + 3u * b_bytes, &slot);
+                    if (!ok) break;
+                    tma_load_4d_pair(smem_u32(s.a + slot * kHaloBytes), mapA, fb, kc * kBK, ti.u0 + dxmin, ti.v0 + dy,
+                                     ti.img, pol_a);
+                    for (int kx = 0; kx < 3; ++kx)
+                        tma_load_3d_pair(smem_u32(s.b + (slot * 3 + kx) * p.b_rows * 128), mapB, fb, kc * kBK,
+                                         ky * 3 + kx, ti.n0 + boff, pol_w);
+                }
+            }
+        } else if (kMode == kModeHalo) {
             const int q = ti.par >> 1, pp = ti.par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             for (int ky = 0; ky < 3 && ok; ++ky) {
@@ -966,7 +1048,37 @@ __device__ void pair_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
         int kit = 0;
-        if (p.halo) {
+        if (p.halo && p.ks == 3) {
+            const int pp = decode_pair_tile(p, t, 0).par & 1;
+            const int dxmin = (p.up && pp == 1) ? 0 : -1;
+            for (int ky = 0; ky < 3 && ok; ++ky)
+                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                    if (!mbar_wait_cluster(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                                           kWhereMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nk = min(4, (p.cin - kc * kBK) / 16);
+                    const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
+                    const uint32_t bbase = smem_u32(s.b + stage * 3 * p.b_rows * 128);
+#pragma unroll
+                    for (int kx = 0; kx < 3; ++kx) {
+                        const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
+                        const uint64_t ad = sw128_kmajor_desc(abase + static_cast<uint32_t>((dx - dxmin) * 128));
+                        const uint64_t bd = sw128_kmajor_desc(bbase + static_cast<uint32_t>(kx * p.b_rows * 128));
+                        for (int k = 0; k < nk; ++k)
+                            umma_f16_pair(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                                          (kit | kx | k) != 0 ? 1u : 0u);
+                    }
+                    umma_commit_pair(smem_u32(&s.empty[stage]));
+                    ++kit;
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+        } else if (p.halo) {
             const int pp = decode_pair_tile(p, t, 0).par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             for (int ky = 0; ky < 3 && ok; ++ky)
@@ -1051,7 +1163,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
             mbar_init(smem_u32(&s.full[i]), fullc);
             mbar_init(smem_u32(&s.empty[i]), 1u);
         }
-        if (kMode == kModeHalo)
+        if (kMode == kModeHalo && p.ks != 3)  // the separate halo-box ring
             for (int i = 0; i < p.a_stages; ++i) {
                 mbar_init(smem_u32(&s.afull[i]), fullc);
                 mbar_init(smem_u32(&s.aempty[i]), 1u);
@@ -1156,8 +1268,8 @@ int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& m
 }
 
 template <int kMode>
-int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, size_t smem, int grid,
-           cudaStream_t stream) {
+int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma16,
+           const CUtensorMap& mb16, size_t smem, int grid, cudaStream_t stream) {
     static bool attr_set[64] = {false};
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
@@ -1166,7 +1278,7 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, si
             cudaFuncSetAttribute(conv_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set[dev] = true;
     }
-    conv_kernel<kMode><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, p);
+    conv_kernel<kMode><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, ma16, mb16, p);
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -1306,7 +1418,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.status = st;
     p.timeout_ns = wait_timeout_ns();
 
-    CUtensorMap ma{}, mb{};
+    CUtensorMap ma{}, mb{}, ma16{}, mb16{};
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(a.taps),
                                   static_cast<uint64_t>(a.cout)};
@@ -1340,6 +1452,24 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                 p.ks = 3;
                 p.stages = std::min(kMaxStages, st3);
                 p.a_stages = p.stages;
+                if (a.cin % kBK == 16 && a.cin > kBK) {
+                    // exact 16-channel boxes for the remainder instead of zero-filled 64-channel ones
+                    const uint32_t box16[4] = {16u, static_cast<uint32_t>(kHaloRows), 1u, 1u};
+                    const uint64_t bdims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(a.taps),
+                                               static_cast<uint64_t>(a.cout)};
+                    const uint64_t bstrides[2] = {static_cast<uint64_t>(a.cin) * 2,
+                                                  static_cast<uint64_t>(a.taps) * a.cin * 2};
+                    const uint32_t bbox16[3] = {16u, 1u, static_cast<uint32_t>(p.BN)};
+                    if (encode_tiled(&ma16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.x, dims, strides, box16,
+                                     CU_TENSOR_MAP_SWIZZLE_32B) == VAE_OK &&
+                        encode_tiled(&mb16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, bdims, bstrides, bbox16,
+                                     CU_TENSOR_MAP_SWIZZLE_32B) == VAE_OK) {
+                        p.rem16 = 1;
+                        p.kfull = a.cin / kBK;
+                    } else {
+                        clear_error();
+                    }
+                }
             } else {
                 p.ks = 1;
                 p.a_stages = 3;
@@ -1371,6 +1501,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2) {
         // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
         p.pair = 1;
+        p.rem16 = 0;  // the pair kernel loads zero-filled 64-channel remainder boxes
         p.ks = 1;
         p.b_rows = p.BN / 2;
         p.typ_tiles = (p.tiles_y + 1) / 2;
@@ -1385,7 +1516,13 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                           CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != VAE_OK) return rc;
         size_t smem;
-        if (mode == kModeHalo) {
+        const int pst3 = (kMaxSmem - 1024 - kTail) / (kHaloBytes + 3 * p.b_rows * 128);
+        if (mode == kModeHalo && pst3 >= 3) {
+            p.ks = 3;  // three-tap stages, as in the single-CTA kernel
+            p.stages = std::min(kMaxStages, pst3);
+            p.a_stages = p.stages;
+            smem = 1024 + static_cast<size_t>(p.stages) * (kHaloBytes + 3 * p.b_rows * 128) + kTail;
+        } else if (mode == kModeHalo) {
             p.a_stages = 4;
             p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail - p.a_stages * kHaloBytes) / (p.b_rows * 128));
             smem = 1024 + static_cast<size_t>(p.a_stages) * kHaloBytes + static_cast<size_t>(p.stages) * p.b_rows * 128 +
@@ -1403,9 +1540,9 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                             ? 1024 + static_cast<size_t>(p.a_stages) * kHaloBytes +
                                   static_cast<size_t>(p.stages) * p.ks * p.BN * 128 + kTail
                             : 1024 + static_cast<size_t>(p.stages) * p.ks * (kABytes + p.BN * 128) + kTail;
-    if (mode == kModeHalo) return launch<kModeHalo>(p, ma, mb, smem, grid, stream);
-    if (mode == kModeGather) return launch<kModeGather>(p, ma, mb, smem, grid, stream);
-    return launch<kModeTma>(p, ma, mb, smem, grid, stream);
+    if (mode == kModeHalo) return launch<kModeHalo>(p, ma, mb, ma16, mb16, smem, grid, stream);
+    if (mode == kModeGather) return launch<kModeGather>(p, ma, mb, ma, mb, smem, grid, stream);
+    return launch<kModeTma>(p, ma, mb, ma, mb, smem, grid, stream);
 }
 
 }  // namespace vae

@@ -71,6 +71,10 @@ SHAPES = [
     (1, 3, 256, 64, 3),
     (1, 4, 130, 144, 288),
     (1, 9, 40, 80, 320),
+    # cin % 64 == 16 on rows of >= 128 pixels: the 16-channel remainder stage
+    (1, 6, 200, 80, 64),
+    (2, 5, 128, 208, 144),
+    (1, 3, 300, 144, 3),
 ]
 
 

@@ -49,6 +49,7 @@ constexpr int kHaloBytes = 17408;    // 130 rows x 128 B, rounded up to 1024 B
 constexpr int kTail = 512;           // barriers, TMEM slot and abort flag
 constexpr int kRemAStride = 4352;    // one 16-channel halo box (130 rows x 32 B), rounded up to 256 B
 constexpr uint32_t kRemABytes = kHaloRows * 32;
+constexpr int kStgBytes = 2048;      // 32 pixels x 16 f32 channels, 64-byte swizzle
 
 // Kernel variants: A tile per tap by TMA; A tile per tap by gather threads
 // (replicate padding); one A "halo" box per (ky, chunk) shared by the three
@@ -88,6 +89,7 @@ struct ConvParams {
     int dup_step;         // DupUp: source channel = dup_base[2q+p] + dup_step * o (1 or 2), or 0
     int dup_base[4];
     int v8_ok;            // f32 y / residual rows 32-byte aligned: 32-byte accesses
+    int epi_tma;          // epilogue writes through staged TMA boxes: 1 store, 2 add onto y (residual == y)
     // NCHW output of kept rows (conv_out): rows [keep_lo, keep_hi) land at
     // destination row (Y - keep_lo + dst_row0) of planes `plane` floats apart.
     int out_nchw, keep_lo, keep_hi, dst_row0;
@@ -145,6 +147,7 @@ __device__ __forceinline__ void tap_offset(const ConvParams& p, int tap, int par
 struct Smem {
     uint8_t* a;          // stages x 16 KB, or (halo mode) a_stages x kHaloBytes
     uint8_t* b;          // stages x BN*128 B
+    uint8_t* stg;        // epilogue staging, 2 KB per epilogue warp (epi_tma)
     uint64_t* full;      // [stages]
     uint64_t* empty;     // [stages]
     uint64_t* afull;     // [a_stages] (halo mode)
@@ -161,7 +164,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.a = base;
     s.b = base + (p.halo ? p.a_stages * kHaloBytes : p.stages * p.ks * kABytes);
-    uint8_t* tail = s.b + p.stages * p.ks * p.b_rows * 128;
+    s.stg = s.b + p.stages * p.ks * p.b_rows * 128;
+    uint8_t* tail = s.stg + (p.epi_tma ? kEpiWarps * kStgBytes : 0);
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
     s.full = bars;
     s.empty = bars + kMaxStages;
@@ -589,7 +593,7 @@ __device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInf
     if (pre_res != nullptr) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) val[i] += pre_res[i];
-    } else if (p.residual != nullptr) {
+    } else if (p.residual != nullptr && p.epi_tma != 2) {
         const float* rs = p.residual + pix * p.cout + o0;
         if (full && p.v8_ok) {
             float r8[16];
@@ -768,8 +772,50 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
     }
 }
 
+// Epilogue of one accumulator row through TMA: each warp stages its 32 pixels x
+// 16 channels (64-byte swizzle) and one lane issues a bulk tensor store, or an
+// f32 add onto y when y is the residual (the add then happens in L2: y + (acc *
+// oscale + bias), the same two roundings as the register path). No global
+// loads or per-lane stores: the warp's traffic is whole 2 KB boxes.
+__device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, int v, int u,
+                                                 long long pix, uint8_t* stg, const CUtensorMap* mapY, int ew,
+                                                 int lane) {
+    const uint32_t sbase = smem_u32(stg + ew * kStgBytes);
+    const int seg = ti.u0 + ew * 32;  // first pixel of this warp's 32 (warp-uniform)
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 64u;
+    const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+    for (int c = 0; c < p.BN / 16; ++c) {
+        uint32_t acc[16];
+        __syncwarp();
+        tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
+        tmem_ld_wait();
+        const int o0 = ti.n0 + c * 16;
+        if (o0 >= p.cout) break;  // warp-uniform
+        float val[16];
+        compute_chunk(p, ti, acc, o0, v, u, 0, 0, pix, val);
+        if (lane == 0) bulk_wait_read_all();  // the previous box left this warp's buffer
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + row_off +
+                                                                        ((static_cast<uint32_t>(k) ^ sw) << 4)),
+                         "f"(val[4 * k]), "f"(val[4 * k + 1]), "f"(val[4 * k + 2]), "f"(val[4 * k + 3])
+                         : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && seg < p.wv) {
+            if (p.epi_tma == 2)
+                tma_reduce_add_4d(mapY, sbase, o0, seg, ti.v0, ti.img);
+            else
+                tma_store_4d(mapY, sbase, o0, seg, ti.v0, ti.img);
+            bulk_commit_group();
+        }
+    }
+}
+
 template <int kMode>
-__device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane) {
+__device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane,
+                              const CUtensorMap* mapY) {
     const int row = ew * 32 + lane;
     int accbuf = 0;
     uint32_t accphase = 0;
@@ -790,6 +836,8 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
             tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
         if (p.rms_out != nullptr) {
             epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
+        } else if (kMode != kModeGather && p.epi_tma) {
+            epilogue_tma_row(p, ti, tbase, v, u, pix, s.stg, mapY, ew, lane);
         } else {
             epilogue_plain_row<kMode != kModeGather>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         }
@@ -798,13 +846,14 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         accbuf ^= 1;
         if (accbuf == 0) accphase ^= 1u;
     }
+    if (p.epi_tma && lane == 0) bulk_wait_all();  // boxes read and written before the CTA exits
 }
 
 template <int kMode>
 __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     conv_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapA16, const __grid_constant__ CUtensorMap mapB16,
-                const ConvParams p) {
+                const __grid_constant__ CUtensorMap mapY, const ConvParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve(smem_raw, p);
     const int warp = threadIdx.x / 32;
@@ -844,6 +893,7 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
             tma_prefetch_desc(&mapA16);
             tma_prefetch_desc(&mapB16);
         }
+        if (p.epi_tma) tma_prefetch_desc(&mapY);
     }
     tc_fence_before();
     __syncthreads();
@@ -851,7 +901,7 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     const uint32_t tmem_base = *s.tmem_slot;
 
     if (warp < kEpiWarps) {
-        role_epilogue<kMode>(p, s, tmem_base, warp, lane);
+        role_epilogue<kMode>(p, s, tmem_base, warp, lane, &mapY);
     } else if (warp == kProducerWarp) {
         if (lane == 0) role_producer<kMode>(p, s, &mapA, &mapB, &mapA16, &mapB16);
     } else if (warp == kMmaWarp) {
@@ -1269,7 +1319,7 @@ int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& m
 
 template <int kMode>
 int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma16,
-           const CUtensorMap& mb16, size_t smem, int grid, cudaStream_t stream) {
+           const CUtensorMap& mb16, const CUtensorMap& my, size_t smem, int grid, cudaStream_t stream) {
     static bool attr_set[64] = {false};
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
@@ -1278,7 +1328,7 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, co
             cudaFuncSetAttribute(conv_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set[dev] = true;
     }
-    conv_kernel<kMode><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, ma16, mb16, p);
+    conv_kernel<kMode><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, ma16, mb16, my, p);
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -1418,7 +1468,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.status = st;
     p.timeout_ns = wait_timeout_ns();
 
-    CUtensorMap ma{}, mb{}, ma16{}, mb16{};
+    CUtensorMap ma{}, mb{}, ma16{}, mb16{}, my{};
     {
         const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(a.taps),
                                   static_cast<uint64_t>(a.cout)};
@@ -1502,6 +1552,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
         p.pair = 1;
         p.rem16 = 0;  // the pair kernel loads zero-filled 64-channel remainder boxes
+        p.epi_tma = 0;
         p.ks = 1;
         p.b_rows = p.BN / 2;
         p.typ_tiles = (p.tiles_y + 1) / 2;
@@ -1536,13 +1587,30 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         return mode == kModeHalo ? launch_pair<kModeHalo>(p, ma, mb, smem, pgrid, stream)
                                  : launch_pair<kModeTma>(p, ma, mb, smem, pgrid, stream);
     }
-    const size_t smem = mode == kModeHalo
-                            ? 1024 + static_cast<size_t>(p.a_stages) * kHaloBytes +
-                                  static_cast<size_t>(p.stages) * p.ks * p.BN * 128 + kTail
-                            : 1024 + static_cast<size_t>(p.stages) * p.ks * (kABytes + p.BN * 128) + kTail;
-    if (mode == kModeHalo) return launch<kModeHalo>(p, ma, mb, ma16, mb16, smem, grid, stream);
-    if (mode == kModeGather) return launch<kModeGather>(p, ma, mb, ma, mb, smem, grid, stream);
-    return launch<kModeTma>(p, ma, mb, ma, mb, smem, grid, stream);
+    size_t ring = mode == kModeHalo
+                      ? static_cast<size_t>(p.a_stages) * kHaloBytes + static_cast<size_t>(p.stages) * p.ks * p.BN * 128
+                      : static_cast<size_t>(p.stages) * p.ks * (kABytes + p.BN * 128);
+    // Staged TMA epilogue: a 128-pixel row segment, plain f32 output written
+    // whole (no residual) or added onto itself (residual == y, no SiLU after).
+    const bool res_self = a.residual != nullptr && a.residual == a.y && !a.silu;
+    if (mode != kModeGather && p.R == 1 && p.Wt == kBM && !p.up && !p.out_f16 && !p.out_nchw &&
+        a.rms_out == nullptr && a.dup_src == nullptr && a.cout % 16 == 0 && a.y != nullptr && aligned16(a.y) &&
+        (a.residual == nullptr || res_self) && 1024 + ring + kEpiWarps * kStgBytes + kTail <= kMaxSmem) {
+        const uint64_t dims[4] = {static_cast<uint64_t>(a.cout), static_cast<uint64_t>(p.W),
+                                  static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.n)};
+        const uint64_t strides[3] = {static_cast<uint64_t>(a.cout) * 4, static_cast<uint64_t>(p.W) * a.cout * 4,
+                                     static_cast<uint64_t>(p.H) * p.W * a.cout * 4};
+        const uint32_t box[4] = {16u, 32u, 1u, 1u};
+        if (encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B) ==
+            VAE_OK)
+            p.epi_tma = res_self ? 2 : 1;
+        else
+            clear_error();
+    }
+    const size_t smem = 1024 + ring + (p.epi_tma ? kEpiWarps * kStgBytes : 0) + kTail;
+    if (mode == kModeHalo) return launch<kModeHalo>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
+    if (mode == kModeGather) return launch<kModeGather>(p, ma, mb, ma, mb, my, smem, grid, stream);
+    return launch<kModeTma>(p, ma, mb, ma, mb, my, smem, grid, stream);
 }
 
 }  // namespace vae

@@ -88,6 +88,7 @@ struct ConvParams {
     int dup_prefetch;     // L2-prefetch each tile's DupUp source span (one source row)
     int dup_step;         // DupUp: source channel = dup_base[2q+p] + dup_step * o (1 or 2), or 0
     int dup_base[4];
+    int dup_v8;           // DupUp rows 32-byte aligned: 32-byte loads of the source window
     int v8_ok;            // f32 y / residual rows 32-byte aligned: 32-byte accesses
     int epi_tma;          // epilogue writes through staged TMA boxes: 1 store, 2 add onto y (residual == y)
     // NCHW output of kept rows (conv_out): rows [keep_lo, keep_hi) land at
@@ -568,6 +569,9 @@ __device__ __forceinline__ void store_chunk(const ConvParams& p, long long pix, 
 // The epilogue value of 16 output channels o0.. of one pixel: oscale * acc +
 // bias + residual + DupUp, then SiLU (channels >= cout are left unspecified).
 // `pre_res`, when given, holds the chunk's 16 residual values already loaded.
+// kWide: the register-hungrier 32-byte DupUp window loads (off in the
+// 320-thread gather kernel).
+template <bool kWide = true>
 __device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInfo& ti, const uint32_t (&r)[16],
                                               int o0, int v, int u, int q, int pp, long long pix, float (&val)[16],
                                               const float* pre_res = nullptr) {
@@ -619,14 +623,36 @@ __device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInf
     if (p.dup_src != nullptr && full && p.dup_step != 0) {
         // Division-free form: the 16 source channels are base + step * o, step
         // 1 or 2, so the loads have constant offsets and all go out at once.
-        const float* ds = p.dup_src + ((static_cast<long long>(ti.img) * p.hv + v) * p.wv + u) * p.dup_cin +
-                          static_cast<long long>(o0) * p.dup_step + p.dup_base[2 * q + pp];
-        if (p.dup_step == 2) {
+        const float* row = p.dup_src + ((static_cast<long long>(ti.img) * p.hv + v) * p.wv + u) * p.dup_cin;
+        const int b = p.dup_base[2 * q + pp];
+        if (kWide && p.dup_v8 && p.dup_step == 2 && b <= 1) {
+            // the 32 floats from 2*o0 (128-byte aligned) cover b + 2i, i < 16
+            float t[32];
+            const float* a0 = row + 2 * o0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) val[i] += __ldg(ds + 2 * i);
+            for (int k = 0; k < 4; ++k) ld_v8_f32_ro(a0 + 8 * k, t + 8 * k);
+            if (b != 0) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) val[i] += t[2 * i + 1];
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) val[i] += t[2 * i];
+            }
+        } else if (kWide && p.dup_v8 && p.dup_step == 1 && b == 0) {
+            float t[16];
+            ld_v8_f32_ro(row + o0, t);
+            ld_v8_f32_ro(row + o0 + 8, t + 8);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) val[i] += t[i];
         } else {
+            const float* ds = row + static_cast<long long>(o0) * p.dup_step + b;
+            if (p.dup_step == 2) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) val[i] += __ldg(ds + i);
+                for (int i = 0; i < 16; ++i) val[i] += __ldg(ds + 2 * i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) val[i] += __ldg(ds + i);
+            }
         }
     } else if (p.dup_src != nullptr) {
         const float* ds =
@@ -646,11 +672,12 @@ __device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInf
     }
 }
 
+template <bool kWide = true>
 __device__ __forceinline__ void epilogue_chunk(const ConvParams& p, const TileInfo& ti, const uint32_t (&r)[16],
                                                int o0, int v, int u, int q, int pp, int Y, int X,
                                                long long pix) {
     float val[16];
-    compute_chunk(p, ti, r, o0, v, u, q, pp, pix, val);
+    compute_chunk<kWide>(p, ti, r, o0, v, u, q, pp, pix, val);
     store_chunk(p, pix, o0, val, Y, X, ti.img);
 }
 
@@ -768,7 +795,7 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
         tmem_ld16(tbase + static_cast<uint32_t>(j), r);
         tmem_ld_wait();
         const int o0 = ti.n0 + j;
-        if (valid && o0 < p.cout) epilogue_chunk(p, ti, r, o0, v, u, q, pp, Y, X, pix);
+        if (valid && o0 < p.cout) epilogue_chunk<kPipe>(p, ti, r, o0, v, u, q, pp, Y, X, pix);
     }
 }
 
@@ -778,8 +805,8 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
 // oscale + bias), the same two roundings as the register path). No global
 // loads or per-lane stores: the warp's traffic is whole 2 KB boxes.
 __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, int v, int u,
-                                                 long long pix, uint8_t* stg, const CUtensorMap* mapY, int ew,
-                                                 int lane) {
+                                                 int q, int pp, long long pix, uint8_t* stg, const CUtensorMap* mapY,
+                                                 int ew, int lane) {
     const uint32_t sbase = smem_u32(stg + ew * kStgBytes);
     const int seg = ti.u0 + ew * 32;  // first pixel of this warp's 32 (warp-uniform)
     const uint32_t row_off = static_cast<uint32_t>(lane) * 64u;
@@ -792,7 +819,7 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
         const int o0 = ti.n0 + c * 16;
         if (o0 >= p.cout) break;  // warp-uniform
         float val[16];
-        compute_chunk(p, ti, acc, o0, v, u, 0, 0, pix, val);
+        compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val);
         if (lane == 0) bulk_wait_read_all();  // the previous box left this warp's buffer
         __syncwarp();
 #pragma unroll
@@ -806,6 +833,8 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
         if (lane == 0 && seg < p.wv) {
             if (p.epi_tma == 2)
                 tma_reduce_add_4d(mapY, sbase, o0, seg, ti.v0, ti.img);
+            else if (p.up)  // output pixels 2u + pp of row 2v + q: the (parity, W/2) view
+                tma_store_5d(mapY, sbase, o0, pp, seg, 2 * ti.v0 + q, ti.img);
             else
                 tma_store_4d(mapY, sbase, o0, seg, ti.v0, ti.img);
             bulk_commit_group();
@@ -813,7 +842,7 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
     }
 }
 
-template <int kMode>
+template <int kMode, bool kRms>
 __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane,
                               const CUtensorMap* mapY) {
     const int row = ew * 32 + lane;
@@ -834,10 +863,10 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         const long long pix = (static_cast<long long>(ti.img) * p.H + Y) * p.W + X;
         const uint32_t tbase =
             tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
-        if (p.rms_out != nullptr) {
+        if (kRms) {
             epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         } else if (kMode != kModeGather && p.epi_tma) {
-            epilogue_tma_row(p, ti, tbase, v, u, pix, s.stg, mapY, ew, lane);
+            epilogue_tma_row(p, ti, tbase, v, u, q, pp, pix, s.stg, mapY, ew, lane);
         } else {
             epilogue_plain_row<kMode != kModeGather>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         }
@@ -849,7 +878,9 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
     if (p.epi_tma && lane == 0) bulk_wait_all();  // boxes read and written before the CTA exits
 }
 
-template <int kMode>
+// kRms: the fused RMS_norm epilogue (a separate instantiation, so the other
+// kernels do not carry its 144-value row in registers).
+template <int kMode, bool kRms>
 __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     conv_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapA16, const __grid_constant__ CUtensorMap mapB16,
@@ -901,7 +932,7 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     const uint32_t tmem_base = *s.tmem_slot;
 
     if (warp < kEpiWarps) {
-        role_epilogue<kMode>(p, s, tmem_base, warp, lane, &mapY);
+        role_epilogue<kMode, kRms>(p, s, tmem_base, warp, lane, &mapY);
     } else if (warp == kProducerWarp) {
         if (lane == 0) role_producer<kMode>(p, s, &mapA, &mapB, &mapA16, &mapB16);
     } else if (warp == kMmaWarp) {
@@ -1317,7 +1348,7 @@ int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& m
     return VAE_OK;
 }
 
-template <int kMode>
+template <int kMode, bool kRms>
 int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma16,
            const CUtensorMap& mb16, const CUtensorMap& my, size_t smem, int grid, cudaStream_t stream) {
     static bool attr_set[64] = {false};
@@ -1325,10 +1356,10 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, co
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
         VAE_CUDA_CHECK(
-            cudaFuncSetAttribute(conv_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+            cudaFuncSetAttribute(conv_kernel<kMode, kRms>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set[dev] = true;
     }
-    conv_kernel<kMode><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, ma16, mb16, my, p);
+    conv_kernel<kMode, kRms><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, ma16, mb16, my, p);
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -1458,6 +1489,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         p.dup_step = a.dup_factor / a.dup_repeats;
         for (int c = 0; c < 4; ++c) p.dup_base[c] = (a.dup_ftoff + c) / a.dup_repeats;
     }
+    p.dup_v8 = (a.dup_src != nullptr && a.dup_cin % 8 == 0 && (reinterpret_cast<uintptr_t>(a.dup_src) & 31) == 0) ? 1 : 0;
     p.dup_prefetch = (a.dup_src != nullptr && p.R == 1 && a.dup_cin % 4 == 0 && aligned16(a.dup_src) &&
                       static_cast<long long>(p.Wt) * a.dup_cin * 4 < (1LL << 31))
                          ? 1
@@ -1592,25 +1624,45 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                       : static_cast<size_t>(p.stages) * p.ks * (kABytes + p.BN * 128);
     // Staged TMA epilogue: a 128-pixel row segment, plain f32 output written
     // whole (no residual) or added onto itself (residual == y, no SiLU after).
-    const bool res_self = a.residual != nullptr && a.residual == a.y && !a.silu;
-    if (mode != kModeGather && p.R == 1 && p.Wt == kBM && !p.up && !p.out_f16 && !p.out_nchw &&
-        a.rms_out == nullptr && a.dup_src == nullptr && a.cout % 16 == 0 && a.y != nullptr && aligned16(a.y) &&
-        (a.residual == nullptr || res_self) && 1024 + ring + kEpiWarps * kStgBytes + kTail <= kMaxSmem) {
-        const uint64_t dims[4] = {static_cast<uint64_t>(a.cout), static_cast<uint64_t>(p.W),
-                                  static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.n)};
-        const uint64_t strides[3] = {static_cast<uint64_t>(a.cout) * 4, static_cast<uint64_t>(p.W) * a.cout * 4,
-                                     static_cast<uint64_t>(p.H) * p.W * a.cout * 4};
-        const uint32_t box[4] = {16u, 32u, 1u, 1u};
-        if (encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B) ==
-            VAE_OK)
+    // The add-reduction keeps the register path's rounding order only without
+    // upsampling and DupUp (whose add comes after the residual's).
+    const bool res_self = a.residual != nullptr && a.residual == a.y && !a.silu && !p.up && a.dup_src == nullptr;
+    if (mode != kModeGather && p.R == 1 && p.Wt == kBM && !p.out_f16 && !p.out_nchw && a.rms_out == nullptr &&
+        a.cout % 16 == 0 && a.y != nullptr && aligned16(a.y) && (a.residual == nullptr || res_self) &&
+        1024 + ring + kEpiWarps * kStgBytes + kTail <= kMaxSmem) {
+        int erc;
+        if (p.up) {  // y viewed as (channel, column parity, W/2, row, image)
+            const uint64_t dims[5] = {static_cast<uint64_t>(a.cout), 2u, static_cast<uint64_t>(p.W / 2),
+                                      static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.n)};
+            const uint64_t strides[4] = {static_cast<uint64_t>(a.cout) * 4, static_cast<uint64_t>(a.cout) * 8,
+                                         static_cast<uint64_t>(p.W) * a.cout * 4,
+                                         static_cast<uint64_t>(p.H) * p.W * a.cout * 4};
+            const uint32_t box[5] = {16u, 1u, 32u, 1u, 1u};
+            erc = encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, a.y, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_64B);
+        } else {
+            const uint64_t dims[4] = {static_cast<uint64_t>(a.cout), static_cast<uint64_t>(p.W),
+                                      static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.n)};
+            const uint64_t strides[3] = {static_cast<uint64_t>(a.cout) * 4, static_cast<uint64_t>(p.W) * a.cout * 4,
+                                         static_cast<uint64_t>(p.H) * p.W * a.cout * 4};
+            const uint32_t box[4] = {16u, 32u, 1u, 1u};
+            erc = encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_64B);
+        }
+        if (erc == VAE_OK)
             p.epi_tma = res_self ? 2 : 1;
         else
             clear_error();
     }
     const size_t smem = 1024 + ring + (p.epi_tma ? kEpiWarps * kStgBytes : 0) + kTail;
-    if (mode == kModeHalo) return launch<kModeHalo>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
-    if (mode == kModeGather) return launch<kModeGather>(p, ma, mb, ma, mb, my, smem, grid, stream);
-    return launch<kModeTma>(p, ma, mb, ma, mb, my, smem, grid, stream);
+    if (p.rms_out != nullptr) {
+        if (mode == kModeHalo) return launch<kModeHalo, true>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
+        if (mode == kModeGather) return launch<kModeGather, true>(p, ma, mb, ma, mb, my, smem, grid, stream);
+        return launch<kModeTma, true>(p, ma, mb, ma, mb, my, smem, grid, stream);
+    }
+    if (mode == kModeHalo) return launch<kModeHalo, false>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
+    if (mode == kModeGather) return launch<kModeGather, false>(p, ma, mb, ma, mb, my, smem, grid, stream);
+    return launch<kModeTma, false>(p, ma, mb, ma, mb, my, smem, grid, stream);
 }
 
 }  // namespace vae

@@ -67,6 +67,49 @@ def conv2d(x, w, b=None, upsample: bool = False, pad: str = "zero"):
     return y.reshape(cout, H, W)
 
 
+def causal_source_frame(f: int, kt: int, t_upsample: bool) -> int:
+    """Source frame that output frame ``f``'s temporal tap ``kt`` (0..2) reads.
+
+    The tap sees upsampled frame vf = f + kt - 2, clamped to the first frame
+    (causal padding replicates it); with the temporal 2x the upsampled frame vf
+    comes from source frame (vf - 1) // 2 + 1 for vf > 0 and 0 for vf = 0, so
+    the first frame is not doubled. ``s2v_vae.rs``, module doc (causal
+    replicate padding, two frames back) and ``conv_any``'s ``src_f``.
+    """
+    vf = max(f + kt - 2, 0)
+    return (vf - 1) // 2 + 1 if (t_upsample and vf > 0) else vf
+
+
+def conv3d_causal(x, w, b=None, upsample: bool = False, t_upsample: bool = False, pad: str = "zero"):
+    """3x3x3 causal convolution over frames, stride 1.
+
+    y[o, f, Y, X] = b[o] + sum_{kt} conv2d(xt[:, s(f, kt)], w[:, :, kt])[o, Y, X]
+    with s = ``causal_source_frame`` and conv2d the 2-D definition above (its
+    spatial nearest 2x and zero / replicate padding). Output frames: F, or
+    2F - 1 with ``t_upsample``. ``s2v_vae.rs``, the 3x3x3 causal implicit-GEMM
+    conv (module doc; ``conv_any``).
+
+    ``x``: [cin][F][h][w]; ``w``: [cout][cin][3][3][3] (kt, ky, kx); returns
+    [cout][F'][H][W].
+    """
+    x = _f64(x)
+    w = _f64(w)
+    cout, cin, kd, kh, kw = w.shape
+    assert (kd, kh, kw) == (3, 3, 3) and x.shape[0] == cin, (w.shape, x.shape)
+    F = x.shape[1]
+    Fo = 2 * F - 1 if t_upsample else F
+    ys = []
+    for f in range(Fo):
+        y = None
+        for kt in range(3):
+            t = conv2d(x[:, causal_source_frame(f, kt, t_upsample)], w[:, :, kt], None, upsample, pad)
+            y = t if y is None else y + t
+        if b is not None:
+            y = y + _f64(b)[:, None, None]
+        ys.append(y)
+    return np.stack(ys, axis=1)
+
+
 def conv2d_at(x, w, b, ys, xs, upsample: bool = False, pad: str = "zero"):
     """``conv2d`` evaluated only at output pixels (ys[i], xs[i]).
 

@@ -28,7 +28,7 @@ __all__ = [
     "NORM_GROUP", "NORM_RMS",
 ]
 
-UPSAMPLE2X, PAD_REPLICATE, EPI_SILU, OUT_F16 = 1, 2, 16, 32
+UPSAMPLE2X, PAD_REPLICATE, EPI_SILU, OUT_F16, UPSAMPLE_T2X = 1, 2, 16, 32, 64
 FAMILY_GN, FAMILY_RMS = 0, 1
 NORM_GROUP, NORM_RMS = 0, 1
 
@@ -57,6 +57,7 @@ SIGNATURES = {
     "vae_set_wait_timeout_ns": ([ctypes.c_ulonglong], _I),
     "vae_selftest_wait_timeout": ([ctypes.c_ulonglong, _P], _I),
     "vae_conv3x3_nhwc": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _P], _I),
+    "vae_conv3d_causal_ndhwc": ([_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _P], _I),
     "vae_conv1x1": ([_P, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _P], _I),
     "vae_rmsnorm_silu": ([_P, _I, _I, _P, _P, _I, _F, _P, _P], _I),
     "vae_groupnorm_workspace_bytes": ([_I, _I, _I, _I], _SZ),
@@ -170,6 +171,32 @@ def conv3x3_nhwc(x, w, bias=None, residual=None, out=None, oscale: float = 1.0, 
     return out
 
 
+def conv3d_causal_ndhwc(x, w, bias=None, residual=None, out=None, oscale: float = 1.0, upsample: bool = False,
+                        t_upsample: bool = False, replicate: bool = False, silu: bool = False,
+                        out_f16: bool = False, stream=None):
+    """3x3x3 causal conv over frames. x f16 [n][f][h][w][cin]; w f16 [cout][3][3][3][cin]."""
+    import torch
+    _need(x, torch.float16, "x", 5)
+    _need(w, torch.float16, "w", 5)
+    _need(bias, torch.float32, "bias", 1)
+    n, f, h, wd, cin = x.shape
+    cout = w.shape[0]
+    if tuple(w.shape[1:]) != (3, 3, 3, cin):
+        raise VaeError(-2, f"w must be [cout][3][3][3][{cin}], got {tuple(w.shape)}")
+    F = 2 * f - 1 if t_upsample else f
+    H, W = (2 * h, 2 * wd) if upsample else (h, wd)
+    odt = torch.float16 if out_f16 else torch.float32
+    if out is None:
+        out = torch.empty((n, F, H, W, cout), dtype=odt, device=x.device)
+    _need(out, odt, "out")
+    _need(residual, torch.float32, "residual")
+    flags = (UPSAMPLE2X if upsample else 0) | (UPSAMPLE_T2X if t_upsample else 0) | \
+            (PAD_REPLICATE if replicate else 0) | (EPI_SILU if silu else 0) | (OUT_F16 if out_f16 else 0)
+    _check(lib().vae_conv3d_causal_ndhwc(_ptr(x), n, f, h, wd, cin, _ptr(w), _ptr(bias), _ptr(residual), _ptr(out),
+                                         cout, float(oscale), flags, _stream(stream)))
+    return out
+
+
 def conv1x1(x, w, bias=None, residual=None, out=None, oscale: float = 1.0, silu: bool = False,
             out_f16: bool = False, stream=None):
     """1x1 conv (GEMM). x f16 [m][cin]; w f16 [cout][cin]."""
@@ -269,6 +296,11 @@ def mid_attention(x, norm_kind: int, gamma, beta, wq, bq, wk, bk, wv, bv, wo, bo
 def pack_conv3x3(w_oihw: np.ndarray) -> np.ndarray:
     """OIHW [cout][cin][3][3] -> the kernel's [cout][3][3][cin] (a permutation)."""
     return np.ascontiguousarray(np.asarray(w_oihw).transpose(0, 2, 3, 1))
+
+
+def pack_conv3d(w_oidhw: np.ndarray) -> np.ndarray:
+    """OIDHW [cout][cin][3][3][3] -> the kernel's [cout][3][3][3][cin] (a permutation)."""
+    return np.ascontiguousarray(np.asarray(w_oidhw).transpose(0, 2, 3, 4, 1))
 
 
 def pack_conv1x1(w_oihw: np.ndarray) -> np.ndarray:

@@ -70,6 +70,9 @@ struct ConvParams {
     int tiles_x, tiles_y, npar;
     int n_tiles, BN, acc_stride;
     int kchunks, total_tiles, stages;
+    int frames_out, frames_in, t_up, nkt;  // 3-D causal conv: output / input frames per image, temporal 2x,
+                                            // temporal taps (3; 1 for 2-D convs, whose frames are 1)
+    int n_in;             // input images (batch x input frames; = n for 2-D convs)
     int rem16, kfull;     // three-tap halo stages with cin % 64 == 16: kfull 64-channel chunks, then one
                           // stage of 16-channel boxes (32-byte swizzle) for all three ky and nine taps
     int halo, a_stages;   // halo mode: a_stages halo boxes; B ring of `stages` x ks taps
@@ -127,14 +130,27 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvParams& p, int t) {
     return ti;
 }
 
-// Source offset of tap `tap` for parity class `par` (see the file comment).
+// Source image of output image `img` for temporal tap kt (0..2, frame f + kt - 2):
+// causal, the frames before the first replicate it; with the temporal 2x the
+// upsampled frame vf comes from source frame vf > 0 ? (vf - 1) / 2 + 1 : 0.
+// 2-D convs (one frame) use kt = 2 only: the image itself.
+__device__ __forceinline__ int src_img(const ConvParams& p, int img, int kt) {
+    if (p.frames_out == 1) return img;
+    const int b = img / p.frames_out, f = img - b * p.frames_out;
+    const int vf = max(f - 2 + kt, 0);
+    const int sf = p.t_up ? (vf > 0 ? (vf - 1) / 2 + 1 : 0) : vf;
+    return b * p.frames_in + sf;
+}
+
+// Source offset of tap `tap` for parity class `par` (see the file comment);
+// a 3x3x3 tap is kt * 9 + ky * 3 + kx.
 __device__ __forceinline__ void tap_offset(const ConvParams& p, int tap, int par, int& dy, int& dx) {
     if (p.taps == 1) {
         dy = 0;
         dx = 0;
         return;
     }
-    const int ky = tap / 3, kx = tap % 3;
+    const int ky = (tap % 9) / 3, kx = tap % 3;
     if (p.up) {
         const int q = par >> 1, pp = par & 1;
         dy = (q + ky + 1) / 2 - 1;
@@ -236,60 +252,67 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
             const int q = ti.par >> 1, pp = ti.par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             const int kc_end = p.rem16 ? p.kfull : p.kchunks;
-            for (int ky = 0; ky < 3 && ok; ++ky) {
-                const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
-                for (int kc = 0; kc < kc_end && ok; ++kc) {
-                    uint32_t slot;
-                    const uint32_t fb = next_b(p.a_tx + 3u * b_bytes, &slot);
-                    if (!ok) break;
-                    tma_load_4d(smem_u32(s.a + slot * kHaloBytes), mapA, fb, kc * kBK, ti.u0 + dxmin, ti.v0 + dy,
-                                ti.img, pol_a);
-                    for (int kx = 0; kx < 3; ++kx)
-                        tma_load_3d(smem_u32(s.b + (slot * 3 + kx) * p.BN * 128), mapB, fb, kc * kBK, ky * 3 + kx,
-                                    ti.n0, pol_w);
-                }
-            }
-            if (p.rem16 && ok) {
-                // the last 16 channels of all three ky and nine taps in one stage
-                uint32_t slot;
-                const uint32_t fb = next_b(3u * kRemABytes + 9u * static_cast<uint32_t>(p.BN) * 32u, &slot);
-                if (ok) {
-                    for (int ky = 0; ky < 3; ++ky) {
-                        const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
-                        tma_load_4d(smem_u32(s.a + slot * kHaloBytes + ky * kRemAStride), mapA16, fb, p.kfull * kBK,
-                                    ti.u0 + dxmin, ti.v0 + dy, ti.img, pol_a);
+            for (int kt = 0; kt < p.nkt && ok; ++kt) {
+                const int simg = src_img(p, ti.img, kt + 3 - p.nkt);
+                for (int ky = 0; ky < 3 && ok; ++ky) {
+                    const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                    for (int kc = 0; kc < kc_end && ok; ++kc) {
+                        uint32_t slot;
+                        const uint32_t fb = next_b(p.a_tx + 3u * b_bytes, &slot);
+                        if (!ok) break;
+                        tma_load_4d(smem_u32(s.a + slot * kHaloBytes), mapA, fb, kc * kBK, ti.u0 + dxmin, ti.v0 + dy,
+                                    simg, pol_a);
+                        for (int kx = 0; kx < 3; ++kx)
+                            tma_load_3d(smem_u32(s.b + (slot * 3 + kx) * p.BN * 128), mapB, fb, kc * kBK,
+                                        kt * 9 + ky * 3 + kx, ti.n0, pol_w);
                     }
-                    for (int tap = 0; tap < 9; ++tap)
-                        tma_load_3d(smem_u32(s.b + slot * 3 * p.BN * 128 + tap * p.BN * 32), mapB16, fb, p.kfull * kBK,
-                                    tap, ti.n0, pol_w);
+                }
+                if (p.rem16 && ok) {
+                    // the last 16 channels of all three ky and nine (ky, kx) taps in one stage
+                    uint32_t slot;
+                    const uint32_t fb = next_b(3u * kRemABytes + 9u * static_cast<uint32_t>(p.BN) * 32u, &slot);
+                    if (ok) {
+                        for (int ky = 0; ky < 3; ++ky) {
+                            const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                            tma_load_4d(smem_u32(s.a + slot * kHaloBytes + ky * kRemAStride), mapA16, fb,
+                                        p.kfull * kBK, ti.u0 + dxmin, ti.v0 + dy, simg, pol_a);
+                        }
+                        for (int tap = 0; tap < 9; ++tap)
+                            tma_load_3d(smem_u32(s.b + slot * 3 * p.BN * 128 + tap * p.BN * 32), mapB16, fb,
+                                        p.kfull * kBK, kt * 9 + tap, ti.n0, pol_w);
+                    }
                 }
             }
         } else if (kMode == kModeHalo) {
             const int q = ti.par >> 1, pp = ti.par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
-            for (int ky = 0; ky < 3 && ok; ++ky) {
-                const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
-                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
-                    if (!mbar_wait(smem_u32(&s.aempty[astage]), aphase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
-                                   kWhereProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t afb = smem_u32(&s.afull[astage]);
-                    mbar_arrive_expect_tx(afb, p.a_tx);
-                    aarmed |= 1u << astage;
-                    aarm_par = (aarm_par & ~(1u << astage)) | (aphase << astage);
-                    tma_load_4d(smem_u32(s.a + astage * kHaloBytes), mapA, afb, kc * kBK, ti.u0 + dxmin, ti.v0 + dy,
-                                ti.img, pol_a);
-                    if (++astage == p.a_stages) {
-                        astage = 0;
-                        aphase ^= 1u;
-                    }
-                    for (int kx = 0; kx < 3; ++kx) {
-                        uint32_t slot;
-                        const uint32_t fb = next_b(b_bytes, &slot);
-                        if (!ok) break;
-                        tma_load_3d(smem_u32(s.b + slot * p.BN * 128), mapB, fb, kc * kBK, ky * 3 + kx, ti.n0, pol_w);
+            for (int kt = 0; kt < p.nkt && ok; ++kt) {
+                const int simg = src_img(p, ti.img, kt + 3 - p.nkt);
+                for (int ky = 0; ky < 3 && ok; ++ky) {
+                    const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                    for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                        if (!mbar_wait(smem_u32(&s.aempty[astage]), aphase ^ 1u, s.abort_flag, p.timeout_ns,
+                                       p.status, kWhereProducerEmpty)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t afb = smem_u32(&s.afull[astage]);
+                        mbar_arrive_expect_tx(afb, p.a_tx);
+                        aarmed |= 1u << astage;
+                        aarm_par = (aarm_par & ~(1u << astage)) | (aphase << astage);
+                        tma_load_4d(smem_u32(s.a + astage * kHaloBytes), mapA, afb, kc * kBK, ti.u0 + dxmin,
+                                    ti.v0 + dy, simg, pol_a);
+                        if (++astage == p.a_stages) {
+                            astage = 0;
+                            aphase ^= 1u;
+                        }
+                        for (int kx = 0; kx < 3; ++kx) {
+                            uint32_t slot;
+                            const uint32_t fb = next_b(b_bytes, &slot);
+                            if (!ok) break;
+                            tma_load_3d(smem_u32(s.b + slot * p.BN * 128), mapB, fb, kc * kBK, kt * 9 + ky * 3 + kx,
+                                        ti.n0, pol_w);
+                        }
                     }
                 }
             }
@@ -297,6 +320,7 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
             for (int tap = 0; tap < p.taps && ok; ++tap) {
                 int dy, dx;
                 tap_offset(p, tap, ti.par, dy, dx);
+                const int simg = src_img(p, ti.img, p.taps == 27 ? tap / 9 : 2);
                 for (int kc = 0; kc < p.kchunks; kc += p.ks) {
                     // one stage = up to ks consecutive 64-channel chunks of this tap
                     const int nck = min(p.ks, p.kchunks - kc);
@@ -307,7 +331,7 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
                     for (int h = 0; h < nck; ++h) {
                         if (kMode == kModeTma)
                             tma_load_4d(smem_u32(s.a + (slot * p.ks + h) * kABytes), mapA, fb, (kc + h) * kBK,
-                                        ti.u0 + dx, ti.v0 + dy, ti.img, pol_a);
+                                        ti.u0 + dx, ti.v0 + dy, simg, pol_a);
                         tma_load_3d(smem_u32(s.b + (slot * p.ks + h) * p.BN * 128), mapB, fb, (kc + h) * kBK, tap,
                                     ti.n0, pol_w);
                     }
@@ -337,6 +361,7 @@ __device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
         for (int tap = 0; tap < p.taps && ok; ++tap) {
             int dy, dx;
             tap_offset(p, tap, ti.par, dy, dx);
+            const int simg = src_img(p, ti.img, p.taps == 27 ? tap / 9 : 2);
             int sy = v + dy, sx = u + dx;
             bool inb;
             if (p.rep) {
@@ -347,7 +372,7 @@ __device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
                 inb = rowvalid && sy >= 0 && sy < p.hv && sx >= 0 && sx < p.wv;
             }
             const __half* src =
-                p.x + ((static_cast<long long>(ti.img) * p.hv + (inb ? sy : 0)) * p.wv + (inb ? sx : 0)) *
+                p.x + ((static_cast<long long>(simg) * p.hv + (inb ? sy : 0)) * p.wv + (inb ? sx : 0)) *
                           p.cin;
             for (int kc = 0; kc < p.kchunks; ++kc) {
                 if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, s.abort_flag, p.timeout_ns,
@@ -415,96 +440,99 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
             const int pp = decode_tile(p, t).par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             const int kc_end = p.rem16 ? p.kfull : p.kchunks;
-            for (int ky = 0; ky < 3 && ok; ++ky) {
-                for (int kc = 0; kc < kc_end && ok; ++kc) {
+            for (int kt = 0; kt < p.nkt && ok; ++kt) {  // temporal taps (3-D); one pass for 2-D
+                for (int ky = 0; ky < 3 && ok; ++ky) {
+                    for (int kc = 0; kc < kc_end && ok; ++kc) {
+                        if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                                       kWhereMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        // All MMAs of the stage go out back to back: the tensor core's
+                        // issue queue then covers this thread's barrier work.
+                        const int nk = min(4, (p.cin - kc * kBK) / 16);
+                        const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
+                        const uint32_t bbase = smem_u32(s.b + stage * 3 * p.BN * 128);
+    #pragma unroll
+                        for (int kx = 0; kx < 3; ++kx) {
+                            const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
+                            // a whole-row offset: the tensor core swizzles on absolute address bits
+                            const uint64_t ad = sw128_kmajor_desc(abase + static_cast<uint32_t>((dx - dxmin) * 128));
+                            const uint64_t bd = sw128_kmajor_desc(bbase + static_cast<uint32_t>(kx * p.BN * 128));
+                            if (nk == 4) {
+    #pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                                             (kit | kx | k) != 0 ? 1u : 0u);
+                            } else {
+                                for (int k = 0; k < nk; ++k)
+                                    umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
+                                             (kit | kx | k) != 0 ? 1u : 0u);
+                            }
+                        }
+                        umma_commit(smem_u32(&s.empty[stage]));
+                        ++kit;
+                        if (++stage == p.stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
+                if (p.rem16 && ok) {
                     if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
                                    kWhereMmaFull)) {
                         ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    // All MMAs of the stage go out back to back: the tensor core's
-                    // issue queue then covers this thread's barrier work.
-                    const int nk = min(4, (p.cin - kc * kBK) / 16);
-                    const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
-                    const uint32_t bbase = smem_u32(s.b + stage * 3 * p.BN * 128);
-#pragma unroll
-                    for (int kx = 0; kx < 3; ++kx) {
-                        const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
-                        // a whole-row offset: the tensor core swizzles on absolute address bits
-                        const uint64_t ad = sw128_kmajor_desc(abase + static_cast<uint32_t>((dx - dxmin) * 128));
-                        const uint64_t bd = sw128_kmajor_desc(bbase + static_cast<uint32_t>(kx * p.BN * 128));
-                        if (nk == 4) {
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                                         (kit | kx | k) != 0 ? 1u : 0u);
-                        } else {
-                            for (int k = 0; k < nk; ++k)
-                                umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                                         (kit | kx | k) != 0 ? 1u : 0u);
+                    } else {
+                        tc_fence_after();
+                        // one K = 16 step per tap; the 64-channel chunks came first, so always accumulate
+                        const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
+                        const uint32_t bbase = smem_u32(s.b + stage * 3 * p.BN * 128);
+    #pragma unroll
+                        for (int ky = 0; ky < 3; ++ky)
+    #pragma unroll
+                            for (int kx = 0; kx < 3; ++kx) {
+                                const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
+                                const uint64_t ad = sw32_kmajor_desc(abase + static_cast<uint32_t>(ky * kRemAStride) +
+                                                                     static_cast<uint32_t>((dx - dxmin) * 32));
+                                const uint64_t bd =
+                                    sw32_kmajor_desc(bbase + static_cast<uint32_t>((ky * 3 + kx) * p.BN * 32));
+                                umma_f16(d, ad, bd, idesc, 1u);
+                            }
+                        umma_commit(smem_u32(&s.empty[stage]));
+                        ++kit;
+                        if (++stage == p.stages) {
+                            stage = 0;
+                            phase ^= 1u;
                         }
-                    }
-                    umma_commit(smem_u32(&s.empty[stage]));
-                    ++kit;
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-            if (p.rem16 && ok) {
-                if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
-                               kWhereMmaFull)) {
-                    ok = false;
-                } else {
-                    tc_fence_after();
-                    // one K = 16 step per tap; the 64-channel chunks came first, so always accumulate
-                    const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
-                    const uint32_t bbase = smem_u32(s.b + stage * 3 * p.BN * 128);
-#pragma unroll
-                    for (int ky = 0; ky < 3; ++ky)
-#pragma unroll
-                        for (int kx = 0; kx < 3; ++kx) {
-                            const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
-                            const uint64_t ad = sw32_kmajor_desc(abase + static_cast<uint32_t>(ky * kRemAStride) +
-                                                                 static_cast<uint32_t>((dx - dxmin) * 32));
-                            const uint64_t bd =
-                                sw32_kmajor_desc(bbase + static_cast<uint32_t>((ky * 3 + kx) * p.BN * 32));
-                            umma_f16(d, ad, bd, idesc, 1u);
-                        }
-                    umma_commit(smem_u32(&s.empty[stage]));
-                    ++kit;
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
                     }
                 }
             }
         } else if (p.halo) {
             const int pp = decode_tile(p, t).par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
-            for (int ky = 0; ky < 3 && ok; ++ky) {
-                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
-                    if (!mbar_wait(smem_u32(&s.afull[astage]), aphase, s.abort_flag, p.timeout_ns, p.status,
-                                   kWhereMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t abase = smem_u32(s.a + astage * kHaloBytes);
-                    for (int kx = 0; kx < 3 && ok; ++kx) {
-                        const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
-                        // a whole-row offset: the tensor core swizzles on absolute address bits
-                        mma_slot(d, true, abase + static_cast<uint32_t>((dx - dxmin) * 128), kc, 1, kit);
-                    }
-                    if (!ok) break;
-                    umma_commit(smem_u32(&s.aempty[astage]));
-                    if (++astage == p.a_stages) {
-                        astage = 0;
-                        aphase ^= 1u;
+            for (int kt = 0; kt < p.nkt && ok; ++kt)
+                for (int ky = 0; ky < 3 && ok; ++ky) {
+                    for (int kc = 0; kc < p.kchunks && ok; ++kc) {
+                        if (!mbar_wait(smem_u32(&s.afull[astage]), aphase, s.abort_flag, p.timeout_ns, p.status,
+                                       kWhereMmaFull)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t abase = smem_u32(s.a + astage * kHaloBytes);
+                        for (int kx = 0; kx < 3 && ok; ++kx) {
+                            const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
+                            // a whole-row offset: the tensor core swizzles on absolute address bits
+                            mma_slot(d, true, abase + static_cast<uint32_t>((dx - dxmin) * 128), kc, 1, kit);
+                        }
+                        if (!ok) break;
+                        umma_commit(smem_u32(&s.aempty[astage]));
+                        if (++astage == p.a_stages) {
+                            astage = 0;
+                            aphase ^= 1u;
+                        }
                     }
                 }
-            }
         } else {
             for (int tap = 0; tap < p.taps && ok; ++tap)
                 for (int kc = 0; kc < p.kchunks && ok; kc += p.ks) mma_slot(d, false, 0u, kc, min(p.ks, p.kchunks - kc), kit);
@@ -1369,7 +1397,11 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, co
 int conv_validate(const ConvArgs& a) {
     if (a.x == nullptr || a.w == nullptr)
         return set_error(VAE_ERR_ARG, "conv: x and w must be non-NULL");
-    if (a.taps != 1 && a.taps != 9) return set_error(VAE_ERR_ARG, "conv: taps must be 1 or 9");
+    if (a.taps != 1 && a.taps != 9 && a.taps != 27) return set_error(VAE_ERR_ARG, "conv: taps must be 1, 9 or 27");
+    if (a.frames_in < 1 || (a.taps != 27 && (a.frames_in != 1 || a.t_up)))
+        return set_error(VAE_ERR_ARG, "conv: frames_in=%d / temporal upsample need the 3x3x3 conv", a.frames_in);
+    if (a.taps == 27 && (a.rms_out != nullptr || a.dup_src != nullptr || a.out_nchw))
+        return set_error(VAE_ERR_ARG, "conv: the 3x3x3 conv has no fused norm, DupUp or NCHW output");
     if (a.n < 1 || a.h_in < 1 || a.w_in < 1)
         return set_error(VAE_ERR_SHAPE, "conv: n=%d h=%d w=%d must be >= 1", a.n, a.h_in, a.w_in);
     if (a.cin < 16 || a.cin % 16 != 0 || a.cin > 8192)
@@ -1380,8 +1412,10 @@ int conv_validate(const ConvArgs& a) {
     if (!aligned16(a.x) || !aligned16(a.w))
         return set_error(VAE_ERR_ALIGN, "conv: x and w must be 16-byte aligned");
     const long long H = a.up ? 2LL * a.h_in : a.h_in, W = a.up ? 2LL * a.w_in : a.w_in;
-    if (static_cast<long long>(a.n) * H * W >= (1LL << 31) || static_cast<long long>(a.w_in) >= (1LL << 31))
-        return set_error(VAE_ERR_SHAPE, "conv: too many output pixels");
+    const long long F = a.t_up ? 2LL * a.frames_in - 1 : a.frames_in;
+    if (static_cast<long long>(a.n) * F * H * W >= (1LL << 31) || static_cast<long long>(a.w_in) >= (1LL << 31) ||
+        static_cast<long long>(a.n) * a.frames_in * a.h_in * a.w_in >= (1LL << 31))
+        return set_error(VAE_ERR_SHAPE, "conv: too many pixels");
     if (a.out_nchw && (a.out_f16 || a.residual != nullptr))
         return set_error(VAE_ERR_ARG, "conv: NCHW output is f32 without residual");
     if (a.rms_out != nullptr) {
@@ -1413,7 +1447,12 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     if (nsm <= 0) return set_error(VAE_ERR_CUDA, "conv: no SM count");
 
     ConvParams p{};
-    p.n = a.n;
+    p.frames_in = a.frames_in;
+    p.t_up = a.t_up ? 1 : 0;
+    p.frames_out = a.t_up ? 2 * a.frames_in - 1 : a.frames_in;
+    p.nkt = a.taps == 27 ? 3 : 1;
+    p.n = a.n * p.frames_out;  // output images: the tile space
+    p.n_in = a.n * a.frames_in;
     p.hv = a.h_in;
     p.wv = a.w_in;
     p.cin = a.cin;
@@ -1518,7 +1557,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     if (mode == kModeTma && halo_geom && (st3 >= 3 || a.cin <= 192)) {
         // one 130-pixel halo box per (ky, chunk), shared by the three kx taps
         const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(p.wv),
-                                  static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n)};
+                                  static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n_in)};
         const uint64_t strides[3] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(p.wv) * a.cin * 2,
                                      static_cast<uint64_t>(p.hv) * p.wv * a.cin * 2};
         const uint32_t box[4] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kHaloRows), 1u, 1u};
@@ -1563,7 +1602,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     }
     if (mode == kModeTma) {
         const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(p.wv),
-                                  static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n)};
+                                  static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n_in)};
         const uint64_t strides[3] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(p.wv) * a.cin * 2,
                                      static_cast<uint64_t>(p.hv) * p.wv * a.cin * 2};
         const uint32_t box[4] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(p.Wt),
@@ -1580,7 +1619,8 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // CTA pairs (cta_group::2) are correct and tested but measured 3-6 % slower
     // than single CTAs on GB300 at every decoder shape, so they run only when
     // requested (VAE_CONV_CTA_PAIR=1 in the environment).
-    if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2) {
+    if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2 &&
+        a.taps != 27) {
         // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
         p.pair = 1;
         p.rem16 = 0;  // the pair kernel loads zero-filled 64-channel remainder boxes
@@ -1686,6 +1726,35 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin, cons
     a.w = w_dev;
     a.cout = cout;
     a.taps = 9;
+    a.bias = bias_dev;
+    a.residual = residual_dev;
+    a.y = y_dev;
+    a.oscale = oscale;
+    a.up = (flags & VAE_UPSAMPLE2X) != 0;
+    a.rep = (flags & VAE_PAD_REPLICATE) != 0;
+    a.silu = (flags & VAE_EPI_SILU) != 0;
+    a.out_f16 = (flags & VAE_OUT_F16) != 0;
+    return conv_run(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int vae_conv3d_causal_ndhwc(const void* x_dev, int n, int f_in, int h_in, int w_in, int cin, const void* w_dev,
+                            const float* bias_dev, const float* residual_dev, void* y_dev, int cout, float oscale,
+                            unsigned flags, vae_stream_t stream) {
+    clear_error();
+    if (flags & ~static_cast<unsigned>(VAE_UPSAMPLE2X | VAE_UPSAMPLE_T2X | VAE_PAD_REPLICATE | VAE_EPI_SILU |
+                                       VAE_OUT_F16))
+        return set_error(VAE_ERR_ARG, "vae_conv3d_causal_ndhwc: unknown flag bits 0x%x", flags);
+    ConvArgs a{};
+    a.x = x_dev;
+    a.n = n;
+    a.frames_in = f_in;
+    a.t_up = (flags & VAE_UPSAMPLE_T2X) != 0;
+    a.h_in = h_in;
+    a.w_in = w_in;
+    a.cin = cin;
+    a.w = w_dev;
+    a.cout = cout;
+    a.taps = 27;
     a.bias = bias_dev;
     a.residual = residual_dev;
     a.y = y_dev;

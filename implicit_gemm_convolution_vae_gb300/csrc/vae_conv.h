@@ -11,7 +11,11 @@ struct ConvArgs {
     int n = 1, h_in = 0, w_in = 0, cin = 0;
     const void* w = nullptr;     // f16 [cout][taps][cin]
     int cout = 0;
-    int taps = 9;                // 9 (3x3) or 1 (1x1)
+    int taps = 9;                // 9 (3x3), 1 (1x1) or 27 (3x3x3 causal over frames)
+    // 3x3x3 causal conv: x holds n images of frames_in frames ([n][frames_in][h][w][cin]);
+    // y holds n images of frames_out = t_up ? 2 * frames_in - 1 : frames_in frames.
+    int frames_in = 1;
+    bool t_up = false;
     const float* bias = nullptr;
     const float* residual = nullptr;  // f32 NHWC [n][H][W][cout]; may alias y
     void* y = nullptr;

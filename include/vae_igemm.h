@@ -55,7 +55,8 @@ enum {
     VAE_UPSAMPLE2X = 1,     /* nearest-2x of the input folded into the gather: output is 2h x 2w */
     VAE_PAD_REPLICATE = 2,  /* out-of-grid reads take the nearest edge pixel (default: zero) */
     VAE_EPI_SILU = 16,      /* SiLU v/(1+e^-v) applied last in the epilogue */
-    VAE_OUT_F16 = 32        /* store the output as f16 (default f32) */
+    VAE_OUT_F16 = 32,       /* store the output as f16 (default f32) */
+    VAE_UPSAMPLE_T2X = 64   /* 3x3x3 conv only: causal temporal 2x folded into the gather */
 };
 
 /* Library version string and the compute capability it was built for. */
@@ -114,6 +115,32 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin,
  *   f32 or f16 (VAE_OUT_F16). Flags: VAE_EPI_SILU, VAE_OUT_F16 only.
  * Requirements as vae_conv3x3_nhwc; m >= 1.
  */
+/*
+ * 3x3x3 causal convolution over frames, the same implicit GEMM with 27 taps
+ * ("s2v_vae.rs" module doc and conv_any: the conv mode 3 of zi_mm, its causal
+ * two-frame look-back, the replicate padding and the nearest upsample in the
+ * gather, src_f for the temporal 2x):
+ *   y[b, f, Y, X, o] = SiLU?( oscale * sum_{kt, ky, kx, c} xt[b, s(f, kt), Y + ky - 1, X + kx - 1, c]
+ *                              * w[o, kt, ky, kx, c] + bias[o] + residual[b, f, Y, X, o] )
+ * with the temporal tap kt = 0, 1, 2 reading upsampled frame vf = max(f + kt - 2, 0)
+ * (causal: frames before the first replicate it) and s(f, kt) = vf, or with
+ * VAE_UPSAMPLE_T2X the source frame (vf > 0 ? (vf - 1) / 2 + 1 : 0).
+ * Spatially as vae_conv3x3_nhwc: xt is x or nearest-2x(x) with
+ * VAE_UPSAMPLE2X; reads outside the (upsampled) grid are 0 or, with
+ * VAE_PAD_REPLICATE, the nearest edge pixel.
+ *   x_dev     f16 [n][f_in][h_in][w_in][cin], 16-byte aligned.
+ *   w_dev     f16 [cout][3][3][3][cin] (K index = ((kt*3+ky)*3+kx)*cin + c).
+ *   bias_dev  f32 [cout] or NULL.
+ *   residual_dev  f32 [n][F][H][W][cout] or NULL; may equal y_dev.
+ *   y_dev     [n][F][H][W][cout] f32, or f16 with VAE_OUT_F16; F = f_in, or
+ *             2*f_in - 1 with VAE_UPSAMPLE_T2X; H, W as vae_conv3x3_nhwc.
+ * Flags: VAE_UPSAMPLE2X, VAE_UPSAMPLE_T2X, VAE_PAD_REPLICATE, VAE_EPI_SILU,
+ * VAE_OUT_F16. Requirements as vae_conv3x3_nhwc, and f_in >= 1.
+ */
+int vae_conv3d_causal_ndhwc(const void* x_dev, int n, int f_in, int h_in, int w_in, int cin,
+                            const void* w_dev, const float* bias_dev, const float* residual_dev,
+                            void* y_dev, int cout, float oscale, unsigned flags, vae_stream_t stream);
+
 int vae_conv1x1(const void* x_dev, int m, int cin, const void* w_dev,
                 const float* bias_dev, const float* residual_dev, void* y_dev, int cout,
                 float oscale, unsigned flags, vae_stream_t stream);

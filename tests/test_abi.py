@@ -58,6 +58,16 @@ def test_conv_rejects_bad_shapes_and_flags(L):
     assert L.vae_conv1x1(FAKE, 10, 16, FAKE, None, None, FAKE, 0, 1.0, 0, None) == -2
 
 
+def test_conv3d_rejects_bad_shapes_and_flags(L):
+    c3 = L.vae_conv3d_causal_ndhwc
+    assert c3(FAKE, 1, 0, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, 0, None) == -1   # no frames
+    assert c3(FAKE, 1, 2, 4, 4, 15, FAKE, None, None, FAKE, 16, 1.0, 0, None) == -2   # cin % 16
+    assert c3(FAKE, 1, 2, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, 1 << 9, None) == -1
+    assert c3(None, 1, 2, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, 0, None) == -1
+    # the temporal 2x flag belongs to the 3x3x3 conv only
+    assert L.vae_conv3x3_nhwc(FAKE, 1, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, vg.UPSAMPLE_T2X, None) == -1
+
+
 def test_norms_reject_bad_shapes(L):
     assert L.vae_rmsnorm_silu(FAKE, 4, 6, None, FAKE, 0, 1.0, FAKE, None) == -2
     assert L.vae_rmsnorm_silu(None, 4, 8, None, FAKE, 0, 1.0, FAKE, None) == -1

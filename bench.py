@@ -195,9 +195,29 @@ def run_kernel(args):
     import implicit_gemm_convolution_vae_gb300 as vg
     vg.build()
     torch.manual_seed(0)
-    h, w, cin, cout = (int(v) for v in args.shape.split(","))
+    vals = [int(v) for v in args.shape.split(",")]
     stream = torch.cuda.current_stream()
-    if args.kernel in ("conv3x3", "upconv3x3"):
+    if args.kernel in ("conv3d", "upconv3d"):
+        # 3x3x3 causal conv over frames; upconv3d folds the spatial and temporal 2x
+        f, h, w, cin, cout = vals
+        up = args.kernel == "upconv3d"
+        x = torch.randn(1, f, h, w, cin, device="cuda").half()
+        wt = (torch.randn(cout, 3, 3, 3, cin, device="cuda") / (27 * cin) ** 0.5).half()
+        b = torch.randn(cout, device="cuda") * 0.1
+        Fo, H, W = (2 * f - 1, 2 * h, 2 * w) if up else (f, h, w)
+        y = torch.empty(1, Fo, H, W, cout, device="cuda")
+        if args.residual:
+            y.normal_()  # the residual is the output itself: the in-place stream update
+        fn = lambda: vg.conv3d_causal_ndhwc(x, wt, b, residual=y if args.residual else None, out=y, upsample=up,
+                                            t_upsample=up)
+        flops = 2.0 * Fo * H * W * cout * 27 * cin
+        nbytes = x.numel() * 2 + y.numel() * 4 * (2 if args.residual else 1)
+        h = w = 0
+    else:
+        h, w, cin, cout = vals
+    if h == 0:
+        pass
+    elif args.kernel in ("conv3x3", "upconv3x3"):
         up = args.kernel == "upconv3x3"
         x = torch.randn(1, h, w, cin, device="cuda").half()
         wt = (torch.randn(cout, 3, 3, cin, device="cuda") / (9 * cin) ** 0.5).half()
@@ -269,8 +289,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", default=None,
-                    help="time one kernel instead: conv3x3, upconv3x3, rmsnorm, groupnorm, attention")
-    ap.add_argument("--shape", default="1024,1024,144,144", help="h,w,cin,cout (attention: h,w,c,c)")
+                    help="time one kernel instead: conv3x3, upconv3x3, conv3d, upconv3d, rmsnorm, groupnorm, "
+                         "attention")
+    ap.add_argument("--shape", default="1024,1024,144,144",
+                    help="h,w,cin,cout (attention: h,w,c,c; conv3d/upconv3d: f,h,w,cin,cout)")
     ap.add_argument("--residual", action="store_true")
     args = ap.parse_args()
     if args.kernel:

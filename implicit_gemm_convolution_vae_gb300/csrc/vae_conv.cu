@@ -120,6 +120,20 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvParams& p, int t) {
     int r = t / p.n_tiles;
     const int tx = r % p.tiles_x;
     r /= p.tiles_x;
+    if (p.frames_out > 1) {
+        // frames vary faster than rows: the tiles in flight hold a few rows of
+        // every frame, so the three temporal taps' source rows stay in L2
+        const int f = r % p.frames_out;
+        r /= p.frames_out;
+        ti.par = r % p.npar;
+        r /= p.npar;
+        const int ty = r % p.tiles_y;
+        ti.img = (r / p.tiles_y) * p.frames_out + f;
+        ti.v0 = ty * p.R;
+        ti.u0 = tx * p.Wt;
+        ti.n0 = nt * p.BN;
+        return ti;
+    }
     ti.par = r % p.npar;
     r /= p.npar;
     const int ty = r % p.tiles_y;
@@ -1474,7 +1488,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.npar = p.up ? 4 : 1;
     // Geometry that allows a halo box: a tile is 128 pixels of one row, 3x3 taps,
     // zero padding (the TMA box fills out-of-range pixels with zeros).
-    const bool halo_geom = !p.rep && !a.no_halo && a.taps == 9 && p.R == 1 && p.Wt == kBM;
+    const bool halo_geom = !p.rep && !a.no_halo && (a.taps == 9 || a.taps == 27) && p.R == 1 && p.Wt == kBM;
     p.BN = choose_bn(a.cout, halo_geom);
     p.b_rows = p.BN;
     p.n_tiles = (a.cout + p.BN - 1) / p.BN;

@@ -114,13 +114,16 @@ struct TileInfo {
     int img, par, v0, u0, n0;
 };
 
+// kT3: the 3x3x3 conv's instantiation (temporal taps, frames); the 2-D
+// kernels compile without any of it.
+template <bool kT3 = false>
 __device__ __forceinline__ TileInfo decode_tile(const ConvParams& p, int t) {
     TileInfo ti;
     const int nt = t % p.n_tiles;
     int r = t / p.n_tiles;
     const int tx = r % p.tiles_x;
     r /= p.tiles_x;
-    if (p.frames_out > 1) {
+    if (kT3 && p.frames_out > 1) {
         // frames vary faster than rows: the tiles in flight hold a few rows of
         // every frame, so the three temporal taps' source rows stay in L2
         const int f = r % p.frames_out;
@@ -148,8 +151,9 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvParams& p, int t) {
 // causal, the frames before the first replicate it; with the temporal 2x the
 // upsampled frame vf comes from source frame vf > 0 ? (vf - 1) / 2 + 1 : 0.
 // 2-D convs (one frame) use kt = 2 only: the image itself.
+template <bool kT3>
 __device__ __forceinline__ int src_img(const ConvParams& p, int img, int kt) {
-    if (p.frames_out == 1) return img;
+    if (!kT3 || p.frames_out == 1) return img;
     const int b = img / p.frames_out, f = img - b * p.frames_out;
     const int vf = max(f - 2 + kt, 0);
     const int sf = p.t_up ? (vf > 0 ? (vf - 1) / 2 + 1 : 0) : vf;
@@ -219,7 +223,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 // ───────────────────────────── roles ─────────────────────────────
 
-template <int kMode>
+template <int kMode, bool kT3>
 __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensorMap* mapA,
                               const CUtensorMap* mapB, const CUtensorMap* mapA16, const CUtensorMap* mapB16) {
     const uint64_t pol_w = policy_evict_last();
@@ -248,7 +252,7 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
         return fb;
     };
     for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(p, t);
+        const TileInfo ti = decode_tile<kT3>(p, t);
         if (p.res_prefetch) {
             // The tile's residual rows, one contiguous span, are pulled into L2 now
             // so the epilogue (a mainloop later) reads them at L2 latency.
@@ -266,8 +270,9 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
             const int q = ti.par >> 1, pp = ti.par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             const int kc_end = p.rem16 ? p.kfull : p.kchunks;
-            for (int kt = 0; kt < p.nkt && ok; ++kt) {
-                const int simg = src_img(p, ti.img, kt + 3 - p.nkt);
+            const int nkt = kT3 ? p.nkt : 1;
+            for (int kt = 0; kt < nkt && ok; ++kt) {
+                const int simg = src_img<kT3>(p, ti.img, kt + 3 - nkt);
                 for (int ky = 0; ky < 3 && ok; ++ky) {
                     const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
                     for (int kc = 0; kc < kc_end && ok; ++kc) {
@@ -300,8 +305,9 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
         } else if (kMode == kModeHalo) {
             const int q = ti.par >> 1, pp = ti.par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
-            for (int kt = 0; kt < p.nkt && ok; ++kt) {
-                const int simg = src_img(p, ti.img, kt + 3 - p.nkt);
+            const int nkt = kT3 ? p.nkt : 1;
+            for (int kt = 0; kt < nkt && ok; ++kt) {
+                const int simg = src_img<kT3>(p, ti.img, kt + 3 - nkt);
                 for (int ky = 0; ky < 3 && ok; ++ky) {
                     const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
                     for (int kc = 0; kc < p.kchunks && ok; ++kc) {
@@ -334,7 +340,7 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
             for (int tap = 0; tap < p.taps && ok; ++tap) {
                 int dy, dx;
                 tap_offset(p, tap, ti.par, dy, dx);
-                const int simg = src_img(p, ti.img, p.taps == 27 ? tap / 9 : 2);
+                const int simg = src_img<kT3>(p, ti.img, p.taps == 27 ? tap / 9 : 2);
                 for (int kc = 0; kc < p.kchunks; kc += p.ks) {
                     // one stage = up to ks consecutive 64-channel chunks of this tap
                     const int nck = min(p.ks, p.kchunks - kc);
@@ -363,19 +369,20 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
 
 // One thread per A row: gathers the row's 64-channel slice for each
 // (tap, chunk) with clamped (replicate) or zero-filled (zero) borders.
+template <bool kT3>
 __device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-        const TileInfo ti = decode_tile(p, t);
+        const TileInfo ti = decode_tile<kT3>(p, t);
         const int rr = gt / p.Wt, cc = gt % p.Wt;
         const int v = ti.v0 + rr, u = ti.u0 + cc;
         const bool rowvalid = gt < p.R * p.Wt && v < p.hv && u < p.wv;
         for (int tap = 0; tap < p.taps && ok; ++tap) {
             int dy, dx;
             tap_offset(p, tap, ti.par, dy, dx);
-            const int simg = src_img(p, ti.img, p.taps == 27 ? tap / 9 : 2);
+            const int simg = src_img<kT3>(p, ti.img, p.taps == 27 ? tap / 9 : 2);
             int sy = v + dy, sx = u + dx;
             bool inb;
             if (p.rep) {
@@ -413,6 +420,7 @@ __device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
     }
 }
 
+template <bool kT3>
 __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base) {
     const uint32_t idesc = idesc_f16_f32(kBM, p.BN);
     int stage = 0, astage = 0;
@@ -451,10 +459,10 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
         const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
         int kit = 0;
         if (p.halo && p.ks == 3) {
-            const int pp = decode_tile(p, t).par & 1;
+            const int pp = decode_tile<kT3>(p, t).par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             const int kc_end = p.rem16 ? p.kfull : p.kchunks;
-            for (int kt = 0; kt < p.nkt && ok; ++kt) {  // temporal taps (3-D); one pass for 2-D
+            for (int kt = 0; kt < (kT3 ? p.nkt : 1) && ok; ++kt) {  // temporal taps (3-D); one pass for 2-D
                 for (int ky = 0; ky < 3 && ok; ++ky) {
                     for (int kc = 0; kc < kc_end && ok; ++kc) {
                         if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
@@ -523,9 +531,9 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
                 }
             }
         } else if (p.halo) {
-            const int pp = decode_tile(p, t).par & 1;
+            const int pp = decode_tile<kT3>(p, t).par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
-            for (int kt = 0; kt < p.nkt && ok; ++kt)
+            for (int kt = 0; kt < (kT3 ? p.nkt : 1) && ok; ++kt)
                 for (int ky = 0; ky < 3 && ok; ++ky) {
                     for (int kc = 0; kc < p.kchunks && ok; ++kc) {
                         if (!mbar_wait(smem_u32(&s.afull[astage]), aphase, s.abort_flag, p.timeout_ns, p.status,
@@ -884,14 +892,14 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
     }
 }
 
-template <int kMode, bool kRms>
+template <int kMode, bool kRms, bool kT3>
 __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane,
                               const CUtensorMap* mapY) {
     const int row = ew * 32 + lane;
     int accbuf = 0;
     uint32_t accphase = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        const TileInfo ti = decode_tile(p, t);
+        const TileInfo ti = decode_tile<kT3>(p, t);
         if (!warp_all(mbar_wait(smem_u32(&s.accf[accbuf]), accphase, s.abort_flag, p.timeout_ns, p.status,
                                 kWhereEpiAccFull)))
             break;
@@ -922,7 +930,7 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
 
 // kRms: the fused RMS_norm epilogue (a separate instantiation, so the other
 // kernels do not carry its 144-value row in registers).
-template <int kMode, bool kRms>
+template <int kMode, bool kRms, bool kT3>
 __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     conv_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapA16, const __grid_constant__ CUtensorMap mapB16,
@@ -974,13 +982,13 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     const uint32_t tmem_base = *s.tmem_slot;
 
     if (warp < kEpiWarps) {
-        role_epilogue<kMode, kRms>(p, s, tmem_base, warp, lane, &mapY);
+        role_epilogue<kMode, kRms, kT3>(p, s, tmem_base, warp, lane, &mapY);
     } else if (warp == kProducerWarp) {
-        if (lane == 0) role_producer<kMode>(p, s, &mapA, &mapB, &mapA16, &mapB16);
+        if (lane == 0) role_producer<kMode, kT3>(p, s, &mapA, &mapB, &mapA16, &mapB16);
     } else if (warp == kMmaWarp) {
-        if (lane == 0) role_mma(p, s, tmem_base);
+        if (lane == 0) role_mma<kT3>(p, s, tmem_base);
     } else if (kMode == kModeGather && warp >= kGatherWarp0) {
-        role_gather(p, s, (warp - kGatherWarp0) * 32 + lane);
+        role_gather<kT3>(p, s, (warp - kGatherWarp0) * 32 + lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -1390,7 +1398,7 @@ int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& m
     return VAE_OK;
 }
 
-template <int kMode, bool kRms>
+template <int kMode, bool kRms, bool kT3 = false>
 int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma16,
            const CUtensorMap& mb16, const CUtensorMap& my, size_t smem, int grid, cudaStream_t stream) {
     static bool attr_set[64] = {false};
@@ -1398,10 +1406,10 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, co
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
         VAE_CUDA_CHECK(
-            cudaFuncSetAttribute(conv_kernel<kMode, kRms>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+            cudaFuncSetAttribute(conv_kernel<kMode, kRms, kT3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set[dev] = true;
     }
-    conv_kernel<kMode, kRms><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, ma16, mb16, my, p);
+    conv_kernel<kMode, kRms, kT3><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, ma16, mb16, my, p);
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -1709,6 +1717,11 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
             clear_error();
     }
     const size_t smem = 1024 + ring + (p.epi_tma ? kEpiWarps * kStgBytes : 0) + kTail;
+    if (a.taps == 27) {  // the 3x3x3 instantiations (no fused norm)
+        if (mode == kModeHalo) return launch<kModeHalo, false, true>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
+        if (mode == kModeGather) return launch<kModeGather, false, true>(p, ma, mb, ma, mb, my, smem, grid, stream);
+        return launch<kModeTma, false, true>(p, ma, mb, ma, mb, my, smem, grid, stream);
+    }
     if (p.rms_out != nullptr) {
         if (mode == kModeHalo) return launch<kModeHalo, true>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
         if (mode == kModeGather) return launch<kModeGather, true>(p, ma, mb, ma, mb, my, smem, grid, stream);

@@ -225,7 +225,11 @@ def run_kernel(args):
         H, W = (2 * h, 2 * w) if up else (h, w)
         y = torch.empty(1, H, W, cout, device="cuda")
         res = torch.randn(1, H, W, cout, device="cuda") if args.residual else None
-        fn = lambda: vg.conv3x3_nhwc(x, wt, b, residual=res, out=y, upsample=up)
+        if args.subpixel and up:  # the sub-pixel form, credited at the 9-tap FLOP count
+            wsub = vg.pack_subpixel_weights(wt)
+            fn = lambda: vg.conv3x3_nhwc(x, wsub, b, residual=res, out=y, upsample=True, subpixel=True)
+        else:
+            fn = lambda: vg.conv3x3_nhwc(x, wt, b, residual=res, out=y, upsample=up)
         flops = 2.0 * H * W * cout * 9 * cin
         nbytes = x.numel() * 2 + y.numel() * 4 * (2 if args.residual else 1)
     elif args.kernel == "rmsnorm":
@@ -294,6 +298,7 @@ def main():
     ap.add_argument("--shape", default="1024,1024,144,144",
                     help="h,w,cin,cout (attention: h,w,c,c; conv3d/upconv3d: f,h,w,cin,cout)")
     ap.add_argument("--residual", action="store_true")
+    ap.add_argument("--subpixel", action="store_true", help="upconv3x3 in the sub-pixel form")
     args = ap.parse_args()
     if args.kernel:
         return run_kernel(args)

@@ -28,7 +28,7 @@ __all__ = [
     "NORM_GROUP", "NORM_RMS",
 ]
 
-UPSAMPLE2X, PAD_REPLICATE, EPI_SILU, OUT_F16, UPSAMPLE_T2X = 1, 2, 16, 32, 64
+UPSAMPLE2X, PAD_REPLICATE, EPI_SILU, OUT_F16, UPSAMPLE_T2X, UPSAMPLE2X_SUBPIXEL = 1, 2, 16, 32, 64, 128
 FAMILY_GN, FAMILY_RMS = 0, 1
 NORM_GROUP, NORM_RMS = 0, 1
 
@@ -58,6 +58,7 @@ SIGNATURES = {
     "vae_selftest_wait_timeout": ([ctypes.c_ulonglong, _P], _I),
     "vae_conv3x3_nhwc": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _P], _I),
     "vae_conv3d_causal_ndhwc": ([_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _P], _I),
+    "vae_pack_subpixel_weights": ([_P, _I, _I, _P, _P], _I),
     "vae_conv1x1": ([_P, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _P], _I),
     "vae_rmsnorm_silu": ([_P, _I, _I, _P, _P, _I, _F, _P, _P], _I),
     "vae_groupnorm_workspace_bytes": ([_I, _I, _I, _I], _SZ),
@@ -147,17 +148,29 @@ def selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None) -> int:
     return lib().vae_selftest_wait_timeout(int(timeout_ns), _stream(stream))
 
 
+def pack_subpixel_weights(w, stream=None):
+    """f16 [cout][3][3][cin] -> the up conv's sub-pixel weights f16 [cout][16][cin] (device)."""
+    import torch
+    _need(w, torch.float16, "w", 4)
+    cout, _, _, cin = w.shape
+    ws = torch.empty((cout, 16, cin), dtype=torch.float16, device=w.device)
+    _check(lib().vae_pack_subpixel_weights(_ptr(w), cout, cin, _ptr(ws), _stream(stream)))
+    return ws
+
+
 def conv3x3_nhwc(x, w, bias=None, residual=None, out=None, oscale: float = 1.0, upsample: bool = False,
-                 replicate: bool = False, silu: bool = False, out_f16: bool = False, stream=None):
-    """3x3 implicit-GEMM conv. x f16 [n][h][w][cin]; w f16 [cout][3][3][cin]."""
+                 replicate: bool = False, silu: bool = False, out_f16: bool = False, subpixel: bool = False,
+                 stream=None):
+    """3x3 implicit-GEMM conv. x f16 [n][h][w][cin]; w f16 [cout][3][3][cin], or with
+    ``subpixel`` (an up conv) the summed weights [cout][16][cin] of pack_subpixel_weights."""
     import torch
     _need(x, torch.float16, "x", 4)
-    _need(w, torch.float16, "w", 4)
+    _need(w, torch.float16, "w", 3 if subpixel else 4)
     _need(bias, torch.float32, "bias", 1)
     n, h, wd, cin = x.shape
     cout = w.shape[0]
-    if tuple(w.shape[1:]) != (3, 3, cin):
-        raise VaeError(-2, f"w must be [cout][3][3][{cin}], got {tuple(w.shape)}")
+    if tuple(w.shape[1:]) != ((16, cin) if subpixel else (3, 3, cin)):
+        raise VaeError(-2, f"w has the wrong shape {tuple(w.shape)}")
     H, W = (2 * h, 2 * wd) if upsample else (h, wd)
     odt = torch.float16 if out_f16 else torch.float32
     if out is None:
@@ -165,7 +178,7 @@ def conv3x3_nhwc(x, w, bias=None, residual=None, out=None, oscale: float = 1.0, 
     _need(out, odt, "out")
     _need(residual, torch.float32, "residual")
     flags = (UPSAMPLE2X if upsample else 0) | (PAD_REPLICATE if replicate else 0) | \
-            (EPI_SILU if silu else 0) | (OUT_F16 if out_f16 else 0)
+            (EPI_SILU if silu else 0) | (OUT_F16 if out_f16 else 0) | (UPSAMPLE2X_SUBPIXEL if subpixel else 0)
     _check(lib().vae_conv3x3_nhwc(_ptr(x), n, h, wd, cin, _ptr(w), _ptr(bias), _ptr(residual), _ptr(out),
                                   cout, float(oscale), flags, _stream(stream)))
     return out
@@ -344,6 +357,7 @@ class _DecoderDesc(ctypes.Structure):
 DECODE_PROFILE = 1
 DECODE_NO_FUSION = 2
 DECODE_FUSE_NORM = 4
+DECODE_SUBPIXEL_UP = 8
 STAGE_NAMES = {0: "conv3x3", 1: "conv1x1", 2: "norm", 3: "cast", 4: "attention", 5: "layout", 6: "copy"}
 
 
@@ -429,9 +443,10 @@ class Decoder:
 
     @staticmethod
     def opts(band_from: int = 0, nbands: int = 0, band_rows: int = 0, guard_log2: int = 8,
-             profile: bool = False, fuse: bool = False) -> DecodeOpts:
+             profile: bool = False, fuse: bool = False, subpixel: bool = False) -> DecodeOpts:
         return DecodeOpts(band_from, nbands, band_rows, guard_log2,
-                          (DECODE_PROFILE if profile else 0) | (DECODE_FUSE_NORM if fuse else 0))
+                          (DECODE_PROFILE if profile else 0) | (DECODE_FUSE_NORM if fuse else 0) |
+                          (DECODE_SUBPIXEL_UP if subpixel else 0))
 
     def profile(self):
         """Stage records of the most recent profiled decode, as dicts (synchronises)."""

@@ -73,6 +73,8 @@ struct ConvParams {
     int frames_out, frames_in, t_up, nkt;  // 3-D causal conv: output / input frames per image, temporal 2x,
                                             // temporal taps (3; 1 for 2-D convs, whose frames are 1)
     int n_in;             // input images (batch x input frames; = n for 2-D convs)
+    int subpix;           // up conv as four 2x2 convs on the source grid (weights [cout][16][cin]):
+                          // tap (ty, tx) of parity class par reads source (v + dymin + ty, u + dxmin + tx)
     int rem16, kfull;     // three-tap halo stages with cin % 64 == 16: kfull 64-channel chunks, then one
                           // stage of 16-channel boxes (32-byte swizzle) for all three ky and nine taps
     int halo, a_stages;   // halo mode: a_stages halo boxes; B ring of `stages` x ks taps
@@ -147,6 +149,10 @@ __device__ __forceinline__ TileInfo decode_tile(const ConvParams& p, int t) {
     return ti;
 }
 
+// Weight tap (second coordinate of the B tensor) of kernel tap `tap` for parity
+// class `par`: the sub-pixel weights hold four taps per parity class.
+__device__ __forceinline__ int b_tap(const ConvParams& p, int par, int tap) { return p.subpix ? par * 4 + tap : tap; }
+
 // Source image of output image `img` for temporal tap kt (0..2, frame f + kt - 2):
 // causal, the frames before the first replicate it; with the temporal 2x the
 // upsampled frame vf comes from source frame vf > 0 ? (vf - 1) / 2 + 1 : 0.
@@ -166,6 +172,11 @@ __device__ __forceinline__ void tap_offset(const ConvParams& p, int tap, int par
     if (p.taps == 1) {
         dy = 0;
         dx = 0;
+        return;
+    }
+    if (p.subpix) {  // four taps per parity class: rows / columns (q|p == 0 ? -1 : 0) + {0, 1}
+        dy = ((par >> 1) == 0 ? -1 : 0) + tap / 2;
+        dx = ((par & 1) == 0 ? -1 : 0) + tap % 2;
         return;
     }
     const int ky = (tap % 9) / 3, kx = tap % 3;
@@ -223,7 +234,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 
 // ───────────────────────────── roles ─────────────────────────────
 
-template <int kMode, bool kT3>
+// kVar: 0 the 2-D conv, 1 the 3x3x3 conv (temporal taps), 2 the sub-pixel up
+// conv (2 x 2 taps per parity class). Each is its own instantiation.
+template <int kMode, int kVar>
 __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensorMap* mapA,
                               const CUtensorMap* mapB, const CUtensorMap* mapA16, const CUtensorMap* mapB16) {
     const uint64_t pol_w = policy_evict_last();
@@ -252,6 +265,8 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
         return fb;
     };
     for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        constexpr bool kT3 = kVar == 1;
+        constexpr int NK = kVar == 2 ? 2 : 3;  // ky and kx taps per stage row
         const TileInfo ti = decode_tile<kT3>(p, t);
         if (p.res_prefetch) {
             // The tile's residual rows, one contiguous span, are pulled into L2 now
@@ -271,34 +286,37 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             const int kc_end = p.rem16 ? p.kfull : p.kchunks;
             const int nkt = kT3 ? p.nkt : 1;
+            const int dymin = q == 0 ? -1 : 0;  // the sub-pixel variant's first source row
             for (int kt = 0; kt < nkt && ok; ++kt) {
                 const int simg = src_img<kT3>(p, ti.img, kt + 3 - nkt);
-                for (int ky = 0; ky < 3 && ok; ++ky) {
-                    const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                for (int ky = 0; ky < NK && ok; ++ky) {
+                    const int dy = kVar == 2 ? dymin + ky : (p.up ? (q + ky + 1) / 2 - 1 : ky - 1);
                     for (int kc = 0; kc < kc_end && ok; ++kc) {
                         uint32_t slot;
-                        const uint32_t fb = next_b(p.a_tx + 3u * b_bytes, &slot);
+                        const uint32_t fb = next_b(p.a_tx + static_cast<uint32_t>(NK) * b_bytes, &slot);
                         if (!ok) break;
                         tma_load_4d(smem_u32(s.a + slot * kHaloBytes), mapA, fb, kc * kBK, ti.u0 + dxmin, ti.v0 + dy,
                                     simg, pol_a);
-                        for (int kx = 0; kx < 3; ++kx)
+                        for (int kx = 0; kx < NK; ++kx)
                             tma_load_3d(smem_u32(s.b + (slot * 3 + kx) * p.BN * 128), mapB, fb, kc * kBK,
-                                        kt * 9 + ky * 3 + kx, ti.n0, pol_w);
+                                        kVar == 2 ? ti.par * 4 + ky * 2 + kx : kt * 9 + ky * 3 + kx, ti.n0, pol_w);
                     }
                 }
                 if (p.rem16 && ok) {
-                    // the last 16 channels of all three ky and nine (ky, kx) taps in one stage
+                    // the last 16 channels of all ky rows and (ky, kx) taps in one stage
                     uint32_t slot;
-                    const uint32_t fb = next_b(3u * kRemABytes + 9u * static_cast<uint32_t>(p.BN) * 32u, &slot);
+                    const uint32_t fb = next_b(static_cast<uint32_t>(NK) * kRemABytes +
+                                                   static_cast<uint32_t>(NK * NK) * static_cast<uint32_t>(p.BN) * 32u,
+                                               &slot);
                     if (ok) {
-                        for (int ky = 0; ky < 3; ++ky) {
-                            const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                        for (int ky = 0; ky < NK; ++ky) {
+                            const int dy = kVar == 2 ? dymin + ky : (p.up ? (q + ky + 1) / 2 - 1 : ky - 1);
                             tma_load_4d(smem_u32(s.a + slot * kHaloBytes + ky * kRemAStride), mapA16, fb,
                                         p.kfull * kBK, ti.u0 + dxmin, ti.v0 + dy, simg, pol_a);
                         }
-                        for (int tap = 0; tap < 9; ++tap)
+                        for (int tap = 0; tap < NK * NK; ++tap)
                             tma_load_3d(smem_u32(s.b + slot * 3 * p.BN * 128 + tap * p.BN * 32), mapB16, fb,
-                                        p.kfull * kBK, kt * 9 + tap, ti.n0, pol_w);
+                                        p.kfull * kBK, kVar == 2 ? ti.par * 4 + tap : kt * 9 + tap, ti.n0, pol_w);
                     }
                 }
             }
@@ -352,8 +370,8 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
                         if (kMode == kModeTma)
                             tma_load_4d(smem_u32(s.a + (slot * p.ks + h) * kABytes), mapA, fb, (kc + h) * kBK,
                                         ti.u0 + dx, ti.v0 + dy, simg, pol_a);
-                        tma_load_3d(smem_u32(s.b + (slot * p.ks + h) * p.BN * 128), mapB, fb, (kc + h) * kBK, tap,
-                                    ti.n0, pol_w);
+                        tma_load_3d(smem_u32(s.b + (slot * p.ks + h) * p.BN * 128), mapB, fb, (kc + h) * kBK,
+                                    b_tap(p, ti.par, tap), ti.n0, pol_w);
                     }
                 }
             }
@@ -369,8 +387,9 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
 
 // One thread per A row: gathers the row's 64-channel slice for each
 // (tap, chunk) with clamped (replicate) or zero-filled (zero) borders.
-template <bool kT3>
+template <int kVar>
 __device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
+    constexpr bool kT3 = kVar == 1;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -420,8 +439,10 @@ __device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
     }
 }
 
-template <bool kT3>
+template <int kVar>
 __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base) {
+    constexpr bool kT3 = kVar == 1;
+    constexpr int NK = kVar == 2 ? 2 : 3;  // ky and kx taps per stage row
     const uint32_t idesc = idesc_f16_f32(kBM, p.BN);
     int stage = 0, astage = 0;
     uint32_t phase = 0, aphase = 0;
@@ -463,7 +484,7 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             const int kc_end = p.rem16 ? p.kfull : p.kchunks;
             for (int kt = 0; kt < (kT3 ? p.nkt : 1) && ok; ++kt) {  // temporal taps (3-D); one pass for 2-D
-                for (int ky = 0; ky < 3 && ok; ++ky) {
+                for (int ky = 0; ky < NK && ok; ++ky) {
                     for (int kc = 0; kc < kc_end && ok; ++kc) {
                         if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
                                        kWhereMmaFull)) {
@@ -477,10 +498,10 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
                         const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
                         const uint32_t bbase = smem_u32(s.b + stage * 3 * p.BN * 128);
     #pragma unroll
-                        for (int kx = 0; kx < 3; ++kx) {
-                            const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
+                        for (int kx = 0; kx < NK; ++kx) {
+                            const int rel = kVar == 2 ? kx : (p.up ? (pp + kx + 1) / 2 - 1 : kx - 1) - dxmin;
                             // a whole-row offset: the tensor core swizzles on absolute address bits
-                            const uint64_t ad = sw128_kmajor_desc(abase + static_cast<uint32_t>((dx - dxmin) * 128));
+                            const uint64_t ad = sw128_kmajor_desc(abase + static_cast<uint32_t>(rel * 128));
                             const uint64_t bd = sw128_kmajor_desc(bbase + static_cast<uint32_t>(kx * p.BN * 128));
                             if (nk == 4) {
     #pragma unroll
@@ -511,14 +532,14 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
                         const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
                         const uint32_t bbase = smem_u32(s.b + stage * 3 * p.BN * 128);
     #pragma unroll
-                        for (int ky = 0; ky < 3; ++ky)
+                        for (int ky = 0; ky < NK; ++ky)
     #pragma unroll
-                            for (int kx = 0; kx < 3; ++kx) {
-                                const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
+                            for (int kx = 0; kx < NK; ++kx) {
+                                const int rel = kVar == 2 ? kx : (p.up ? (pp + kx + 1) / 2 - 1 : kx - 1) - dxmin;
                                 const uint64_t ad = sw32_kmajor_desc(abase + static_cast<uint32_t>(ky * kRemAStride) +
-                                                                     static_cast<uint32_t>((dx - dxmin) * 32));
+                                                                     static_cast<uint32_t>(rel * 32));
                                 const uint64_t bd =
-                                    sw32_kmajor_desc(bbase + static_cast<uint32_t>((ky * 3 + kx) * p.BN * 32));
+                                    sw32_kmajor_desc(bbase + static_cast<uint32_t>((ky * NK + kx) * p.BN * 32));
                                 umma_f16(d, ad, bd, idesc, 1u);
                             }
                         umma_commit(smem_u32(&s.empty[stage]));
@@ -892,14 +913,14 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
     }
 }
 
-template <int kMode, bool kRms, bool kT3>
+template <int kMode, bool kRms, int kVar>
 __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane,
                               const CUtensorMap* mapY) {
     const int row = ew * 32 + lane;
     int accbuf = 0;
     uint32_t accphase = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
-        const TileInfo ti = decode_tile<kT3>(p, t);
+        const TileInfo ti = decode_tile<kVar == 1>(p, t);
         if (!warp_all(mbar_wait(smem_u32(&s.accf[accbuf]), accphase, s.abort_flag, p.timeout_ns, p.status,
                                 kWhereEpiAccFull)))
             break;
@@ -930,7 +951,7 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
 
 // kRms: the fused RMS_norm epilogue (a separate instantiation, so the other
 // kernels do not carry its 144-value row in registers).
-template <int kMode, bool kRms, bool kT3>
+template <int kMode, bool kRms, int kVar>
 __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     conv_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapA16, const __grid_constant__ CUtensorMap mapB16,
@@ -982,13 +1003,13 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
     const uint32_t tmem_base = *s.tmem_slot;
 
     if (warp < kEpiWarps) {
-        role_epilogue<kMode, kRms, kT3>(p, s, tmem_base, warp, lane, &mapY);
+        role_epilogue<kMode, kRms, kVar>(p, s, tmem_base, warp, lane, &mapY);
     } else if (warp == kProducerWarp) {
-        if (lane == 0) role_producer<kMode, kT3>(p, s, &mapA, &mapB, &mapA16, &mapB16);
+        if (lane == 0) role_producer<kMode, kVar>(p, s, &mapA, &mapB, &mapA16, &mapB16);
     } else if (warp == kMmaWarp) {
-        if (lane == 0) role_mma<kT3>(p, s, tmem_base);
+        if (lane == 0) role_mma<kVar>(p, s, tmem_base);
     } else if (kMode == kModeGather && warp >= kGatherWarp0) {
-        role_gather<kT3>(p, s, (warp - kGatherWarp0) * 32 + lane);
+        role_gather<kVar>(p, s, (warp - kGatherWarp0) * 32 + lane);
     }
     tc_fence_before();
     __syncthreads();
@@ -1398,7 +1419,7 @@ int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& m
     return VAE_OK;
 }
 
-template <int kMode, bool kRms, bool kT3 = false>
+template <int kMode, bool kRms, int kVar = 0>
 int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma16,
            const CUtensorMap& mb16, const CUtensorMap& my, size_t smem, int grid, cudaStream_t stream) {
     static bool attr_set[64] = {false};
@@ -1406,10 +1427,10 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, co
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
         VAE_CUDA_CHECK(
-            cudaFuncSetAttribute(conv_kernel<kMode, kRms, kT3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+            cudaFuncSetAttribute(conv_kernel<kMode, kRms, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set[dev] = true;
     }
-    conv_kernel<kMode, kRms, kT3><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, ma16, mb16, my, p);
+    conv_kernel<kMode, kRms, kVar><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, ma16, mb16, my, p);
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -1424,6 +1445,8 @@ int conv_validate(const ConvArgs& a) {
         return set_error(VAE_ERR_ARG, "conv: frames_in=%d / temporal upsample need the 3x3x3 conv", a.frames_in);
     if (a.taps == 27 && (a.rms_out != nullptr || a.dup_src != nullptr || a.out_nchw))
         return set_error(VAE_ERR_ARG, "conv: the 3x3x3 conv has no fused norm, DupUp or NCHW output");
+    if (a.subpix && (!a.up || a.taps != 9 || a.rms_out != nullptr))
+        return set_error(VAE_ERR_ARG, "conv: the sub-pixel form is the 3x3 up conv's (no fused norm)");
     if (a.n < 1 || a.h_in < 1 || a.w_in < 1)
         return set_error(VAE_ERR_SHAPE, "conv: n=%d h=%d w=%d must be >= 1", a.n, a.h_in, a.w_in);
     if (a.cin < 16 || a.cin % 16 != 0 || a.cin > 8192)
@@ -1479,7 +1502,8 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.wv = a.w_in;
     p.cin = a.cin;
     p.cout = a.cout;
-    p.taps = a.taps;
+    p.subpix = a.subpix ? 1 : 0;
+    p.taps = a.subpix ? 4 : a.taps;  // taps per parity class
     p.up = a.up ? 1 : 0;
     p.rep = a.rep ? 1 : 0;
     p.H = p.up ? 2 * a.h_in : a.h_in;
@@ -1562,10 +1586,11 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.timeout_ns = wait_timeout_ns();
 
     CUtensorMap ma{}, mb{}, ma16{}, mb16{}, my{};
+    const int wtaps = a.subpix ? 16 : a.taps;  // weight taps: the sub-pixel form holds 4 per parity class
     {
-        const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(a.taps),
+        const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(wtaps),
                                   static_cast<uint64_t>(a.cout)};
-        const uint64_t strides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(a.taps) * a.cin * 2};
+        const uint64_t strides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(wtaps) * a.cin * 2};
         const uint32_t box[3] = {static_cast<uint32_t>(kBK), 1u, static_cast<uint32_t>(p.BN)};
         rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B);
@@ -1576,7 +1601,9 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // tap per stage, which measured faster than per-tap A tiles only for
     // narrow inputs (cin <= 192).
     const int st3 = (kMaxSmem - 1024 - kTail) / (kHaloBytes + 3 * p.BN * 128);
-    if (mode == kModeTma && halo_geom && (st3 >= 3 || a.cin <= 192)) {
+    // (The one-tap halo ring has no sub-pixel form: that variant takes the halo
+    // path only with three-tap stages.)
+    if (mode == kModeTma && halo_geom && (st3 >= 3 || (a.cin <= 192 && !a.subpix))) {
         // one 130-pixel halo box per (ky, chunk), shared by the three kx taps
         const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(p.wv),
                                   static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n_in)};
@@ -1598,10 +1625,10 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                 if (a.cin % kBK == 16 && a.cin > kBK) {
                     // exact 16-channel boxes for the remainder instead of zero-filled 64-channel ones
                     const uint32_t box16[4] = {16u, static_cast<uint32_t>(kHaloRows), 1u, 1u};
-                    const uint64_t bdims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(a.taps),
+                    const uint64_t bdims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(wtaps),
                                                static_cast<uint64_t>(a.cout)};
                     const uint64_t bstrides[2] = {static_cast<uint64_t>(a.cin) * 2,
-                                                  static_cast<uint64_t>(a.taps) * a.cin * 2};
+                                                  static_cast<uint64_t>(wtaps) * a.cin * 2};
                     const uint32_t bbox16[3] = {16u, 1u, static_cast<uint32_t>(p.BN)};
                     if (encode_tiled(&ma16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.x, dims, strides, box16,
                                      CU_TENSOR_MAP_SWIZZLE_32B) == VAE_OK &&
@@ -1642,7 +1669,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // than single CTAs on GB300 at every decoder shape, so they run only when
     // requested (VAE_CONV_CTA_PAIR=1 in the environment).
     if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2 &&
-        a.taps != 27) {
+        a.taps != 27 && !a.subpix) {
         // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
         p.pair = 1;
         p.rem16 = 0;  // the pair kernel loads zero-filled 64-channel remainder boxes
@@ -1653,9 +1680,9 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         const long long pt = static_cast<long long>(p.n) * p.typ_tiles * p.npar * p.tiles_x * p.n_tiles;
         if (pt >= (1LL << 31)) return set_error(VAE_ERR_SHAPE, "conv: too many tiles");
         p.pair_tiles = static_cast<int>(pt);
-        const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(a.taps),
+        const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(wtaps),
                                   static_cast<uint64_t>(a.cout)};
-        const uint64_t strides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(a.taps) * a.cin * 2};
+        const uint64_t strides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(wtaps) * a.cin * 2};
         const uint32_t box[3] = {static_cast<uint32_t>(kBK), 1u, static_cast<uint32_t>(p.b_rows)};
         rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B);
@@ -1718,9 +1745,14 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     }
     const size_t smem = 1024 + ring + (p.epi_tma ? kEpiWarps * kStgBytes : 0) + kTail;
     if (a.taps == 27) {  // the 3x3x3 instantiations (no fused norm)
-        if (mode == kModeHalo) return launch<kModeHalo, false, true>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
-        if (mode == kModeGather) return launch<kModeGather, false, true>(p, ma, mb, ma, mb, my, smem, grid, stream);
-        return launch<kModeTma, false, true>(p, ma, mb, ma, mb, my, smem, grid, stream);
+        if (mode == kModeHalo) return launch<kModeHalo, false, 1>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
+        if (mode == kModeGather) return launch<kModeGather, false, 1>(p, ma, mb, ma, mb, my, smem, grid, stream);
+        return launch<kModeTma, false, 1>(p, ma, mb, ma, mb, my, smem, grid, stream);
+    }
+    if (a.subpix) {  // the sub-pixel up conv instantiations
+        if (mode == kModeHalo) return launch<kModeHalo, false, 2>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
+        if (mode == kModeGather) return launch<kModeGather, false, 2>(p, ma, mb, ma, mb, my, smem, grid, stream);
+        return launch<kModeTma, false, 2>(p, ma, mb, ma, mb, my, smem, grid, stream);
     }
     if (p.rms_out != nullptr) {
         if (mode == kModeHalo) return launch<kModeHalo, true>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
@@ -1730,6 +1762,47 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     if (mode == kModeHalo) return launch<kModeHalo, false>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
     if (mode == kModeGather) return launch<kModeGather, false>(p, ma, mb, ma, mb, my, smem, grid, stream);
     return launch<kModeTma, false>(p, ma, mb, ma, mb, my, smem, grid, stream);
+}
+
+// Summed weights of the up conv's sub-pixel form: w [cout][9][cin] (tap
+// ky*3+kx) -> ws [cout][16][cin] (tap (q*2+p)*4 + ty*2 + tx). Row ty of parity q
+// collects ky in {0} | {1, 2} (q = 0) or {0, 1} | {2} (q = 1); columns alike.
+// Summed in f32 in (ky, kx) order, rounded to f16 once.
+__global__ void pack_subpixel_kernel(const __half* __restrict__ w, int cout, int cin, __half* __restrict__ ws) {
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= static_cast<long long>(cout) * cin) return;
+    const int o = static_cast<int>(i / cin), c = static_cast<int>(i % cin);
+    float t[9];
+#pragma unroll
+    for (int k = 0; k < 9; ++k) t[k] = __half2float(w[(static_cast<long long>(o) * 9 + k) * cin + c]);
+    // first and last source row (tap index range) of row ty for parity q
+    const int lo[2][2] = {{0, 1}, {0, 2}}, hi[2][2] = {{0, 2}, {1, 2}};
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp)
+#pragma unroll
+            for (int ty = 0; ty < 2; ++ty)
+#pragma unroll
+                for (int tx = 0; tx < 2; ++tx) {
+                    float acc = 0.f;
+                    for (int ky = lo[q][ty]; ky <= hi[q][ty]; ++ky)
+                        for (int kx = lo[pp][tx]; kx <= hi[pp][tx]; ++kx) acc += t[ky * 3 + kx];
+                    ws[(static_cast<long long>(o) * 16 + (q * 2 + pp) * 4 + ty * 2 + tx) * cin + c] = __float2half_rn(acc);
+                }
+}
+
+int pack_subpixel_run(const void* w, int cout, int cin, void* ws, cudaStream_t stream) {
+    if (w == nullptr || ws == nullptr) return set_error(VAE_ERR_ARG, "pack_subpixel: w and ws must be non-NULL");
+    if (cout < 1 || cout > (1 << 20) || cin < 1 || cin > 8192)
+        return set_error(VAE_ERR_SHAPE, "pack_subpixel: cout=%d cin=%d", cout, cin);
+    int rc = check_device();
+    if (rc != VAE_OK) return rc;
+    const long long n = static_cast<long long>(cout) * cin;
+    pack_subpixel_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+        static_cast<const __half*>(w), cout, cin, static_cast<__half*>(ws));
+    VAE_CUDA_CHECK(cudaGetLastError());
+    return VAE_OK;
 }
 
 }  // namespace vae
@@ -1742,8 +1815,11 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin, cons
                      const float* bias_dev, const float* residual_dev, void* y_dev, int cout, float oscale,
                      unsigned flags, vae_stream_t stream) {
     clear_error();
-    if (flags & ~static_cast<unsigned>(VAE_UPSAMPLE2X | VAE_PAD_REPLICATE | VAE_EPI_SILU | VAE_OUT_F16))
+    if (flags & ~static_cast<unsigned>(VAE_UPSAMPLE2X | VAE_UPSAMPLE2X_SUBPIXEL | VAE_PAD_REPLICATE | VAE_EPI_SILU |
+                                       VAE_OUT_F16))
         return set_error(VAE_ERR_ARG, "vae_conv3x3_nhwc: unknown flag bits 0x%x", flags);
+    if ((flags & VAE_UPSAMPLE2X_SUBPIXEL) && !(flags & VAE_UPSAMPLE2X))
+        return set_error(VAE_ERR_ARG, "vae_conv3x3_nhwc: the sub-pixel form needs VAE_UPSAMPLE2X");
     ConvArgs a{};
     a.x = x_dev;
     a.n = n;
@@ -1753,6 +1829,7 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin, cons
     a.w = w_dev;
     a.cout = cout;
     a.taps = 9;
+    a.subpix = (flags & VAE_UPSAMPLE2X_SUBPIXEL) != 0;
     a.bias = bias_dev;
     a.residual = residual_dev;
     a.y = y_dev;
@@ -1762,6 +1839,13 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin, cons
     a.silu = (flags & VAE_EPI_SILU) != 0;
     a.out_f16 = (flags & VAE_OUT_F16) != 0;
     return conv_run(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int vae_pack_subpixel_weights(const void* w_dev, int cout, int cin, void* w_sub_dev, vae_stream_t stream) {
+    clear_error();
+    if (!aligned16(w_dev) || !aligned16(w_sub_dev))
+        return set_error(VAE_ERR_ALIGN, "vae_pack_subpixel_weights: pointers must be 16-byte aligned");
+    return pack_subpixel_run(w_dev, cout, cin, w_sub_dev, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int vae_conv3d_causal_ndhwc(const void* x_dev, int n, int f_in, int h_in, int w_in, int cin, const void* w_dev,

@@ -16,6 +16,9 @@ struct ConvArgs {
     // y holds n images of frames_out = t_up ? 2 * frames_in - 1 : frames_in frames.
     int frames_in = 1;
     bool t_up = false;
+    // The up conv (up, taps 9) as four 2x2 convs on the source grid: w holds the
+    // summed weights [cout][16][cin], tap (q*2+p)*4 + ty*2 + tx (vae_pack_subpixel_weights).
+    bool subpix = false;
     const float* bias = nullptr;
     const float* residual = nullptr;  // f32 NHWC [n][H][W][cout]; may alias y
     void* y = nullptr;
@@ -42,6 +45,8 @@ struct ConvArgs {
 };
 
 int conv_validate(const ConvArgs& a);
+// w [cout][3][3][cin] f16 -> the sub-pixel form's summed weights [cout][16][cin] f16.
+int pack_subpixel_run(const void* w, int cout, int cin, void* ws, cudaStream_t stream);
 int conv_run(const ConvArgs& a, cudaStream_t stream);
 
 }  // namespace vae

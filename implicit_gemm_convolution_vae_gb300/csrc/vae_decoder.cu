@@ -56,6 +56,7 @@ struct DAttn {
 struct DUp {
     std::vector<DRes> res;
     DConv up;
+    __half* wsub = nullptr;  // the up conv's sub-pixel weights [cout][16][cin] (VAE_DECODE_SUBPIXEL_UP)
     int in_dim = 0, out_dim = 0, ft = 1;
 };
 
@@ -199,6 +200,7 @@ struct Exec {
     float guard = 256.f;
     vae_decoder* prof = nullptr;  // non-null: record events around stages
     bool fuse = false;            // VAE_DECODE_FUSE_NORM without VAE_DECODE_NO_FUSION
+    bool subpix = false;          // VAE_DECODE_SUBPIXEL_UP
     // RMS_norm rides in the epilogue of a ResNet's first conv (whose f32 output
     // only feeds that norm) when its CTA holds all of a pixel's channels (one N
     // tile of <= 144). Measured on GB300: a win there (no f32 write, no norm
@@ -382,6 +384,10 @@ struct Exec {
             ConvArgs a = c3(xn, f.n(), w, u.up, y);
             a.up = true;
             a.oscale = guard;
+            if (subpix && u.wsub != nullptr) {  // the four 2x2 convs with the summed weights
+                a.w = u.wsub;
+                a.subpix = true;
+            }
             if (d->dupup) {
                 const float* src = f32(bufs[in_b], hw * u.in_dim);
                 a.dup_src = src + (dry ? 0 : skip_px * u.in_dim);
@@ -467,6 +473,7 @@ int run_decode(Exec& X, int h0, int w0, const vae_decode_opts* opts, const float
     int rc;
     X.guard = std::ldexp(1.0f, opts ? (opts->guard_log2 < 0 ? 8 : std::min(opts->guard_log2, 14)) : 8);
     X.fuse = opts != nullptr && (opts->flags & VAE_DECODE_FUSE_NORM) != 0 && (opts->flags & VAE_DECODE_NO_FUSION) == 0;
+    X.subpix = opts != nullptr && (opts->flags & VAE_DECODE_SUBPIXEL_UP) != 0;
     int nbands = 1;
     if (opts && opts->band_rows > 0) nbands = (hf + opts->band_rows - 1) / opts->band_rows;
     if (opts && opts->nbands > 1) nbands = opts->nbands;
@@ -668,6 +675,19 @@ int vae_decoder_create(const vae_decoder_desc* desc, vae_decoder_t* out) {
                     U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: DupUp of block %d: in %d out %d ft %d", i,
                                      u.in_dim, u.out_dim, u.ft);
             }
+            if (U.rc == VAE_OK) {  // the sub-pixel weights, for decodes that ask for that form
+                void* ws = nullptr;
+                const size_t bytes = static_cast<size_t>(u.up.cout) * 16 * u.up.cin * 2;
+                if (cudaMalloc(&ws, bytes) != cudaSuccess) {
+                    U.rc = set_error(VAE_ERR_NOMEM, "decoder_create: cudaMalloc(%zu) for sub-pixel weights", bytes);
+                } else {
+                    d->allocs.push_back(ws);
+                    u.wsub = static_cast<__half*>(ws);
+                    U.rc = pack_subpixel_run(u.up.w, u.up.cout, u.up.cin, ws, nullptr);
+                    if (U.rc == VAE_OK && cudaDeviceSynchronize() != cudaSuccess)
+                        U.rc = set_error(VAE_ERR_CUDA, "decoder_create: packing the sub-pixel weights failed");
+                }
+            }
             ch = u.up.cout;
         }
         d->ups.push_back(std::move(u));
@@ -731,7 +751,8 @@ static int decode_impl(vae_decoder_t dec, const float* z, int h0, int w0, float*
     if (dec == nullptr || z == nullptr || out == nullptr || ws == nullptr)
         return set_error(VAE_ERR_ARG, "decode: NULL argument");
     if (opts != nullptr &&
-        (opts->flags & ~static_cast<unsigned>(VAE_DECODE_PROFILE | VAE_DECODE_NO_FUSION | VAE_DECODE_FUSE_NORM)) != 0)
+        (opts->flags & ~static_cast<unsigned>(VAE_DECODE_PROFILE | VAE_DECODE_NO_FUSION | VAE_DECODE_FUSE_NORM |
+                                              VAE_DECODE_SUBPIXEL_UP)) != 0)
         return set_error(VAE_ERR_ARG, "decode: unknown opts.flags 0x%x", opts->flags);
     int rc = check_device();
     if (rc != VAE_OK) return rc;

@@ -56,7 +56,9 @@ enum {
     VAE_PAD_REPLICATE = 2,  /* out-of-grid reads take the nearest edge pixel (default: zero) */
     VAE_EPI_SILU = 16,      /* SiLU v/(1+e^-v) applied last in the epilogue */
     VAE_OUT_F16 = 32,       /* store the output as f16 (default f32) */
-    VAE_UPSAMPLE_T2X = 64   /* 3x3x3 conv only: causal temporal 2x folded into the gather */
+    VAE_UPSAMPLE_T2X = 64,  /* 3x3x3 conv only: causal temporal 2x folded into the gather */
+    VAE_UPSAMPLE2X_SUBPIXEL = 128 /* with VAE_UPSAMPLE2X: the up conv as four 2x2 convs (w_dev from
+                                     vae_pack_subpixel_weights); 4/9 of the MACs, weight sums rounded */
 };
 
 /* Library version string and the compute capability it was built for. */
@@ -91,7 +93,8 @@ int vae_selftest_wait_timeout(unsigned long long timeout_ns, vae_stream_t stream
  * implicit-GEMM recipe; "s2v_vae.rs" replicate padding.)
  *
  *   x_dev     f16 NHWC [n][h_in][w_in][cin], 16-byte aligned.
- *   w_dev     f16 [cout][3][3][cin] (tap-major: K index = (ky*3+kx)*cin + c).
+ *   w_dev     f16 [cout][3][3][cin] (tap-major: K index = (ky*3+kx)*cin + c), or with
+ *             VAE_UPSAMPLE2X_SUBPIXEL the summed weights of vae_pack_subpixel_weights.
  *   bias_dev  f32 [cout] or NULL (no bias).
  *   residual_dev  f32 NHWC [n][H][W][cout] or NULL; may equal y_dev (in place).
  *   y_dev     NHWC [n][H][W][cout], f32, or f16 with VAE_OUT_F16;
@@ -115,6 +118,21 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin,
  *   f32 or f16 (VAE_OUT_F16). Flags: VAE_EPI_SILU, VAE_OUT_F16 only.
  * Requirements as vae_conv3x3_nhwc; m >= 1.
  */
+/*
+ * Sub-pixel (phase) form of the nearest-2x up conv (an optional speed-up, not
+ * on the pages; SURVEY's NEXT-3): output (2v+q, 2u+p) reads source rows
+ * v + floor((q + ky - 1) / 2), so the three ky taps land on two source rows per
+ * parity q (ky {0} | {1, 2} for q = 0, {0, 1} | {2} for q = 1), and likewise the
+ * columns. Summing the weights that read one source pixel turns each parity
+ * class into a 2x2 conv on the source grid: exact in real arithmetic, 4/9 of the
+ * MACs; the sums are rounded to f16 once, which changes the rounding.
+ *   w_dev      f16 [cout][3][3][cin] (the vae_conv3x3_nhwc layout).
+ *   w_sub_dev  f16 [cout][16][cin], tap (q*2+p)*4 + ty*2 + tx; caller-owned.
+ * Use with vae_conv3x3_nhwc(..., VAE_UPSAMPLE2X | VAE_UPSAMPLE2X_SUBPIXEL).
+ * Requirements: 1 <= cout <= 2^20, 1 <= cin <= 8192, 16-byte aligned pointers.
+ */
+int vae_pack_subpixel_weights(const void* w_dev, int cout, int cin, void* w_sub_dev, vae_stream_t stream);
+
 /*
  * 3x3x3 causal convolution over frames, the same implicit GEMM with 27 taps
  * ("s2v_vae.rs" module doc and conv_any: the conv mode 3 of zi_mm, its causal
@@ -308,7 +326,7 @@ typedef struct {
     int nbands;      /* number of equal kept-row bands (0 or 1 with band_rows 0: whole frame) */
     int band_rows;   /* alternative to nbands: at most this many kept rows per band */
     int guard_log2;  /* f16 range guard g of the raw-stream casts (default 8 when < 0) */
-    unsigned flags;  /* 0, or VAE_DECODE_PROFILE | VAE_DECODE_FUSE_NORM | VAE_DECODE_NO_FUSION */
+    unsigned flags;  /* 0, or VAE_DECODE_PROFILE | VAE_DECODE_FUSE_NORM | VAE_DECODE_NO_FUSION | VAE_DECODE_SUBPIXEL_UP */
 } vae_decode_opts;
 
 /* vae_decode_opts.flags: record CUDA events around every stage of this
@@ -324,7 +342,11 @@ enum {
      * Same bits either way. Off by default: on GB300 the per-pixel norm
      * epilogue takes longer than the conv mainloop it overlaps, and the pair
      * (conv + separate RMS_norm) measured faster. */
-    VAE_DECODE_FUSE_NORM = 4
+    VAE_DECODE_FUSE_NORM = 4,
+    /* Run the up convs in their sub-pixel form (four 2x2 convs with summed
+     * weights, see vae_pack_subpixel_weights): 4/9 of their MACs, the weight sums
+     * rounded to f16 once. Off by default (it changes the rounding). */
+    VAE_DECODE_SUBPIXEL_UP = 8
 };
 
 /* Stage kinds of a profiled decode. */

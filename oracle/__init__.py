@@ -36,14 +36,15 @@ The whole decoders (``decode_gn``, ``decode_rms``) are pinned only by the
 composition of pinned parts: parity unpinned against any outside
 implementation (no trained weights or third-party decoder exist here).
 """
-from .ops import (conv2d, conv2d_at, conv3d_causal, causal_source_frame, upsample2x, silu, group_norm,
-                  rms_norm, dupup, attention, attention_rows, linear_tokens)
+from .ops import (conv2d, conv2d_at, conv3d_causal, causal_source_frame, subpixel_up_weights, conv2d_up_subpixel,
+                  upsample2x, silu, group_norm, rms_norm, dupup, attention, attention_rows, linear_tokens)
 from .decoder import (resnet, up_block, decode_gn, decode_rms, decode, Rows, grow, half,
                       levels, plan_band, plan_bands, decode_rms_banded, head_rms,
                       run_blocks_window, output_rows_window)
 
 __all__ = [
-    "conv2d", "conv2d_at", "conv3d_causal", "causal_source_frame", "upsample2x", "silu", "group_norm", "rms_norm", "dupup",
+    "conv2d", "conv2d_at", "conv3d_causal", "causal_source_frame", "subpixel_up_weights", "conv2d_up_subpixel",
+    "upsample2x", "silu", "group_norm", "rms_norm", "dupup",
     "attention", "attention_rows", "linear_tokens", "resnet", "up_block", "decode_gn", "decode_rms", "decode",
     "Rows", "grow", "half", "levels", "plan_band", "plan_bands", "decode_rms_banded",
     "head_rms", "run_blocks_window", "output_rows_window",

@@ -110,6 +110,58 @@ def conv3d_causal(x, w, b=None, upsample: bool = False, t_upsample: bool = False
     return np.stack(ys, axis=1)
 
 
+def subpixel_up_weights(w):
+    """Summed weights of the up conv's phase (sub-pixel) decomposition.
+
+    With nearest-2x before a 3x3 conv, output (2v+q, 2u+p) reads source row
+    v + floor((q + ky - 1) / 2) for tap ky: two distinct rows per parity q (ky 0 |
+    ky 1, 2 for q = 0; ky 0, 1 | ky 2 for q = 1), and likewise for columns. The
+    taps that read one source pixel are summed:
+    ws[q, p, ty, tx] = sum of w[:, :, ky, kx] over ky in R(q, ty), kx in R(p, tx),
+    so the parity class is a 2x2 conv on the source grid at rows
+    v + ty + (-1 if q == 0 else 0) (exact in real arithmetic).
+    ``w``: [cout][cin][3][3]; returns [2][2][2][2][cout][cin] (q, p, ty, tx).
+    """
+    w = _f64(w)
+    rows = {0: ([0], [1, 2]), 1: ([0, 1], [2])}
+    ws = np.zeros((2, 2, 2, 2) + w.shape[:2], _F)
+    for q in range(2):
+        for p in range(2):
+            for ty in range(2):
+                for tx in range(2):
+                    for ky in rows[q][ty]:
+                        for kx in rows[p][tx]:
+                            ws[q, p, ty, tx] += w[:, :, ky, kx]
+    return ws
+
+
+def conv2d_up_subpixel(x, w, b=None, pad: str = "zero"):
+    """conv2d(upsample2x(x), w, b) evaluated as four 2x2 convs on the source
+    grid with ``subpixel_up_weights`` (a check of that decomposition).
+
+    ``x``: [cin][h][w]; returns [cout][2h][2w].
+    """
+    x = _f64(x)
+    ws = subpixel_up_weights(w)
+    cin, h, wd = x.shape
+    cout = ws.shape[4]
+    mode = {"zero": "constant", "replicate": "edge"}[pad]
+    xp = np.pad(x, ((0, 0), (1, 1), (1, 1)), mode=mode)
+    y = np.zeros((cout, 2 * h, 2 * wd), _F)
+    for q in range(2):
+        for p in range(2):
+            acc = np.zeros((cout, h * wd), _F)
+            for ty in range(2):
+                for tx in range(2):
+                    oy, ox = ty + (0 if q == 0 else 1), tx + (0 if p == 0 else 1)  # offset into the 1-padded grid
+                    tap = xp[:, oy:oy + h, ox:ox + wd].reshape(cin, h * wd)
+                    acc += ws[q, p, ty, tx] @ tap
+            y[:, q::2, p::2] = acc.reshape(cout, h, wd)
+    if b is not None:
+        y += _f64(b)[:, None, None]
+    return y
+
+
 def conv2d_at(x, w, b, ys, xs, upsample: bool = False, pad: str = "zero"):
     """``conv2d`` evaluated only at output pixels (ys[i], xs[i]).
 

@@ -164,3 +164,39 @@ def test_full_size_stage_sampled(stage):
     got = out[0, torch.from_numpy(ys).cuda(), torch.from_numpy(xs).cuda()].cpu().numpy()
     ref = oracle.conv2d_at(np.moveaxis(x[0], -1, 0), wt, b, ys, xs, upsample=up)
     assert rel_err(got, ref) <= CONV_TOL
+
+
+@pytest.mark.parametrize("n,h,w,cin,cout", SHAPES)
+@pytest.mark.parametrize("rep", [False, True])
+def test_subpixel_up_conv_matches_the_plain_definition(n, h, w, cin, cout, rep):
+    """The up conv's sub-pixel form (summed weights, four 2x2 convs) against the
+    oracle's conv(upsample2x(x)): the f16 rounding of the weight sums stays well
+    inside the conv tolerance."""
+    torch = torch_mod()
+    case = conv_case(seed=1, n=n, h=h, w=w, cin=cin, cout=cout, name=f"shape.{n}.{h}.{w}.{cin}.{cout}")
+    ws = vg.pack_subpixel_weights(to_dev(vg.pack_conv3x3(case["w"])))
+    out = sentinel_like((n, 2 * h, 2 * w, cout), torch.float32)
+    vg.conv3x3_nhwc(to_dev(case["x"]), ws, to_dev(case["b"]), out=out, upsample=True, replicate=rep, subpixel=True)
+    vg.sync_status()
+    got = out.cpu().numpy()
+    assert not np.isnan(got).any()
+    assert rel_err(got, _ref(case, upsample=True, replicate=rep)) <= CONV_TOL
+
+
+def test_subpixel_up_conv_full_size_sampled():
+    """The 512^2 -> 1024^2, 288 -> 144 up conv of the 1024^2 decoder in the sub-pixel form."""
+    torch = torch_mod()
+    h = w = 512
+    cin, cout = 288, 144
+    x = f16_normal(7, "sub.x", (1, h, w, cin), 1.0)
+    wt = f16_normal(7, "sub.w", (cout, cin, 3, 3), (2.0 / (9 * cin)) ** 0.5)
+    b = (stream_normal(7, "sub.b", (cout,)) * 0.1).astype(np.float32)
+    ws = vg.pack_subpixel_weights(to_dev(vg.pack_conv3x3(wt)))
+    out = sentinel_like((1, 2 * h, 2 * w, cout), torch.float32)
+    vg.conv3x3_nhwc(to_dev(x), ws, to_dev(b), out=out, upsample=True, subpixel=True)
+    vg.sync_status()
+    assert not torch.isnan(out).any().item()
+    ys, xs = _sample_points(2 * h, 2 * w, 400, 8)
+    got = out[0, torch.from_numpy(ys).cuda(), torch.from_numpy(xs).cuda()].cpu().numpy()
+    ref = oracle.conv2d_at(np.moveaxis(x[0], -1, 0), wt, b, ys, xs, upsample=True)
+    assert rel_err(got, ref) <= CONV_TOL

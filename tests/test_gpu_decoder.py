@@ -73,6 +73,20 @@ def test_qwen_decoder_config4_full_1024():
     check_psnr(out.cpu().numpy(), oracle.decode_rms(dec, z))
 
 
+def test_subpixel_up_convs_in_both_families():
+    """VAE_DECODE_SUBPIXEL_UP: the up convs as four 2x2 convs with summed weights
+    (only the f16 rounding of the sums differs from the plain definition), for the
+    FLUX-class decoder at config 3 and the 1024^2 decoder's widths at latent 32^2."""
+    dec = flux_decoder(seed=0)
+    z = latent_normal(0, 16, 32, 32)
+    out, _ = gpu_decode(dec, z, opts=vg.Decoder.opts(subpixel=True))
+    check_psnr(out.cpu().numpy(), oracle.decode_gn(dec, z))
+    dec = qwen_decoder(seed=0)
+    z = latent_channel_stats(0, 16, 32, 32)
+    out, _ = gpu_decode(dec, z, opts=vg.Decoder.opts(subpixel=True))
+    check_psnr(out.cpu().numpy(), oracle.decode_rms(dec, z))
+
+
 def test_up_block_config2():
     """One GroupNorm up block at 128^2 x 256 (2 ResNets, nearest-2x + conv), composed
     from the library's GroupNorm, conv and cast entry points."""

@@ -159,3 +159,29 @@ def test_conv2d_at_matches_full(upsample, pad):
     xs[:4] = [0, W - 1, 0, W - 1]
     got = oracle.conv2d_at(x, wt, b, ys, xs, upsample=upsample, pad=pad)
     np.testing.assert_allclose(got, full[:, ys, xs].T, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("pad", ["zero", "replicate"])
+def test_subpixel_decomposition_of_the_up_conv_is_exact(pad):
+    """The up conv as four 2x2 convs with summed weights equals
+    conv(upsample2x(x)) in exact arithmetic: f64 agreement to 1e-12."""
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((3, 5, 6))
+    w = rng.standard_normal((4, 3, 3, 3))
+    b = rng.standard_normal(4)
+    ref = oracle.conv2d(x, w, b, upsample=True, pad=pad)
+    got = oracle.conv2d_up_subpixel(x, w, b, pad=pad)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_subpixel_weights_sum_to_the_kernel():
+    """Each parity class's four summed taps hold all nine weights once."""
+    rng = np.random.default_rng(42)
+    w = rng.standard_normal((2, 3, 3, 3))
+    ws = oracle.subpixel_up_weights(w)
+    for q in range(2):
+        for p in range(2):
+            np.testing.assert_allclose(ws[q, p].sum(axis=(0, 1)), w.sum(axis=(2, 3)), rtol=1e-12, atol=1e-12)
+    # parity (0, 0): top-left tap alone, then the 1x2 / 2x1 / 2x2 sums
+    np.testing.assert_allclose(ws[0, 0, 0, 0], w[:, :, 0, 0])
+    np.testing.assert_allclose(ws[0, 0, 1, 1], w[:, :, 1:, 1:].sum(axis=(2, 3)))

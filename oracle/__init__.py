@@ -16,7 +16,10 @@ of what the decoder computes, written from the pages' own definitions:
   ``attention``, ``run_blocks``, ``output_rows`` and the band planner
   (``grow``, ``half``, ``plan_band``);
 - ``s2v_vae.rs`` (cortiq-engine 0.8.72): replicate padding, read for 2-D as a
-  clamp to the edge of the (upsampled) grid.
+  clamp to the edge of the (upsampled) grid; the 3x3x3 causal conv;
+- ``vae3d.rs`` (cortiq-engine 0.5.87, the video VAE's encoder half):
+  reflect padding (``EncConv::apply``), the far-side reflect pad of the
+  stride-2 downsample (``reflect_pad_far``) and the encoder level loop.
 
 A library primitive (numpy's matmul) serves as the channel contraction of a
 conv tap and of the attention products; nothing is blocked, fused or
@@ -36,16 +39,16 @@ The whole decoders (``decode_gn``, ``decode_rms``) are pinned only by the
 composition of pinned parts: parity unpinned against any outside
 implementation (no trained weights or third-party decoder exist here).
 """
-from .ops import (conv2d, conv2d_at, conv3d_causal, causal_source_frame, subpixel_up_weights, conv2d_up_subpixel,
+from .ops import (conv2d, conv2d_at, conv2d_down, conv3d_causal, causal_source_frame, subpixel_up_weights, conv2d_up_subpixel,
                   upsample2x, silu, group_norm, rms_norm, dupup, attention, attention_rows, linear_tokens)
-from .decoder import (resnet, up_block, decode_gn, decode_rms, decode, Rows, grow, half,
+from .decoder import (resnet, up_block, down_block, decode_gn, decode_rms, decode, Rows, grow, half,
                       levels, plan_band, plan_bands, decode_rms_banded, head_rms,
                       run_blocks_window, output_rows_window)
 
 __all__ = [
-    "conv2d", "conv2d_at", "conv3d_causal", "causal_source_frame", "subpixel_up_weights", "conv2d_up_subpixel",
+    "conv2d", "conv2d_at", "conv2d_down", "conv3d_causal", "causal_source_frame", "subpixel_up_weights", "conv2d_up_subpixel",
     "upsample2x", "silu", "group_norm", "rms_norm", "dupup",
-    "attention", "attention_rows", "linear_tokens", "resnet", "up_block", "decode_gn", "decode_rms", "decode",
+    "attention", "attention_rows", "linear_tokens", "resnet", "up_block", "down_block", "decode_gn", "decode_rms", "decode",
     "Rows", "grow", "half", "levels", "plan_band", "plan_bands", "decode_rms_banded",
     "head_rms", "run_blocks_window", "output_rows_window",
 ]

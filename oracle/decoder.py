@@ -14,7 +14,7 @@ from typing import Callable, List, Optional
 
 import numpy as np
 
-from .ops import conv2d, silu, group_norm, rms_norm, dupup, attention
+from .ops import conv2d, conv2d_down, silu, group_norm, rms_norm, dupup, attention
 
 
 def _norm(x, nm, family: str, groups: int, eps: float):
@@ -23,16 +23,18 @@ def _norm(x, nm, family: str, groups: int, eps: float):
     return rms_norm(x, nm.gamma)
 
 
-def resnet(x, r, family: str, groups: int = 32, eps: float = 1e-6):
+def resnet(x, r, family: str, groups: int = 32, eps: float = 1e-6, pad: str = "zero"):
     """One ResNet unit: skip + conv2(silu(norm2(conv1(silu(norm1(x)))))).
 
     skip = x, or a 1x1 conv of x when the channel count changes.
     ``vae.rs``, ``ResnetBlock::apply`` (GroupNorm family) and
     ``qi21_vae.rs``, ``Rec::resnet`` (RMS_norm family; conv1's bias is
-    added on read by the second norm, the same sum).
+    added on read by the second norm, the same sum). The encoder's ResNets
+    (``vae3d.rs``, ``VideoVaeEncoder::encode_tile``) are the same unit with
+    reflect-padded 3x3 convs (``pad="reflect"``).
     """
-    h = conv2d(silu(_norm(x, r.norm1, family, groups, eps)), r.conv1.w, r.conv1.b)
-    h = conv2d(silu(_norm(h, r.norm2, family, groups, eps)), r.conv2.w, r.conv2.b)
+    h = conv2d(silu(_norm(x, r.norm1, family, groups, eps)), r.conv1.w, r.conv1.b, pad=pad)
+    h = conv2d(silu(_norm(h, r.norm2, family, groups, eps)), r.conv2.w, r.conv2.b, pad=pad)
     skip = conv2d(x, r.shortcut.w, r.shortcut.b) if r.shortcut is not None else np.asarray(x, np.float64)
     return skip + h
 
@@ -53,6 +55,21 @@ def up_block(x, u, family: str, with_dupup: bool, groups: int = 32, eps: float =
         x = conv2d(x, u.up.w, u.up.b, upsample=True)
         if with_dupup:
             x = x + dupup(cp, u.out_dim, u.ft)
+    return x
+
+
+def down_block(x, blk, groups: int = 32, eps: float = 1e-6):
+    """An encoder level: its GroupNorm ResNets with reflect-padded convs, then
+    (if present) the downsample: the far-side reflect pad and the unpadded
+    stride-2 3x3 conv (``conv2d_down``).
+
+    ``vae3d.rs``, ``VideoVaeEncoder::encode_tile`` (the level loop) and
+    ``reflect_pad_far``. ``blk`` has ``resnets`` and ``down`` (a conv or None).
+    """
+    for r in blk.resnets:
+        x = resnet(x, r, "gn", groups, eps, pad="reflect")
+    if blk.down is not None:
+        x = conv2d_down(x, blk.down.w, blk.down.b, pad="reflect")
     return x
 
 

@@ -39,12 +39,16 @@ def conv2d(x, w, b=None, upsample: bool = False, pad: str = "zero"):
 
     y[o, Y, X] = b[o] + sum_{c, ky, kx} w[o, c, ky, kx] * xt[c, Y+ky-r, X+kx-r],
     r = k//2, where xt is ``x`` (or ``upsample2x(x)`` when ``upsample``) and
-    reads outside the grid are 0 (``pad="zero"``) or the nearest edge pixel
-    (``pad="replicate"``, a clamp on the upsampled grid).
+    reads outside the grid are 0 (``pad="zero"``), the nearest edge pixel
+    (``pad="replicate"``, a clamp on the upsampled grid) or the pixel mirrored
+    about the edge, the edge itself not repeated (``pad="reflect"``: index -1
+    reads 1, index n reads n - 2; it needs at least two rows and columns).
 
     ``vae.rs``, ``Conv2d::apply`` (zero padding, pad = k/2, bias added per
     output channel) and ``VaeDecoder::decode`` (upsample, then conv);
-    replicate padding from ``s2v_vae.rs``'s causal-replicate conv, read for 2-D.
+    replicate padding from ``s2v_vae.rs``'s causal-replicate conv, read for 2-D;
+    reflect padding from ``vae3d.rs``, ``EncConv::apply`` (the encoder's
+    stride-1 convs: reflect on H and W by k/2).
 
     ``x``: [cin][h][w]; ``w``: [cout][cin][k][k]; returns [cout][H][W].
     Each tap is one channel contraction (a matmul) over a shifted view.
@@ -55,7 +59,9 @@ def conv2d(x, w, b=None, upsample: bool = False, pad: str = "zero"):
     assert k == k2 and x.shape[0] == cin, (w.shape, x.shape)
     _, H, W = x.shape
     r = k // 2
-    mode = {"zero": "constant", "replicate": "edge"}[pad]
+    mode = {"zero": "constant", "replicate": "edge", "reflect": "reflect"}[pad]
+    if pad == "reflect":
+        assert H >= 2 and W >= 2, "reflect padding needs two rows and columns"
     xp = np.pad(x, ((0, 0), (r, r), (r, r)), mode=mode)
     y = np.zeros((cout, H * W), _F)
     for ky in range(k):
@@ -65,6 +71,40 @@ def conv2d(x, w, b=None, upsample: bool = False, pad: str = "zero"):
     if b is not None:
         y += _f64(b)[:, None]
     return y.reshape(cout, H, W)
+
+
+def conv2d_down(x, w, b=None, pad: str = "reflect"):
+    """The encoder's downsample conv: one row and one column padded onto the
+    FAR side (bottom and right), then an unpadded stride-2 k x k convolution.
+
+    y[o, Y, X] = b[o] + sum_{c, ky, kx} w[o, c, ky, kx] * xp[c, 2Y+ky, 2X+kx],
+    xp = ``x`` with row h and column w appended: mirrored (``pad="reflect"``:
+    they repeat rows / columns h - 2 and w - 2), copied from the edge
+    (``"replicate"``) or zero (``"zero"``). The output is
+    ((h + 1 - k) // 2 + 1) x ((w + 1 - k) // 2 + 1), i.e. h//2 x w//2 for k = 3.
+
+    ``vae3d.rs``, ``reflect_pad_far`` (the far-side reflect pad) and the
+    downsample ``EncConv`` (stride 2, pad 0) of ``VideoVaeEncoder``;
+    ``s2v_vae.rs``, ``conv_down`` (the stride-2 conv of the encoder's frame).
+    ``x``: [cin][h][w]; ``w``: [cout][cin][k][k].
+    """
+    x = _f64(x)
+    w = _f64(w)
+    cout, cin, k, k2 = w.shape
+    assert k == k2 and x.shape[0] == cin, (w.shape, x.shape)
+    _, h, wd = x.shape
+    mode = {"zero": "constant", "replicate": "edge", "reflect": "reflect"}[pad]
+    assert h >= 2 and wd >= 2, "the far-side pad needs two rows and columns"
+    xp = np.pad(x, ((0, 0), (0, 1), (0, 1)), mode=mode)
+    Ho, Wo = (h + 1 - k) // 2 + 1, (wd + 1 - k) // 2 + 1
+    y = np.zeros((cout, Ho * Wo), _F)
+    for ky in range(k):
+        for kx in range(k):
+            tap = xp[:, ky:ky + 2 * Ho - 1:2, kx:kx + 2 * Wo - 1:2].reshape(cin, Ho * Wo)
+            y += w[:, :, ky, kx] @ tap
+    if b is not None:
+        y += _f64(b)[:, None]
+    return y.reshape(cout, Ho, Wo)
 
 
 def causal_source_frame(f: int, kt: int, t_upsample: bool) -> int:
@@ -162,13 +202,14 @@ def conv2d_up_subpixel(x, w, b=None, pad: str = "zero"):
     return y
 
 
-def conv2d_at(x, w, b, ys, xs, upsample: bool = False, pad: str = "zero"):
-    """``conv2d`` evaluated only at output pixels (ys[i], xs[i]).
+def conv2d_at(x, w, b, ys, xs, upsample: bool = False, pad: str = "zero", down: bool = False):
+    """``conv2d`` (or, with ``down``, ``conv2d_down``) evaluated only at output
+    pixels (ys[i], xs[i]).
 
-    The same definition as ``conv2d``, one output pixel at a time, so that
-    very large convs can be checked on a sample. ``x`` may be any array
-    indexable as [c][y][x] (e.g. a transposed view of an NHWC tensor); only
-    the receptive fields of the sampled pixels are read.
+    The same definitions, one output pixel at a time, so that very large
+    convs can be checked on a sample. ``x`` may be any array indexable as
+    [c][y][x] (e.g. a transposed view of an NHWC tensor); only the receptive
+    fields of the sampled pixels are read.
     Returns [len(ys)][cout].
     """
     w = _f64(w)
@@ -176,6 +217,7 @@ def conv2d_at(x, w, b, ys, xs, upsample: bool = False, pad: str = "zero"):
     r = k // 2
     h_in, w_in = x.shape[1], x.shape[2]
     H, W = (2 * h_in, 2 * w_in) if upsample else (h_in, w_in)
+    assert not (upsample and down)
     ys = np.asarray(ys, np.int64)
     xs = np.asarray(xs, np.int64)
     out = np.zeros((len(ys), cout), _F)
@@ -183,9 +225,19 @@ def conv2d_at(x, w, b, ys, xs, upsample: bool = False, pad: str = "zero"):
         out += _f64(b)[None, :]
     for ky in range(k):
         for kx in range(k):
-            Y = ys + ky - r
-            X = xs + kx - r
-            if pad == "replicate":
+            if down:  # the far-side pad: source rows 2Y + ky, column 2X + kx
+                Y = 2 * ys + ky
+                X = 2 * xs + kx
+            else:
+                Y = ys + ky - r
+                X = xs + kx - r
+            if pad == "reflect":
+                Y = np.where(Y < 0, -Y, Y)
+                Y = np.where(Y >= H, 2 * (H - 1) - Y, Y)
+                X = np.where(X < 0, -X, X)
+                X = np.where(X >= W, 2 * (W - 1) - X, X)
+                inside = np.ones(len(ys), bool)
+            elif pad == "replicate":
                 Y = np.clip(Y, 0, H - 1)
                 X = np.clip(X, 0, W - 1)
                 inside = np.ones(len(ys), bool)

@@ -35,8 +35,8 @@ import numpy as np
 
 __all__ = [
     "rng_for", "f16_normal", "conv_weight", "bias_vec", "conv_case",
-    "Conv", "Norm", "Resnet", "Attn", "UpBlock", "Decoder",
-    "flux_decoder", "qwen_decoder", "gn_up_block", "latent_normal",
+    "Conv", "Norm", "Resnet", "Attn", "UpBlock", "DownBlock", "Decoder",
+    "flux_decoder", "qwen_decoder", "gn_up_block", "gn_down_block", "latent_normal",
     "latent_channel_stats", "stream_normal",
 ]
 
@@ -155,6 +155,14 @@ class UpBlock:
     in_dim: int = 0
     out_dim: int = 0
     ft: int = 1                        # DupUp temporal factor (rms family)
+
+
+@dataclass
+class DownBlock:
+    resnets: List[Resnet]
+    down: Optional[Conv] = None        # 3x3 stride-2 conv after the far-side pad
+    in_dim: int = 0
+    out_dim: int = 0
 
 
 @dataclass
@@ -283,3 +291,12 @@ def gn_up_block(seed: int = 0, c: int = 256, nres: int = 2, affine: bool = False
     """One GroupNorm up block: ``nres`` ResNets c->c, then nearest-2x + 3x3 conv c->c."""
     res = [_resnet(seed, f"blk.res{r}", c, c, "gn", affine) for r in range(nres)]
     return UpBlock(resnets=res, up=_conv(seed, "blk.upconv", c, c, 3), in_dim=c, out_dim=c)
+
+
+def gn_down_block(seed: int = 0, cin: int = 128, cout: int = 128, nres: int = 2, affine: bool = True,
+                  down: bool = True) -> DownBlock:
+    """One encoder level: ``nres`` GroupNorm ResNets (the first cin->cout, with
+    a 1x1 shortcut when the widths differ), then a stride-2 3x3 conv cout->cout."""
+    res = [_resnet(seed, f"enc.res{r}", cin if r == 0 else cout, cout, "gn", affine) for r in range(nres)]
+    return DownBlock(resnets=res, down=_conv(seed, "enc.down", cout, cout, 3) if down else None,
+                     in_dim=cin, out_dim=cout)

@@ -217,12 +217,13 @@ def run_kernel(args):
         h, w, cin, cout = vals
     if h == 0:
         pass
-    elif args.kernel in ("conv3x3", "upconv3x3"):
+    elif args.kernel in ("conv3x3", "upconv3x3", "downconv3x3"):
         up = args.kernel == "upconv3x3"
+        down = args.kernel == "downconv3x3"  # the encoder's far-side-padded stride-2 conv
         x = torch.randn(1, h, w, cin, device="cuda").half()
         wt = (torch.randn(cout, 3, 3, cin, device="cuda") / (9 * cin) ** 0.5).half()
         b = torch.randn(cout, device="cuda") * 0.1
-        H, W = (2 * h, 2 * w) if up else (h, w)
+        H, W = (2 * h, 2 * w) if up else ((h // 2, w // 2) if down else (h, w))
         y = torch.empty(1, H, W, cout, device="cuda")
         res = None
         if args.residual:
@@ -232,7 +233,8 @@ def run_kernel(args):
             wsub = vg.pack_subpixel_weights(wt)
             fn = lambda: vg.conv3x3_nhwc(x, wsub, b, residual=res, out=y, upsample=True, subpixel=True)
         else:
-            fn = lambda: vg.conv3x3_nhwc(x, wt, b, residual=res, out=y, upsample=up)
+            fn = lambda: vg.conv3x3_nhwc(x, wt, b, residual=res, out=y, upsample=up, down=down,
+                                         reflect=args.reflect or down)
         flops = 2.0 * H * W * cout * 9 * cin
         nbytes = x.numel() * 2 + y.numel() * 4 * (2 if args.residual else 1)
     elif args.kernel == "rmsnorm":
@@ -296,12 +298,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", default=None,
-                    help="time one kernel instead: conv3x3, upconv3x3, conv3d, upconv3d, rmsnorm, groupnorm, "
+                    help="time one kernel instead: conv3x3, upconv3x3, downconv3x3, conv3d, upconv3d, rmsnorm, groupnorm, "
                          "attention")
     ap.add_argument("--shape", default="1024,1024,144,144",
                     help="h,w,cin,cout (attention: h,w,c,c; conv3d/upconv3d: f,h,w,cin,cout)")
     ap.add_argument("--residual", action="store_true")
     ap.add_argument("--subpixel", action="store_true", help="upconv3x3 in the sub-pixel form")
+    ap.add_argument("--reflect", action="store_true", help="conv3x3 with reflect padding (the encoder's)")
     args = ap.parse_args()
     if args.kernel:
         return run_kernel(args)

@@ -24,11 +24,12 @@ __all__ = [
     "selftest_wait_timeout", "conv3x3_nhwc", "conv1x1", "rmsnorm_silu", "groupnorm_silu",
     "groupnorm_workspace_bytes", "cast_f16", "mid_attention", "mid_attention_workspace_bytes",
     "Decoder", "pack_conv3x3", "pack_conv1x1",
-    "UPSAMPLE2X", "PAD_REPLICATE", "EPI_SILU", "OUT_F16", "FAMILY_GN", "FAMILY_RMS",
+    "UPSAMPLE2X", "PAD_REPLICATE", "PAD_REFLECT", "DOWNSAMPLE2X", "EPI_SILU", "OUT_F16", "FAMILY_GN", "FAMILY_RMS",
     "NORM_GROUP", "NORM_RMS",
 ]
 
 UPSAMPLE2X, PAD_REPLICATE, EPI_SILU, OUT_F16, UPSAMPLE_T2X, UPSAMPLE2X_SUBPIXEL = 1, 2, 16, 32, 64, 128
+PAD_REFLECT, DOWNSAMPLE2X = 256, 512
 FAMILY_GN, FAMILY_RMS = 0, 1
 NORM_GROUP, NORM_RMS = 0, 1
 
@@ -160,9 +161,11 @@ def pack_subpixel_weights(w, stream=None):
 
 def conv3x3_nhwc(x, w, bias=None, residual=None, out=None, oscale: float = 1.0, upsample: bool = False,
                  replicate: bool = False, silu: bool = False, out_f16: bool = False, subpixel: bool = False,
-                 stream=None):
+                 reflect: bool = False, down: bool = False, stream=None):
     """3x3 implicit-GEMM conv. x f16 [n][h][w][cin]; w f16 [cout][3][3][cin], or with
-    ``subpixel`` (an up conv) the summed weights [cout][16][cin] of pack_subpixel_weights."""
+    ``subpixel`` (an up conv) the summed weights [cout][16][cin] of pack_subpixel_weights.
+    ``reflect``: mirror padding; ``down``: the encoder's far-side-padded stride-2
+    downsample (output [n][h//2][w//2][cout])."""
     import torch
     _need(x, torch.float16, "x", 4)
     _need(w, torch.float16, "w", 3 if subpixel else 4)
@@ -171,14 +174,18 @@ def conv3x3_nhwc(x, w, bias=None, residual=None, out=None, oscale: float = 1.0, 
     cout = w.shape[0]
     if tuple(w.shape[1:]) != ((16, cin) if subpixel else (3, 3, cin)):
         raise VaeError(-2, f"w has the wrong shape {tuple(w.shape)}")
-    H, W = (2 * h, 2 * wd) if upsample else (h, wd)
+    H, W = (2 * h, 2 * wd) if upsample else ((h // 2, wd // 2) if down else (h, wd))
     odt = torch.float16 if out_f16 else torch.float32
     if out is None:
         out = torch.empty((n, H, W, cout), dtype=odt, device=x.device)
     _need(out, odt, "out")
     _need(residual, torch.float32, "residual")
+    for t, nm in ((out, "out"), (residual, "residual")):
+        if t is not None and t.numel() != n * H * W * cout:
+            raise VaeError(-2, f"{nm} must hold [n][{H}][{W}][{cout}], got {tuple(t.shape)}")
     flags = (UPSAMPLE2X if upsample else 0) | (PAD_REPLICATE if replicate else 0) | \
-            (EPI_SILU if silu else 0) | (OUT_F16 if out_f16 else 0) | (UPSAMPLE2X_SUBPIXEL if subpixel else 0)
+            (EPI_SILU if silu else 0) | (OUT_F16 if out_f16 else 0) | (UPSAMPLE2X_SUBPIXEL if subpixel else 0) | \
+            (PAD_REFLECT if reflect else 0) | (DOWNSAMPLE2X if down else 0)
     _check(lib().vae_conv3x3_nhwc(_ptr(x), n, h, wd, cin, _ptr(w), _ptr(bias), _ptr(residual), _ptr(out),
                                   cout, float(oscale), flags, _stream(stream)))
     return out

@@ -14,8 +14,9 @@
 //    dy = floor((q+ky-1)/2), dx = floor((p+kx-1)/2). So every tap of every
 //    tile is a dense rectangular box of the f16 input and the whole gather
 //    is a 4-D TMA tile load; zero padding comes from TMA's out-of-bounds fill.
-//  - Replicate padding clamps source coordinates per pixel, which a box
-//    cannot express; those launches use 128 gather threads instead (one A row
+//  - Replicate and reflect padding remap source coordinates per pixel, and
+//    the encoder's stride-2 downsample reads every other pixel; a box cannot
+//    express those, so such launches use 128 gather threads instead (one A row
 //    each, 16-byte loads, stores into the 128B-swizzled layout).
 //  - B (weights [cout][taps][cin]) is a 3-D TMA tile load per (tap, chunk).
 //  - One elected thread issues tcgen05.mma (M=128, N=BN, K=16 steps) into one
@@ -65,6 +66,8 @@ struct ConvParams {
     int n, hv, wv;        // images, virtual grid rows/cols (= input grid)
     int cin, cout, taps;  // taps: 9 or 1
     int up, rep;          // nearest-2x fold, replicate padding
+    int refl, down;       // reflect padding; the stride-2 downsample (far-side pad; virtual grid = output)
+    int hs, ws;           // source grid of the gather (= hv, wv except for the downsample)
     int H, W;             // output grid
     int R, Wt;            // tile rows, tile cols on the virtual grid
     int tiles_x, tiles_y, npar;
@@ -386,7 +389,9 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
 }
 
 // One thread per A row: gathers the row's 64-channel slice for each
-// (tap, chunk) with clamped (replicate) or zero-filled (zero) borders.
+// (tap, chunk) with clamped (replicate), mirrored (reflect) or zero-filled
+// (zero) borders. The downsample's row v reads source rows 2v + ky (the far
+// side padded by one); every other conv's reads v + dy.
 template <int kVar>
 __device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
     constexpr bool kT3 = kVar == 1;
@@ -402,17 +407,21 @@ __device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
             int dy, dx;
             tap_offset(p, tap, ti.par, dy, dx);
             const int simg = src_img<kT3>(p, ti.img, p.taps == 27 ? tap / 9 : 2);
-            int sy = v + dy, sx = u + dx;
+            int sy = p.down ? 2 * v + dy + 1 : v + dy, sx = p.down ? 2 * u + dx + 1 : u + dx;
             bool inb;
             if (p.rep) {
-                sy = min(max(sy, 0), p.hv - 1);
-                sx = min(max(sx, 0), p.wv - 1);
+                sy = min(max(sy, 0), p.hs - 1);
+                sx = min(max(sx, 0), p.ws - 1);
+                inb = rowvalid;
+            } else if (p.refl) {  // at most one pixel outside (hs, ws >= 2): one mirror suffices
+                sy = sy < 0 ? -sy : (sy >= p.hs ? 2 * (p.hs - 1) - sy : sy);
+                sx = sx < 0 ? -sx : (sx >= p.ws ? 2 * (p.ws - 1) - sx : sx);
                 inb = rowvalid;
             } else {
-                inb = rowvalid && sy >= 0 && sy < p.hv && sx >= 0 && sx < p.wv;
+                inb = rowvalid && sy >= 0 && sy < p.hs && sx >= 0 && sx < p.ws;
             }
             const __half* src =
-                p.x + ((static_cast<long long>(simg) * p.hv + (inb ? sy : 0)) * p.wv + (inb ? sx : 0)) *
+                p.x + ((static_cast<long long>(simg) * p.hs + (inb ? sy : 0)) * p.ws + (inb ? sx : 0)) *
                           p.cin;
             for (int kc = 0; kc < p.kchunks; ++kc) {
                 if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, s.abort_flag, p.timeout_ns,
@@ -1453,7 +1462,18 @@ int conv_validate(const ConvArgs& a) {
         return set_error(VAE_ERR_SHAPE, "conv: cin=%d must be a multiple of 16 in [16, 8192]", a.cin);
     if (a.cout < 1 || a.cout > (1 << 20))
         return set_error(VAE_ERR_SHAPE, "conv: cout=%d out of [1, 2^20]", a.cout);
-    if (a.taps == 1 && (a.up || a.rep)) return set_error(VAE_ERR_ARG, "conv1x1: no upsample/replicate");
+    if (a.taps == 1 && (a.up || a.rep || a.refl || a.down))
+        return set_error(VAE_ERR_ARG, "conv1x1: no upsample, downsample or padding mode");
+    if (static_cast<int>(a.rep) + static_cast<int>(a.refl) > 1)
+        return set_error(VAE_ERR_ARG, "conv: at most one padding mode (replicate or reflect)");
+    if (a.refl && a.up) return set_error(VAE_ERR_ARG, "conv: reflect padding does not combine with the upsample");
+    if (a.down && (a.up || a.taps != 9 || a.subpix))
+        return set_error(VAE_ERR_ARG, "conv: the downsample is a plain 3x3 conv (no upsample)");
+    if (a.taps == 27 && a.refl) return set_error(VAE_ERR_ARG, "conv: the 3x3x3 conv takes zero or replicate padding");
+    if ((a.refl || a.down) && (a.h_in < 2 || a.w_in < 2))
+        return set_error(VAE_ERR_SHAPE, "conv: reflect padding and the downsample need h, w >= 2 (h=%d w=%d)",
+                         a.h_in, a.w_in);
+    if (a.down && a.dup_src != nullptr) return set_error(VAE_ERR_ARG, "conv: no DupUp on the downsample");
     if (!aligned16(a.x) || !aligned16(a.w))
         return set_error(VAE_ERR_ALIGN, "conv: x and w must be 16-byte aligned");
     const long long H = a.up ? 2LL * a.h_in : a.h_in, W = a.up ? 2LL * a.w_in : a.w_in;
@@ -1498,16 +1518,21 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.nkt = a.taps == 27 ? 3 : 1;
     p.n = a.n * p.frames_out;  // output images: the tile space
     p.n_in = a.n * a.frames_in;
-    p.hv = a.h_in;
-    p.wv = a.w_in;
+    p.hs = a.h_in;
+    p.ws = a.w_in;
+    p.down = a.down ? 1 : 0;
+    p.refl = a.refl ? 1 : 0;
+    p.hv = a.down ? a.h_in / 2 : a.h_in;  // the downsample tiles its output grid
+    p.wv = a.down ? a.w_in / 2 : a.w_in;
     p.cin = a.cin;
     p.cout = a.cout;
     p.subpix = a.subpix ? 1 : 0;
     p.taps = a.subpix ? 4 : a.taps;  // taps per parity class
     p.up = a.up ? 1 : 0;
     p.rep = a.rep ? 1 : 0;
-    p.H = p.up ? 2 * a.h_in : a.h_in;
-    p.W = p.up ? 2 * a.w_in : a.w_in;
+    p.H = p.up ? 2 * a.h_in : p.hv;
+    p.W = p.up ? 2 * a.w_in : p.wv;
+    const bool gather = a.rep || a.refl || a.down;  // per-pixel source remaps: gather threads
     if (p.wv >= kBM) {
         p.Wt = kBM;
         p.R = 1;
@@ -1520,7 +1545,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.npar = p.up ? 4 : 1;
     // Geometry that allows a halo box: a tile is 128 pixels of one row, 3x3 taps,
     // zero padding (the TMA box fills out-of-range pixels with zeros).
-    const bool halo_geom = !p.rep && !a.no_halo && (a.taps == 9 || a.taps == 27) && p.R == 1 && p.Wt == kBM;
+    const bool halo_geom = !gather && !a.no_halo && (a.taps == 9 || a.taps == 27) && p.R == 1 && p.Wt == kBM;
     p.BN = choose_bn(a.cout, halo_geom);
     p.b_rows = p.BN;
     p.n_tiles = (a.cout + p.BN - 1) / p.BN;
@@ -1533,7 +1558,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // Two K chunks per stage halve the per-stage barrier/commit overhead of the
     // MMA thread (measured +10-21 % on the wide convs) when two such stages fit.
     p.ks = 1;
-    if (!a.rep && p.kchunks >= 2 && 2 * 2 * (kABytes + p.BN * 128) <= kMaxSmem - 1024 - kTail) p.ks = 2;
+    if (!gather && p.kchunks >= 2 && 2 * 2 * (kABytes + p.BN * 128) <= kMaxSmem - 1024 - kTail) p.ks = 2;
     const int stage_bytes = p.ks * (kABytes + p.BN * 128);
     p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail) / stage_bytes);
     p.a_tx = static_cast<uint32_t>(128 * p.Wt * p.R);
@@ -1596,7 +1621,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                           CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != VAE_OK) return rc;
     }
-    int mode = p.rep ? kModeGather : kModeTma;
+    int mode = gather ? kModeGather : kModeTma;
     // Halo stages: three-tap stages whenever three fit (any cin); otherwise one
     // tap per stage, which measured faster than per-tap A tiles only for
     // narrow inputs (cin <= 192).
@@ -1816,7 +1841,7 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin, cons
                      unsigned flags, vae_stream_t stream) {
     clear_error();
     if (flags & ~static_cast<unsigned>(VAE_UPSAMPLE2X | VAE_UPSAMPLE2X_SUBPIXEL | VAE_PAD_REPLICATE | VAE_EPI_SILU |
-                                       VAE_OUT_F16))
+                                       VAE_OUT_F16 | VAE_PAD_REFLECT | VAE_DOWNSAMPLE2X))
         return set_error(VAE_ERR_ARG, "vae_conv3x3_nhwc: unknown flag bits 0x%x", flags);
     if ((flags & VAE_UPSAMPLE2X_SUBPIXEL) && !(flags & VAE_UPSAMPLE2X))
         return set_error(VAE_ERR_ARG, "vae_conv3x3_nhwc: the sub-pixel form needs VAE_UPSAMPLE2X");
@@ -1836,6 +1861,8 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin, cons
     a.oscale = oscale;
     a.up = (flags & VAE_UPSAMPLE2X) != 0;
     a.rep = (flags & VAE_PAD_REPLICATE) != 0;
+    a.refl = (flags & VAE_PAD_REFLECT) != 0;
+    a.down = (flags & VAE_DOWNSAMPLE2X) != 0;
     a.silu = (flags & VAE_EPI_SILU) != 0;
     a.out_f16 = (flags & VAE_OUT_F16) != 0;
     return conv_run(a, reinterpret_cast<cudaStream_t>(stream));

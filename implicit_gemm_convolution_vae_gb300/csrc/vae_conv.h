@@ -24,6 +24,11 @@ struct ConvArgs {
     void* y = nullptr;
     float oscale = 1.0f;
     bool up = false, rep = false, silu = false, out_f16 = false;
+    // Reflect padding (mirror about the edge, the edge not repeated).
+    bool refl = false;
+    // The encoder's downsample: x padded by one row and column on the far side
+    // (zero / rep / refl), then an unpadded stride-2 conv; output h_in/2 x w_in/2.
+    bool down = false;
     bool no_halo = false;        // force the per-tap A path (tests and sweeps)
     bool no_pair = false;        // force the single-CTA kernel
     // NCHW f32 output of output rows [keep_lo, keep_hi) at destination row

@@ -57,8 +57,12 @@ enum {
     VAE_EPI_SILU = 16,      /* SiLU v/(1+e^-v) applied last in the epilogue */
     VAE_OUT_F16 = 32,       /* store the output as f16 (default f32) */
     VAE_UPSAMPLE_T2X = 64,  /* 3x3x3 conv only: causal temporal 2x folded into the gather */
-    VAE_UPSAMPLE2X_SUBPIXEL = 128 /* with VAE_UPSAMPLE2X: the up conv as four 2x2 convs (w_dev from
-                                     vae_pack_subpixel_weights); 4/9 of the MACs, weight sums rounded */
+    VAE_UPSAMPLE2X_SUBPIXEL = 128, /* with VAE_UPSAMPLE2X: the up conv as four 2x2 convs (w_dev from
+                                      vae_pack_subpixel_weights); 4/9 of the MACs, weight sums rounded */
+    VAE_PAD_REFLECT = 256,  /* out-of-grid reads mirror about the edge, the edge not repeated
+                               (-1 reads 1, n reads n - 2); needs h_in, w_in >= 2 */
+    VAE_DOWNSAMPLE2X = 512  /* the encoder's downsample: one row and column padded on the far
+                               side only, then an unpadded stride-2 3x3 conv: output h_in/2 x w_in/2 */
 };
 
 /* Library version string and the compute capability it was built for. */
@@ -88,9 +92,14 @@ int vae_selftest_wait_timeout(unsigned long long timeout_ns, vae_stream_t stream
  *   y[p, o] = SiLU?( oscale * sum_{tap, c} xt[p + d_tap, c] * w[o, tap, c]
  *                    + bias[o] + residual[p, o] )
  * where xt is x, or nearest-2x(x) with VAE_UPSAMPLE2X, and reads outside the
- * (upsampled) grid are 0 or, with VAE_PAD_REPLICATE, the nearest edge pixel.
+ * (upsampled) grid are 0, or with VAE_PAD_REPLICATE the nearest edge pixel, or
+ * with VAE_PAD_REFLECT the pixel mirrored about the edge.
+ * With VAE_DOWNSAMPLE2X (the encoder's downsample) output (Y, X) reads source
+ * (2Y + ky, 2X + kx) of x padded by one row and column on the far side (by the
+ * padding flag: zero, replicate or reflect); H = h_in / 2, W = w_in / 2 (floor).
  * ("vae.rs" Conv2d::apply; "qi21_vae.rs" conv_s and the module doc's
- * implicit-GEMM recipe; "s2v_vae.rs" replicate padding.)
+ * implicit-GEMM recipe; "s2v_vae.rs" replicate padding and conv_down;
+ * "vae3d.rs" EncConv::apply (reflect) and reflect_pad_far.)
  *
  *   x_dev     f16 NHWC [n][h_in][w_in][cin], 16-byte aligned.
  *   w_dev     f16 [cout][3][3][cin] (tap-major: K index = (ky*3+kx)*cin + c), or with
@@ -98,11 +107,15 @@ int vae_selftest_wait_timeout(unsigned long long timeout_ns, vae_stream_t stream
  *   bias_dev  f32 [cout] or NULL (no bias).
  *   residual_dev  f32 NHWC [n][H][W][cout] or NULL; may equal y_dev (in place).
  *   y_dev     NHWC [n][H][W][cout], f32, or f16 with VAE_OUT_F16;
- *             H = h_in, W = w_in, or 2*h_in, 2*w_in with VAE_UPSAMPLE2X.
+ *             H = h_in, W = w_in, or 2*h_in, 2*w_in with VAE_UPSAMPLE2X,
+ *             or h_in/2, w_in/2 with VAE_DOWNSAMPLE2X.
  *   oscale    multiplies the f32 accumulator (the undo of a 2^-g input guard).
  * Requirements: n, h_in, w_in >= 1; cin % 16 == 0, 16 <= cin <= 8192;
  * 1 <= cout <= 2^20; x_dev, w_dev 16-byte aligned. Outputs of any cout are
- * supported (vector stores when cout % 16 == 0).
+ * supported (vector stores when cout % 16 == 0). VAE_PAD_REFLECT and
+ * VAE_DOWNSAMPLE2X need h_in, w_in >= 2; at most one padding flag; the
+ * upsample and the downsample exclude each other, and reflect padding does not
+ * combine with the upsample (VAE_ERR_ARG / VAE_ERR_SHAPE otherwise).
  */
 int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin,
                      const void* w_dev, const float* bias_dev, const float* residual_dev,
@@ -120,7 +133,7 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin,
  */
 /*
  * Sub-pixel (phase) form of the nearest-2x up conv (an optional speed-up, not
- * on the pages; SURVEY's NEXT-3): output (2v+q, 2u+p) reads source rows
+ * on the pages): output (2v+q, 2u+p) reads source rows
  * v + floor((q + ky - 1) / 2), so the three ky taps land on two source rows per
  * parity q (ky {0} | {1, 2} for q = 0, {0, 1} | {2} for q = 1), and likewise the
  * columns. Summing the weights that read one source pixel turns each parity

@@ -52,10 +52,26 @@ def test_conv_rejects_bad_shapes_and_flags(L):
     assert "multiple of 16" in vg.last_error()
     assert L.vae_conv3x3_nhwc(FAKE, 1, 0, 4, 16, FAKE, None, None, FAKE, 16, 1.0, 0, None) == -2
     assert L.vae_conv3x3_nhwc(None, 1, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, 0, None) == -1
-    assert L.vae_conv3x3_nhwc(FAKE, 1, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, 1 << 9, None) == -1
+    assert L.vae_conv3x3_nhwc(FAKE, 1, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, 1 << 12, None) == -1
     assert L.vae_conv3x3_nhwc(FAKE + 8, 1, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, 0, None) == -3
     assert L.vae_conv1x1(FAKE, 10, 16, FAKE, None, None, FAKE, 16, 1.0, vg.UPSAMPLE2X, None) == -1
     assert L.vae_conv1x1(FAKE, 10, 16, FAKE, None, None, FAKE, 0, 1.0, 0, None) == -2
+
+
+def test_conv_rejects_bad_padding_and_downsample_combinations(L):
+    c = L.vae_conv3x3_nhwc
+    refl, rep, up, down = vg.PAD_REFLECT, vg.PAD_REPLICATE, vg.UPSAMPLE2X, vg.DOWNSAMPLE2X
+    assert c(FAKE, 1, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, refl | rep, None) == -1
+    assert "one padding" in vg.last_error()
+    assert c(FAKE, 1, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, refl | up, None) == -1
+    assert c(FAKE, 1, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, down | up, None) == -1
+    assert c(FAKE, 1, 1, 4, 16, FAKE, None, None, FAKE, 16, 1.0, refl, None) == -2
+    assert c(FAKE, 1, 4, 1, 16, FAKE, None, None, FAKE, 16, 1.0, down, None) == -2
+    assert "h, w >= 2" in vg.last_error()
+    # the 3x3x3 conv has no reflect padding or downsample flag
+    c3 = L.vae_conv3d_causal_ndhwc
+    assert c3(FAKE, 1, 2, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, refl, None) == -1
+    assert c3(FAKE, 1, 2, 4, 4, 16, FAKE, None, None, FAKE, 16, 1.0, down, None) == -1
 
 
 def test_conv3d_rejects_bad_shapes_and_flags(L):

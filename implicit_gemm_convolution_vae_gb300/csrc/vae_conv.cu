@@ -14,10 +14,13 @@
 //    dy = floor((q+ky-1)/2), dx = floor((p+kx-1)/2). So every tap of every
 //    tile is a dense rectangular box of the f16 input and the whole gather
 //    is a 4-D TMA tile load; zero padding comes from TMA's out-of-bounds fill.
-//  - Replicate and reflect padding remap source coordinates per pixel, and
-//    the encoder's stride-2 downsample reads every other pixel; a box cannot
-//    express those, so such launches use 128 gather threads instead (one A row
-//    each, 16-byte loads, stores into the 128B-swizzled layout).
+//  - Replicate padding and the encoder's stride-2 downsample remap source
+//    coordinates per pixel, which a box cannot express; those launches use
+//    128 gather threads instead (one A row each, 16-byte loads, stores into the
+//    128B-swizzled layout). Reflect padding on rows of >= 128 pixels keeps the
+//    halo boxes: the producer mirrors the row coordinate, and the MMA thread
+//    copies the mirrored edge column inside the landed box (column -1 <- 1,
+//    W <- W - 2) before it issues the stage; smaller grids gather.
 //  - B (weights [cout][taps][cin]) is a 3-D TMA tile load per (tap, chunk).
 //  - One elected thread issues tcgen05.mma (M=128, N=BN, K=16 steps) into one
 //    of two TMEM accumulators; four epilogue warps drain the other
@@ -228,6 +231,25 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
     return s;
 }
 
+// Reflect padding inside a landed 128B-swizzled halo box whose row 0 holds
+// source column `cbase`: the rows of columns -1 and W take columns 1 and W - 2
+// (generic-proxy copies, then a proxy fence before the MMAs read the box).
+// The box base is 1024-byte aligned, so row r's 16-byte chunk j sits at
+// r * 128 + ((j ^ (r & 7)) * 16).
+__device__ __forceinline__ void reflect_fix_box(uint8_t* box, int cbase, int W) {
+    bool fixed = false;
+    auto copy_row = [&](int rs, int rd) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(box + sw128_off(static_cast<uint32_t>(rd), static_cast<uint32_t>(j))) =
+                *reinterpret_cast<const uint4*>(box + sw128_off(static_cast<uint32_t>(rs), static_cast<uint32_t>(j)));
+        fixed = true;
+    };
+    if (cbase <= -1) copy_row(1 - cbase, -1 - cbase);
+    if (W - cbase <= kHaloRows - 1) copy_row(W - 2 - cbase, W - cbase);
+    if (fixed) fence_proxy_async_smem();
+}
+
 // Waits on a barrier during the final drain: bounded, but not cut short by
 // the abort flag (the point is to let in-flight async work land).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const ConvParams& p) {
@@ -294,11 +316,13 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
                 const int simg = src_img<kT3>(p, ti.img, kt + 3 - nkt);
                 for (int ky = 0; ky < NK && ok; ++ky) {
                     const int dy = kVar == 2 ? dymin + ky : (p.up ? (q + ky + 1) / 2 - 1 : ky - 1);
+                    int sy = ti.v0 + dy;
+                    if (kVar == 0 && p.refl) sy = sy < 0 ? -sy : (sy >= p.hs ? 2 * (p.hs - 1) - sy : sy);
                     for (int kc = 0; kc < kc_end && ok; ++kc) {
                         uint32_t slot;
                         const uint32_t fb = next_b(p.a_tx + static_cast<uint32_t>(NK) * b_bytes, &slot);
                         if (!ok) break;
-                        tma_load_4d(smem_u32(s.a + slot * kHaloBytes), mapA, fb, kc * kBK, ti.u0 + dxmin, ti.v0 + dy,
+                        tma_load_4d(smem_u32(s.a + slot * kHaloBytes), mapA, fb, kc * kBK, ti.u0 + dxmin, sy,
                                     simg, pol_a);
                         for (int kx = 0; kx < NK; ++kx)
                             tma_load_3d(smem_u32(s.b + (slot * 3 + kx) * p.BN * 128), mapB, fb, kc * kBK,
@@ -489,9 +513,12 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
         const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
         int kit = 0;
         if (p.halo && p.ks == 3) {
-            const int pp = decode_tile<kT3>(p, t).par & 1;
+            const TileInfo ti = decode_tile<kT3>(p, t);
+            const int pp = ti.par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             const int kc_end = p.rem16 ? p.kfull : p.kchunks;
+            // reflect padding: this tile's boxes hold column -1 or W (row 0 = column u0 - 1)
+            const bool refl_fix = kVar == 0 && p.refl && (ti.u0 == 0 || ti.u0 + kBM >= p.ws);
             for (int kt = 0; kt < (kT3 ? p.nkt : 1) && ok; ++kt) {  // temporal taps (3-D); one pass for 2-D
                 for (int ky = 0; ky < NK && ok; ++ky) {
                     for (int kc = 0; kc < kc_end && ok; ++kc) {
@@ -501,6 +528,7 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
                             break;
                         }
                         tc_fence_after();
+                        if (refl_fix) reflect_fix_box(s.a + stage * kHaloBytes, ti.u0 - 1, p.ws);
                         // All MMAs of the stage go out back to back: the tensor core's
                         // issue queue then covers this thread's barrier work.
                         const int nk = min(4, (p.cin - kc * kBK) / 16);
@@ -1385,6 +1413,21 @@ bool cta_pair_enabled() {
 // per-tap tiles (BN = 256) by 1.3-1.7x at 288, 576 and 1152 output channels
 // and tie at 192 and 768, while BN = 256 stays ahead when cout is a multiple of
 // 256 (256, 512, 1024).
+// The N tile of at most 144 columns with the least padding (ties: the widest).
+int choose_bn_small(int cout) {
+    const int c16 = (cout + 15) / 16 * 16;
+    if (c16 <= 144) return c16;
+    int best = 144, best_cost = (c16 + 143) / 144 * 144;
+    for (int bn = 144; bn >= 64; bn -= 16) {
+        const int cost = (c16 + bn - 1) / bn * bn;
+        if (cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
 int choose_bn(int cout, bool halo3) {
     const int c16 = (cout + 15) / 16 * 16;
     if (halo3 && c16 % 256 != 0) {
@@ -1532,7 +1575,9 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.rep = a.rep ? 1 : 0;
     p.H = p.up ? 2 * a.h_in : p.hv;
     p.W = p.up ? 2 * a.w_in : p.wv;
-    const bool gather = a.rep || a.refl || a.down;  // per-pixel source remaps: gather threads
+    // per-pixel source remaps: gather threads (reflect only where no halo box can serve)
+    const bool refl_halo = a.refl && !a.no_halo && a.taps == 9 && p.wv >= kBM;
+    const bool gather = a.rep || a.down || (a.refl && !refl_halo);
     if (p.wv >= kBM) {
         p.Wt = kBM;
         p.R = 1;
@@ -1546,7 +1591,8 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // Geometry that allows a halo box: a tile is 128 pixels of one row, 3x3 taps,
     // zero padding (the TMA box fills out-of-range pixels with zeros).
     const bool halo_geom = !gather && !a.no_halo && (a.taps == 9 || a.taps == 27) && p.R == 1 && p.Wt == kBM;
-    p.BN = choose_bn(a.cout, halo_geom);
+    // reflect padding needs the three-tap halo stages (the edge fix runs per stage): N <= 144
+    p.BN = refl_halo ? choose_bn_small(a.cout) : choose_bn(a.cout, halo_geom);
     p.b_rows = p.BN;
     p.n_tiles = (a.cout + p.BN - 1) / p.BN;
     p.acc_stride = (p.BN + 31) / 32 * 32;
@@ -1628,7 +1674,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     const int st3 = (kMaxSmem - 1024 - kTail) / (kHaloBytes + 3 * p.BN * 128);
     // (The one-tap halo ring has no sub-pixel form: that variant takes the halo
     // path only with three-tap stages.)
-    if (mode == kModeTma && halo_geom && (st3 >= 3 || (a.cin <= 192 && !a.subpix))) {
+    if (mode == kModeTma && halo_geom && (st3 >= 3 || (a.cin <= 192 && !a.subpix && !a.refl))) {
         // one 130-pixel halo box per (ky, chunk), shared by the three kx taps
         const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(p.wv),
                                   static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n_in)};
@@ -1647,7 +1693,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                 p.ks = 3;
                 p.stages = std::min(kMaxStages, st3);
                 p.a_stages = p.stages;
-                if (a.cin % kBK == 16 && a.cin > kBK) {
+                if (a.cin % kBK == 16 && a.cin > kBK && !a.refl) {
                     // exact 16-channel boxes for the remainder instead of zero-filled 64-channel ones
                     const uint32_t box16[4] = {16u, static_cast<uint32_t>(kHaloRows), 1u, 1u};
                     const uint64_t bdims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(wtaps),
@@ -1674,6 +1720,12 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
             clear_error();
         }
     }
+    if (a.refl && mode != kModeHalo) {
+        // only the halo stages carry the reflect fix: anything else gathers
+        mode = kModeGather;
+        p.ks = 1;
+        p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail) / (kABytes + p.BN * 128));
+    }
     if (mode == kModeTma) {
         const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(p.wv),
                                   static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n_in)};
@@ -1694,7 +1746,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // than single CTAs on GB300 at every decoder shape, so they run only when
     // requested (VAE_CONV_CTA_PAIR=1 in the environment).
     if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2 &&
-        a.taps != 27 && !a.subpix) {
+        a.taps != 27 && !a.subpix && !a.refl) {
         // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
         p.pair = 1;
         p.rem16 = 0;  // the pair kernel loads zero-filled 64-channel remainder boxes

@@ -55,6 +55,13 @@ SHAPES = [
     (1, 5, 257, 64, 3),
     (1, 4, 260, 128, 128),
     (1, 9, 40, 80, 320),
+    # rows of >= 128 pixels (the halo boxes with the mirrored edge columns): exactly one
+    # tile wide, a one-pixel last tile, two tiles, a 16-channel K remainder, two N tiles
+    (1, 3, 128, 64, 64),
+    (2, 4, 129, 32, 48),
+    (1, 3, 256, 128, 144),
+    (1, 5, 150, 80, 64),
+    (1, 3, 140, 64, 256),
 ]
 
 

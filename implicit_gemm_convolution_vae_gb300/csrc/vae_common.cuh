@@ -33,6 +33,7 @@ enum : int {
     kWhereDrain = 6,
     kWhereSelftest = 7,
     kWhereAttn = 8,
+    kWhereFixer = 9,
 };
 
 // ───────────────────────────── PTX wrappers ─────────────────────────────

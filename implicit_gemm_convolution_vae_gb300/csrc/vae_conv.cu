@@ -18,9 +18,10 @@
 //    coordinates per pixel, which a box cannot express; those launches use
 //    128 gather threads instead (one A row each, 16-byte loads, stores into the
 //    128B-swizzled layout). Reflect padding on rows of >= 128 pixels keeps the
-//    halo boxes: the producer mirrors the row coordinate, and the MMA thread
-//    copies the mirrored edge column inside the landed box (column -1 <- 1,
-//    W <- W - 2) before it issues the stage; smaller grids gather.
+//    halo boxes: the producer mirrors the row coordinate, and a fixer warp
+//    copies the mirrored edge column inside each landed box (column -1 <- 1,
+//    W <- W - 2) and passes the stage on to the MMA thread (whose own proxy
+//    fence would stall the tensor pipe); smaller grids gather.
 //  - B (weights [cout][taps][cin]) is a 3-D TMA tile load per (tap, chunk).
 //  - One elected thread issues tcgen05.mma (M=128, N=BN, K=16 steps) into one
 //    of two TMEM accumulators; four epilogue warps drain the other
@@ -207,6 +208,7 @@ struct Smem {
     uint64_t* accf;      // [2]
     uint64_t* acce;      // [2]
     uint64_t* drain;     // [1]
+    uint64_t* fixed;     // [stages] (reflect padding: the fixer warp hands each stage to the MMA thread)
     uint32_t* tmem_slot;
     int* abort_flag;
 };
@@ -226,7 +228,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
     s.accf = s.aempty + kMaxAStages;
     s.acce = s.accf + 2;
     s.drain = s.acce + 2;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.fixed = s.drain + 1;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.fixed + kMaxStages);
     s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
     return s;
 }
@@ -472,6 +475,32 @@ __device__ void role_gather(const ConvParams& p, const Smem& s, int gt) {
     }
 }
 
+// Reflect padding on the three-tap halo stages: for every stage, in ring order,
+// waits for the landed copies, mirrors the edge columns of edge tiles' boxes,
+// and hands the stage to the MMA thread (the `fixed` barrier completes once per
+// use of a slot, in lockstep with `full`).
+__device__ void role_fixer(const ConvParams& p, const Smem& s) {
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        const TileInfo ti = decode_tile<false>(p, t);
+        const bool edge = ti.u0 == 0 || ti.u0 + kBM >= p.ws;
+        for (int i = 0; i < 3 * p.kchunks; ++i) {
+            if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status, kWhereFixer)) {
+                ok = false;
+                break;
+            }
+            if (edge) reflect_fix_box(s.a + stage * kHaloBytes, ti.u0 - 1, p.ws);
+            mbar_arrive(smem_u32(&s.fixed[stage]));
+            if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
 template <int kVar>
 __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base) {
     constexpr bool kT3 = kVar == 1;
@@ -517,18 +546,17 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
             const int pp = ti.par & 1;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             const int kc_end = p.rem16 ? p.kfull : p.kchunks;
-            // reflect padding: this tile's boxes hold column -1 or W (row 0 = column u0 - 1)
-            const bool refl_fix = kVar == 0 && p.refl && (ti.u0 == 0 || ti.u0 + kBM >= p.ws);
+            // reflect padding: the fixer warp has mirrored the edge columns; wait for it
+            const uint64_t* ready = (kVar == 0 && p.refl) ? s.fixed : s.full;
             for (int kt = 0; kt < (kT3 ? p.nkt : 1) && ok; ++kt) {  // temporal taps (3-D); one pass for 2-D
                 for (int ky = 0; ky < NK && ok; ++ky) {
                     for (int kc = 0; kc < kc_end && ok; ++kc) {
-                        if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                        if (!mbar_wait(smem_u32(&ready[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
                                        kWhereMmaFull)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        if (refl_fix) reflect_fix_box(s.a + stage * kHaloBytes, ti.u0 - 1, p.ws);
                         // All MMAs of the stage go out back to back: the tensor core's
                         // issue queue then covers this thread's barrier work.
                         const int nk = min(4, (p.cin - kc * kBK) / 16);
@@ -989,7 +1017,7 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
 // kRms: the fused RMS_norm epilogue (a separate instantiation, so the other
 // kernels do not carry its 144-value row in registers).
 template <int kMode, bool kRms, int kVar>
-__global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
+__global__ void __launch_bounds__(kMode == kModeGather ? 320 : (kMode == kModeHalo ? 224 : 192), 1)
     conv_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapA16, const __grid_constant__ CUtensorMap mapB16,
                 const __grid_constant__ CUtensorMap mapY, const ConvParams p) {
@@ -1014,6 +1042,8 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
             mbar_init(smem_u32(&s.acce[i]), static_cast<uint32_t>(kEpiWarps * 32));
         }
         mbar_init(smem_u32(s.drain), 1u);
+        if (kMode == kModeHalo && p.refl)
+            for (int i = 0; i < p.stages; ++i) mbar_init(smem_u32(&s.fixed[i]), 1u);
         fence_mbar_init();
     }
     const uint32_t tmem_cols = p.acc_stride * 2 <= 32 ? 32u
@@ -1047,6 +1077,8 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 192, 1)
         if (lane == 0) role_mma<kVar>(p, s, tmem_base);
     } else if (kMode == kModeGather && warp >= kGatherWarp0) {
         role_gather<kVar>(p, s, (warp - kGatherWarp0) * 32 + lane);
+    } else if (kMode == kModeHalo && kVar == 0 && warp == kGatherWarp0) {
+        if (lane == 0) role_fixer(p, s);  // launched only for reflect padding
     }
     tc_fence_before();
     __syncthreads();
@@ -1482,7 +1514,8 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, co
             cudaFuncSetAttribute(conv_kernel<kMode, kRms, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set[dev] = true;
     }
-    conv_kernel<kMode, kRms, kVar><<<grid, kMode == kModeGather ? 320 : 192, smem, stream>>>(ma, mb, ma16, mb16, my, p);
+    const int threads = kMode == kModeGather ? 320 : (kMode == kModeHalo && p.refl ? 224 : 192);
+    conv_kernel<kMode, kRms, kVar><<<grid, threads, smem, stream>>>(ma, mb, ma16, mb16, my, p);
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }

@@ -234,23 +234,29 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
     return s;
 }
 
-// Reflect padding inside a landed 128B-swizzled halo box whose row 0 holds
-// source column `cbase`: the rows of columns -1 and W take columns 1 and W - 2
-// (generic-proxy copies, then a proxy fence before the MMAs read the box).
-// The box base is 1024-byte aligned, so row r's 16-byte chunk j sits at
-// r * 128 + ((j ^ (r & 7)) * 16).
-__device__ __forceinline__ void reflect_fix_box(uint8_t* box, int cbase, int W) {
+// Reflect padding inside a landed halo box whose row 0 holds source column
+// `cbase`: the rows of columns -1 and W take columns 1 and W - 2 (generic-proxy
+// copies; the caller fences before the MMAs read the box). kRow = 128: a
+// 64-channel box, 128-byte swizzle, 1024-byte aligned, so row r's 16-byte
+// chunk j sits at r * 128 + ((j ^ (r & 7)) * 16). kRow = 32: a 16-channel box,
+// 32-byte swizzle, 256-byte aligned: chunk j of row r at r * 32 + ((j ^ ((r >> 2) & 1)) * 16).
+// Returns whether it wrote anything.
+template <int kRow>
+__device__ __forceinline__ bool reflect_fix_box(uint8_t* box, int cbase, int W) {
     bool fixed = false;
+    auto off = [](int r, int j) -> uint32_t {
+        return kRow == 128 ? sw128_off(static_cast<uint32_t>(r), static_cast<uint32_t>(j))
+                           : static_cast<uint32_t>(r * 32 + ((j ^ ((r >> 2) & 1)) << 4));
+    };
     auto copy_row = [&](int rs, int rd) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(box + sw128_off(static_cast<uint32_t>(rd), static_cast<uint32_t>(j))) =
-                *reinterpret_cast<const uint4*>(box + sw128_off(static_cast<uint32_t>(rs), static_cast<uint32_t>(j)));
+        for (int j = 0; j < kRow / 16; ++j)
+            *reinterpret_cast<uint4*>(box + off(rd, j)) = *reinterpret_cast<const uint4*>(box + off(rs, j));
         fixed = true;
     };
     if (cbase <= -1) copy_row(1 - cbase, -1 - cbase);
     if (W - cbase <= kHaloRows - 1) copy_row(W - 2 - cbase, W - cbase);
-    if (fixed) fence_proxy_async_smem();
+    return fixed;
 }
 
 // Waits on a barrier during the final drain: bounded, but not cut short by
@@ -341,8 +347,10 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
                     if (ok) {
                         for (int ky = 0; ky < NK; ++ky) {
                             const int dy = kVar == 2 ? dymin + ky : (p.up ? (q + ky + 1) / 2 - 1 : ky - 1);
+                            int sy = ti.v0 + dy;
+                            if (kVar == 0 && p.refl) sy = sy < 0 ? -sy : (sy >= p.hs ? 2 * (p.hs - 1) - sy : sy);
                             tma_load_4d(smem_u32(s.a + slot * kHaloBytes + ky * kRemAStride), mapA16, fb,
-                                        p.kfull * kBK, ti.u0 + dxmin, ti.v0 + dy, simg, pol_a);
+                                        p.kfull * kBK, ti.u0 + dxmin, sy, simg, pol_a);
                         }
                         for (int tap = 0; tap < NK * NK; ++tap)
                             tma_load_3d(smem_u32(s.b + slot * 3 * p.BN * 128 + tap * p.BN * 32), mapB16, fb,
@@ -486,12 +494,22 @@ __device__ void role_fixer(const ConvParams& p, const Smem& s) {
     for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile<false>(p, t);
         const bool edge = ti.u0 == 0 || ti.u0 + kBM >= p.ws;
-        for (int i = 0; i < 3 * p.kchunks; ++i) {
+        const int nfull = 3 * (p.rem16 ? p.kfull : p.kchunks);
+        for (int i = 0; i < nfull + (p.rem16 ? 1 : 0); ++i) {
             if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status, kWhereFixer)) {
                 ok = false;
                 break;
             }
-            if (edge) reflect_fix_box(s.a + stage * kHaloBytes, ti.u0 - 1, p.ws);
+            if (edge) {
+                uint8_t* box = s.a + stage * kHaloBytes;
+                bool fixed = false;
+                if (i < nfull) {
+                    fixed = reflect_fix_box<128>(box, ti.u0 - 1, p.ws);
+                } else {  // the 16-channel remainder stage: one 32-byte-swizzled box per ky
+                    for (int ky = 0; ky < 3; ++ky) fixed |= reflect_fix_box<32>(box + ky * kRemAStride, ti.u0 - 1, p.ws);
+                }
+                if (fixed) fence_proxy_async_smem();
+            }
             mbar_arrive(smem_u32(&s.fixed[stage]));
             if (++stage == p.stages) {
                 stage = 0;
@@ -588,7 +606,7 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
                     }
                 }
                 if (p.rem16 && ok) {
-                    if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                    if (!mbar_wait(smem_u32(&ready[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
                                    kWhereMmaFull)) {
                         ok = false;
                     } else {
@@ -1726,7 +1744,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                 p.ks = 3;
                 p.stages = std::min(kMaxStages, st3);
                 p.a_stages = p.stages;
-                if (a.cin % kBK == 16 && a.cin > kBK && !a.refl) {
+                if (a.cin % kBK == 16 && a.cin > kBK) {
                     // exact 16-channel boxes for the remainder instead of zero-filled 64-channel ones
                     const uint32_t box16[4] = {16u, static_cast<uint32_t>(kHaloRows), 1u, 1u};
                     const uint64_t bdims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(wtaps),

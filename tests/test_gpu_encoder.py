@@ -61,6 +61,8 @@ SHAPES = [
     (2, 4, 129, 32, 48),
     (1, 3, 256, 128, 144),
     (1, 5, 150, 80, 64),
+    (1, 4, 129, 144, 144),
+    (1, 3, 256, 208, 96),
     (1, 3, 140, 64, 256),
 ]
 

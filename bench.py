@@ -243,6 +243,33 @@ def run_kernel(args):
         y = torch.empty(h * w, cin, dtype=torch.float16, device="cuda")
         fn = lambda: vg.rmsnorm_silu(x, g, silu=True, out=y)
         flops, nbytes = 0.0, x.numel() * 6
+    elif args.kernel in ("convgn", "convgn_fused"):
+        # a 3x3 conv (f32 out, in-place residual) followed by GroupNorm(32)+SiLU -> f16:
+        # convgn = conv + the standalone two-pass GroupNorm; convgn_fused = the conv
+        # taking the statistics in its epilogue + the one-read apply
+        x = torch.randn(1, h, w, cin, device="cuda").half()
+        wt = (torch.randn(cout, 3, 3, cin, device="cuda") / (9 * cin) ** 0.5).half()
+        b = torch.randn(cout, device="cuda") * 0.1
+        y = torch.randn(1, h, w, cout, device="cuda")
+        g = torch.ones(cout, device="cuda")
+        bb = torch.zeros(cout, device="cuda")
+        yn = torch.empty(1, h * w, cout, dtype=torch.float16, device="cuda")
+        refl = args.reflect
+        if args.kernel == "convgn":
+            wsp = torch.empty(vg.groupnorm_workspace_bytes(1, h * w, cout, 32), dtype=torch.uint8, device="cuda")
+
+            def fn():
+                vg.conv3x3_nhwc(x, wt, b, residual=y, out=y, reflect=refl)
+                vg.groupnorm_silu(y.reshape(1, h * w, cout), 32, g, bb, silu=True, out=yn, workspace=wsp)
+        else:
+            wsp = torch.empty(vg.conv3x3_gn_workspace_bytes(1, h, w, cout, 32, vg.PAD_REFLECT if refl else 0),
+                              dtype=torch.uint8, device="cuda")
+
+            def fn():
+                _, st = vg.conv3x3_nhwc_gn(x, wt, 32, b, residual=y, out=y, reflect=refl, workspace=wsp)
+                vg.groupnorm_apply(y.reshape(1, h * w, cout), 32, st, g, bb, silu=True, out=yn)
+        flops = 2.0 * h * w * cout * 9 * cin
+        nbytes = x.numel() * 2 + y.numel() * 4 * 2 + y.numel() * (4 + 2)
     elif args.kernel == "groupnorm":
         x = torch.randn(1, h * w, cin, device="cuda")
         g = torch.ones(cin, device="cuda")
@@ -298,7 +325,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", default=None,
-                    help="time one kernel instead: conv3x3, upconv3x3, downconv3x3, conv3d, upconv3d, rmsnorm, groupnorm, "
+                    help="time one kernel instead: conv3x3, upconv3x3, downconv3x3, conv3d, upconv3d, convgn, convgn_fused, "
+                         "rmsnorm, groupnorm, "
                          "attention")
     ap.add_argument("--shape", default="1024,1024,144,144",
                     help="h,w,cin,cout (attention: h,w,c,c; conv3d/upconv3d: f,h,w,cin,cout)")

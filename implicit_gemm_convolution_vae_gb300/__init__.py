@@ -21,7 +21,8 @@ from .build import LIB_PATH, build  # noqa: F401  (build is re-exported)
 
 __all__ = [
     "VaeError", "lib", "version", "last_error", "sync_status", "set_wait_timeout_ns",
-    "selftest_wait_timeout", "conv3x3_nhwc", "conv1x1", "rmsnorm_silu", "groupnorm_silu",
+    "selftest_wait_timeout", "conv3x3_nhwc", "conv3x3_nhwc_gn", "conv3x3_gn_workspace_bytes", "groupnorm_apply",
+    "conv1x1", "rmsnorm_silu", "groupnorm_silu",
     "groupnorm_workspace_bytes", "cast_f16", "mid_attention", "mid_attention_workspace_bytes",
     "Decoder", "pack_conv3x3", "pack_conv1x1",
     "UPSAMPLE2X", "PAD_REPLICATE", "PAD_REFLECT", "DOWNSAMPLE2X", "EPI_SILU", "OUT_F16", "FAMILY_GN", "FAMILY_RMS",
@@ -61,6 +62,9 @@ SIGNATURES = {
     "vae_conv3d_causal_ndhwc": ([_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _P], _I),
     "vae_pack_subpixel_weights": ([_P, _I, _I, _P, _P], _I),
     "vae_conv1x1": ([_P, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _P], _I),
+    "vae_conv3x3_gn_workspace_bytes": ([_I, _I, _I, _I, _I, ctypes.c_uint], _SZ),
+    "vae_conv3x3_nhwc_gn": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _I, _F, _P, _P, _SZ, _P], _I),
+    "vae_groupnorm_apply": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _F, _P, _P], _I),
     "vae_rmsnorm_silu": ([_P, _I, _I, _P, _P, _I, _F, _P, _P], _I),
     "vae_groupnorm_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "vae_groupnorm_silu": ([_P, _I, _I, _I, _I, _F, _P, _P, _P, _I, _F, _P, _P, _SZ, _P], _I),
@@ -188,6 +192,62 @@ def conv3x3_nhwc(x, w, bias=None, residual=None, out=None, oscale: float = 1.0, 
             (PAD_REFLECT if reflect else 0) | (DOWNSAMPLE2X if down else 0)
     _check(lib().vae_conv3x3_nhwc(_ptr(x), n, h, wd, cin, _ptr(w), _ptr(bias), _ptr(residual), _ptr(out),
                                   cout, float(oscale), flags, _stream(stream)))
+    return out
+
+
+def conv3x3_nhwc_gn(x, w, groups: int, bias=None, residual=None, out=None, oscale: float = 1.0,
+                    upsample: bool = False, replicate: bool = False, reflect: bool = False, down: bool = False,
+                    silu: bool = False, eps: float = 1e-6, workspace=None, stream=None):
+    """3x3 conv (f32 output) that also returns the GroupNorm statistics of its
+    output: (y [n][H][W][cout] f32, stats [n][groups][2] f32 = (mean, rstd))."""
+    import torch
+    _need(x, torch.float16, "x", 4)
+    _need(w, torch.float16, "w", 4)
+    _need(bias, torch.float32, "bias", 1)
+    n, h, wd, cin = x.shape
+    cout = w.shape[0]
+    if tuple(w.shape[1:]) != (3, 3, cin):
+        raise VaeError(-2, f"w has the wrong shape {tuple(w.shape)}")
+    H, W = (2 * h, 2 * wd) if upsample else ((h // 2, wd // 2) if down else (h, wd))
+    if out is None:
+        out = torch.empty((n, H, W, cout), dtype=torch.float32, device=x.device)
+    _need(out, torch.float32, "out")
+    _need(residual, torch.float32, "residual")
+    for t, nm in ((out, "out"), (residual, "residual")):
+        if t is not None and t.numel() != n * H * W * cout:
+            raise VaeError(-2, f"{nm} must hold [n][{H}][{W}][{cout}], got {tuple(t.shape)}")
+    flags = (UPSAMPLE2X if upsample else 0) | (PAD_REPLICATE if replicate else 0) | (EPI_SILU if silu else 0) | \
+            (PAD_REFLECT if reflect else 0) | (DOWNSAMPLE2X if down else 0)
+    need = conv3x3_gn_workspace_bytes(n, h, wd, cout, groups, flags)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    stats = torch.empty((n, groups, 2), dtype=torch.float32, device=x.device)
+    _check(lib().vae_conv3x3_nhwc_gn(_ptr(x), n, h, wd, cin, _ptr(w), _ptr(bias), _ptr(residual), _ptr(out), cout,
+                                     float(oscale), flags, int(groups), float(eps), _ptr(stats), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)))
+    return out, stats
+
+
+def conv3x3_gn_workspace_bytes(n: int, h: int, w: int, cout: int, groups: int, flags: int = 0) -> int:
+    return int(lib().vae_conv3x3_gn_workspace_bytes(n, h, w, cout, groups, flags))
+
+
+def groupnorm_apply(x, groups: int, stats, gamma, beta, silu: bool = False, out_scale: float = 1.0, out=None,
+                    stream=None):
+    """GroupNorm from precomputed statistics. x f32 [n][hw][c] -> f16 [n][hw][c]."""
+    import torch
+    _need(x, torch.float32, "x", 3)
+    _need(stats, torch.float32, "stats")
+    _need(gamma, torch.float32, "gamma", 1)
+    _need(beta, torch.float32, "beta", 1)
+    n, hw, c = x.shape
+    if stats.numel() != n * groups * 2:
+        raise VaeError(-2, f"stats must hold [n][{groups}][2], got {tuple(stats.shape)}")
+    if out is None:
+        out = torch.empty((n, hw, c), dtype=torch.float16, device=x.device)
+    _need(out, torch.float16, "out")
+    _check(lib().vae_groupnorm_apply(_ptr(x), n, hw, c, groups, _ptr(stats), _ptr(gamma), _ptr(beta),
+                                     1 if silu else 0, float(out_scale), _ptr(out), _stream(stream)))
     return out
 
 

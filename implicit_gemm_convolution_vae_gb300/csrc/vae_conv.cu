@@ -38,6 +38,7 @@
 #include <cstdlib>
 
 #include "vae_conv.h"
+#include "vae_norm.h"
 #include "vae_rms.cuh"
 
 namespace vae {
@@ -60,6 +61,10 @@ constexpr int kStgBytes = 2048;      // 32 pixels x 16 f32 channels, 64-byte swi
 // (replicate padding); one A "halo" box per (ky, chunk) shared by the three
 // kx taps through descriptor start offsets of whole 128-byte rows.
 constexpr int kModeTma = 0, kModeGather = 1, kModeHalo = 2;
+// Variants (the kernel's kVar): 0 the 2-D conv, 1 the 3x3x3 conv, 2 the
+// sub-pixel up conv, 3 the 2-D conv whose epilogue also emits GroupNorm
+// partial statistics of its output.
+constexpr bool is_2d(int var) { return var == 0 || var == 3; }
 constexpr int kEpiWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -115,6 +120,10 @@ struct ConvParams {
     const float* rms_gamma;
     __half* rms_out;
     int rms_silu;
+    // GroupNorm partial statistics of the output (variant 3): per (image,
+    // chunk = M tile * 4 + epilogue warp, group) one record (count, mean, M2, 0).
+    float4* gn_part;
+    int gn_groups, gn_cpg, gn_nchunks;
     DevStatus* status;
     unsigned long long timeout_ns;
 };
@@ -326,7 +335,7 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
                 for (int ky = 0; ky < NK && ok; ++ky) {
                     const int dy = kVar == 2 ? dymin + ky : (p.up ? (q + ky + 1) / 2 - 1 : ky - 1);
                     int sy = ti.v0 + dy;
-                    if (kVar == 0 && p.refl) sy = sy < 0 ? -sy : (sy >= p.hs ? 2 * (p.hs - 1) - sy : sy);
+                    if (is_2d(kVar) && p.refl) sy = sy < 0 ? -sy : (sy >= p.hs ? 2 * (p.hs - 1) - sy : sy);
                     for (int kc = 0; kc < kc_end && ok; ++kc) {
                         uint32_t slot;
                         const uint32_t fb = next_b(p.a_tx + static_cast<uint32_t>(NK) * b_bytes, &slot);
@@ -348,7 +357,7 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
                         for (int ky = 0; ky < NK; ++ky) {
                             const int dy = kVar == 2 ? dymin + ky : (p.up ? (q + ky + 1) / 2 - 1 : ky - 1);
                             int sy = ti.v0 + dy;
-                            if (kVar == 0 && p.refl) sy = sy < 0 ? -sy : (sy >= p.hs ? 2 * (p.hs - 1) - sy : sy);
+                            if (is_2d(kVar) && p.refl) sy = sy < 0 ? -sy : (sy >= p.hs ? 2 * (p.hs - 1) - sy : sy);
                             tma_load_4d(smem_u32(s.a + slot * kHaloBytes + ky * kRemAStride), mapA16, fb,
                                         p.kfull * kBK, ti.u0 + dxmin, sy, simg, pol_a);
                         }
@@ -565,7 +574,7 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             const int kc_end = p.rem16 ? p.kfull : p.kchunks;
             // reflect padding: the fixer warp has mirrored the edge columns; wait for it
-            const uint64_t* ready = (kVar == 0 && p.refl) ? s.fixed : s.full;
+            const uint64_t* ready = (is_2d(kVar) && p.refl) ? s.fixed : s.full;
             for (int kt = 0; kt < (kT3 ? p.nkt : 1) && ok; ++kt) {  // temporal taps (3-D); one pass for 2-D
                 for (int ky = 0; ky < NK && ok; ++ky) {
                     for (int kc = 0; kc < kc_end && ok; ++kc) {
@@ -826,6 +835,86 @@ __device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInf
     }
 }
 
+// Running (count, mean, M2) of a group wider than 16 channels across the
+// chunks of one warp's pixels.
+struct GnRun {
+    float n, mean, m2;
+};
+
+__device__ __forceinline__ void gn_merge(GnRun& a, float nb, float mb, float m2b) {
+    if (nb <= 0.f) return;
+    const float n = a.n + nb;
+    const float d = mb - a.mean;
+    const float f = nb / n;
+    a.mean += d * f;
+    a.m2 += m2b + d * d * a.n * f;
+    a.n = n;
+}
+
+// GroupNorm partial statistics of one 16-channel chunk (channels o0..o0+15)
+// of this warp's 32 pixels: for each group part of W channels in the chunk,
+// the count, mean and M2 over the valid pixels, two-pass within the warp
+// (all lanes end with the same values). A group of <= 16 channels is one
+// part; wider groups merge their parts across chunks (Chan's formula). Lane 0
+// writes the record of each completed group.
+template <int W>
+__device__ __forceinline__ void gn_chunk_w(const ConvParams& p, const TileInfo& ti, const float (&val)[16],
+                                           bool valid, int o0, int chunk, int lane, GnRun& run) {
+    constexpr int G = 16 / W;
+    const float cnt = static_cast<float>(__popc(__ballot_sync(0xffffffffu, valid)) * W);
+    float s[G], d[G];
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < W; ++i) a += val[k * W + i];
+        s[k] = valid ? a : 0.f;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int k = 0; k < G; ++k) s[k] += __shfl_xor_sync(0xffffffffu, s[k], off);
+#pragma unroll
+    for (int k = 0; k < G; ++k) {
+        s[k] = cnt > 0.f ? s[k] / cnt : 0.f;  // the part's mean
+        float a = 0.f;
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            const float e = val[k * W + i] - s[k];
+            a += e * e;
+        }
+        d[k] = valid ? a : 0.f;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int k = 0; k < G; ++k) d[k] += __shfl_xor_sync(0xffffffffu, d[k], off);
+    float4* rec = p.gn_part + (static_cast<long long>(ti.img) * p.gn_nchunks + chunk) * p.gn_groups;
+    if (W < 16 || p.gn_cpg == 16) {
+        if (lane == 0)
+#pragma unroll
+            for (int k = 0; k < G; ++k) rec[(o0 + k * W) / p.gn_cpg] = make_float4(cnt, s[k], d[k], 0.f);
+    } else {
+        gn_merge(run, cnt, s[0], d[0]);
+        if ((o0 + 16) % p.gn_cpg == 0) {
+            if (lane == 0) rec[o0 / p.gn_cpg] = make_float4(run.n, run.mean, run.m2, 0.f);
+            run = GnRun{0.f, 0.f, 0.f};
+        }
+    }
+}
+
+__device__ __forceinline__ void gn_chunk(const ConvParams& p, const TileInfo& ti, const float (&val)[16], bool valid,
+                                         int o0, int ew, int lane, GnRun& run) {
+    const int mt = ((ti.v0 / p.R) * p.npar + ti.par) * p.tiles_x + ti.u0 / p.Wt;  // M tile within the image
+    const int chunk = mt * kEpiWarps + ew;
+    if (p.gn_cpg == 4)
+        gn_chunk_w<4>(p, ti, val, valid, o0, chunk, lane, run);
+    else if (p.gn_cpg == 8)
+        gn_chunk_w<8>(p, ti, val, valid, o0, chunk, lane, run);
+    else
+        gn_chunk_w<16>(p, ti, val, valid, o0, chunk, lane, run);
+}
+
 template <bool kWide = true>
 __device__ __forceinline__ void epilogue_chunk(const ConvParams& p, const TileInfo& ti, const uint32_t (&r)[16],
                                                int o0, int v, int u, int q, int pp, int Y, int X,
@@ -903,9 +992,11 @@ __device__ __forceinline__ void epilogue_rms_row(const ConvParams& p, const Tile
 
 // Epilogue of one accumulator row (pixel) without a fused norm. kPipe: the
 // register-hungry pipelined residual path (off in the 320-thread gather kernel).
-template <bool kPipe>
+template <bool kPipe, bool kGn = false>
 __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, bool valid,
-                                                   int v, int u, int q, int pp, int Y, int X, long long pix) {
+                                                   int v, int u, int q, int pp, int Y, int X, long long pix,
+                                                   int ew = 0, int lane = 0) {
+    GnRun run{0.f, 0.f, 0.f};
     if (kPipe && p.residual != nullptr && p.v8_ok && !p.out_nchw) {
         // Residual loads run two chunks ahead of their use (a three-slot
         // register ring), so three are in flight instead of one.
@@ -925,7 +1016,15 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
             tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
             tmem_ld_wait();
             const int o0 = ti.n0 + c * 16;
-            if (valid && o0 < p.cout) {
+            if (kGn) {
+                if (o0 >= p.cout) return;  // warp-uniform
+                float val[16];
+                if (valid) {
+                    compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, rr);
+                    store_chunk(p, pix, o0, val, Y, X, ti.img);
+                }
+                gn_chunk(p, ti, val, valid, o0, ew, lane, run);
+            } else if (valid && o0 < p.cout) {
                 float val[16];
                 compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, rr);
                 store_chunk(p, pix, o0, val, Y, X, ti.img);
@@ -949,7 +1048,17 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
         tmem_ld16(tbase + static_cast<uint32_t>(j), r);
         tmem_ld_wait();
         const int o0 = ti.n0 + j;
-        if (valid && o0 < p.cout) epilogue_chunk<kPipe>(p, ti, r, o0, v, u, q, pp, Y, X, pix);
+        if (kGn) {
+            if (o0 >= p.cout) break;  // warp-uniform
+            float val[16];
+            if (valid) {
+                compute_chunk<kPipe>(p, ti, r, o0, v, u, q, pp, pix, val);
+                store_chunk(p, pix, o0, val, Y, X, ti.img);
+            }
+            gn_chunk(p, ti, val, valid, o0, ew, lane, run);
+        } else if (valid && o0 < p.cout) {
+            epilogue_chunk<kPipe>(p, ti, r, o0, v, u, q, pp, Y, X, pix);
+        }
     }
 }
 
@@ -958,9 +1067,11 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
 // f32 add onto y when y is the residual (the add then happens in L2: y + (acc *
 // oscale + bias), the same two roundings as the register path). No global
 // loads or per-lane stores: the warp's traffic is whole 2 KB boxes.
+template <bool kGn = false>
 __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, int v, int u,
                                                  int q, int pp, long long pix, uint8_t* stg, const CUtensorMap* mapY,
-                                                 int ew, int lane) {
+                                                 int ew, int lane, bool valid = true) {
+    GnRun run{0.f, 0.f, 0.f};
     const uint32_t sbase = smem_u32(stg + ew * kStgBytes);
     const int seg = ti.u0 + ew * 32;  // first pixel of this warp's 32 (warp-uniform)
     const uint32_t row_off = static_cast<uint32_t>(lane) * 64u;
@@ -972,8 +1083,15 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
         tmem_ld_wait();
         const int o0 = ti.n0 + c * 16;
         if (o0 >= p.cout) break;  // warp-uniform
+        // pixels past the row's end read no residual or DupUp source; their values are not stored
         float val[16];
-        compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val);
+        if (valid) {
+            compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) val[i] = 0.f;
+        }
+        if (kGn) gn_chunk(p, ti, val, valid, o0, ew, lane, run);
         if (lane == 0) bulk_wait_read_all();  // the previous box left this warp's buffer
         __syncwarp();
 #pragma unroll
@@ -1020,9 +1138,10 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         if (kRms) {
             epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         } else if (kMode != kModeGather && p.epi_tma) {
-            epilogue_tma_row(p, ti, tbase, v, u, q, pp, pix, s.stg, mapY, ew, lane);
+            epilogue_tma_row<kVar == 3>(p, ti, tbase, v, u, q, pp, pix, s.stg, mapY, ew, lane, valid);
         } else {
-            epilogue_plain_row<kMode != kModeGather>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
+            epilogue_plain_row<kMode != kModeGather, kVar == 3>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix, ew,
+                                                                 lane);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&s.acce[accbuf]));
@@ -1095,7 +1214,7 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : (kMode == kModeHa
         if (lane == 0) role_mma<kVar>(p, s, tmem_base);
     } else if (kMode == kModeGather && warp >= kGatherWarp0) {
         role_gather<kVar>(p, s, (warp - kGatherWarp0) * 32 + lane);
-    } else if (kMode == kModeHalo && kVar == 0 && warp == kGatherWarp0) {
+    } else if (kMode == kModeHalo && is_2d(kVar) && warp == kGatherWarp0) {
         if (lane == 0) role_fixer(p, s);  // launched only for reflect padding
     }
     tc_fence_before();
@@ -1540,6 +1659,15 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, co
 
 }  // namespace
 
+int conv_gn_chunks(int h_in, int w_in, bool up, bool down) {
+    // the tiling of conv_run: the virtual grid, its tile shape and the parity classes
+    const int hv = down ? h_in / 2 : h_in, wv = down ? w_in / 2 : w_in;
+    if (hv < 1 || wv < 1) return -1;
+    const int Wt = wv >= kBM ? kBM : wv, R = wv >= kBM ? 1 : kBM / wv;
+    const long long tiles = static_cast<long long>((hv + R - 1) / R) * (up ? 4 : 1) * ((wv + Wt - 1) / Wt);
+    return tiles * kEpiWarps >= (1LL << 31) ? -1 : static_cast<int>(tiles * kEpiWarps);
+}
+
 int conv_validate(const ConvArgs& a) {
     if (a.x == nullptr || a.w == nullptr)
         return set_error(VAE_ERR_ARG, "conv: x and w must be non-NULL");
@@ -1568,6 +1696,16 @@ int conv_validate(const ConvArgs& a) {
         return set_error(VAE_ERR_SHAPE, "conv: reflect padding and the downsample need h, w >= 2 (h=%d w=%d)",
                          a.h_in, a.w_in);
     if (a.down && a.dup_src != nullptr) return set_error(VAE_ERR_ARG, "conv: no DupUp on the downsample");
+    if (a.gn_part != nullptr) {
+        if (a.taps != 9 || a.subpix || a.out_f16 || a.out_nchw || a.rms_out != nullptr || a.y == nullptr)
+            return set_error(VAE_ERR_ARG, "conv: GroupNorm statistics need a 2-D 3x3 conv with an f32 output");
+        const int cpg = a.gn_groups >= 1 && a.cout % a.gn_groups == 0 ? a.cout / a.gn_groups : 0;
+        if (a.cout % 16 != 0 || cpg == 0 || cpg % 4 != 0 || (cpg > 16 && cpg % 16 != 0))
+            return set_error(VAE_ERR_SHAPE,
+                             "conv: GroupNorm statistics need cout %% 16 == 0 and C/groups in {4, 8} or a multiple "
+                             "of 16 (cout=%d groups=%d)", a.cout, a.gn_groups);
+        if (!aligned16(a.gn_part)) return set_error(VAE_ERR_ALIGN, "conv: the statistics workspace must be 16-byte aligned");
+    }
     if (!aligned16(a.x) || !aligned16(a.w))
         return set_error(VAE_ERR_ALIGN, "conv: x and w must be 16-byte aligned");
     const long long H = a.up ? 2LL * a.h_in : a.h_in, W = a.up ? 2LL * a.w_in : a.w_in;
@@ -1704,6 +1842,15 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.rms_gamma = a.rms_gamma;
     p.rms_out = static_cast<__half*>(a.rms_out);
     p.rms_silu = a.rms_silu ? 1 : 0;
+    p.gn_part = static_cast<float4*>(a.gn_part);
+    if (a.gn_part != nullptr) {
+        p.gn_groups = a.gn_groups;
+        p.gn_cpg = a.cout / a.gn_groups;
+        p.gn_nchunks = p.tiles_y * p.npar * p.tiles_x * kEpiWarps;
+        if (p.gn_cpg > 16 && p.BN % p.gn_cpg != 0)
+            return set_error(VAE_ERR_SHAPE, "conv: a group of %d channels straddles the %d-column N tiles", p.gn_cpg,
+                             p.BN);
+    }
     p.status = st;
     p.timeout_ns = wait_timeout_ns();
 
@@ -1797,7 +1944,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // than single CTAs on GB300 at every decoder shape, so they run only when
     // requested (VAE_CONV_CTA_PAIR=1 in the environment).
     if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2 &&
-        a.taps != 27 && !a.subpix && !a.refl) {
+        a.taps != 27 && !a.subpix && !a.refl && a.gn_part == nullptr) {
         // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
         p.pair = 1;
         p.rem16 = 0;  // the pair kernel loads zero-filled 64-channel remainder boxes
@@ -1845,7 +1992,8 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // upsampling and DupUp (whose add comes after the residual's).
     const bool res_self = a.residual != nullptr && a.residual == a.y && !a.silu && !p.up && a.dup_src == nullptr;
     if (mode != kModeGather && p.R == 1 && p.Wt == kBM && !p.out_f16 && !p.out_nchw && a.rms_out == nullptr &&
-        a.cout % 16 == 0 && a.y != nullptr && aligned16(a.y) && (a.residual == nullptr || res_self) &&
+        a.cout % 16 == 0 && a.y != nullptr && aligned16(a.y) &&
+        (a.residual == nullptr || res_self || a.gn_part != nullptr) &&
         1024 + ring + kEpiWarps * kStgBytes + kTail <= kMaxSmem) {
         int erc;
         if (p.up) {  // y viewed as (channel, column parity, W/2, row, image)
@@ -1866,8 +2014,8 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
             erc = encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, dims, strides, box,
                                CU_TENSOR_MAP_SWIZZLE_64B);
         }
-        if (erc == VAE_OK)
-            p.epi_tma = res_self ? 2 : 1;
+        if (erc == VAE_OK)  // with statistics the values are needed in registers: the residual is read, not added
+            p.epi_tma = res_self && a.gn_part == nullptr ? 2 : 1;
         else
             clear_error();
     }
@@ -1876,6 +2024,11 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         if (mode == kModeHalo) return launch<kModeHalo, false, 1>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
         if (mode == kModeGather) return launch<kModeGather, false, 1>(p, ma, mb, ma, mb, my, smem, grid, stream);
         return launch<kModeTma, false, 1>(p, ma, mb, ma, mb, my, smem, grid, stream);
+    }
+    if (a.gn_part != nullptr) {  // the 2-D conv with the GroupNorm statistics epilogue
+        if (mode == kModeHalo) return launch<kModeHalo, false, 3>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
+        if (mode == kModeGather) return launch<kModeGather, false, 3>(p, ma, mb, ma, mb, my, smem, grid, stream);
+        return launch<kModeTma, false, 3>(p, ma, mb, ma, mb, my, smem, grid, stream);
     }
     if (a.subpix) {  // the sub-pixel up conv instantiations
         if (mode == kModeHalo) return launch<kModeHalo, false, 2>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
@@ -1969,6 +2122,56 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin, cons
     a.silu = (flags & VAE_EPI_SILU) != 0;
     a.out_f16 = (flags & VAE_OUT_F16) != 0;
     return conv_run(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t vae_conv3x3_gn_workspace_bytes(int n, int h_in, int w_in, int cout, int groups, unsigned flags) {
+    clear_error();
+    const int nch = conv_gn_chunks(h_in, w_in, (flags & VAE_UPSAMPLE2X) != 0, (flags & VAE_DOWNSAMPLE2X) != 0);
+    if (n < 1 || nch < 1 || groups < 1 || cout < 1 || cout % groups != 0) return 0;
+    return static_cast<size_t>(n) * nch * groups * sizeof(float4);
+}
+
+int vae_conv3x3_nhwc_gn(const void* x_dev, int n, int h_in, int w_in, int cin, const void* w_dev,
+                        const float* bias_dev, const float* residual_dev, float* y_dev, int cout, float oscale,
+                        unsigned flags, int groups, float eps, float* gn_stats_dev, void* workspace_dev,
+                        size_t ws_bytes, vae_stream_t stream) {
+    clear_error();
+    if (flags & ~static_cast<unsigned>(VAE_UPSAMPLE2X | VAE_PAD_REPLICATE | VAE_EPI_SILU | VAE_PAD_REFLECT |
+                                       VAE_DOWNSAMPLE2X))
+        return set_error(VAE_ERR_ARG, "vae_conv3x3_nhwc_gn: unsupported flag bits 0x%x", flags);
+    if (gn_stats_dev == nullptr || workspace_dev == nullptr)
+        return set_error(VAE_ERR_ARG, "vae_conv3x3_nhwc_gn: gn_stats and workspace must be non-NULL");
+    const size_t need = vae_conv3x3_gn_workspace_bytes(n, h_in, w_in, cout, groups, flags);
+    if (need == 0) return set_error(VAE_ERR_SHAPE, "vae_conv3x3_nhwc_gn: n=%d h=%d w=%d cout=%d groups=%d", n, h_in,
+                                    w_in, cout, groups);
+    if (ws_bytes < need)
+        return set_error(VAE_ERR_NOMEM, "vae_conv3x3_nhwc_gn: workspace %zu bytes < %zu needed", ws_bytes, need);
+    ConvArgs a{};
+    a.x = x_dev;
+    a.n = n;
+    a.h_in = h_in;
+    a.w_in = w_in;
+    a.cin = cin;
+    a.w = w_dev;
+    a.cout = cout;
+    a.taps = 9;
+    a.bias = bias_dev;
+    a.residual = residual_dev;
+    a.y = y_dev;
+    a.oscale = oscale;
+    a.up = (flags & VAE_UPSAMPLE2X) != 0;
+    a.rep = (flags & VAE_PAD_REPLICATE) != 0;
+    a.refl = (flags & VAE_PAD_REFLECT) != 0;
+    a.down = (flags & VAE_DOWNSAMPLE2X) != 0;
+    a.silu = (flags & VAE_EPI_SILU) != 0;
+    a.gn_part = workspace_dev;
+    a.gn_groups = groups;
+    if (!(eps >= 0.f)) return set_error(VAE_ERR_ARG, "vae_conv3x3_nhwc_gn: eps must be >= 0");
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int rc = conv_run(a, st);
+    if (rc != VAE_OK) return rc;
+    return gn_stats_from_records(workspace_dev, n, conv_gn_chunks(h_in, w_in, a.up, a.down), groups, eps,
+                                 gn_stats_dev, st);
 }
 
 int vae_pack_subpixel_weights(const void* w_dev, int cout, int cin, void* w_sub_dev, vae_stream_t stream) {

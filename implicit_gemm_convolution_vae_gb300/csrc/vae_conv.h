@@ -47,7 +47,15 @@ struct ConvArgs {
     const float* rms_gamma = nullptr;
     void* rms_out = nullptr;
     bool rms_silu = false;
+    // GroupNorm partial statistics of the f32 output (2-D 3x3 convs): records
+    // float4 (count, mean, M2, 0) at [n][conv_gn_chunks(...)][gn_groups],
+    // each written once; statistics of the values stored in y.
+    void* gn_part = nullptr;
+    int gn_groups = 0;
 };
+
+// Records per image of the GroupNorm statistics epilogue: 4 per M tile.
+int conv_gn_chunks(int h_in, int w_in, bool up, bool down);
 
 int conv_validate(const ConvArgs& a);
 // w [cout][3][3][cin] f16 -> the sub-pixel form's summed weights [cout][16][cin] f16.

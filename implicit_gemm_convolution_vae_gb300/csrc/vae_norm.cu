@@ -239,6 +239,40 @@ __global__ void __launch_bounds__(kGnThreads) gn_finalize_kernel(const float* __
     }
 }
 
+// Pass 2 for statistics that a conv epilogue produced: merges the (count,
+// mean, M2) records [img][nchunks][groups] of one (group, image) in a fixed
+// order (strided per thread, then a tree), as gn_finalize_kernel does.
+__global__ void __launch_bounds__(kGnThreads) gn_finalize_records_kernel(const float4* __restrict__ rec,
+                                                                         int nchunks, int groups, float eps,
+                                                                         float* __restrict__ stats) {
+    __shared__ float sn[kGnThreads], sm[kGnThreads], sq[kGnThreads];
+    const int g = blockIdx.x, img = blockIdx.y, t = threadIdx.x;
+    float na = 0.f, ma = 0.f, m2a = 0.f;
+    for (int ch = t; ch < nchunks; ch += kGnThreads) {
+        const float4 r = __ldg(rec + (static_cast<long long>(img) * nchunks + ch) * groups + g);
+        chan_merge(na, ma, m2a, r.x, r.y, r.z);
+    }
+    sn[t] = na;
+    sm[t] = ma;
+    sq[t] = m2a;
+    __syncthreads();
+    for (int st = kGnThreads / 2; st > 0; st >>= 1) {
+        if (t < st) {
+            float a = sn[t], b = sm[t], q = sq[t];
+            chan_merge(a, b, q, sn[t + st], sm[t + st], sq[t + st]);
+            sn[t] = a;
+            sm[t] = b;
+            sq[t] = q;
+        }
+        __syncthreads();
+    }
+    if (t == 0) {
+        const float var = sn[0] > 0.f ? sq[0] / sn[0] : 0.f;
+        stats[(static_cast<long long>(img) * groups + g) * 2] = sm[0];
+        stats[(static_cast<long long>(img) * groups + g) * 2 + 1] = 1.0f / sqrtf(var + eps);
+    }
+}
+
 __global__ void __launch_bounds__(256) gn_apply_kernel(const float* __restrict__ x, long long total4, int hw,
                                                        int c, int groups, const float* __restrict__ bias,
                                                        const float* __restrict__ gamma,
@@ -374,6 +408,35 @@ int gn_run(const float* x, int n, int hw, int c, int groups, float eps, const fl
     return VAE_OK;
 }
 
+int gn_stats_from_records(const void* rec, int n, int nchunks, int groups, float eps, float* stats,
+                          cudaStream_t stream) {
+    if (rec == nullptr || stats == nullptr) return set_error(VAE_ERR_ARG, "groupnorm: NULL records or statistics");
+    if (n < 1 || nchunks < 1 || groups < 1 || groups > 65535)
+        return set_error(VAE_ERR_SHAPE, "groupnorm: n=%d chunks=%d groups=%d", n, nchunks, groups);
+    if (!(eps >= 0.f)) return set_error(VAE_ERR_ARG, "groupnorm: eps must be >= 0");
+    gn_finalize_records_kernel<<<dim3(groups, n), kGnThreads, 0, stream>>>(static_cast<const float4*>(rec), nchunks,
+                                                                           groups, eps, stats);
+    VAE_CUDA_CHECK(cudaGetLastError());
+    return VAE_OK;
+}
+
+int gn_apply_run(const float* x, int n, int hw, int c, int groups, const float* stats, const float* gamma,
+                 const float* beta, int silu, float out_scale, void* y, cudaStream_t stream) {
+    if (x == nullptr || stats == nullptr || gamma == nullptr || beta == nullptr || y == nullptr)
+        return set_error(VAE_ERR_ARG, "groupnorm_apply: x, statistics, gamma, beta and y must be non-NULL");
+    if (n < 1 || hw < 1 || c < 4 || c % 4 != 0 || groups < 1 || c % groups != 0)
+        return set_error(VAE_ERR_SHAPE, "groupnorm_apply: n=%d hw=%d c=%d groups=%d unsupported", n, hw, c, groups);
+    if (!aligned16(x) || !aligned16(gamma) || !aligned16(beta) || !aligned16(y))
+        return set_error(VAE_ERR_ALIGN, "groupnorm_apply: pointers must be 16-byte aligned");
+    int rc = check_device();
+    if (rc != VAE_OK) return rc;
+    const long long total4 = static_cast<long long>(n) * hw * (c / 4);
+    gn_apply_kernel<<<grid_for(total4, 256), 256, 0, stream>>>(x, total4, hw, c, groups, nullptr, gamma, beta, stats,
+                                                               silu, out_scale, static_cast<__half*>(y));
+    VAE_CUDA_CHECK(cudaGetLastError());
+    return VAE_OK;
+}
+
 int rms_run(const float* x, long long m, int c, const float* bias, const float* gamma, int silu,
             float out_scale, void* y, cudaStream_t stream) {
     if (x == nullptr || gamma == nullptr || y == nullptr)
@@ -495,6 +558,14 @@ int vae_rmsnorm_silu(const float* x_dev, int m, int c, const float* bias_in_dev,
     clear_error();
     return rms_run(x_dev, m, c, bias_in_dev, gamma_dev, silu, out_scale, y_dev,
                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+int vae_groupnorm_apply(const float* x_dev, int n, int hw, int c, int groups, const float* gn_stats_dev,
+                        const float* gamma_dev, const float* beta_dev, int silu, float out_scale, void* y_dev,
+                        vae_stream_t stream) {
+    clear_error();
+    return gn_apply_run(x_dev, n, hw, c, groups, gn_stats_dev, gamma_dev, beta_dev, silu, out_scale, y_dev,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t vae_groupnorm_workspace_bytes(int n, int hw, int c, int groups) {

@@ -209,6 +209,42 @@ int vae_groupnorm_silu(const float* x_dev, int n, int hw, int c, int groups, flo
                        void* workspace_dev, size_t workspace_bytes, vae_stream_t stream);
 
 /*
+ * GroupNorm with its statistics taken by the conv that produces its input (an
+ * optional restructuring, not on the pages): the two-pass GroupNorm of
+ * "s2v_vae.rs" (s2v_gn_part reads the tensor for per-block partial sums,
+ * s2v_gn_apply reads it again to normalise) loses its first read because the
+ * 3x3 conv's epilogue, which holds every output value in registers anyway,
+ * emits the partial statistics of what it stores.
+ *
+ * vae_conv3x3_nhwc_gn: the conv of vae_conv3x3_nhwc (f32 output only), and
+ *   gn_stats_dev f32 [n][groups][2] = (mean, 1 / sqrt(var + eps)) of the
+ *   stored output per (image, group of cout/groups consecutive channels),
+ *   biased variance over H * W * cout/groups values ("vae.rs"
+ *   GroupNorm::apply). Each epilogue warp writes one (count, mean, M2)
+ *   record per group for its 32 pixels (two-pass within the warp) into
+ *   workspace_dev; a second kernel merges the records with Chan's formula in
+ *   a fixed order (deterministic).
+ *   Flags: VAE_UPSAMPLE2X, VAE_PAD_REPLICATE, VAE_PAD_REFLECT,
+ *   VAE_DOWNSAMPLE2X, VAE_EPI_SILU (statistics of the SiLU output then).
+ *   workspace_dev: >= vae_conv3x3_gn_workspace_bytes(...) bytes, 16-byte
+ *   aligned, contents ignored on entry. Requirements as vae_conv3x3_nhwc plus
+ *   cout % 16 == 0 and cout / groups in {4, 8} or a multiple of 16 (every
+ *   group of the FLUX-class widths 128 / 256 / 512 with 32 groups).
+ * vae_groupnorm_apply: y = SiLU?((x - mean) * rstd * gamma[c] + beta[c]) * out_scale
+ *   -> f16, one read of x, with gn_stats_dev from vae_conv3x3_nhwc_gn.
+ *   x_dev f32 [n][hw][c]; y_dev f16 [n][hw][c]; 16-byte aligned;
+ *   c % 4 == 0, c % groups == 0.
+ */
+size_t vae_conv3x3_gn_workspace_bytes(int n, int h_in, int w_in, int cout, int groups, unsigned flags);
+int vae_conv3x3_nhwc_gn(const void* x_dev, int n, int h_in, int w_in, int cin, const void* w_dev,
+                        const float* bias_dev, const float* residual_dev, float* y_dev, int cout,
+                        float oscale, unsigned flags, int groups, float eps, float* gn_stats_dev,
+                        void* workspace_dev, size_t workspace_bytes, vae_stream_t stream);
+int vae_groupnorm_apply(const float* x_dev, int n, int hw, int c, int groups, const float* gn_stats_dev,
+                        const float* gamma_dev, const float* beta_dev, int silu, float out_scale,
+                        void* y_dev, vae_stream_t stream);
+
+/*
  * GroupNorm exactly as vae_groupnorm_silu, for callers that cannot allocate
  * device memory. The pages have no counterpart to this entry point.
  *

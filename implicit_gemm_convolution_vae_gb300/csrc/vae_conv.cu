@@ -1700,7 +1700,7 @@ int conv_validate(const ConvArgs& a) {
         if (a.taps != 9 || a.subpix || a.out_f16 || a.out_nchw || a.rms_out != nullptr || a.y == nullptr)
             return set_error(VAE_ERR_ARG, "conv: GroupNorm statistics need a 2-D 3x3 conv with an f32 output");
         const int cpg = a.gn_groups >= 1 && a.cout % a.gn_groups == 0 ? a.cout / a.gn_groups : 0;
-        if (a.cout % 16 != 0 || cpg == 0 || cpg % 4 != 0 || (cpg > 16 && cpg % 16 != 0))
+        if (a.cout % 16 != 0 || !(cpg == 4 || cpg == 8 || (cpg > 0 && cpg % 16 == 0)))
             return set_error(VAE_ERR_SHAPE,
                              "conv: GroupNorm statistics need cout %% 16 == 0 and C/groups in {4, 8} or a multiple "
                              "of 16 (cout=%d groups=%d)", a.cout, a.gn_groups);

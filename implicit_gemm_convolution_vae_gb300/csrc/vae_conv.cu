@@ -121,7 +121,8 @@ struct ConvParams {
     __half* rms_out;
     int rms_silu;
     // GroupNorm partial statistics of the output (variant 3): per (image,
-    // chunk = M tile * 4 + epilogue warp, group) one record (count, mean, M2, 0).
+    // chunk = M tile * 4 + epilogue warp, group) one record (count, K, S1, S2):
+    // shifted sums S1 = sum (v - K), S2 = sum (v - K)^2.
     float4* gn_part;
     int gn_groups, gn_cpg, gn_nchunks;
     DevStatus* status;
@@ -835,84 +836,85 @@ __device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInf
     }
 }
 
-// Running (count, mean, M2) of a group wider than 16 channels across the
-// chunks of one warp's pixels.
+// Per-lane shifted sums of a group wider than 16 channels, carried across the
+// chunks the group spans (K: the shift, the same in every lane).
 struct GnRun {
-    float n, mean, m2;
+    float K, a, q;
 };
 
-__device__ __forceinline__ void gn_merge(GnRun& a, float nb, float mb, float m2b) {
-    if (nb <= 0.f) return;
-    const float n = a.n + nb;
-    const float d = mb - a.mean;
-    const float f = nb / n;
-    a.mean += d * f;
-    a.m2 += m2b + d * d * a.n * f;
-    a.n = n;
-}
-
 // GroupNorm partial statistics of one 16-channel chunk (channels o0..o0+15)
-// of this warp's 32 pixels: for each group part of W channels in the chunk,
-// the count, mean and M2 over the valid pixels, two-pass within the warp
-// (all lanes end with the same values). A group of <= 16 channels is one
-// part; wider groups merge their parts across chunks (Chan's formula). Lane 0
-// writes the record of each completed group.
+// of this warp's 32 pixels, as shifted sums: per group (part) of W channels,
+// K = lane 0's value of the part's first channel (lane 0 is valid whenever any
+// lane is: invalid pixels trail), S1 = sum (v - K) and S2 = sum (v - K)^2 over
+// the valid pixels, reduced across the warp with independent shuffle chains
+// (the epilogue warp is alone on its scheduler, so it pays latency, not
+// issue slots). Lane 0 writes one record (count, K, S1, S2) per group; the
+// merge turns it into (count, mean, M2). `npx`: the warp's valid pixels.
 template <int W>
 __device__ __forceinline__ void gn_chunk_w(const ConvParams& p, const TileInfo& ti, const float (&val)[16],
-                                           bool valid, int o0, int chunk, int lane, GnRun& run) {
+                                           bool valid, int o0, int chunk, int lane, float npx, GnRun& run) {
     constexpr int G = 16 / W;
-    const float cnt = static_cast<float>(__popc(__ballot_sync(0xffffffffu, valid)) * W);
-    float s[G], d[G];
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-        float a = 0.f;
-#pragma unroll
-        for (int i = 0; i < W; ++i) a += val[k * W + i];
-        s[k] = valid ? a : 0.f;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-        for (int k = 0; k < G; ++k) s[k] += __shfl_xor_sync(0xffffffffu, s[k], off);
-#pragma unroll
-    for (int k = 0; k < G; ++k) {
-        s[k] = cnt > 0.f ? s[k] / cnt : 0.f;  // the part's mean
-        float a = 0.f;
-#pragma unroll
-        for (int i = 0; i < W; ++i) {
-            const float e = val[k * W + i] - s[k];
-            a += e * e;
-        }
-        d[k] = valid ? a : 0.f;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-        for (int k = 0; k < G; ++k) d[k] += __shfl_xor_sync(0xffffffffu, d[k], off);
     float4* rec = p.gn_part + (static_cast<long long>(ti.img) * p.gn_nchunks + chunk) * p.gn_groups;
     if (W < 16 || p.gn_cpg == 16) {
-        if (lane == 0)
+        float K[G], a[G], q[G];
 #pragma unroll
-            for (int k = 0; k < G; ++k) rec[(o0 + k * W) / p.gn_cpg] = make_float4(cnt, s[k], d[k], 0.f);
+        for (int k = 0; k < G; ++k) K[k] = __shfl_sync(0xffffffffu, val[k * W], 0);
+#pragma unroll
+        for (int k = 0; k < G; ++k) {
+            float sa = 0.f, sq = 0.f;
+#pragma unroll
+            for (int i = 0; i < W; ++i) {
+                const float d = val[k * W + i] - K[k];
+                sa += d;
+                sq += d * d;
+            }
+            a[k] = valid ? sa : 0.f;
+            q[k] = valid ? sq : 0.f;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int k = 0; k < G; ++k) {
+                a[k] += __shfl_xor_sync(0xffffffffu, a[k], off);
+                q[k] += __shfl_xor_sync(0xffffffffu, q[k], off);
+            }
+        if (lane == 0) {
+            const int g0 = o0 / p.gn_cpg;
+#pragma unroll
+            for (int k = 0; k < G; ++k) rec[g0 + k] = make_float4(npx * W, K[k], a[k], q[k]);
+        }
     } else {
-        gn_merge(run, cnt, s[0], d[0]);
+        if (o0 % p.gn_cpg == 0) run = GnRun{__shfl_sync(0xffffffffu, val[0], 0), 0.f, 0.f};
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float d = val[i] - run.K;
+                run.a += d;
+                run.q += d * d;
+            }
+        }
         if ((o0 + 16) % p.gn_cpg == 0) {
-            if (lane == 0) rec[o0 / p.gn_cpg] = make_float4(run.n, run.mean, run.m2, 0.f);
-            run = GnRun{0.f, 0.f, 0.f};
+            float a = run.a, q = run.q;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, off);
+                q += __shfl_xor_sync(0xffffffffu, q, off);
+            }
+            if (lane == 0) rec[o0 / p.gn_cpg] = make_float4(npx * p.gn_cpg, run.K, a, q);
         }
     }
 }
 
 __device__ __forceinline__ void gn_chunk(const ConvParams& p, const TileInfo& ti, const float (&val)[16], bool valid,
-                                         int o0, int ew, int lane, GnRun& run) {
+                                         int o0, int ew, int lane, float npx, GnRun& run) {
     const int mt = ((ti.v0 / p.R) * p.npar + ti.par) * p.tiles_x + ti.u0 / p.Wt;  // M tile within the image
     const int chunk = mt * kEpiWarps + ew;
     if (p.gn_cpg == 4)
-        gn_chunk_w<4>(p, ti, val, valid, o0, chunk, lane, run);
+        gn_chunk_w<4>(p, ti, val, valid, o0, chunk, lane, npx, run);
     else if (p.gn_cpg == 8)
-        gn_chunk_w<8>(p, ti, val, valid, o0, chunk, lane, run);
+        gn_chunk_w<8>(p, ti, val, valid, o0, chunk, lane, npx, run);
     else
-        gn_chunk_w<16>(p, ti, val, valid, o0, chunk, lane, run);
+        gn_chunk_w<16>(p, ti, val, valid, o0, chunk, lane, npx, run);
 }
 
 template <bool kWide = true>
@@ -997,6 +999,7 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
                                                    int v, int u, int q, int pp, int Y, int X, long long pix,
                                                    int ew = 0, int lane = 0) {
     GnRun run{0.f, 0.f, 0.f};
+    const float npx = kGn ? static_cast<float>(__popc(__ballot_sync(0xffffffffu, valid))) : 0.f;
     if (kPipe && p.residual != nullptr && p.v8_ok && !p.out_nchw) {
         // Residual loads run two chunks ahead of their use (a three-slot
         // register ring), so three are in flight instead of one.
@@ -1023,7 +1026,7 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
                     compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, rr);
                     store_chunk(p, pix, o0, val, Y, X, ti.img);
                 }
-                gn_chunk(p, ti, val, valid, o0, ew, lane, run);
+                gn_chunk(p, ti, val, valid, o0, ew, lane, npx, run);
             } else if (valid && o0 < p.cout) {
                 float val[16];
                 compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, rr);
@@ -1055,7 +1058,7 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
                 compute_chunk<kPipe>(p, ti, r, o0, v, u, q, pp, pix, val);
                 store_chunk(p, pix, o0, val, Y, X, ti.img);
             }
-            gn_chunk(p, ti, val, valid, o0, ew, lane, run);
+            gn_chunk(p, ti, val, valid, o0, ew, lane, npx, run);
         } else if (valid && o0 < p.cout) {
             epilogue_chunk<kPipe>(p, ti, r, o0, v, u, q, pp, Y, X, pix);
         }
@@ -1072,6 +1075,7 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
                                                  int q, int pp, long long pix, uint8_t* stg, const CUtensorMap* mapY,
                                                  int ew, int lane, bool valid = true) {
     GnRun run{0.f, 0.f, 0.f};
+    const float npx = kGn ? static_cast<float>(__popc(__ballot_sync(0xffffffffu, valid))) : 0.f;
     const uint32_t sbase = smem_u32(stg + ew * kStgBytes);
     const int seg = ti.u0 + ew * 32;  // first pixel of this warp's 32 (warp-uniform)
     const uint32_t row_off = static_cast<uint32_t>(lane) * 64u;
@@ -1091,7 +1095,7 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
 #pragma unroll
             for (int i = 0; i < 16; ++i) val[i] = 0.f;
         }
-        if (kGn) gn_chunk(p, ti, val, valid, o0, ew, lane, run);
+        if (kGn) gn_chunk(p, ti, val, valid, o0, ew, lane, npx, run);
         if (lane == 0) bulk_wait_read_all();  // the previous box left this warp's buffer
         __syncwarp();
 #pragma unroll

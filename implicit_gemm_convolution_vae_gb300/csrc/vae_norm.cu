@@ -239,9 +239,10 @@ __global__ void __launch_bounds__(kGnThreads) gn_finalize_kernel(const float* __
     }
 }
 
-// Pass 2 for statistics that a conv epilogue produced: merges the (count,
-// mean, M2) records [img][nchunks][groups] of one (group, image) in a fixed
-// order (strided per thread, then a tree), as gn_finalize_kernel does.
+// Pass 2 for statistics that a conv epilogue produced: turns each (count, K,
+// S1, S2) record of shifted sums [img][nchunks][groups] into (count, mean =
+// K + S1/count, M2 = S2 - S1^2/count) and merges those of one (group, image)
+// in a fixed order (strided per thread, then a tree), as gn_finalize_kernel does.
 __global__ void __launch_bounds__(kGnThreads) gn_finalize_records_kernel(const float4* __restrict__ rec,
                                                                          int nchunks, int groups, float eps,
                                                                          float* __restrict__ stats) {
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(kGnThreads) gn_finalize_records_kernel(const f
     float na = 0.f, ma = 0.f, m2a = 0.f;
     for (int ch = t; ch < nchunks; ch += kGnThreads) {
         const float4 r = __ldg(rec + (static_cast<long long>(img) * nchunks + ch) * groups + g);
-        chan_merge(na, ma, m2a, r.x, r.y, r.z);
+        if (r.x > 0.f) chan_merge(na, ma, m2a, r.x, r.y + r.z / r.x, fmaxf(r.w - r.z * r.z / r.x, 0.f));
     }
     sn[t] = na;
     sm[t] = ma;

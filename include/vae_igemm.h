@@ -220,10 +220,11 @@ int vae_groupnorm_silu(const float* x_dev, int n, int hw, int c, int groups, flo
  *   gn_stats_dev f32 [n][groups][2] = (mean, 1 / sqrt(var + eps)) of the
  *   stored output per (image, group of cout/groups consecutive channels),
  *   biased variance over H * W * cout/groups values ("vae.rs"
- *   GroupNorm::apply). Each epilogue warp writes one (count, mean, M2)
- *   record per group for its 32 pixels (two-pass within the warp) into
- *   workspace_dev; a second kernel merges the records with Chan's formula in
- *   a fixed order (deterministic).
+ *   GroupNorm::apply). Each epilogue warp writes one record per group for
+ *   its 32 pixels into workspace_dev: shifted sums (count, K, sum (v - K),
+ *   sum (v - K)^2), K one of the group's values; a second kernel turns them
+ *   into (count, mean, M2) and merges them with Chan's formula in a fixed
+ *   order (deterministic).
  *   Flags: VAE_UPSAMPLE2X, VAE_PAD_REPLICATE, VAE_PAD_REFLECT,
  *   VAE_DOWNSAMPLE2X, VAE_EPI_SILU (statistics of the SiLU output then).
  *   workspace_dev: >= vae_conv3x3_gn_workspace_bytes(...) bytes, 16-byte

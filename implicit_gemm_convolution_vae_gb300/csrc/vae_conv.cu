@@ -108,6 +108,7 @@ struct ConvParams {
     int dup_v8;           // DupUp rows 32-byte aligned: 32-byte loads of the source window
     int v8_ok;            // f32 y / residual rows 32-byte aligned: 32-byte accesses
     int epi_tma;          // epilogue writes through staged TMA boxes: 1 store, 2 add onto y (residual == y)
+    int bias_smem;        // the bias (cout floats) is copied to shared memory at kernel start
     // NCHW output of kept rows (conv_out): rows [keep_lo, keep_hi) land at
     // destination row (Y - keep_lo + dst_row0) of planes `plane` floats apart.
     int out_nchw, keep_lo, keep_hi, dst_row0;
@@ -211,6 +212,7 @@ struct Smem {
     uint8_t* a;          // stages x 16 KB, or (halo mode) a_stages x kHaloBytes
     uint8_t* b;          // stages x BN*128 B
     uint8_t* stg;        // epilogue staging, 2 KB per epilogue warp (epi_tma)
+    float* bias;         // [cout] copy of the bias (bias_smem)
     uint64_t* full;      // [stages]
     uint64_t* empty;     // [stages]
     uint64_t* afull;     // [a_stages] (halo mode)
@@ -229,7 +231,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
     s.a = base;
     s.b = base + (p.halo ? p.a_stages * kHaloBytes : p.stages * p.ks * kABytes);
     s.stg = s.b + p.stages * p.ks * p.b_rows * 128;
-    uint8_t* tail = s.stg + (p.epi_tma ? kEpiWarps * kStgBytes : 0);
+    s.bias = reinterpret_cast<float*>(s.stg + (p.epi_tma ? kEpiWarps * kStgBytes : 0));
+    uint8_t* tail = reinterpret_cast<uint8_t*>(s.bias) + (p.bias_smem ? (p.cout * 4 + 15) / 16 * 16 : 0);
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
     s.full = bars;
     s.empty = bars + kMaxStages;
@@ -738,11 +741,20 @@ __device__ __forceinline__ void store_chunk(const ConvParams& p, long long pix, 
 template <bool kWide = true>
 __device__ __forceinline__ void compute_chunk(const ConvParams& p, const TileInfo& ti, const uint32_t (&r)[16],
                                               int o0, int v, int u, int q, int pp, long long pix, float (&val)[16],
-                                              const float* pre_res = nullptr) {
+                                              const float* pre_res = nullptr, const float* sbias = nullptr) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) val[i] = __uint_as_float(r[i]) * p.oscale;
     const bool full = p.vec_ok && (o0 + 16 <= p.cout);
-    if (p.bias != nullptr) {
+    if (sbias != nullptr && full) {  // the shared-memory copy of the bias
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float4 b = reinterpret_cast<const float4*>(sbias + o0)[i];
+            val[4 * i] += b.x;
+            val[4 * i + 1] += b.y;
+            val[4 * i + 2] += b.z;
+            val[4 * i + 3] += b.w;
+        }
+    } else if (p.bias != nullptr) {
         if (full) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -997,7 +1009,7 @@ __device__ __forceinline__ void epilogue_rms_row(const ConvParams& p, const Tile
 template <bool kPipe, bool kGn = false>
 __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, bool valid,
                                                    int v, int u, int q, int pp, int Y, int X, long long pix,
-                                                   int ew = 0, int lane = 0) {
+                                                   int ew = 0, int lane = 0, const float* sbias = nullptr) {
     GnRun run{0.f, 0.f, 0.f};
     const float npx = kGn ? static_cast<float>(__popc(__ballot_sync(0xffffffffu, valid))) : 0.f;
     if (kPipe && p.residual != nullptr && p.v8_ok && !p.out_nchw) {
@@ -1023,13 +1035,13 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
                 if (o0 >= p.cout) return;  // warp-uniform
                 float val[16];
                 if (valid) {
-                    compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, rr);
+                    compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, rr, sbias);
                     store_chunk(p, pix, o0, val, Y, X, ti.img);
                 }
                 gn_chunk(p, ti, val, valid, o0, ew, lane, npx, run);
             } else if (valid && o0 < p.cout) {
                 float val[16];
-                compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, rr);
+                compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, rr, sbias);
                 store_chunk(p, pix, o0, val, Y, X, ti.img);
             }
         };
@@ -1073,24 +1085,20 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
 template <bool kGn = false>
 __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, int v, int u,
                                                  int q, int pp, long long pix, uint8_t* stg, const CUtensorMap* mapY,
-                                                 int ew, int lane, bool valid = true) {
+                                                 int ew, int lane, bool valid = true, const float* sbias = nullptr) {
     GnRun run{0.f, 0.f, 0.f};
     const float npx = kGn ? static_cast<float>(__popc(__ballot_sync(0xffffffffu, valid))) : 0.f;
     const uint32_t sbase = smem_u32(stg + ew * kStgBytes);
     const int seg = ti.u0 + ew * 32;  // first pixel of this warp's 32 (warp-uniform)
     const uint32_t row_off = static_cast<uint32_t>(lane) * 64u;
     const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
-    for (int c = 0; c < p.BN / 16; ++c) {
-        uint32_t acc[16];
-        __syncwarp();
-        tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
-        tmem_ld_wait();
+    const int nch = (min(p.BN, p.cout - ti.n0) + 15) / 16;  // 16-column chunks of this tile
+    auto process = [&](int c, uint32_t (&acc)[16]) {
         const int o0 = ti.n0 + c * 16;
-        if (o0 >= p.cout) break;  // warp-uniform
         // pixels past the row's end read no residual or DupUp source; their values are not stored
         float val[16];
         if (valid) {
-            compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val);
+            compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, nullptr, sbias);
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) val[i] = 0.f;
@@ -1115,6 +1123,20 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
                 tma_store_4d(mapY, sbase, o0, seg, ti.v0, ti.img);
             bulk_commit_group();
         }
+    };
+    // The TMEM load of chunk c + 1 is in flight while chunk c is computed and stored.
+    uint32_t a0[16], a1[16];
+    __syncwarp();
+    tmem_ld16(tbase, a0);
+    tmem_ld_wait_regs(a0);
+    for (int c = 0; c < nch; c += 2) {
+        if (c + 1 < nch) tmem_ld16(tbase + static_cast<uint32_t>((c + 1) * 16), a1);
+        process(c, a0);
+        if (c + 1 >= nch) break;
+        tmem_ld_wait_regs(a1);
+        if (c + 2 < nch) tmem_ld16(tbase + static_cast<uint32_t>((c + 2) * 16), a0);
+        process(c + 1, a1);
+        if (c + 2 < nch) tmem_ld_wait_regs(a0);
     }
 }
 
@@ -1142,10 +1164,11 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         if (kRms) {
             epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         } else if (kMode != kModeGather && p.epi_tma) {
-            epilogue_tma_row<kVar == 3>(p, ti, tbase, v, u, q, pp, pix, s.stg, mapY, ew, lane, valid);
+            epilogue_tma_row<kVar == 3>(p, ti, tbase, v, u, q, pp, pix, s.stg, mapY, ew, lane, valid,
+                                        p.bias_smem ? s.bias : nullptr);
         } else {
             epilogue_plain_row<kMode != kModeGather, kVar == 3>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix, ew,
-                                                                 lane);
+                                                                 lane, p.bias_smem ? s.bias : nullptr);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&s.acce[accbuf]));
@@ -1187,6 +1210,8 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : (kMode == kModeHa
             for (int i = 0; i < p.stages; ++i) mbar_init(smem_u32(&s.fixed[i]), 1u);
         fence_mbar_init();
     }
+    if (p.bias_smem)  // visible to the epilogue after the __syncthreads below
+        for (int i = threadIdx.x; i < p.cout; i += blockDim.x) s.bias[i] = __ldg(p.bias + i);
     const uint32_t tmem_cols = p.acc_stride * 2 <= 32 ? 32u
                                : p.acc_stride * 2 <= 64 ? 64u
                                : p.acc_stride * 2 <= 128 ? 128u
@@ -2023,7 +2048,14 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         else
             clear_error();
     }
-    const size_t smem = 1024 + ring + (p.epi_tma ? kEpiWarps * kStgBytes : 0) + kTail;
+    size_t smem = 1024 + ring + (p.epi_tma ? kEpiWarps * kStgBytes : 0) + kTail;
+    // A shared-memory copy of the bias where it fits: the epilogue's bias reads
+    // otherwise miss the small L1 left beside the pipeline's shared memory.
+    const size_t bias_bytes = static_cast<size_t>(a.cout * 4 + 15) / 16 * 16;
+    if (a.bias != nullptr && aligned16(a.bias) && smem + bias_bytes <= kMaxSmem) {
+        p.bias_smem = 1;
+        smem += bias_bytes;
+    }
     if (a.taps == 27) {  // the 3x3x3 instantiations (no fused norm)
         if (mode == kModeHalo) return launch<kModeHalo, false, 1>(p, ma, mb, ma16, mb16, my, smem, grid, stream);
         if (mode == kModeGather) return launch<kModeGather, false, 1>(p, ma, mb, ma, mb, my, smem, grid, stream);

@@ -274,38 +274,58 @@ __global__ void __launch_bounds__(kGnThreads) gn_finalize_records_kernel(const f
     }
 }
 
-__global__ void __launch_bounds__(256) gn_apply_kernel(const float* __restrict__ x, long long total4, int hw,
-                                                       int c, int groups, const float* __restrict__ bias,
+// Pass 3: one block row of a 2-D grid per image (blockIdx.y); thread t owns
+// float4 column t % tpr of rows t / tpr, t / tpr + rpar, ... so its channels,
+// their gamma / beta and their groups' statistics are loaded once and the row
+// loop has no index division.
+__global__ void __launch_bounds__(256) gn_apply_kernel(const float* __restrict__ x, int hw, int c, int groups,
+                                                       const float* __restrict__ bias,
                                                        const float* __restrict__ gamma,
                                                        const float* __restrict__ beta,
                                                        const float* __restrict__ stats, int silu,
                                                        float out_scale, __half* __restrict__ y) {
     const int c4 = c / 4;
     const int cpg = c / groups;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total4;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int col = static_cast<int>(i % c4);
-        const long long img = i / (static_cast<long long>(hw) * c4);
-        float4 v = __ldg(reinterpret_cast<const float4*>(x) + i);
+    const int tpr = min(c4, 256);
+    const int rpar = 256 / tpr;
+    const int t = threadIdx.x;
+    const int rl = t / tpr;
+    if (rl >= rpar) return;
+    const long long img = blockIdx.y;
+    const float* xs = x + img * hw * static_cast<long long>(c);
+    __half* ys = y + img * hw * static_cast<long long>(c);
+    for (int col = t % tpr; col < c4; col += tpr) {
+        float b4[4] = {0.f, 0.f, 0.f, 0.f}, sc[4], sh[4];
         if (bias != nullptr) {
             const float4 b = __ldg(reinterpret_cast<const float4*>(bias) + col);
-            v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
+            b4[0] = b.x; b4[1] = b.y; b4[2] = b.z; b4[3] = b.w;
         }
         const float4 ga = __ldg(reinterpret_cast<const float4*>(gamma) + col);
         const float4 be = __ldg(reinterpret_cast<const float4*>(beta) + col);
-        const float vv[4] = {v.x, v.y, v.z, v.w};
         const float gg[4] = {ga.x, ga.y, ga.z, ga.w};
         const float bb[4] = {be.x, be.y, be.z, be.w};
-        float o[4];
+        float mu[4], rs[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int ch = col * 4 + k;
-            const float* st = stats + (img * groups + ch / cpg) * 2;
-            float r = (vv[k] - __ldg(st)) * __ldg(st + 1) * gg[k] + bb[k];
-            if (silu) r = silu_f(r);
-            o[k] = r * out_scale;
+            const float* st = stats + (img * groups + (col * 4 + k) / cpg) * 2;
+            mu[k] = __ldg(st);
+            rs[k] = __ldg(st + 1);
+            sc[k] = gg[k];
+            sh[k] = bb[k];
         }
-        reinterpret_cast<uint2*>(y)[i] = pack4_f16(o[0], o[1], o[2], o[3]);
+        for (long long r = static_cast<long long>(blockIdx.x) * rpar + rl; r < hw;
+             r += static_cast<long long>(gridDim.x) * rpar) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(xs + r * c) + col);
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+            float o[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float q = ((vv[k] + b4[k]) - mu[k]) * rs[k] * sc[k] + sh[k];
+                if (silu) q = silu_f(q);
+                o[k] = q * out_scale;
+            }
+            reinterpret_cast<uint2*>(ys + r * c)[col] = pack4_f16(o[0], o[1], o[2], o[3]);
+        }
     }
 }
 
@@ -347,6 +367,17 @@ int grid_for(long long work, int per_block) {
 }
 
 }  // namespace
+
+// Pass 3's grid: (row blocks, images), about 8 blocks of 256 threads per SM in all.
+dim3 gn_apply_grid(int n, int hw, int c) {
+    const int c4 = c / 4;
+    const int rpar = 256 / std::min(c4, 256);
+    const long long rows_per_block_min = rpar;
+    long long want = std::max(1LL, (static_cast<long long>(sm_count() > 0 ? sm_count() : 148) * 8 + n - 1) / n);
+    want = std::min(want, (static_cast<long long>(hw) + rows_per_block_min - 1) / rows_per_block_min);
+    want = std::min(want, 65535LL);
+    return dim3(static_cast<unsigned>(want), static_cast<unsigned>(n));
+}
 
 int gn_plan(int n, int hw, int c, int groups, GnPlan* plan) {
     if (n < 1 || hw < 1 || c < 4 || c % 4 != 0 || groups < 1 || groups > 1024 || c % groups != 0 ||
@@ -401,10 +432,8 @@ int gn_run(const float* x, int n, int hw, int c, int groups, float eps, const fl
     gn_finalize_kernel<<<dim3(groups, n), kGnThreads, 0, stream>>>(part, hw, groups, c / groups,
                                                                    plan.chunk_rows, plan.nchunks, eps, stats);
     VAE_CUDA_CHECK(cudaGetLastError());
-    const long long total4 = static_cast<long long>(n) * hw * (c / 4);
-    gn_apply_kernel<<<grid_for(total4, 256), 256, 0, stream>>>(x, total4, hw, c, groups, bias, gamma, beta,
-                                                               stats, silu, out_scale,
-                                                               static_cast<__half*>(y));
+    gn_apply_kernel<<<gn_apply_grid(n, hw, c), 256, 0, stream>>>(x, hw, c, groups, bias, gamma, beta, stats, silu,
+                                                                 out_scale, static_cast<__half*>(y));
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -431,9 +460,8 @@ int gn_apply_run(const float* x, int n, int hw, int c, int groups, const float* 
         return set_error(VAE_ERR_ALIGN, "groupnorm_apply: pointers must be 16-byte aligned");
     int rc = check_device();
     if (rc != VAE_OK) return rc;
-    const long long total4 = static_cast<long long>(n) * hw * (c / 4);
-    gn_apply_kernel<<<grid_for(total4, 256), 256, 0, stream>>>(x, total4, hw, c, groups, nullptr, gamma, beta, stats,
-                                                               silu, out_scale, static_cast<__half*>(y));
+    gn_apply_kernel<<<gn_apply_grid(n, hw, c), 256, 0, stream>>>(x, hw, c, groups, nullptr, gamma, beta, stats, silu,
+                                                                 out_scale, static_cast<__half*>(y));
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }

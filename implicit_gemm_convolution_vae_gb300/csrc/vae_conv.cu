@@ -917,6 +917,65 @@ __device__ __forceinline__ void gn_chunk_w(const ConvParams& p, const TileInfo& 
     }
 }
 
+// The same statistics for the staged TMA epilogue, read back from the warp's
+// staging box (32 pixels x 16 channels, 64-byte swizzle: pixel r's channel j at
+// r * 64 + (((j >> 2) ^ ((r >> 1) & 3)) * 16) + (j & 3) * 4) instead of being
+// shuffled out of registers: lane l sums channel l & 15 over one half of the
+// pixels (the halves read rows of opposite parity, so the two half-warps hit
+// disjoint banks), then log2(W) + 1 shuffle rounds combine a group's lanes.
+// Invalid pixels (r >= npx) trail and are skipped. Returns after the record
+// of each completed group is written by its leader lane.
+__device__ __forceinline__ void gn_chunk_stg(const ConvParams& p, const TileInfo& ti, const uint8_t* box, int o0,
+                                             int chunk, int lane, int npx, GnRun& run) {
+    const int j = lane & 15, h = lane >> 4;
+    const int cpg = p.gn_cpg;
+    const int w = cpg < 16 ? cpg : 16;  // channels of each group part in this chunk
+    auto at = [&](int r) -> float {
+        return *reinterpret_cast<const float*>(box + r * 64 + ((((j >> 2) ^ ((r >> 1) & 3))) << 4) + (j & 3) * 4);
+    };
+    float K;
+    if (w < 16 || cpg == 16) {
+        const int jg = j & ~(w - 1);  // the part's first channel
+        K = *reinterpret_cast<const float*>(box + ((((jg >> 2) ^ 0)) << 4) + (jg & 3) * 4);  // pixel 0
+    } else {
+        if (o0 % cpg == 0) run = GnRun{*reinterpret_cast<const float*>(box), 0.f, 0.f};  // pixel 0, channel 0
+        K = run.K;
+    }
+    float a = 0.f, q = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int r = h * 16 + ((i + h) & 15);
+        if (r < npx) {
+            const float d = at(r) - K;
+            a += d;
+            q += d * d;
+        }
+    }
+    float4* rec = p.gn_part + (static_cast<long long>(ti.img) * p.gn_nchunks + chunk) * p.gn_groups;
+    if (w < 16 || cpg == 16) {
+        a += __shfl_xor_sync(0xffffffffu, a, 16);
+        q += __shfl_xor_sync(0xffffffffu, q, 16);
+        for (int off = 1; off < w; off <<= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, off);
+            q += __shfl_xor_sync(0xffffffffu, q, off);
+        }
+        if (h == 0 && (j & (w - 1)) == 0) rec[(o0 + j) / cpg] = make_float4(static_cast<float>(npx * w), K, a, q);
+    } else {
+        run.a += a;
+        run.q += q;
+        if ((o0 + 16) % cpg == 0) {
+            a = run.a;
+            q = run.q;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, off);
+                q += __shfl_xor_sync(0xffffffffu, q, off);
+            }
+            if (lane == 0) rec[o0 / cpg] = make_float4(static_cast<float>(npx * cpg), K, a, q);
+        }
+    }
+}
+
 __device__ __forceinline__ void gn_chunk(const ConvParams& p, const TileInfo& ti, const float (&val)[16], bool valid,
                                          int o0, int ew, int lane, float npx, GnRun& run) {
     const int mt = ((ti.v0 / p.R) * p.npar + ti.par) * p.tiles_x + ti.u0 / p.Wt;  // M tile within the image
@@ -1087,7 +1146,7 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
                                                  int q, int pp, long long pix, uint8_t* stg, const CUtensorMap* mapY,
                                                  int ew, int lane, bool valid = true, const float* sbias = nullptr) {
     GnRun run{0.f, 0.f, 0.f};
-    const float npx = kGn ? static_cast<float>(__popc(__ballot_sync(0xffffffffu, valid))) : 0.f;
+    const int npx_i = kGn ? __popc(__ballot_sync(0xffffffffu, valid)) : 0;
     const uint32_t sbase = smem_u32(stg + ew * kStgBytes);
     const int seg = ti.u0 + ew * 32;  // first pixel of this warp's 32 (warp-uniform)
     const uint32_t row_off = static_cast<uint32_t>(lane) * 64u;
@@ -1103,7 +1162,6 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
 #pragma unroll
             for (int i = 0; i < 16; ++i) val[i] = 0.f;
         }
-        if (kGn) gn_chunk(p, ti, val, valid, o0, ew, lane, npx, run);
         if (lane == 0) bulk_wait_read_all();  // the previous box left this warp's buffer
         __syncwarp();
 #pragma unroll
@@ -1122,6 +1180,10 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
             else
                 tma_store_4d(mapY, sbase, o0, seg, ti.v0, ti.img);
             bulk_commit_group();
+        }
+        if (kGn) {  // the statistics read the staged box (alongside the store's own read)
+            const int mt = ((ti.v0 / p.R) * p.npar + ti.par) * p.tiles_x + ti.u0 / p.Wt;
+            gn_chunk_stg(p, ti, stg + ew * kStgBytes, o0, mt * kEpiWarps + ew, lane, npx_i, run);
         }
     };
     // The TMEM load of chunk c + 1 is in flight while chunk c is computed and stored.

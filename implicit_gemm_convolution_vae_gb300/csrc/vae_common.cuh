@@ -254,6 +254,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// One f32 from shared memory, kept in program order with the other volatile
+// shared-memory accesses (a plain load could be hoisted above staging stores
+// that are inline assembly).
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // The same wait, tied to the 16 registers a tcgen05.ld filled: the compiler
 // cannot move their uses above it (for loads kept in flight across other work).
 __device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[16]) {

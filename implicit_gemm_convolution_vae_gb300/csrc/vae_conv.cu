@@ -930,27 +930,36 @@ __device__ __forceinline__ void gn_chunk_stg(const ConvParams& p, const TileInfo
     const int j = lane & 15, h = lane >> 4;
     const int cpg = p.gn_cpg;
     const int w = cpg < 16 ? cpg : 16;  // channels of each group part in this chunk
-    auto at = [&](int r) -> float {
-        return *reinterpret_cast<const float*>(box + r * 64 + ((((j >> 2) ^ ((r >> 1) & 3))) << 4) + (j & 3) * 4);
-    };
-    float K;
-    if (w < 16 || cpg == 16) {
-        const int jg = j & ~(w - 1);  // the part's first channel
-        K = *reinterpret_cast<const float*>(box + ((((jg >> 2) ^ 0)) << 4) + (jg & 3) * 4);  // pixel 0
-    } else {
-        if (o0 % cpg == 0) run = GnRun{*reinterpret_cast<const float*>(box), 0.f, 0.f};  // pixel 0, channel 0
-        K = run.K;
-    }
-    float a = 0.f, q = 0.f;
+    const uint32_t sb = smem_u32(box);
+    const uint32_t jo = static_cast<uint32_t>((j & 3) * 4);
+    // all 16 loads go out back to back (every row is inside the box; invalid rows are masked below)
+    float v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const int r = h * 16 + ((i + h) & 15);
-        if (r < npx) {
-            const float d = at(r) - K;
-            a += d;
-            q += d * d;
-        }
+        v[i] = ld_shared_f32(sb + static_cast<uint32_t>(r * 64) +
+                             (static_cast<uint32_t>((j >> 2) ^ ((r >> 1) & 3)) << 4) + jo);
     }
+    float K;
+    if (w < 16 || cpg == 16) {
+        const int jg = j & ~(w - 1);  // the part's first channel, pixel 0
+        K = ld_shared_f32(sb + (static_cast<uint32_t>(jg >> 2) << 4) + static_cast<uint32_t>((jg & 3) * 4));
+    } else {
+        if (o0 % cpg == 0) run = GnRun{ld_shared_f32(sb), 0.f, 0.f};  // pixel 0, channel 0
+        K = run.K;
+    }
+    float a0 = 0.f, a1 = 0.f, q0 = 0.f, q1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const int r0 = h * 16 + ((i + h) & 15), r1 = h * 16 + ((i + 1 + h) & 15);
+        const float d0 = r0 < npx ? v[i] - K : 0.f;
+        const float d1 = r1 < npx ? v[i + 1] - K : 0.f;
+        a0 += d0;
+        q0 += d0 * d0;
+        a1 += d1;
+        q1 += d1 * d1;
+    }
+    float a = a0 + a1, q = q0 + q1;
     float4* rec = p.gn_part + (static_cast<long long>(ti.img) * p.gn_nchunks + chunk) * p.gn_groups;
     if (w < 16 || cpg == 16) {
         a += __shfl_xor_sync(0xffffffffu, a, 16);
@@ -1186,19 +1195,12 @@ __device__ __forceinline__ void epilogue_tma_row(const ConvParams& p, const Tile
             gn_chunk_stg(p, ti, stg + ew * kStgBytes, o0, mt * kEpiWarps + ew, lane, npx_i, run);
         }
     };
-    // The TMEM load of chunk c + 1 is in flight while chunk c is computed and stored.
-    uint32_t a0[16], a1[16];
-    __syncwarp();
-    tmem_ld16(tbase, a0);
-    tmem_ld_wait_regs(a0);
-    for (int c = 0; c < nch; c += 2) {
-        if (c + 1 < nch) tmem_ld16(tbase + static_cast<uint32_t>((c + 1) * 16), a1);
-        process(c, a0);
-        if (c + 1 >= nch) break;
-        tmem_ld_wait_regs(a1);
-        if (c + 2 < nch) tmem_ld16(tbase + static_cast<uint32_t>((c + 2) * 16), a0);
-        process(c + 1, a1);
-        if (c + 2 < nch) tmem_ld_wait_regs(a0);
+    for (int c = 0; c < nch; ++c) {
+        uint32_t acc[16];
+        __syncwarp();
+        tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
+        tmem_ld_wait_regs(acc);
+        process(c, acc);
     }
 }
 
@@ -1750,6 +1752,17 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, co
 
 }  // namespace
 
+// The shared-memory bias copy is opt-in (VAE_CONV_BIAS_SMEM=1): measured 1-3 %
+// slower than the L1-cached loads on GB300 (the tensor core's operand reads
+// already take most of the shared-memory bandwidth).
+bool bias_smem_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("VAE_CONV_BIAS_SMEM");
+        return e != nullptr && e[0] == '1';
+    }();
+    return on;
+}
+
 int conv_gn_chunks(int h_in, int w_in, bool up, bool down) {
     // the tiling of conv_run: the virtual grid, its tile shape and the parity classes
     const int hv = down ? h_in / 2 : h_in, wv = down ? w_in / 2 : w_in;
@@ -2114,7 +2127,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // A shared-memory copy of the bias where it fits: the epilogue's bias reads
     // otherwise miss the small L1 left beside the pipeline's shared memory.
     const size_t bias_bytes = static_cast<size_t>(a.cout * 4 + 15) / 16 * 16;
-    if (a.bias != nullptr && aligned16(a.bias) && smem + bias_bytes <= kMaxSmem) {
+    if (bias_smem_enabled() && a.bias != nullptr && aligned16(a.bias) && smem + bias_bytes <= kMaxSmem) {
         p.bias_smem = 1;
         smem += bias_bytes;
     }

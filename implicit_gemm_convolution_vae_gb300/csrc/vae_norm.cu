@@ -249,9 +249,19 @@ __global__ void __launch_bounds__(kGnThreads) gn_finalize_records_kernel(const f
     __shared__ float sn[kGnThreads], sm[kGnThreads], sq[kGnThreads];
     const int g = blockIdx.x, img = blockIdx.y, t = threadIdx.x;
     float na = 0.f, ma = 0.f, m2a = 0.f;
-    for (int ch = t; ch < nchunks; ch += kGnThreads) {
-        const float4 r = __ldg(rec + (static_cast<long long>(img) * nchunks + ch) * groups + g);
-        if (r.x > 0.f) chan_merge(na, ma, m2a, r.x, r.y + r.z / r.x, fmaxf(r.w - r.z * r.z / r.x, 0.f));
+    const float4* base = rec + static_cast<long long>(img) * nchunks * groups + g;
+    constexpr int kU = 8;  // records in flight per thread
+    for (int ch0 = t; ch0 < nchunks; ch0 += kU * kGnThreads) {
+        float4 r[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int ch = ch0 + u * kGnThreads;
+            r[u] = ch < nchunks ? __ldg(base + static_cast<long long>(ch) * groups) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+            if (r[u].x > 0.f)
+                chan_merge(na, ma, m2a, r[u].x, r[u].y + r[u].z / r[u].x, fmaxf(r[u].w - r[u].z * r[u].z / r[u].x, 0.f));
     }
     sn[t] = na;
     sm[t] = ma;

@@ -159,7 +159,7 @@ def subpixel_up_weights(w):
     taps that read one source pixel are summed:
     ws[q, p, ty, tx] = sum of w[:, :, ky, kx] over ky in R(q, ty), kx in R(p, tx),
     so the parity class is a 2x2 conv on the source grid at rows
-    v + ty + (-1 if q == 0 else 0) (exact in real arithmetic).
+    v + ty + (-1 if q == 0 else 0) (the phase decomposition; exact in real arithmetic).
     ``w``: [cout][cin][3][3]; returns [2][2][2][2][cout][cin] (q, p, ty, tx).
     """
     w = _f64(w)

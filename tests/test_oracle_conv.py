@@ -163,7 +163,7 @@ def test_conv2d_at_matches_full(upsample, pad):
 
 @pytest.mark.parametrize("pad", ["zero", "replicate"])
 def test_subpixel_decomposition_of_the_up_conv_is_exact(pad):
-    """The up conv as four 2x2 convs with summed weights equals
+    """The up conv as four 2x2 convs with summed weights (the phase form) equals
     conv(upsample2x(x)) in exact arithmetic: f64 agreement to 1e-12."""
     rng = np.random.default_rng(41)
     x = rng.standard_normal((3, 5, 6))

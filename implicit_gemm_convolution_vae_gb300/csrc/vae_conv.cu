@@ -22,6 +22,12 @@
 //    copies the mirrored edge column inside each landed box (column -1 <- 1,
 //    W <- W - 2) and passes the stage on to the MMA thread (whose own proxy
 //    fence would stall the tensor pipe); smaller grids gather.
+//  - The encoder's stride-2 downsample on even widths with >= 128 output
+//    columns: x viewed as (channel, column parity, W/2, row, image) makes tap
+//    (ky, kx) of 128 output pixels one box (parity kx & 1, first column
+//    u0 + kx / 2, row 2v + ky); the far-side pad is TMA's zero fill, or, for
+//    reflect padding, the mirrored row coordinate and one row copy by the
+//    fixer warp (column W <- W - 2 sits one row before it in the kx = 2 box).
 //  - B (weights [cout][taps][cin]) is a 3-D TMA tile load per (tap, chunk).
 //  - One elected thread issues tcgen05.mma (M=128, N=BN, K=16 steps) into one
 //    of two TMEM accumulators; four epilogue warps drain the other
@@ -76,6 +82,7 @@ struct ConvParams {
     int cin, cout, taps;  // taps: 9 or 1
     int up, rep;          // nearest-2x fold, replicate padding
     int refl, down;       // reflect padding; the stride-2 downsample (far-side pad; virtual grid = output)
+    int down_tma;         // the downsample's taps as TMA boxes of a (channel, column parity, W/2, row, image) view
     int hs, ws;           // source grid of the gather (= hv, wv except for the downsample)
     int H, W;             // output grid
     int R, Wt;            // tile rows, tile cols on the virtual grid
@@ -254,6 +261,14 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
 // chunk j sits at r * 128 + ((j ^ (r & 7)) * 16). kRow = 32: a 16-channel box,
 // 32-byte swizzle, 256-byte aligned: chunk j of row r at r * 32 + ((j ^ ((r >> 2) & 1)) * 16).
 // Returns whether it wrote anything.
+// Copies row rs of a 1024-byte-aligned, 128-byte-swizzled box onto row rd.
+__device__ __forceinline__ void copy_row_sw128(uint8_t* box, int rs, int rd) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(box + sw128_off(static_cast<uint32_t>(rd), static_cast<uint32_t>(j))) =
+            *reinterpret_cast<const uint4*>(box + sw128_off(static_cast<uint32_t>(rs), static_cast<uint32_t>(j)));
+}
+
 template <int kRow>
 __device__ __forceinline__ bool reflect_fix_box(uint8_t* box, int cbase, int W) {
     bool fixed = false;
@@ -418,7 +433,13 @@ __device__ void role_producer(const ConvParams& p, const Smem& s, const CUtensor
                         next_b(static_cast<uint32_t>(nck) * (b_bytes + (kMode == kModeGather ? 0u : p.a_tx)), &slot);
                     if (!ok) break;
                     for (int h = 0; h < nck; ++h) {
-                        if (kMode == kModeTma)
+                        if (kMode == kModeTma && is_2d(kVar) && p.down_tma) {
+                            // tap (ky, kx) = (dy + 1, dx + 1): column parity kx & 1, first column u0 + kx / 2
+                            int sy = 2 * ti.v0 + dy + 1;
+                            if (p.refl && sy >= p.hs) sy = 2 * (p.hs - 1) - sy;
+                            tma_load_5d(smem_u32(s.a + (slot * p.ks + h) * kABytes), mapA, fb, (kc + h) * kBK,
+                                        (dx + 1) & 1, ti.u0 + ((dx + 1) >> 1), sy, simg, pol_a);
+                        } else if (kMode == kModeTma)
                             tma_load_4d(smem_u32(s.a + (slot * p.ks + h) * kABytes), mapA, fb, (kc + h) * kBK,
                                         ti.u0 + dx, ti.v0 + dy, simg, pol_a);
                         tma_load_3d(smem_u32(s.b + (slot * p.ks + h) * p.BN * 128), mapB, fb, (kc + h) * kBK,
@@ -504,6 +525,34 @@ __device__ void role_fixer(const ConvParams& p, const Smem& s) {
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    if (!p.halo) {
+        // the reflect-padded downsample's per-tap stages: in the last column tile
+        // the kx = 2 boxes' row of column W takes column W - 2 (the row before it)
+        for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+            const TileInfo ti = decode_tile<false>(p, t);
+            const int i = p.wv - 1 - ti.u0;  // the row holding the last output pixel
+            const bool edge = (p.ws % 2 == 0) && i >= 1 && i < kBM;
+            for (int tap = 0; tap < p.taps && ok; ++tap)
+                for (int kc = 0; kc < p.kchunks; kc += p.ks) {
+                    if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                                   kWhereFixer)) {
+                        ok = false;
+                        break;
+                    }
+                    if (edge && tap % 3 == 2) {
+                        const int nck = min(p.ks, p.kchunks - kc);
+                        for (int h = 0; h < nck; ++h) copy_row_sw128(s.a + (stage * p.ks + h) * kABytes, i - 1, i);
+                        fence_proxy_async_smem();
+                    }
+                    mbar_arrive(smem_u32(&s.fixed[stage]));
+                    if (++stage == p.stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+        }
+        return;
+    }
     for (int t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         const TileInfo ti = decode_tile<false>(p, t);
         const bool edge = ti.u0 == 0 || ti.u0 + kBM >= p.ws;
@@ -544,8 +593,10 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
     bool ok = true;
     // Issues the MMAs of one B-ring slot: chunk kc0 (and the next ones of the
     // slot, per-tap path) against the A tile at `a_addr` (halo) or in the slot.
+    // reflect-padded downsample: stages come through the fixer warp
+    const uint64_t* tap_ready = (is_2d(kVar) && p.refl && p.down_tma) ? s.fixed : s.full;
     auto mma_slot = [&](uint32_t d, bool halo_a, uint32_t a_addr, int kc0, int nck, int& kit) {
-        if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status, kWhereMmaFull)) {
+        if (!mbar_wait(smem_u32(&tap_ready[stage]), phase, s.abort_flag, p.timeout_ns, p.status, kWhereMmaFull)) {
             ok = false;
             return;
         }
@@ -1245,7 +1296,7 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
 // kRms: the fused RMS_norm epilogue (a separate instantiation, so the other
 // kernels do not carry its 144-value row in registers).
 template <int kMode, bool kRms, int kVar>
-__global__ void __launch_bounds__(kMode == kModeGather ? 320 : (kMode == kModeHalo ? 224 : 192), 1)
+__global__ void __launch_bounds__(kMode == kModeGather ? 320 : 224, 1)
     conv_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                 const __grid_constant__ CUtensorMap mapA16, const __grid_constant__ CUtensorMap mapB16,
                 const __grid_constant__ CUtensorMap mapY, const ConvParams p) {
@@ -1270,7 +1321,7 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : (kMode == kModeHa
             mbar_init(smem_u32(&s.acce[i]), static_cast<uint32_t>(kEpiWarps * 32));
         }
         mbar_init(smem_u32(s.drain), 1u);
-        if (kMode == kModeHalo && p.refl)
+        if (kMode != kModeGather && p.refl)
             for (int i = 0; i < p.stages; ++i) mbar_init(smem_u32(&s.fixed[i]), 1u);
         fence_mbar_init();
     }
@@ -1307,7 +1358,7 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : (kMode == kModeHa
         if (lane == 0) role_mma<kVar>(p, s, tmem_base);
     } else if (kMode == kModeGather && warp >= kGatherWarp0) {
         role_gather<kVar>(p, s, (warp - kGatherWarp0) * 32 + lane);
-    } else if (kMode == kModeHalo && is_2d(kVar) && warp == kGatherWarp0) {
+    } else if (kMode != kModeGather && is_2d(kVar) && warp == kGatherWarp0) {
         if (lane == 0) role_fixer(p, s);  // launched only for reflect padding
     }
     tc_fence_before();
@@ -1744,7 +1795,7 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, co
             cudaFuncSetAttribute(conv_kernel<kMode, kRms, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set[dev] = true;
     }
-    const int threads = kMode == kModeGather ? 320 : (kMode == kModeHalo && p.refl ? 224 : 192);
+    const int threads = kMode == kModeGather ? 320 : (p.refl ? 224 : 192);
     conv_kernel<kMode, kRms, kVar><<<grid, threads, smem, stream>>>(ma, mb, ma16, mb16, my, p);
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
@@ -1869,8 +1920,12 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.H = p.up ? 2 * a.h_in : p.hv;
     p.W = p.up ? 2 * a.w_in : p.wv;
     // per-pixel source remaps: gather threads (reflect only where no halo box can serve)
-    const bool refl_halo = a.refl && !a.no_halo && a.taps == 9 && p.wv >= kBM;
-    const bool gather = a.rep || a.down || (a.refl && !refl_halo);
+    const bool refl_halo = a.refl && !a.down && !a.no_halo && a.taps == 9 && p.wv >= kBM;
+    // the downsample as TMA boxes: even widths, one-row tiles; with reflect padding
+    // the last tile must hold at least two output pixels (the fix copies within a box)
+    const bool down_tma = a.down && !a.rep && a.taps == 9 && a.w_in % 2 == 0 && p.wv >= kBM &&
+                          (!a.refl || (p.wv - 1) % kBM != 0);
+    const bool gather = a.rep || (a.down && !down_tma) || (a.refl && !a.down && !refl_halo);
     if (p.wv >= kBM) {
         p.Wt = kBM;
         p.R = 1;
@@ -1883,7 +1938,8 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.npar = p.up ? 4 : 1;
     // Geometry that allows a halo box: a tile is 128 pixels of one row, 3x3 taps,
     // zero padding (the TMA box fills out-of-range pixels with zeros).
-    const bool halo_geom = !gather && !a.no_halo && (a.taps == 9 || a.taps == 27) && p.R == 1 && p.Wt == kBM;
+    const bool halo_geom = !gather && !a.down && !a.no_halo && (a.taps == 9 || a.taps == 27) && p.R == 1 &&
+                           p.Wt == kBM;
     // reflect padding needs the three-tap halo stages (the edge fix runs per stage): N <= 144
     p.BN = refl_halo ? choose_bn_small(a.cout) : choose_bn(a.cout, halo_geom);
     p.b_rows = p.BN;
@@ -2022,13 +2078,30 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
             clear_error();
         }
     }
-    if (a.refl && mode != kModeHalo) {
+    if (a.refl && !a.down && mode != kModeHalo) {
         // only the halo stages carry the reflect fix: anything else gathers
         mode = kModeGather;
         p.ks = 1;
         p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail) / (kABytes + p.BN * 128));
     }
-    if (mode == kModeTma) {
+    if (mode == kModeTma && down_tma) {
+        // x as (channel, column parity, W/2, row, image): pixel (row, 2j + parity)
+        const uint64_t dims[5] = {static_cast<uint64_t>(a.cin), 2u, static_cast<uint64_t>(a.w_in / 2),
+                                  static_cast<uint64_t>(a.h_in), static_cast<uint64_t>(p.n_in)};
+        const uint64_t strides[4] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(a.cin) * 4,
+                                     static_cast<uint64_t>(a.w_in) * a.cin * 2,
+                                     static_cast<uint64_t>(a.h_in) * a.w_in * a.cin * 2};
+        const uint32_t box[5] = {static_cast<uint32_t>(kBK), 1u, static_cast<uint32_t>(kBM), 1u, 1u};
+        if (encode_tiled(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, a.x, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_128B) == VAE_OK) {
+            p.down_tma = 1;
+        } else {
+            clear_error();
+            mode = kModeGather;
+            p.ks = 1;
+            p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail) / (kABytes + p.BN * 128));
+        }
+    } else if (mode == kModeTma) {
         const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(p.wv),
                                   static_cast<uint64_t>(p.hv), static_cast<uint64_t>(p.n_in)};
         const uint64_t strides[3] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(p.wv) * a.cin * 2,
@@ -2048,7 +2121,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // than single CTAs on GB300 at every decoder shape, so they run only when
     // requested (VAE_CONV_CTA_PAIR=1 in the environment).
     if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2 &&
-        a.taps != 27 && !a.subpix && !a.refl && a.gn_part == nullptr) {
+        a.taps != 27 && !a.subpix && !a.refl && !a.down && a.gn_part == nullptr) {
         // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
         p.pair = 1;
         p.rem16 = 0;  // the pair kernel loads zero-filled 64-channel remainder boxes

@@ -64,6 +64,10 @@ SHAPES = [
     (1, 4, 129, 144, 144),
     (1, 3, 256, 208, 96),
     (1, 3, 140, 64, 256),
+    # the downsample's TMA path (even widths, >= 128 output columns): a 3-tile row with
+    # a ragged last tile, and 258 columns (129 outputs: its reflect form gathers)
+    (1, 5, 600, 32, 48),
+    (1, 4, 258, 64, 64),
 ]
 
 

@@ -114,7 +114,8 @@ struct ConvParams {
     int dup_base[4];
     int dup_v8;           // DupUp rows 32-byte aligned: 32-byte loads of the source window
     int v8_ok;            // f32 y / residual rows 32-byte aligned: 32-byte accesses
-    int epi_tma;          // epilogue writes through staged TMA boxes: 1 store, 2 add onto y (residual == y)
+    int epi_tma;          // epilogue writes through staged TMA boxes: 1 store, 2 add onto y (residual == y),
+                          // 3 the fused RMS_norm's f16 rows (rms_out)
     int bias_smem;        // the bias (cout floats) is copied to shared memory at kernel start
     // NCHW output of kept rows (conv_out): rows [keep_lo, keep_hi) land at
     // destination row (Y - keep_lo + dst_row0) of planes `plane` floats apart.
@@ -1123,6 +1124,77 @@ __device__ __forceinline__ void epilogue_rms_row(const ConvParams& p, const Tile
     }
 }
 
+// Fused RMS_norm through the staged TMA epilogue (one-row tiles, one N tile,
+// no f32 output, no residual): a first pass over the accumulator's 16-column
+// chunks forms the pixel's sum of squares in the standalone kernel's exact order
+// (4 partial sums: channel quad i goes to part[i % 4], chunks in order, then
+// the butterfly), a second pass reloads the chunks from TMEM, recomputes the
+// same values, normalises them and stores f16 boxes (32 pixels x 16 channels,
+// 32-byte rows, 32-byte swizzle) with TMA. No pixel row is held in registers.
+__device__ __forceinline__ void epilogue_tma_rms_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, bool valid,
+                                                     int v, int u, int q, int pp, long long pix, uint8_t* stg,
+                                                     const CUtensorMap* mapY, int ew, int lane) {
+    const int nch = p.cout / 16;
+    float part[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int c = 0; c < nch; ++c) {
+        uint32_t acc[16];
+        __syncwarp();
+        tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
+        tmem_ld_wait_regs(acc);
+        float val[16];
+        compute_chunk(p, ti, acc, c * 16, v, u, q, pp, pix, val);
+#pragma unroll
+        for (int l = 0; l < 4; ++l) part[l] = rms_acc4(part[l], val[4 * l], val[4 * l + 1], val[4 * l + 2], val[4 * l + 3]);
+    }
+    part[0] = __fadd_rn(part[0], part[2]);
+    part[1] = __fadd_rn(part[1], part[3]);
+    part[0] = __fadd_rn(part[0], part[1]);
+    const float inv = rms_inv(part[0], p.cout);
+    const uint32_t sbase = smem_u32(stg + ew * kStgBytes);
+    const int seg = ti.u0 + ew * 32;
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 32u;
+    const uint32_t sw = static_cast<uint32_t>((lane >> 2) & 1);
+    for (int c = 0; c < nch; ++c) {
+        uint32_t acc[16];
+        __syncwarp();
+        tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
+        tmem_ld_wait_regs(acc);
+        float val[16];
+        compute_chunk(p, ti, acc, c * 16, v, u, q, pp, pix, val);
+        uint32_t h[8];
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+            const int o = c * 16 + 4 * i4;
+            const float4 g = __ldg(reinterpret_cast<const float4*>(p.rms_gamma + o));
+            float a[4] = {rms_apply(val[4 * i4], inv, g.x), rms_apply(val[4 * i4 + 1], inv, g.y),
+                          rms_apply(val[4 * i4 + 2], inv, g.z), rms_apply(val[4 * i4 + 3], inv, g.w)};
+            if (p.rms_silu) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a[e] = silu_f(a[e]);
+            }
+            __half2 t0 = __floats2half2_rn(a[0], a[1]);
+            __half2 t1 = __floats2half2_rn(a[2], a[3]);
+            h[2 * i4] = *reinterpret_cast<uint32_t*>(&t0);
+            h[2 * i4 + 1] = *reinterpret_cast<uint32_t*>(&t1);
+        }
+        if (lane == 0) bulk_wait_read_all();  // the previous box left this warp's buffer
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + row_off +
+                                                                        ((static_cast<uint32_t>(k) ^ sw) << 4)),
+                         "r"(h[4 * k]), "r"(h[4 * k + 1]), "r"(h[4 * k + 2]), "r"(h[4 * k + 3])
+                         : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && seg < p.wv) {
+            tma_store_4d(mapY, sbase, c * 16, seg, ti.v0, ti.img);
+            bulk_commit_group();
+        }
+    }
+    (void)valid;
+}
+
 // Epilogue of one accumulator row (pixel) without a fused norm. kPipe: the
 // register-hungry pipelined residual path (off in the 320-thread gather kernel).
 template <bool kPipe, bool kGn = false>
@@ -1276,7 +1348,9 @@ __device__ void role_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         const long long pix = (static_cast<long long>(ti.img) * p.H + Y) * p.W + X;
         const uint32_t tbase =
             tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
-        if (kRms) {
+        if (kRms && kMode != kModeGather && p.epi_tma == 3) {
+            epilogue_tma_rms_row(p, ti, tbase, valid, v, u, q, pp, pix, s.stg, mapY, ew, lane);
+        } else if (kRms) {
             epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         } else if (kMode != kModeGather && p.epi_tma) {
             epilogue_tma_row<kVar == 3>(p, ti, tbase, v, u, q, pp, pix, s.stg, mapY, ew, lane, valid,
@@ -2193,6 +2267,21 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         }
         if (erc == VAE_OK)  // with statistics the values are needed in registers: the residual is read, not added
             p.epi_tma = res_self && a.gn_part == nullptr ? 2 : 1;
+        else
+            clear_error();
+    }
+    // Fused RMS_norm with f16 rows only (a ResNet's first conv): staged f16 TMA boxes.
+    if (mode != kModeGather && !p.epi_tma && a.rms_out != nullptr && a.y == nullptr && a.residual == nullptr &&
+        a.dup_src == nullptr && !p.up && p.R == 1 && p.Wt == kBM && p.n_tiles == 1 && a.cout % 16 == 0 &&
+        aligned16(a.rms_gamma) && 1024 + ring + kEpiWarps * kStgBytes + kTail <= kMaxSmem) {
+        const uint64_t dims[4] = {static_cast<uint64_t>(a.cout), static_cast<uint64_t>(p.W),
+                                  static_cast<uint64_t>(p.H), static_cast<uint64_t>(p.n)};
+        const uint64_t strides[3] = {static_cast<uint64_t>(a.cout) * 2, static_cast<uint64_t>(p.W) * a.cout * 2,
+                                     static_cast<uint64_t>(p.H) * p.W * a.cout * 2};
+        const uint32_t box[4] = {16u, 32u, 1u, 1u};
+        if (encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.rms_out, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_32B) == VAE_OK)
+            p.epi_tma = 3;
         else
             clear_error();
     }

@@ -171,7 +171,8 @@ def test_host_buffer_decode_matches_device_decode():
     assert torch.equal(oh, dev_out.cpu())
 
 
-@pytest.mark.parametrize("widths,nres,hw", [((64, 32, 32, 16), 2, (12, 10)), ((1152, 576, 288, 144), 3, (16, 16))])
+@pytest.mark.parametrize("widths,nres,hw", [((64, 32, 32, 16), 2, (12, 10)), ((1152, 576, 288, 144), 3, (16, 16)),
+                                            ((1152, 576, 288, 144), 2, (20, 18))])
 def test_fused_norms_are_bit_identical_to_separate_norms(widths, nres, hw):
     """RMS_norm fused into the producing conv's epilogue gives the same bits as
     the standalone RMS_norm kernel (one shared evaluation order)."""

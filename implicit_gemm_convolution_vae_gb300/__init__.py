@@ -425,6 +425,7 @@ DECODE_PROFILE = 1
 DECODE_NO_FUSION = 2
 DECODE_FUSE_NORM = 4
 DECODE_SUBPIXEL_UP = 8
+DECODE_PROFILE_FULLRES = 16
 STAGE_NAMES = {0: "conv3x3", 1: "conv1x1", 2: "norm", 3: "cast", 4: "attention", 5: "layout", 6: "copy"}
 
 
@@ -510,10 +511,12 @@ class Decoder:
 
     @staticmethod
     def opts(band_from: int = 0, nbands: int = 0, band_rows: int = 0, guard_log2: int = 8,
-             profile: bool = False, fuse: bool = False, subpixel: bool = False) -> DecodeOpts:
+             profile=False, fuse: bool = False, subpixel: bool = False) -> DecodeOpts:
+        """profile: False, True (events around every stage) or "fullres" (only around
+        the full-resolution ResNet convs)."""
+        prof = (DECODE_PROFILE if profile else 0) | (DECODE_PROFILE_FULLRES if profile == "fullres" else 0)
         return DecodeOpts(band_from, nbands, band_rows, guard_log2,
-                          (DECODE_PROFILE if profile else 0) | (DECODE_FUSE_NORM if fuse else 0) |
-                          (DECODE_SUBPIXEL_UP if subpixel else 0))
+                          prof | (DECODE_FUSE_NORM if fuse else 0) | (DECODE_SUBPIXEL_UP if subpixel else 0))
 
     def profile(self):
         """Stage records of the most recent profiled decode, as dicts (synchronises)."""

@@ -199,6 +199,7 @@ struct Exec {
     size_t off[kNBuf] = {};
     float guard = 256.f;
     vae_decoder* prof = nullptr;  // non-null: record events around stages
+    int prof_only_w = 0;          // > 0: only the 3x3 convs with cin == cout on rows this wide
     bool fuse = false;            // VAE_DECODE_FUSE_NORM without VAE_DECODE_NO_FUSION
     bool subpix = false;          // VAE_DECODE_SUBPIXEL_UP
     // RMS_norm rides in the epilogue of a ResNet's first conv (whose f32 output
@@ -213,6 +214,7 @@ struct Exec {
     // Starts a profiled stage; returns its record index (or -1).
     int begin(int kind, int launches, int h, int w, int cin, int cout, double flops, double bytes) {
         if (dry || prof == nullptr) return -1;
+        if (prof_only_w > 0 && !(kind == VAE_STAGE_CONV3X3 && w == prof_only_w && cin == cout)) return -1;
         const int i = static_cast<int>(prof->recs.size());
         const size_t ev = prof->rec_ev.size() * 2;
         while (prof->events.size() < ev + 2) {
@@ -752,7 +754,7 @@ static int decode_impl(vae_decoder_t dec, const float* z, int h0, int w0, float*
         return set_error(VAE_ERR_ARG, "decode: NULL argument");
     if (opts != nullptr &&
         (opts->flags & ~static_cast<unsigned>(VAE_DECODE_PROFILE | VAE_DECODE_NO_FUSION | VAE_DECODE_FUSE_NORM |
-                                              VAE_DECODE_SUBPIXEL_UP)) != 0)
+                                              VAE_DECODE_SUBPIXEL_UP | VAE_DECODE_PROFILE_FULLRES)) != 0)
         return set_error(VAE_ERR_ARG, "decode: unknown opts.flags 0x%x", opts->flags);
     int rc = check_device();
     if (rc != VAE_OK) return rc;
@@ -764,8 +766,11 @@ static int decode_impl(vae_decoder_t dec, const float* z, int h0, int w0, float*
     if (!aligned16(ws)) return set_error(VAE_ERR_ALIGN, "decode: workspace must be 16-byte aligned");
     X.dry = false;
     X.base = static_cast<uint8_t*>(ws);
-    if (opts != nullptr && (opts->flags & VAE_DECODE_PROFILE)) X.prof = dec;
     const int lf = levels_total(dec);
+    if (opts != nullptr && (opts->flags & VAE_DECODE_PROFILE)) {
+        X.prof = dec;
+        if (opts->flags & VAE_DECODE_PROFILE_FULLRES) X.prof_only_w = w0 << lf;
+    }
     const size_t zbytes = static_cast<size_t>(dec->zc) * h0 * w0 * 4;
     const size_t obytes = static_cast<size_t>(dec->conv_out.cout) * (static_cast<size_t>(h0) << lf) * (w0 << lf) * 4;
     const float* zd = z;

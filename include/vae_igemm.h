@@ -376,7 +376,8 @@ typedef struct {
     int nbands;      /* number of equal kept-row bands (0 or 1 with band_rows 0: whole frame) */
     int band_rows;   /* alternative to nbands: at most this many kept rows per band */
     int guard_log2;  /* f16 range guard g of the raw-stream casts (default 8 when < 0) */
-    unsigned flags;  /* 0, or VAE_DECODE_PROFILE | VAE_DECODE_FUSE_NORM | VAE_DECODE_NO_FUSION | VAE_DECODE_SUBPIXEL_UP */
+    unsigned flags;  /* 0, or VAE_DECODE_PROFILE (| VAE_DECODE_PROFILE_FULLRES) | VAE_DECODE_FUSE_NORM |
+                        VAE_DECODE_NO_FUSION | VAE_DECODE_SUBPIXEL_UP */
 } vae_decode_opts;
 
 /* vae_decode_opts.flags: record CUDA events around every stage of this
@@ -396,7 +397,11 @@ enum {
     /* Run the up convs in their sub-pixel form (four 2x2 convs with summed
      * weights, see vae_pack_subpixel_weights): 4/9 of their MACs, the weight sums
      * rounded to f16 once. Off by default (it changes the rounding). */
-    VAE_DECODE_SUBPIXEL_UP = 8
+    VAE_DECODE_SUBPIXEL_UP = 8,
+    /* With VAE_DECODE_PROFILE: record events only around the full-resolution
+     * ResNet convs (3x3, cin == cout, output rows as wide as the image), so a
+     * timed decode carries 2 events per such launch instead of 2 per stage. */
+    VAE_DECODE_PROFILE_FULLRES = 16
 };
 
 /* Stage kinds of a profiled decode. */

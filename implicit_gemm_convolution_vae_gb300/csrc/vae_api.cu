@@ -1,6 +1,7 @@
 // Library-wide plumbing: last-error text, the per-device status word, wait
 // timeouts, device checks, tensor-map encoding, and the failure-detection
 // self test (a bounded wait on a barrier phase that never completes).
+#include <cstdlib>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -63,6 +64,14 @@ DevStatus* device_status_ptr() {
 }
 
 unsigned long long wait_timeout_ns() { return g_timeout_ns; }
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("VAE_PDL");
+        return !(e != nullptr && e[0] == '0');
+    }();
+    return on;
+}
 
 int sm_count() {
     int dev;

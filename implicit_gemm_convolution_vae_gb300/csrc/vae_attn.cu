@@ -312,6 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mq);
         tma_prefetch_desc(&mk);
     }
+    pdl_wait();  // q, k come from the projections launched before
+    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -487,6 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mp);
         tma_prefetch_desc(&mv);
     }
+    pdl_wait();  // P, the flags and V come from kernels launched before
+    pdl_launch_dependents();
     __syncthreads();
     // The tile's "some row rescaled at block j" flags, one bit per key block.
     for (int j = 1 + threadIdx.x; j < p.nkb; j += blockDim.x) {
@@ -646,10 +650,10 @@ static int attn_core_run(const __half* q, const __half* k, const __half* vt, int
         const int nt = std::min(L.group, L.qtiles - t0);
         sp.q_tile0 = t0;
         pp.q_tile0 = t0;
-        attn_scores_kernel<<<static_cast<unsigned>(nt), kThreads, smem, stream>>>(mq, mk, sp);
-        VAE_CUDA_CHECK(cudaGetLastError());
-        attn_pv_kernel<<<static_cast<unsigned>(nt * L.ndv), kThreads, smem, stream>>>(mp, mv, pp);
-        VAE_CUDA_CHECK(cudaGetLastError());
+        VAE_CUDA_CHECK(launch_kernel(attn_scores_kernel, dim3(static_cast<unsigned>(nt)), dim3(kThreads), smem,
+                                     stream, mq, mk, sp));
+        VAE_CUDA_CHECK(launch_kernel(attn_pv_kernel, dim3(static_cast<unsigned>(nt * L.ndv)), dim3(kThreads), smem,
+                                     stream, mp, mv, pp));
     }
     return VAE_OK;
 }

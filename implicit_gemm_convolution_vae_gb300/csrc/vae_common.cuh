@@ -4,6 +4,8 @@
 // error/status plumbing. Every kernel of the library includes this file.
 #pragma once
 
+#include <utility>
+
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -55,6 +57,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
+
+// Waits until the grids this one depends on (programmatic dependent launch)
+// have completed and their memory is visible; a no-op without that launch mode.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next grid on the stream launch now (it waits in pdl_wait for this one).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -482,6 +490,29 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
                  CUtensorMapSwizzle swizzle);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Programmatic dependent launch: every kernel of the library waits for the
+// grid before it on the stream (griddepcontrol.wait) before it touches global
+// memory, so it may be launched while that grid is still running and overlap
+// its launch and prologue (barrier set-up, TMEM allocation, descriptor
+// prefetch) with the other grid's tail. Off with VAE_PDL=0 in the environment.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 #define VAE_CUDA_CHECK(expr)                                                                   \
     do {                                                                                       \

@@ -1399,8 +1399,6 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 224, 1)
             for (int i = 0; i < p.stages; ++i) mbar_init(smem_u32(&s.fixed[i]), 1u);
         fence_mbar_init();
     }
-    if (p.bias_smem)  // visible to the epilogue after the __syncthreads below
-        for (int i = threadIdx.x; i < p.cout; i += blockDim.x) s.bias[i] = __ldg(p.bias + i);
     const uint32_t tmem_cols = p.acc_stride * 2 <= 32 ? 32u
                                : p.acc_stride * 2 <= 64 ? 64u
                                : p.acc_stride * 2 <= 128 ? 128u
@@ -1419,6 +1417,11 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 224, 1)
         }
         if (p.epi_tma) tma_prefetch_desc(&mapY);
     }
+    // everything above touches only shared memory, TMEM and kernel parameters
+    pdl_wait();
+    pdl_launch_dependents();
+    if (p.bias_smem)  // visible to the epilogue after the __syncthreads below
+        for (int i = threadIdx.x; i < p.cout; i += blockDim.x) s.bias[i] = __ldg(p.bias + i);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1870,7 +1873,8 @@ int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, co
         attr_set[dev] = true;
     }
     const int threads = kMode == kModeGather ? 320 : (p.refl ? 224 : 192);
-    conv_kernel<kMode, kRms, kVar><<<grid, threads, smem, stream>>>(ma, mb, ma16, mb16, my, p);
+    VAE_CUDA_CHECK(launch_kernel(conv_kernel<kMode, kRms, kVar>, dim3(grid), dim3(threads), smem, stream, ma, mb, ma16,
+                                 mb16, my, p));
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }

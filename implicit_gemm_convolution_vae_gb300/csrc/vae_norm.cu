@@ -27,6 +27,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
                                                       const float* __restrict__ bias,
                                                       const float* __restrict__ gamma, int silu,
                                                       float out_scale, __half* __restrict__ y) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int c4 = c / 4;
     const int lane = threadIdx.x % G;
     const long long group = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / G;
@@ -75,6 +77,8 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const float* __restric
                                                           const float* __restrict__ bias,
                                                           const float* __restrict__ gamma, int silu,
                                                           float out_scale, __half* __restrict__ y) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int c4 = c / 4;
     const int lane = threadIdx.x % G;
     const long long pix = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / G;
@@ -143,6 +147,8 @@ __global__ void __launch_bounds__(kGnThreads) gn_partial_kernel(const float* __r
                                                                 int groups, int chunk_rows, int nchunks,
                                                                 const float* __restrict__ bias,
                                                                 float* __restrict__ part) {
+    pdl_wait();
+    pdl_launch_dependents();
     extern __shared__ float sh[];  // [rpar][c] mean, then [rpar][c] M2
     const int chunk = blockIdx.x, img = blockIdx.y;
     const int c4 = c / 4;
@@ -210,6 +216,8 @@ __global__ void __launch_bounds__(kGnThreads) gn_finalize_kernel(const float* __
                                                                  int groups, int cpg, int chunk_rows,
                                                                  int nchunks, float eps,
                                                                  float* __restrict__ stats) {
+    pdl_wait();
+    pdl_launch_dependents();
     __shared__ float sn[kGnThreads], sm[kGnThreads], sq[kGnThreads];
     const int g = blockIdx.x, img = blockIdx.y, t = threadIdx.x;
     float na = 0.f, ma = 0.f, m2a = 0.f;
@@ -246,6 +254,8 @@ __global__ void __launch_bounds__(kGnThreads) gn_finalize_kernel(const float* __
 __global__ void __launch_bounds__(kGnThreads) gn_finalize_records_kernel(const float4* __restrict__ rec,
                                                                          int nchunks, int groups, float eps,
                                                                          float* __restrict__ stats) {
+    pdl_wait();
+    pdl_launch_dependents();
     __shared__ float sn[kGnThreads], sm[kGnThreads], sq[kGnThreads];
     const int g = blockIdx.x, img = blockIdx.y, t = threadIdx.x;
     float na = 0.f, ma = 0.f, m2a = 0.f;
@@ -294,6 +304,8 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const float* __restrict__
                                                        const float* __restrict__ beta,
                                                        const float* __restrict__ stats, int silu,
                                                        float out_scale, __half* __restrict__ y) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int c4 = c / 4;
     const int cpg = c / groups;
     const int tpr = min(c4, 256);
@@ -345,6 +357,8 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const float* __restrict__
 __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ x, long long total4, int c,
                                                    const float* __restrict__ bias, float scale,
                                                    __half* __restrict__ y) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int c4 = c / 4;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total4;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -361,6 +375,8 @@ __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ x, 
 // z / scaling + shift; mul = 1, add = 0 otherwise).
 __global__ void __launch_bounds__(256) latent_nhwc_kernel(const float* __restrict__ z, int c, long long hw,
                                                           float mul, float add, __half* __restrict__ y) {
+    pdl_wait();
+    pdl_launch_dependents();
     const long long total = hw * c;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -436,14 +452,14 @@ int gn_run(const float* x, int n, int hw, int c, int groups, float eps, const fl
         VAE_CUDA_CHECK(cudaFuncSetAttribute(gn_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(shm)));
     }
-    gn_partial_kernel<<<dim3(plan.nchunks, n), kGnThreads, shm, stream>>>(x, hw, c, groups, plan.chunk_rows,
-                                                                          plan.nchunks, bias, part);
+    VAE_CUDA_CHECK(launch_kernel(gn_partial_kernel, dim3(plan.nchunks, n), dim3(kGnThreads), shm, stream, x, hw, c,
+        groups, plan.chunk_rows, plan.nchunks, bias, part));
     VAE_CUDA_CHECK(cudaGetLastError());
-    gn_finalize_kernel<<<dim3(groups, n), kGnThreads, 0, stream>>>(part, hw, groups, c / groups,
-                                                                   plan.chunk_rows, plan.nchunks, eps, stats);
+    VAE_CUDA_CHECK(launch_kernel(gn_finalize_kernel, dim3(groups, n), dim3(kGnThreads), 0, stream, part, hw, groups,
+        c / groups, plan.chunk_rows, plan.nchunks, eps, stats));
     VAE_CUDA_CHECK(cudaGetLastError());
-    gn_apply_kernel<<<gn_apply_grid(n, hw, c), 256, 0, stream>>>(x, hw, c, groups, bias, gamma, beta, stats, silu,
-                                                                 out_scale, static_cast<__half*>(y));
+    VAE_CUDA_CHECK(launch_kernel(gn_apply_kernel, dim3(gn_apply_grid(n, hw, c)), dim3(256), 0, stream, x, hw, c,
+        groups, bias, gamma, beta, stats, silu, out_scale, static_cast<__half*>(y)));
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -454,8 +470,8 @@ int gn_stats_from_records(const void* rec, int n, int nchunks, int groups, float
     if (n < 1 || nchunks < 1 || groups < 1 || groups > 65535)
         return set_error(VAE_ERR_SHAPE, "groupnorm: n=%d chunks=%d groups=%d", n, nchunks, groups);
     if (!(eps >= 0.f)) return set_error(VAE_ERR_ARG, "groupnorm: eps must be >= 0");
-    gn_finalize_records_kernel<<<dim3(groups, n), kGnThreads, 0, stream>>>(static_cast<const float4*>(rec), nchunks,
-                                                                           groups, eps, stats);
+    VAE_CUDA_CHECK(launch_kernel(gn_finalize_records_kernel, dim3(groups, n), dim3(kGnThreads), 0, stream,
+        static_cast<const float4*>(rec), nchunks, groups, eps, stats));
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -470,8 +486,8 @@ int gn_apply_run(const float* x, int n, int hw, int c, int groups, const float* 
         return set_error(VAE_ERR_ALIGN, "groupnorm_apply: pointers must be 16-byte aligned");
     int rc = check_device();
     if (rc != VAE_OK) return rc;
-    gn_apply_kernel<<<gn_apply_grid(n, hw, c), 256, 0, stream>>>(x, hw, c, groups, nullptr, gamma, beta, stats, silu,
-                                                                 out_scale, static_cast<__half*>(y));
+    VAE_CUDA_CHECK(launch_kernel(gn_apply_kernel, dim3(gn_apply_grid(n, hw, c)), dim3(256), 0, stream, x, hw, c,
+        groups, nullptr, gamma, beta, stats, silu, out_scale, static_cast<__half*>(y)));
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -494,19 +510,26 @@ int rms_run(const float* x, long long m, int c, const float* bias, const float* 
         if (blocks > 0x7fffffffLL) return set_error(VAE_ERR_SHAPE, "rmsnorm: m=%lld too large", m);
         const int grid = static_cast<int>(blocks);
         if (G == 4)
-            rmsnorm_reg_kernel<4><<<grid, 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+            VAE_CUDA_CHECK(launch_kernel(rmsnorm_reg_kernel<4>, dim3(grid), dim3(256), 0, stream, x, m, c, bias,
+                gamma, silu, out_scale, yh));
         else if (G == 8)
-            rmsnorm_reg_kernel<8><<<grid, 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+            VAE_CUDA_CHECK(launch_kernel(rmsnorm_reg_kernel<8>, dim3(grid), dim3(256), 0, stream, x, m, c, bias,
+                gamma, silu, out_scale, yh));
         else if (G == 16)
-            rmsnorm_reg_kernel<16><<<grid, 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+            VAE_CUDA_CHECK(launch_kernel(rmsnorm_reg_kernel<16>, dim3(grid), dim3(256), 0, stream, x, m, c, bias,
+                gamma, silu, out_scale, yh));
         else
-            rmsnorm_reg_kernel<32><<<grid, 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+            VAE_CUDA_CHECK(launch_kernel(rmsnorm_reg_kernel<32>, dim3(grid), dim3(256), 0, stream, x, m, c, bias,
+                gamma, silu, out_scale, yh));
     } else if (c4 >= 128) {
-        rmsnorm_kernel<32><<<grid_for(m * 32, 256), 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+        VAE_CUDA_CHECK(launch_kernel(rmsnorm_kernel<32>, dim3(grid_for(m * 32, 256)), dim3(256), 0, stream, x, m, c,
+            bias, gamma, silu, out_scale, yh));
     } else if (c4 >= 32) {
-        rmsnorm_kernel<16><<<grid_for(m * 16, 256), 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+        VAE_CUDA_CHECK(launch_kernel(rmsnorm_kernel<16>, dim3(grid_for(m * 16, 256)), dim3(256), 0, stream, x, m, c,
+            bias, gamma, silu, out_scale, yh));
     } else {
-        rmsnorm_kernel<8><<<grid_for(m * 8, 256), 256, 0, stream>>>(x, m, c, bias, gamma, silu, out_scale, yh);
+        VAE_CUDA_CHECK(launch_kernel(rmsnorm_kernel<8>, dim3(grid_for(m * 8, 256)), dim3(256), 0, stream, x, m, c,
+            bias, gamma, silu, out_scale, yh));
     }
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
@@ -522,13 +545,15 @@ int cast_run(const float* x, size_t count, int c, const float* bias, float scale
     if (rc != VAE_OK) return rc;
     if (count == 0) return VAE_OK;
     const long long total4 = static_cast<long long>(count / 4);
-    cast_kernel<<<grid_for(total4, 256), 256, 0, stream>>>(x, total4, c, bias, scale, static_cast<__half*>(y));
+    VAE_CUDA_CHECK(launch_kernel(cast_kernel, dim3(grid_for(total4, 256)), dim3(256), 0, stream, x, total4, c, bias,
+        scale, static_cast<__half*>(y)));
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
 
 int latent_run(const float* z, int c, long long hw, float mul, float add, void* y, cudaStream_t stream) {
-    latent_nhwc_kernel<<<grid_for(hw * c, 256), 256, 0, stream>>>(z, c, hw, mul, add, static_cast<__half*>(y));
+    VAE_CUDA_CHECK(launch_kernel(latent_nhwc_kernel, dim3(grid_for(hw * c, 256)), dim3(256), 0, stream, z, c, hw, mul,
+        add, static_cast<__half*>(y)));
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }

@@ -313,7 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mk);
     }
     pdl_wait();  // q, k come from the projections launched before
-    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -325,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         if (lane == 0) scores_mma(p, s, tmem);
     }
+    pdl_launch_dependents();  // this CTA's work is done
     tc_fence_before();
     __syncthreads();
     if (warp == 5) {
@@ -490,7 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mv);
     }
     pdl_wait();  // P, the flags and V come from kernels launched before
-    pdl_launch_dependents();
     __syncthreads();
     // The tile's "some row rescaled at block j" flags, one bit per key block.
     for (int j = 1 + threadIdx.x; j < p.nkb; j += blockDim.x) {
@@ -508,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         if (lane == 0) pv_mma(p, s, tmem, fl);
     }
+    pdl_launch_dependents();  // this CTA's work is done
     tc_fence_before();
     __syncthreads();
     if (warp == 5) {

@@ -1419,7 +1419,6 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 224, 1)
     }
     // everything above touches only shared memory, TMEM and kernel parameters
     pdl_wait();
-    pdl_launch_dependents();
     if (p.bias_smem)  // visible to the epilogue after the __syncthreads below
         for (int i = threadIdx.x; i < p.cout; i += blockDim.x) s.bias[i] = __ldg(p.bias + i);
     tc_fence_before();
@@ -1438,6 +1437,8 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 224, 1)
     } else if (kMode != kModeGather && is_2d(kVar) && warp == kGatherWarp0) {
         if (lane == 0) role_fixer(p, s);  // launched only for reflect padding
     }
+    // this CTA's work is done: the next grid may launch (it waits for this one to finish)
+    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {

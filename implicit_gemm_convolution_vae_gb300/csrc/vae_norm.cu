@@ -28,7 +28,6 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ 
                                                       const float* __restrict__ gamma, int silu,
                                                       float out_scale, __half* __restrict__ y) {
     pdl_wait();
-    pdl_launch_dependents();
     const int c4 = c / 4;
     const int lane = threadIdx.x % G;
     const long long group = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / G;
@@ -78,7 +77,6 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const float* __restric
                                                           const float* __restrict__ gamma, int silu,
                                                           float out_scale, __half* __restrict__ y) {
     pdl_wait();
-    pdl_launch_dependents();
     const int c4 = c / 4;
     const int lane = threadIdx.x % G;
     const long long pix = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) / G;
@@ -148,7 +146,6 @@ __global__ void __launch_bounds__(kGnThreads) gn_partial_kernel(const float* __r
                                                                 const float* __restrict__ bias,
                                                                 float* __restrict__ part) {
     pdl_wait();
-    pdl_launch_dependents();
     extern __shared__ float sh[];  // [rpar][c] mean, then [rpar][c] M2
     const int chunk = blockIdx.x, img = blockIdx.y;
     const int c4 = c / 4;
@@ -217,7 +214,6 @@ __global__ void __launch_bounds__(kGnThreads) gn_finalize_kernel(const float* __
                                                                  int nchunks, float eps,
                                                                  float* __restrict__ stats) {
     pdl_wait();
-    pdl_launch_dependents();
     __shared__ float sn[kGnThreads], sm[kGnThreads], sq[kGnThreads];
     const int g = blockIdx.x, img = blockIdx.y, t = threadIdx.x;
     float na = 0.f, ma = 0.f, m2a = 0.f;
@@ -255,7 +251,6 @@ __global__ void __launch_bounds__(kGnThreads) gn_finalize_records_kernel(const f
                                                                          int nchunks, int groups, float eps,
                                                                          float* __restrict__ stats) {
     pdl_wait();
-    pdl_launch_dependents();
     __shared__ float sn[kGnThreads], sm[kGnThreads], sq[kGnThreads];
     const int g = blockIdx.x, img = blockIdx.y, t = threadIdx.x;
     float na = 0.f, ma = 0.f, m2a = 0.f;
@@ -305,7 +300,6 @@ __global__ void __launch_bounds__(256) gn_apply_kernel(const float* __restrict__
                                                        const float* __restrict__ stats, int silu,
                                                        float out_scale, __half* __restrict__ y) {
     pdl_wait();
-    pdl_launch_dependents();
     const int c4 = c / 4;
     const int cpg = c / groups;
     const int tpr = min(c4, 256);
@@ -358,7 +352,6 @@ __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ x, 
                                                    const float* __restrict__ bias, float scale,
                                                    __half* __restrict__ y) {
     pdl_wait();
-    pdl_launch_dependents();
     const int c4 = c / 4;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total4;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -376,7 +369,6 @@ __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ x, 
 __global__ void __launch_bounds__(256) latent_nhwc_kernel(const float* __restrict__ z, int c, long long hw,
                                                           float mul, float add, __half* __restrict__ y) {
     pdl_wait();
-    pdl_launch_dependents();
     const long long total = hw * c;
     for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {

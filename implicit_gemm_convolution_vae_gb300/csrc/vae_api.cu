@@ -68,7 +68,7 @@ unsigned long long wait_timeout_ns() { return g_timeout_ns; }
 bool pdl_enabled() {
     static const bool on = [] {
         const char* e = std::getenv("VAE_PDL");
-        return !(e != nullptr && e[0] == '0');
+        return e != nullptr && e[0] == '1';
     }();
     return on;
 }

@@ -495,7 +495,8 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // grid before it on the stream (griddepcontrol.wait) before it touches global
 // memory, so it may be launched while that grid is still running and overlap
 // its launch and prologue (barrier set-up, TMEM allocation, descriptor
-// prefetch) with the other grid's tail. Off with VAE_PDL=0 in the environment.
+// prefetch) with the other grid's tail. Opt-in (VAE_PDL=1 in the environment):
+// the 1024^2 decode measured 14.8 ms with it against 14.3 ms without on GB300.
 bool pdl_enabled();
 
 template <typename... KArgs, typename... Args>

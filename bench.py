@@ -243,6 +243,16 @@ def run_kernel(args):
         y = torch.empty(h * w, cin, dtype=torch.float16, device="cuda")
         fn = lambda: vg.rmsnorm_silu(x, g, silu=True, out=y)
         flops, nbytes = 0.0, x.numel() * 6
+    elif args.kernel == "conv3x3rms":
+        # a ResNet's first conv with its second RMS_norm(+SiLU) in the epilogue (f16 rows only)
+        x = torch.randn(1, h, w, cin, device="cuda").half()
+        wt = (torch.randn(cout, 3, 3, cin, device="cuda") / (9 * cin) ** 0.5).half()
+        b = torch.randn(cout, device="cuda") * 0.1
+        g = torch.ones(cout, device="cuda")
+        yn = torch.empty(1, h, w, cout, dtype=torch.float16, device="cuda")
+        fn = lambda: vg.conv3x3_nhwc_rms(x, wt, g, b, out=yn, silu=True)
+        flops = 2.0 * h * w * cout * 9 * cin
+        nbytes = x.numel() * 2 + yn.numel() * 2
     elif args.kernel in ("convgn", "convgn_fused"):
         # a 3x3 conv (f32 out, in-place residual) followed by GroupNorm(32)+SiLU -> f16:
         # convgn = conv + the standalone two-pass GroupNorm; convgn_fused = the conv
@@ -325,7 +335,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", default=None,
-                    help="time one kernel instead: conv3x3, upconv3x3, downconv3x3, conv3d, upconv3d, convgn, convgn_fused, "
+                    help="time one kernel instead: conv3x3, upconv3x3, downconv3x3, conv3x3rms, conv3d, upconv3d, convgn, "
+                         "convgn_fused, "
                          "rmsnorm, groupnorm, "
                          "attention")
     ap.add_argument("--shape", default="1024,1024,144,144",

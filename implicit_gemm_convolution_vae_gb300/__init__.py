@@ -21,7 +21,7 @@ from .build import LIB_PATH, build  # noqa: F401  (build is re-exported)
 
 __all__ = [
     "VaeError", "lib", "version", "last_error", "sync_status", "set_wait_timeout_ns",
-    "selftest_wait_timeout", "conv3x3_nhwc", "conv3x3_nhwc_gn", "conv3x3_gn_workspace_bytes", "groupnorm_apply",
+    "selftest_wait_timeout", "conv3x3_nhwc", "conv3x3_nhwc_rms", "conv3x3_nhwc_gn", "conv3x3_gn_workspace_bytes", "groupnorm_apply",
     "conv1x1", "rmsnorm_silu", "groupnorm_silu",
     "groupnorm_workspace_bytes", "cast_f16", "mid_attention", "mid_attention_workspace_bytes",
     "Decoder", "pack_conv3x3", "pack_conv1x1",
@@ -62,6 +62,7 @@ SIGNATURES = {
     "vae_conv3d_causal_ndhwc": ([_P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _P], _I),
     "vae_pack_subpixel_weights": ([_P, _I, _I, _P, _P], _I),
     "vae_conv1x1": ([_P, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _P], _I),
+    "vae_conv3x3_nhwc_rms": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _F, ctypes.c_uint, _P, _I, _P, _P], _I),
     "vae_conv3x3_gn_workspace_bytes": ([_I, _I, _I, _I, _I, ctypes.c_uint], _SZ),
     "vae_conv3x3_nhwc_gn": ([_P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _F, ctypes.c_uint, _I, _F, _P, _P, _SZ, _P], _I),
     "vae_groupnorm_apply": ([_P, _I, _I, _I, _I, _P, _P, _P, _I, _F, _P, _P], _I),
@@ -226,6 +227,33 @@ def conv3x3_nhwc_gn(x, w, groups: int, bias=None, residual=None, out=None, oscal
                                      float(oscale), flags, int(groups), float(eps), _ptr(stats), _ptr(workspace),
                                      workspace.numel(), _stream(stream)))
     return out, stats
+
+
+def conv3x3_nhwc_rms(x, w, gamma, bias=None, out=None, y=None, oscale: float = 1.0, silu: bool = True,
+                     replicate: bool = False, reflect: bool = False, down: bool = False, stream=None):
+    """3x3 conv with RMS_norm(+SiLU) of each output pixel in its epilogue: f16
+    [n][H][W][cout] (and, if ``y`` is given, the f32 conv output into it)."""
+    import torch
+    _need(x, torch.float16, "x", 4)
+    _need(w, torch.float16, "w", 4)
+    _need(gamma, torch.float32, "gamma", 1)
+    _need(bias, torch.float32, "bias", 1)
+    n, h, wd, cin = x.shape
+    cout = w.shape[0]
+    if tuple(w.shape[1:]) != (3, 3, cin):
+        raise VaeError(-2, f"w has the wrong shape {tuple(w.shape)}")
+    H, W = (h // 2, wd // 2) if down else (h, wd)
+    if out is None:
+        out = torch.empty((n, H, W, cout), dtype=torch.float16, device=x.device)
+    _need(out, torch.float16, "out")
+    _need(y, torch.float32, "y")
+    for t, nm in ((out, "out"), (y, "y")):
+        if t is not None and t.numel() != n * H * W * cout:
+            raise VaeError(-2, f"{nm} must hold [n][{H}][{W}][{cout}], got {tuple(t.shape)}")
+    flags = (PAD_REPLICATE if replicate else 0) | (PAD_REFLECT if reflect else 0) | (DOWNSAMPLE2X if down else 0)
+    _check(lib().vae_conv3x3_nhwc_rms(_ptr(x), n, h, wd, cin, _ptr(w), _ptr(bias), _ptr(y), cout, float(oscale),
+                                      flags, _ptr(gamma), 1 if silu else 0, _ptr(out), _stream(stream)))
+    return out
 
 
 def conv3x3_gn_workspace_bytes(n: int, h: int, w: int, cout: int, groups: int, flags: int = 0) -> int:
@@ -511,12 +539,15 @@ class Decoder:
 
     @staticmethod
     def opts(band_from: int = 0, nbands: int = 0, band_rows: int = 0, guard_log2: int = 8,
-             profile=False, fuse: bool = False, subpixel: bool = False) -> DecodeOpts:
+             profile=False, fuse: Optional[bool] = None, subpixel: bool = False) -> DecodeOpts:
         """profile: False, True (events around every stage) or "fullres" (only around
-        the full-resolution ResNet convs)."""
+        the full-resolution ResNet convs). fuse: None (the library's default: the
+        second RMS_norm of a ResNet fused into its first conv where the staged
+        epilogue applies), True (fused wherever possible), False (separate norms)."""
         prof = (DECODE_PROFILE if profile else 0) | (DECODE_PROFILE_FULLRES if profile == "fullres" else 0)
+        fz = 0 if fuse is None else (DECODE_FUSE_NORM if fuse else DECODE_NO_FUSION)
         return DecodeOpts(band_from, nbands, band_rows, guard_log2,
-                          prof | (DECODE_FUSE_NORM if fuse else 0) | (DECODE_SUBPIXEL_UP if subpixel else 0))
+                          prof | fz | (DECODE_SUBPIXEL_UP if subpixel else 0))
 
     def profile(self):
         """Stage records of the most recent profiled decode, as dicts (synchronises)."""

@@ -2452,6 +2452,34 @@ int vae_conv3x3_nhwc_gn(const void* x_dev, int n, int h_in, int w_in, int cin, c
                                  gn_stats_dev, st);
 }
 
+int vae_conv3x3_nhwc_rms(const void* x_dev, int n, int h_in, int w_in, int cin, const void* w_dev,
+                         const float* bias_dev, float* y_dev, int cout, float oscale, unsigned flags,
+                         const float* gamma_dev, int silu, void* rms_dev, vae_stream_t stream) {
+    clear_error();
+    if (flags & ~static_cast<unsigned>(VAE_PAD_REPLICATE | VAE_PAD_REFLECT | VAE_DOWNSAMPLE2X))
+        return set_error(VAE_ERR_ARG, "vae_conv3x3_nhwc_rms: unsupported flag bits 0x%x", flags);
+    if (rms_dev == nullptr) return set_error(VAE_ERR_ARG, "vae_conv3x3_nhwc_rms: rms_dev must be non-NULL");
+    ConvArgs a{};
+    a.x = x_dev;
+    a.n = n;
+    a.h_in = h_in;
+    a.w_in = w_in;
+    a.cin = cin;
+    a.w = w_dev;
+    a.cout = cout;
+    a.taps = 9;
+    a.bias = bias_dev;
+    a.y = y_dev;
+    a.oscale = oscale;
+    a.rep = (flags & VAE_PAD_REPLICATE) != 0;
+    a.refl = (flags & VAE_PAD_REFLECT) != 0;
+    a.down = (flags & VAE_DOWNSAMPLE2X) != 0;
+    a.rms_out = rms_dev;
+    a.rms_gamma = gamma_dev;
+    a.rms_silu = silu != 0;
+    return conv_run(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int vae_pack_subpixel_weights(const void* w_dev, int cout, int cin, void* w_sub_dev, vae_stream_t stream) {
     clear_error();
     if (!aligned16(w_dev) || !aligned16(w_sub_dev))

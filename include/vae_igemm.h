@@ -132,6 +132,25 @@ int vae_conv3x3_nhwc(const void* x_dev, int n, int h_in, int w_in, int cin,
  * Requirements as vae_conv3x3_nhwc; m >= 1.
  */
 /*
+ * 3x3 conv with RMS_norm(+SiLU) of each output pixel fused into its epilogue
+ * ("qi21_vae.rs" qv_rmsn applied to the conv's output; the decoders use it for
+ * a ResNet's first conv, whose output only feeds that norm):
+ *   v = oscale * sum x~ * w + bias;  rms_dev[p, c] = f16( SiLU?( v[c] * sqrt(C) / max(||v||, 1e-12) * gamma[c] ) )
+ * with the standalone vae_rmsnorm_silu's exact evaluation order (same bits as
+ * vae_conv3x3_nhwc followed by vae_rmsnorm_silu with out_scale 1).
+ *   y_dev     f32 NHWC [n][H][W][cout] also stored when non-NULL, else only rms_dev.
+ *   rms_dev   f16 NHWC [n][H][W][cout]; gamma_dev f32 [cout]; 16-byte aligned.
+ * Requirements as vae_conv3x3_nhwc plus 16 <= cout <= 144, cout % 16 == 0 (one
+ * CTA holds all of a pixel's channels); no residual, no upsample. Flags:
+ * VAE_PAD_REPLICATE, VAE_PAD_REFLECT, VAE_DOWNSAMPLE2X. Rows of >= 128 pixels
+ * with y_dev NULL take the staged two-pass epilogue (TMEM read twice, f16 rows
+ * stored by TMA); other cases keep the pixel's row in registers.
+ */
+int vae_conv3x3_nhwc_rms(const void* x_dev, int n, int h_in, int w_in, int cin, const void* w_dev,
+                         const float* bias_dev, float* y_dev, int cout, float oscale, unsigned flags,
+                         const float* gamma_dev, int silu, void* rms_dev, vae_stream_t stream);
+
+/*
  * Sub-pixel (phase) form of the nearest-2x up conv (an optional speed-up, not
  * on the pages): output (2v+q, 2u+p) reads source rows
  * v + floor((q + ky - 1) / 2), so the three ky taps land on two source rows per
@@ -384,15 +403,14 @@ typedef struct {
  * decode (read back with vae_decode_profile). */
 enum {
     VAE_DECODE_PROFILE = 1,
-    /* Run every RMS_norm as its own kernel (the default); overrides
-     * VAE_DECODE_FUSE_NORM. */
+    /* Run every RMS_norm as its own kernel; overrides VAE_DECODE_FUSE_NORM. */
     VAE_DECODE_NO_FUSION = 2,
-    /* Compute a ResNet's second RMS_norm (+SiLU) in the epilogue of its first
-     * conv where one CTA holds all <= 144 channels of a pixel, instead of
-     * writing the f32 conv output and normalising it in a separate kernel.
-     * Same bits either way. Off by default: on GB300 the per-pixel norm
-     * epilogue takes longer than the conv mainloop it overlaps, and the pair
-     * (conv + separate RMS_norm) measured faster. */
+    /* By default a ResNet's second RMS_norm (+SiLU) is computed in the epilogue
+     * of its first conv where one CTA holds all <= 144 channels of a pixel and
+     * rows are >= 128 pixels wide (two passes over the accumulator in TMEM, f16
+     * rows stored by TMA, no f32 conv output). This flag also fuses it on
+     * narrower images (a register-held pixel row, slower on GB300). Same bits
+     * as the separate norm either way. */
     VAE_DECODE_FUSE_NORM = 4,
     /* Run the up convs in their sub-pixel form (four 2x2 convs with summed
      * weights, see vae_pack_subpixel_weights): 4/9 of their MACs, the weight sums

@@ -200,3 +200,30 @@ def test_subpixel_up_conv_full_size_sampled():
     got = out[0, torch.from_numpy(ys).cuda(), torch.from_numpy(xs).cuda()].cpu().numpy()
     ref = oracle.conv2d_at(np.moveaxis(x[0], -1, 0), wt, b, ys, xs, upsample=True)
     assert rel_err(got, ref) <= CONV_TOL
+
+
+@pytest.mark.parametrize("n,h,w,cin,cout,kw", [
+    (1, 6, 256, 144, 144, {}),                    # staged two-pass epilogue (rows of >= 128 pixels)
+    (1, 5, 200, 64, 64, {}),                      # ragged last tile
+    (2, 9, 40, 32, 48, {}),                       # rows shorter than a tile: the register form
+    (1, 4, 130, 80, 16, {"reflect": True}),
+    (1, 8, 300, 64, 144, {"down": True}),
+])
+@pytest.mark.parametrize("with_y", [False, True])
+def test_conv_with_fused_rmsnorm_is_bit_identical(n, h, w, cin, cout, kw, with_y):
+    """vae_conv3x3_nhwc_rms gives the same bits as vae_conv3x3_nhwc followed by
+    vae_rmsnorm_silu (one shared evaluation order), with and without the f32 output."""
+    torch = torch_mod()
+    case = conv_case(seed=31, n=n, h=h, w=w, cin=cin, cout=cout, name=f"rmsf.{n}.{h}.{w}.{cin}.{cout}")
+    x = to_dev(case["x"])
+    wt = to_dev(vg.pack_conv3x3(case["w"]))
+    b = to_dev(case["b"])
+    gamma = to_dev((1.0 + 0.25 * stream_normal(31, "rmsf.gamma", (cout,))).astype(np.float32))
+    y_ref = vg.conv3x3_nhwc(x, wt, b, **kw)
+    ref = vg.rmsnorm_silu(y_ref.reshape(-1, cout), gamma, silu=True)
+    y = sentinel_like(tuple(y_ref.shape), torch.float32) if with_y else None
+    got = vg.conv3x3_nhwc_rms(x, wt, gamma, b, y=y, silu=True, **kw)
+    vg.sync_status()
+    assert torch.equal(got.reshape(-1, cout), ref)
+    if with_y:
+        assert torch.equal(y, y_ref)

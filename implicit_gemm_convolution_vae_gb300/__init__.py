@@ -541,9 +541,9 @@ class Decoder:
     def opts(band_from: int = 0, nbands: int = 0, band_rows: int = 0, guard_log2: int = 8,
              profile=False, fuse: Optional[bool] = None, subpixel: bool = False) -> DecodeOpts:
         """profile: False, True (events around every stage) or "fullres" (only around
-        the full-resolution ResNet convs). fuse: None (the library's default: the
-        second RMS_norm of a ResNet fused into its first conv where the staged
-        epilogue applies), True (fused wherever possible), False (separate norms)."""
+        the full-resolution ResNet convs). fuse: None (the library's default:
+        separate norms), True (a ResNet's second RMS_norm fused into its first
+        conv wherever one CTA holds a pixel's channels), False (separate norms)."""
         prof = (DECODE_PROFILE if profile else 0) | (DECODE_PROFILE_FULLRES if profile == "fullres" else 0)
         fz = 0 if fuse is None else (DECODE_FUSE_NORM if fuse else DECODE_NO_FUSION)
         return DecodeOpts(band_from, nbands, band_rows, guard_log2,

@@ -200,19 +200,18 @@ struct Exec {
     float guard = 256.f;
     vae_decoder* prof = nullptr;  // non-null: record events around stages
     int prof_only_w = 0;          // > 0: only the 3x3 convs with cin == cout on rows this wide
-    bool fuse_auto = true;        // without VAE_DECODE_NO_FUSION
-    bool fuse_forced = false;     // VAE_DECODE_FUSE_NORM without VAE_DECODE_NO_FUSION
+    bool fuse = false;            // VAE_DECODE_FUSE_NORM without VAE_DECODE_NO_FUSION
     bool subpix = false;          // VAE_DECODE_SUBPIXEL_UP
-    // A ResNet's second RMS_norm rides in the epilogue of its first conv (whose
-    // f32 output only feeds that norm) when the conv's CTA holds all of a pixel's
-    // channels (one N tile of <= 144). By default only where the staged two-pass
-    // epilogue applies (rows of >= 128 pixels): it writes the f16 rows and no f32
-    // output, and measured faster than the conv plus the separate norm. Forced
-    // (VAE_DECODE_FUSE_NORM) it also takes narrower images, whose epilogue keeps
-    // the pixel's row in registers and is slower. Same bits either way.
+    // With VAE_DECODE_FUSE_NORM a ResNet's second RMS_norm rides in the epilogue
+    // of its first conv (whose f32 output only feeds that norm) when the conv's
+    // CTA holds all of a pixel's channels (one N tile of <= 144): on rows of >= 128
+    // pixels the staged two-pass epilogue (f16 rows only), else a register-held
+    // row. Same bits as the separate norm. Off by default: on GB300 the 1024^2
+    // conv with the staged norm took 0.478 ms against 0.328 + 0.138 ms for the
+    // conv and the separate norm (the epilogue becomes the limit).
     bool fusable(int cout, int w) const {
-        return d->family == VAE_FAMILY_RMS && cout <= 144 && cout % 16 == 0 &&
-               (fuse_forced || (fuse_auto && w >= 128));
+        (void)w;
+        return fuse && d->family == VAE_FAMILY_RMS && cout <= 144 && cout % 16 == 0;
     }
 
     // Starts a profiled stage; returns its record index (or -1).
@@ -478,8 +477,7 @@ int run_decode(Exec& X, int h0, int w0, const vae_decode_opts* opts, const float
     const long long hw0 = static_cast<long long>(h0) * w0;
     int rc;
     X.guard = std::ldexp(1.0f, opts ? (opts->guard_log2 < 0 ? 8 : std::min(opts->guard_log2, 14)) : 8);
-    X.fuse_auto = opts == nullptr || (opts->flags & VAE_DECODE_NO_FUSION) == 0;
-    X.fuse_forced = X.fuse_auto && opts != nullptr && (opts->flags & VAE_DECODE_FUSE_NORM) != 0;
+    X.fuse = opts != nullptr && (opts->flags & VAE_DECODE_FUSE_NORM) != 0 && (opts->flags & VAE_DECODE_NO_FUSION) == 0;
     X.subpix = opts != nullptr && (opts->flags & VAE_DECODE_SUBPIXEL_UP) != 0;
     int nbands = 1;
     if (opts && opts->band_rows > 0) nbands = (hf + opts->band_rows - 1) / opts->band_rows;

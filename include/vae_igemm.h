@@ -403,14 +403,16 @@ typedef struct {
  * decode (read back with vae_decode_profile). */
 enum {
     VAE_DECODE_PROFILE = 1,
-    /* Run every RMS_norm as its own kernel; overrides VAE_DECODE_FUSE_NORM. */
+    /* Run every RMS_norm as its own kernel (the default); overrides
+     * VAE_DECODE_FUSE_NORM. */
     VAE_DECODE_NO_FUSION = 2,
-    /* By default a ResNet's second RMS_norm (+SiLU) is computed in the epilogue
-     * of its first conv where one CTA holds all <= 144 channels of a pixel and
-     * rows are >= 128 pixels wide (two passes over the accumulator in TMEM, f16
-     * rows stored by TMA, no f32 conv output). This flag also fuses it on
-     * narrower images (a register-held pixel row, slower on GB300). Same bits
-     * as the separate norm either way. */
+    /* Compute a ResNet's second RMS_norm (+SiLU) in the epilogue of its first
+     * conv where one CTA holds all <= 144 channels of a pixel (vae_conv3x3_nhwc_rms:
+     * on rows of >= 128 pixels two passes over the accumulator in TMEM with f16
+     * rows stored by TMA, else a register-held pixel row), instead of writing the
+     * f32 conv output and normalising it in a separate kernel. Same bits either
+     * way. Off by default: on GB300 the conv with the norm in its epilogue takes
+     * longer than the conv plus the separate norm. */
     VAE_DECODE_FUSE_NORM = 4,
     /* Run the up convs in their sub-pixel form (four 2x2 convs with summed
      * weights, see vae_pack_subpixel_weights): 4/9 of their MACs, the weight sums

@@ -174,10 +174,9 @@ def test_host_buffer_decode_matches_device_decode():
 @pytest.mark.parametrize("widths,nres,hw", [((64, 32, 32, 16), 2, (12, 10)), ((1152, 576, 288, 144), 3, (16, 16)),
                                             ((1152, 576, 288, 144), 2, (20, 18))])
 def test_fused_norms_are_bit_identical_to_separate_norms(widths, nres, hw):
-    """RMS_norm fused into the producing conv's epilogue (the default staged
-    two-pass form on rows of >= 128 pixels, and the forced register form
-    everywhere) gives the same bits as the standalone RMS_norm kernel (one
-    shared evaluation order)."""
+    """RMS_norm fused into the producing conv's epilogue (the staged two-pass
+    form on rows of >= 128 pixels, the register form on narrower ones) gives the
+    same bits as the standalone RMS_norm kernel (one shared evaluation order)."""
     torch = torch_mod()
     dec = qwen_decoder(seed=7, widths=widths, nres=nres)
     z = latent_channel_stats(7, 16, *hw)

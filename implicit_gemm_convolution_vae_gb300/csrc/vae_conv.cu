@@ -1700,7 +1700,8 @@ __device__ void pair_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
     drain_wait(smem_u32(s.drain), 0u, p);
 }
 
-__device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane, int rank) {
+__device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane, int rank,
+                              const CUtensorMap* mapY) {
     const int row = ew * 32 + lane;
     int accbuf = 0;
     uint32_t accphase = 0;
@@ -1721,6 +1722,8 @@ __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
             tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
         if (p.rms_out != nullptr) {
             epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
+        } else if (p.epi_tma) {
+            epilogue_tma_row<false>(p, ti, tbase, v, u, q, pp, pix, s.stg, mapY, ew, lane, valid);
         } else {
             epilogue_plain_row<true>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
         }
@@ -1730,12 +1733,13 @@ __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         accbuf ^= 1;
         if (accbuf == 0) accphase ^= 1u;
     }
+    if (p.epi_tma && lane == 0) bulk_wait_all();  // boxes read and written before the CTA exits
 }
 
 template <int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     conv_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                     const ConvParams p) {
+                     const __grid_constant__ CUtensorMap mapY, const ConvParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve(smem_raw, p);
     const int warp = threadIdx.x / 32;
@@ -1772,6 +1776,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     if (warp == kProducerWarp && lane == 0) {
         tma_prefetch_desc(&mapA);
         tma_prefetch_desc(&mapB);
+        if (p.epi_tma) tma_prefetch_desc(&mapY);
     }
     tc_fence_before();
     __syncthreads();
@@ -1780,7 +1785,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const uint32_t tmem_base = *s.tmem_slot;
 
     if (warp < kEpiWarps) {
-        pair_epilogue(p, s, tmem_base, warp, lane, rank);
+        pair_epilogue(p, s, tmem_base, warp, lane, rank, &mapY);
     } else if (warp == kProducerWarp) {
         if (lane == 0) pair_producer<kMode>(p, s, &mapA, &mapB, rank);
     } else if (warp == kMmaWarp) {
@@ -1852,8 +1857,8 @@ int choose_bn(int cout, bool halo3) {
 }
 
 template <int kMode>
-int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, size_t smem, int grid,
-                cudaStream_t stream) {
+int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my, size_t smem,
+                int grid, cudaStream_t stream) {
     static bool attr_set[64] = {false};
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
@@ -1862,7 +1867,7 @@ int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& m
             cudaFuncSetAttribute(conv_pair_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set[dev] = true;
     }
-    conv_pair_kernel<kMode><<<grid, 192, smem, stream>>>(ma, mb, p);
+    conv_pair_kernel<kMode><<<grid, 192, smem, stream>>>(ma, mb, my, p);
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -2202,61 +2207,16 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         }
     }
     const int grid = static_cast<int>(std::min<long long>(total, nsm));
-    // CTA pairs (cta_group::2) are correct and tested but measured 3-6 % slower
-    // than single CTAs on GB300 at every decoder shape, so they run only when
-    // requested (VAE_CONV_CTA_PAIR=1 in the environment).
-    if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2 &&
-        a.taps != 27 && !a.subpix && !a.refl && !a.down && a.gn_part == nullptr) {
-        // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
-        p.pair = 1;
-        p.rem16 = 0;  // the pair kernel loads zero-filled 64-channel remainder boxes
-        p.epi_tma = 0;
-        p.ks = 1;
-        p.b_rows = p.BN / 2;
-        p.typ_tiles = (p.tiles_y + 1) / 2;
-        const long long pt = static_cast<long long>(p.n) * p.typ_tiles * p.npar * p.tiles_x * p.n_tiles;
-        if (pt >= (1LL << 31)) return set_error(VAE_ERR_SHAPE, "conv: too many tiles");
-        p.pair_tiles = static_cast<int>(pt);
-        const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(wtaps),
-                                  static_cast<uint64_t>(a.cout)};
-        const uint64_t strides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(wtaps) * a.cin * 2};
-        const uint32_t box[3] = {static_cast<uint32_t>(kBK), 1u, static_cast<uint32_t>(p.b_rows)};
-        rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, dims, strides, box,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
-        if (rc != VAE_OK) return rc;
-        size_t smem;
-        const int pst3 = (kMaxSmem - 1024 - kTail) / (kHaloBytes + 3 * p.b_rows * 128);
-        if (mode == kModeHalo && pst3 >= 3) {
-            p.ks = 3;  // three-tap stages, as in the single-CTA kernel
-            p.stages = std::min(kMaxStages, pst3);
-            p.a_stages = p.stages;
-            smem = 1024 + static_cast<size_t>(p.stages) * (kHaloBytes + 3 * p.b_rows * 128) + kTail;
-        } else if (mode == kModeHalo) {
-            p.a_stages = 4;
-            p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail - p.a_stages * kHaloBytes) / (p.b_rows * 128));
-            smem = 1024 + static_cast<size_t>(p.a_stages) * kHaloBytes + static_cast<size_t>(p.stages) * p.b_rows * 128 +
-                   kTail;
-        } else {
-            const int sb = kABytes + p.b_rows * 128;
-            p.stages = std::min(kMaxStages, (kMaxSmem - 1024 - kTail) / sb);
-            smem = 1024 + static_cast<size_t>(p.stages) * sb + kTail;
-        }
-        const int pgrid = 2 * static_cast<int>(std::min<long long>(pt, nsm / 2));
-        return mode == kModeHalo ? launch_pair<kModeHalo>(p, ma, mb, smem, pgrid, stream)
-                                 : launch_pair<kModeTma>(p, ma, mb, smem, pgrid, stream);
-    }
-    size_t ring = mode == kModeHalo
-                      ? static_cast<size_t>(p.a_stages) * kHaloBytes + static_cast<size_t>(p.stages) * p.ks * p.BN * 128
-                      : static_cast<size_t>(p.stages) * p.ks * (kABytes + p.BN * 128);
-    // Staged TMA epilogue: a 128-pixel row segment, plain f32 output written
-    // whole (no residual) or added onto itself (residual == y, no SiLU after).
-    // The add-reduction keeps the register path's rounding order only without
-    // upsampling and DupUp (whose add comes after the residual's).
+    // The staged TMA epilogue's output view: a 128-pixel row segment, plain f32
+    // output written whole (no residual) or added onto itself (residual == y, no
+    // SiLU after). The add-reduction keeps the register path's rounding order
+    // only without upsampling and DupUp (whose add comes after the residual's).
     const bool res_self = a.residual != nullptr && a.residual == a.y && !a.silu && !p.up && a.dup_src == nullptr;
-    if (mode != kModeGather && p.R == 1 && p.Wt == kBM && !p.out_f16 && !p.out_nchw && a.rms_out == nullptr &&
-        a.cout % 16 == 0 && a.y != nullptr && aligned16(a.y) &&
-        (a.residual == nullptr || res_self || a.gn_part != nullptr) &&
-        1024 + ring + kEpiWarps * kStgBytes + kTail <= kMaxSmem) {
+    auto encode_epi = [&]() -> bool {
+        if (!(mode != kModeGather && p.R == 1 && p.Wt == kBM && !p.out_f16 && !p.out_nchw && a.rms_out == nullptr &&
+              a.cout % 16 == 0 && a.y != nullptr && aligned16(a.y) &&
+              (a.residual == nullptr || res_self || a.gn_part != nullptr)))
+            return false;
         int erc;
         if (p.up) {  // y viewed as (channel, column parity, W/2, row, image)
             const uint64_t dims[5] = {static_cast<uint64_t>(a.cout), 2u, static_cast<uint64_t>(p.W / 2),
@@ -2276,11 +2236,65 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
             erc = encode_tiled(&my, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.y, dims, strides, box,
                                CU_TENSOR_MAP_SWIZZLE_64B);
         }
-        if (erc == VAE_OK)  // with statistics the values are needed in registers: the residual is read, not added
-            p.epi_tma = res_self && a.gn_part == nullptr ? 2 : 1;
-        else
+        if (erc != VAE_OK) {
             clear_error();
+            return false;
+        }
+        return true;
+    };
+    // CTA pairs (cta_group::2) are correct and tested but measured 3-6 % slower
+    // than single CTAs on GB300 at every decoder shape, so they run only when
+    // requested (VAE_CONV_CTA_PAIR=1 in the environment).
+    if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2 &&
+        a.taps != 27 && !a.subpix && !a.refl && !a.down && a.gn_part == nullptr) {
+        // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
+        p.pair = 1;
+        p.rem16 = 0;  // the pair kernel loads zero-filled 64-channel remainder boxes
+        p.epi_tma = 0;
+        p.bias_smem = 0;
+        const size_t stg = encode_epi() ? static_cast<size_t>(kEpiWarps) * kStgBytes : 0;
+        if (stg) p.epi_tma = res_self ? 2 : 1;
+        p.ks = 1;
+        p.b_rows = p.BN / 2;
+        p.typ_tiles = (p.tiles_y + 1) / 2;
+        const long long pt = static_cast<long long>(p.n) * p.typ_tiles * p.npar * p.tiles_x * p.n_tiles;
+        if (pt >= (1LL << 31)) return set_error(VAE_ERR_SHAPE, "conv: too many tiles");
+        p.pair_tiles = static_cast<int>(pt);
+        const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(wtaps),
+                                  static_cast<uint64_t>(a.cout)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(wtaps) * a.cin * 2};
+        const uint32_t box[3] = {static_cast<uint32_t>(kBK), 1u, static_cast<uint32_t>(p.b_rows)};
+        rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != VAE_OK) return rc;
+        size_t smem;
+        const int room = kMaxSmem - 1024 - kTail - static_cast<int>(stg);
+        const int pst3 = room / (kHaloBytes + 3 * p.b_rows * 128);
+        if (mode == kModeHalo && pst3 >= 3) {
+            p.ks = 3;  // three-tap stages, as in the single-CTA kernel
+            p.stages = std::min(kMaxStages, pst3);
+            p.a_stages = p.stages;
+            smem = 1024 + static_cast<size_t>(p.stages) * (kHaloBytes + 3 * p.b_rows * 128) + stg + kTail;
+        } else if (mode == kModeHalo) {
+            p.a_stages = 4;
+            p.stages = std::min(kMaxStages, (room - p.a_stages * kHaloBytes) / (p.b_rows * 128));
+            smem = 1024 + static_cast<size_t>(p.a_stages) * kHaloBytes + static_cast<size_t>(p.stages) * p.b_rows * 128 +
+                   stg + kTail;
+        } else {
+            const int sb = kABytes + p.b_rows * 128;
+            p.stages = std::min(kMaxStages, room / sb);
+            smem = 1024 + static_cast<size_t>(p.stages) * sb + stg + kTail;
+        }
+        const int pgrid = 2 * static_cast<int>(std::min<long long>(pt, nsm / 2));
+        return mode == kModeHalo ? launch_pair<kModeHalo>(p, ma, mb, my, smem, pgrid, stream)
+                                 : launch_pair<kModeTma>(p, ma, mb, my, smem, pgrid, stream);
     }
+    size_t ring = mode == kModeHalo
+                      ? static_cast<size_t>(p.a_stages) * kHaloBytes + static_cast<size_t>(p.stages) * p.ks * p.BN * 128
+                      : static_cast<size_t>(p.stages) * p.ks * (kABytes + p.BN * 128);
+    if (1024 + ring + kEpiWarps * kStgBytes + kTail <= kMaxSmem && encode_epi())
+        // with statistics the values are needed in registers: the residual is read, not added
+        p.epi_tma = res_self && a.gn_part == nullptr ? 2 : 1;
     // Fused RMS_norm with f16 rows only (a ResNet's first conv): staged f16 TMA boxes.
     if (mode != kModeGather && !p.epi_tma && a.rms_out != nullptr && a.y == nullptr && a.residual == nullptr &&
         a.dup_src == nullptr && !p.up && p.R == 1 && p.Wt == kBM && p.n_tiles == 1 && a.cout % 16 == 0 &&

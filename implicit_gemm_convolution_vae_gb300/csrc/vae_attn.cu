@@ -39,8 +39,13 @@ namespace vae {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStageBytes = 64 * 1024;  // scores: two (Q, K) 64-channel chunk pairs; PV: a 64-key P half + V^T half
+constexpr int kStageBytes = 64 * 1024;  // PV: a 64-key P half + V^T half
 constexpr int kStages = 3;
+// scores: one 64-channel chunk of Q (128 rows) and of K (256 keys) per stage
+constexpr int kScStageBytes = 48 * 1024;
+constexpr int kScStages = 4;
+static_assert(kScStages * kScStageBytes <= kStages * kStageBytes, "scores ring over the shared ring bytes");
+constexpr int kRingBars = 4;  // barrier slots of each ring array
 static_assert(1024 + kStages * kStageBytes + 256 <= 232448, "attention shared memory over 227 KB");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxDv = 384;
@@ -92,7 +97,7 @@ __device__ __forceinline__ void st_v8_b32(void* dst, const uint32_t (&v)[8]) {
 
 struct ASmem {
     uint8_t* ring;
-    uint64_t *full, *empty;    // [kStages]
+    uint64_t *full, *empty;    // [kRingBars]
     uint64_t *s_full, *s_free;  // [2] (scores)
     uint64_t* resc_ready;       // (PV) MMAs up to PV(j-1) done before a flagged block j
     uint64_t* scaled;           // (PV) O scaled by alpha_j
@@ -108,8 +113,8 @@ __device__ __forceinline__ ASmem carve_attn(uint8_t* raw) {
     s.ring = base;
     uint64_t* b = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes);
     s.full = b;
-    s.empty = b + kStages;
-    s.s_full = b + 2 * kStages;
+    s.empty = b + kRingBars;
+    s.s_full = b + 2 * kRingBars;
     s.s_free = s.s_full + 2;
     s.resc_ready = s.s_free + 2;
     s.scaled = s.resc_ready + 1;
@@ -131,12 +136,13 @@ __device__ __forceinline__ bool wwait_(uint64_t* bar, uint32_t parity, const ASm
     return warp_all(wait_(bar, parity, s, st, timeout));
 }
 
-// Ring bookkeeping shared by the producers and MMA threads.
-struct Ring {
+// Ring bookkeeping shared by the producers and MMA threads (N slots).
+template <int N>
+struct RingT {
     int stage = 0;
     uint32_t phase = 0, armed = 0, arm_par = 0;
     __device__ __forceinline__ void next() {
-        if (++stage == kStages) {
+        if (++stage == N) {
             stage = 0;
             phase ^= 1u;
         }
@@ -148,11 +154,12 @@ struct Ring {
     // Lets every copy this thread started land before the CTA can exit.
     __device__ __forceinline__ void drain(const ASmem& s, DevStatus* st, unsigned long long timeout) const {
         int never = 0;
-        for (int i = 0; i < kStages; ++i)
+        for (int i = 0; i < N; ++i)
             if (armed & (1u << i))
                 (void)mbar_wait(smem_u32(&s.full[i]), (arm_par >> i) & 1u, &never, timeout, st, kWhereDrain);
     }
 };
+using Ring = RingT<kStages>;
 
 __device__ __forceinline__ void mma_drain(const ASmem& s, DevStatus* st, unsigned long long timeout) {
     umma_commit(smem_u32(s.drain));
@@ -165,53 +172,49 @@ __device__ __forceinline__ void mma_drain(const ASmem& s, DevStatus* st, unsigne
 __device__ void scores_producer(const ScoreParams& p, const ASmem& s, const CUtensorMap* mq, const CUtensorMap* mk,
                                 int q0) {
     const uint64_t pol = policy_evict_normal();
-    Ring r;
-    for (int j = 0; j < p.nkb; ++j)
-        for (int cc = 0; cc < p.nchunk_c; cc += 2) {
+    RingT<kScStages> r;
+    const int npair = (p.nkb + 1) / 2;
+    for (int jj = 0; jj < npair; ++jj)  // 256 keys per pass: each Q chunk serves two key blocks
+        for (int cc = 0; cc < p.nchunk_c; ++cc) {
             if (!wait_(&s.empty[r.stage], r.phase ^ 1u, s, p.status, p.timeout_ns)) {
                 r.drain(s, p.status, p.timeout_ns);
                 return;
             }
-            const int nck = min(2, p.nchunk_c - cc);
             const uint32_t fb = smem_u32(&s.full[r.stage]);
-            mbar_arrive_expect_tx(fb, 32768u * static_cast<uint32_t>(nck));
+            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(kScStageBytes));
             r.arm();
-            uint8_t* st = s.ring + r.stage * kStageBytes;
-            for (int h = 0; h < nck; ++h) {
-                tma_load_2d(smem_u32(st + h * 32768), mq, fb, (cc + h) * 64, q0, pol);
-                tma_load_2d(smem_u32(st + h * 32768 + 16384), mk, fb, (cc + h) * 64, j * 128, pol);
-            }
+            uint8_t* st = s.ring + r.stage * kScStageBytes;
+            tma_load_2d(smem_u32(st), mq, fb, cc * 64, q0, pol);
+            tma_load_2d(smem_u32(st + 16384), mk, fb, cc * 64, jj * 256, pol);  // keys >= m read as zeros
             r.next();
         }
     r.drain(s, p.status, p.timeout_ns);
 }
 
 __device__ void scores_mma(const ScoreParams& p, const ASmem& s, uint32_t tmem) {
-    const uint32_t id_s = idesc_f16_f32(128, 128);
-    Ring r;
+    const uint32_t id_s = idesc_f16_f32(128, 256);
+    RingT<kScStages> r;
     bool ok = true;
-    for (int j = 0; j < p.nkb && ok; ++j) {
-        const int b = j & 1;
-        if (j >= 2) {  // the softmax has read S(j - 2) out of this buffer
-            if (!wait_(&s.s_free[b], static_cast<uint32_t>(((j - 2) >> 1) & 1), s, p.status, p.timeout_ns)) break;
+    const int npair = (p.nkb + 1) / 2;
+    for (int jj = 0; jj < npair && ok; ++jj) {
+        const int b = jj & 1;
+        if (jj >= 2) {  // the softmax has read S(jj - 2) out of this buffer
+            if (!wait_(&s.s_free[b], static_cast<uint32_t>(((jj - 2) >> 1) & 1), s, p.status, p.timeout_ns)) break;
             tc_fence_after();
         }
-        for (int cc = 0; cc < p.nchunk_c; cc += 2) {
+        for (int cc = 0; cc < p.nchunk_c; ++cc) {
             if (!wait_(&s.full[r.stage], r.phase, s, p.status, p.timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint8_t* st = s.ring + r.stage * kStageBytes;
-            const int nck = min(2, p.nchunk_c - cc);
-            for (int h = 0; h < nck; ++h) {
-                const uint64_t ad = sw128_kmajor_desc(smem_u32(st + h * 32768));
-                const uint64_t bd = sw128_kmajor_desc(smem_u32(st + h * 32768 + 16384));
+            uint8_t* st = s.ring + r.stage * kScStageBytes;
+            const uint64_t ad = sw128_kmajor_desc(smem_u32(st));
+            const uint64_t bd = sw128_kmajor_desc(smem_u32(st + 16384));
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    umma_f16(tmem + static_cast<uint32_t>(b * 128), ad + 2 * k, bd + 2 * k, id_s,
-                             (cc | h | k) != 0 ? 1u : 0u);
-            }
+            for (int k = 0; k < 4; ++k)  // S(128 x 256) += Q_c K_c^T, K = 16 per step
+                umma_f16(tmem + static_cast<uint32_t>(b * 256), ad + static_cast<uint64_t>(2 * k),
+                         bd + static_cast<uint64_t>(2 * k), id_s, (cc | k) != 0 ? 1u : 0u);
             umma_commit(smem_u32(&s.empty[r.stage]));
             r.next();
         }
@@ -220,38 +223,38 @@ __device__ void scores_mma(const ScoreParams& p, const ASmem& s, uint32_t tmem) 
     mma_drain(s, p.status, p.timeout_ns);
 }
 
+// One thread per query row. Per pass of 256 keys (two key blocks): the row max
+// from a first read of S, the rescale decision (the running max moves only when
+// the new one exceeds it by more than 2^8, so P = 2^(s - m) <= 256 fits f16),
+// then a second read of S for P (f16), the row sum and the per-block rescale
+// factors and flags the PV kernel replays (the pass's second block never
+// rescales).
 __device__ void scores_softmax(const ScoreParams& p, const ASmem& s, uint32_t tmem, int warp, int lane, int tl) {
     const int r = warp * 32 + lane;
     const int row = tl * 128 + r;  // row of the group buffers
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     __half* prow = p.p + static_cast<size_t>(row) * p.kcols;
     float m_run = -INFINITY, l = 0.f;
-    for (int j = 0; j < p.nkb; ++j) {
-        const int b = j & 1;
-        if (!wwait_(&s.s_full[b], static_cast<uint32_t>((j >> 1) & 1), s, p.status, p.timeout_ns)) return;
+    const int npair = (p.nkb + 1) / 2;
+    for (int jj = 0; jj < npair; ++jj) {
+        const int b = jj & 1;
+        if (!wwait_(&s.s_full[b], static_cast<uint32_t>((jj >> 1) & 1), s, p.status, p.timeout_ns)) return;
         tc_fence_after();
-        float sv[128];
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
+        const int kbase = jj * 256;
+        const uint32_t sb = tmem + lane_off + static_cast<uint32_t>(b * 256);
+        float mx = -INFINITY;
+        for (int g = 0; g < 16; ++g) {
             uint32_t rr[16];
             __syncwarp();
-            tmem_ld16(tmem + lane_off + static_cast<uint32_t>(b * 128 + g * 16), rr);
+            tmem_ld16(sb + static_cast<uint32_t>(g * 16), rr);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) sv[g * 16 + i] = __uint_as_float(rr[i]);
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&s.s_free[b]));
-        const int nvalid = min(128, p.m - j * 128);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 128; ++i) {
-            sv[i] = i < nvalid ? sv[i] * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, sv[i]);
+            for (int i = 0; i < 16; ++i)
+                if (kbase + g * 16 + i < p.m) mx = fmaxf(mx, __uint_as_float(rr[i]) * p.scale_log2);
         }
         float alpha = 1.f;
         bool resc = false;
-        if (j == 0) {
+        if (jj == 0) {
             m_run = mx;
         } else if (mx > m_run + 8.f) {
             alpha = exp2f(m_run - mx);
@@ -259,25 +262,37 @@ __device__ void scores_softmax(const ScoreParams& p, const ASmem& s, uint32_t tm
             resc = true;
         }
         const bool any = __any_sync(0xffffffffu, resc);
-        if (j >= 1) {
-            p.alpha[static_cast<size_t>(j) * p.grows + row] = alpha;
-            if (lane == 0) p.flags[(static_cast<size_t>(tl) * p.nkb + j) * 4 + warp] = any ? 1u : 0u;
+        const int j0 = 2 * jj, j1 = 2 * jj + 1;
+        if (j0 >= 1) {
+            p.alpha[static_cast<size_t>(j0) * p.grows + row] = alpha;
+            if (lane == 0) p.flags[(static_cast<size_t>(tl) * p.nkb + j0) * 4 + warp] = any ? 1u : 0u;
+        }
+        if (j1 < p.nkb) {
+            p.alpha[static_cast<size_t>(j1) * p.grows + row] = 1.f;
+            if (lane == 0) p.flags[(static_cast<size_t>(tl) * p.nkb + j1) * 4 + warp] = 0u;
         }
         l *= alpha;
         float sum = 0.f;
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
+        const int ngr = min(16, (p.nkb * 128 - kbase) / 16);  // 16-key groups with P columns
+        for (int g = 0; g < ngr; ++g) {
+            uint32_t rr[16];
+            __syncwarp();
+            tmem_ld16(sb + static_cast<uint32_t>(g * 16), rr);
+            tmem_ld_wait();
             uint32_t h[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float a = exp2f(sv[g * 16 + 2 * i] - m_run);
-                const float c = exp2f(sv[g * 16 + 2 * i + 1] - m_run);
+                const int key = kbase + g * 16 + 2 * i;
+                const float a = key < p.m ? exp2f(__uint_as_float(rr[2 * i]) * p.scale_log2 - m_run) : 0.f;
+                const float c = key + 1 < p.m ? exp2f(__uint_as_float(rr[2 * i + 1]) * p.scale_log2 - m_run) : 0.f;
                 sum += a + c;
                 __half2 t = __floats2half2_rn(a, c);
                 h[i] = *reinterpret_cast<uint32_t*>(&t);
             }
-            st_v8_b32(prow + j * 128 + g * 16, h);
+            st_v8_b32(prow + kbase + g * 16, h);
         }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s.s_free[b]));
         l += sum;
     }
     p.lsum[row] = l;
@@ -293,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q0 = (p.q_tile0 + tl) * 128;
     if (threadIdx.x == 0) {
         *s.abort_flag = 0;
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kScStages; ++i) {
             mbar_init(smem_u32(&s.full[i]), 1u);
             mbar_init(smem_u32(&s.empty[i]), 1u);
         }
@@ -617,7 +632,8 @@ static int attn_core_run(const __half* q, const __half* k, const __half* vt, int
         const uint32_t box[2] = {64u, 128u};
         rc = encode_tiled(&mq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, q, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != VAE_OK) return rc;
-        rc = encode_tiled(&mk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, k, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        const uint32_t kbox[2] = {64u, 256u};  // two key blocks per box
+        rc = encode_tiled(&mk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, k, dims, strides, kbox, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != VAE_OK) return rc;
     }
     {

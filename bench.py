@@ -170,6 +170,23 @@ def cores_used():
     return os.cpu_count() or 1
 
 
+def reduce_max(x: float, dist) -> float:
+    """The maximum of x over all ranks (x itself without a process group): the
+    job's time is its slowest rank's."""
+    if dist is None:
+        return x
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_unit: float, units_per_rank: int, world: int, seconds: float) -> float:
+    """Throughput of the whole job: the units every rank processed over the slowest rank's time."""
+    return flops_per_unit * units_per_rank * world / seconds / 1e12
+
+
 def run_reference(args, rank):
     if rank != 0:
         return
@@ -402,12 +419,9 @@ def main():
     clocks = clock_sampler_stop(cp, cf, clk_path, local)
     vg.sync_status()
     recs = D.profile()
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(ms, dist)
     ms_step = ms / args.steps
-    value = step_flops * args.steps * world / (ms / 1e3) / 1e12
+    value = whole_job_tflops(step_flops, args.steps, world, ms / 1e3)
 
     # the roofline kernel from the events recorded inside the timed region
     sust, burst, hbm, src = peaks()
@@ -455,11 +469,8 @@ def main():
         D.decode_host(zh, oh, ws2)
     torch.cuda.synchronize()
     t_e2e = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([t_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_e2e = float(t.item())
-    e2e_val = step_flops * args.steps * world / t_e2e / 1e12
+    t_e2e = reduce_max(t_e2e, dist)
+    e2e_val = whole_job_tflops(step_flops, args.steps, world, t_e2e)
 
     # The opt-in sub-pixel form of the up convs (it changes the rounding, so it is
     # reported beside the contract's number, not as it): device decodes, events.

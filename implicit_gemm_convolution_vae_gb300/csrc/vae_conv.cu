@@ -2242,7 +2242,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         }
         return true;
     };
-    // CTA pairs (cta_group::2) are correct and tested but measured 3-6 % slower
+    // CTA pairs (cta_group::2) are correct and tested but measured 22-30 % slower
     // than single CTAs on GB300 at every decoder shape, so they run only when
     // requested (VAE_CONV_CTA_PAIR=1 in the environment).
     if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2 &&

@@ -121,6 +121,21 @@ def clock_sampler_stop(p, f, path, gpu_index):
             "samples": len(sm)}
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the conv kernel's sources (csrc/vae_conv.cu, vae_common.cuh,
+    vae_conv.h, in that order) with C++ comments and blank space removed, so
+    that edits to comments alone keep a capture valid."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for f in ("vae_conv.cu", "vae_common.cuh", "vae_conv.h"):
+        src = open(os.path.join(ROOT, "implicit_gemm_convolution_vae_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update(re.sub(r"\s+", "", src).encode())
+    return h.hexdigest()
+
+
 def traffic_from_profiles():
     """DRAM bytes per launch of the dominant conv from the committed ncu summary,
     if it was taken on the current kernel source (else None)."""
@@ -133,10 +148,7 @@ def traffic_from_profiles():
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    h = hashlib.sha256()
-    for f in ("vae_conv.cu", "vae_common.cuh", "vae_conv.h"):
-        h.update(open(os.path.join(ROOT, "implicit_gemm_convolution_vae_gb300", "csrc", f), "rb").read())
-    if kv.get("kernel_source_sha256") != h.hexdigest():
+    if kv.get("kernel_source_sha256") != kernel_source_hash():
         return None
     try:
         return float(kv["dram_bytes_per_launch"])

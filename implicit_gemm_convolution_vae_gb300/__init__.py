@@ -24,7 +24,7 @@ __all__ = [
     "selftest_wait_timeout", "conv3x3_nhwc", "conv3x3_nhwc_rms", "conv3x3_nhwc_gn", "conv3x3_gn_workspace_bytes", "groupnorm_apply",
     "conv1x1", "rmsnorm_silu", "groupnorm_silu",
     "groupnorm_workspace_bytes", "cast_f16", "mid_attention", "mid_attention_workspace_bytes",
-    "Decoder", "pack_conv3x3", "pack_conv1x1",
+    "Decoder", "DecodeGraph", "pack_conv3x3", "pack_conv1x1",
     "UPSAMPLE2X", "PAD_REPLICATE", "PAD_REFLECT", "DOWNSAMPLE2X", "EPI_SILU", "OUT_F16", "FAMILY_GN", "FAMILY_RMS",
     "NORM_GROUP", "NORM_RMS",
 ]
@@ -79,6 +79,9 @@ SIGNATURES = {
     "vae_decode": ([_P, _P, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "vae_decode_host": ([_P, _P, _I, _I, _P, _P, _P, _SZ, _P], _I),
     "vae_decode_profile": ([_P, _P, _I, ctypes.POINTER(_I)], _I),
+    "vae_decode_graph_create": ([_P, _P, _I, _I, _P, _P, _P, _SZ, _P, ctypes.POINTER(_P)], _I),
+    "vae_decode_graph_launch": ([_P, _P], _I),
+    "vae_decode_graph_destroy": ([_P], _I),
 }
 
 
@@ -565,6 +568,18 @@ class Decoder:
                                           ctypes.byref(n)))
         return int(n.value)
 
+    def graph(self, z, out, workspace, opts: Optional[DecodeOpts] = None, stream=None) -> "DecodeGraph":
+        """Capture the decode of ``z`` into ``out`` (both CUDA, fixed from now on) as a
+        CUDA graph; ``DecodeGraph.launch()`` replays it. Runs one eager decode first."""
+        import torch
+        _need(z, torch.float32, "z", 3)
+        _need(out, torch.float32, "out", 3)
+        zc, h0, w0 = z.shape
+        g = _P()
+        _check(lib().vae_decode_graph_create(self._h, _ptr(z), h0, w0, _ptr(out), ctypes.byref(opts) if opts else None,
+                                             _ptr(workspace), workspace.numel(), _stream(stream), ctypes.byref(g)))
+        return DecodeGraph(g, (z, out, workspace))
+
     def decode(self, z, out=None, opts: Optional[DecodeOpts] = None, workspace=None, stream=None):
         """z f32 [zc][h0][w0] (CUDA) -> out f32 [nch][h0<<ups][w0<<ups] (CUDA)."""
         import torch
@@ -602,3 +617,19 @@ class Decoder:
             self.close()
         except Exception:
             pass
+
+
+class DecodeGraph:
+    """A captured decode (see ``Decoder.graph``); keeps its buffers alive."""
+
+    def __init__(self, handle, keep):
+        self._g = handle
+        self._keep = keep
+
+    def launch(self, stream=None):
+        _check(lib().vae_decode_graph_launch(self._g, _stream(stream)))
+
+    def __del__(self):
+        if getattr(self, "_g", None) is not None and _LIB is not None:
+            lib().vae_decode_graph_destroy(self._g)
+            self._g = None

@@ -807,4 +807,80 @@ int vae_decode_host(vae_decoder_t dec, const float* z_host, int h0, int w0, floa
                        reinterpret_cast<cudaStream_t>(stream), true);
 }
 
+struct vae_decode_graph {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+int vae_decode_graph_create(vae_decoder_t dec, const float* z_dev, int h0, int w0, float* out_dev,
+                            const vae_decode_opts* opts, void* workspace_dev, size_t workspace_bytes,
+                            vae_stream_t stream, vae_decode_graph_t* graph) {
+    clear_error();
+    if (graph == nullptr) return set_error(VAE_ERR_ARG, "decode_graph_create: NULL graph");
+    *graph = nullptr;
+    if (opts != nullptr && (opts->flags & VAE_DECODE_PROFILE))
+        return set_error(VAE_ERR_ARG, "decode_graph_create: a captured decode records no profile events");
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // One eager decode first: it validates everything and performs the one-time
+    // per-kernel set-up, so the capture below records kernel launches only.
+    int rc = decode_impl(dec, z_dev, h0, w0, out_dev, opts, workspace_dev, workspace_bytes, st, false);
+    if (rc != VAE_OK) return rc;
+    cudaStream_t cap;
+    VAE_CUDA_CHECK(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking));
+    // the capture stream starts after the eager decode (it reads z and writes the workspace)
+    cudaEvent_t ev;
+    cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(ev, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cap, ev, 0);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(cap);
+    if (ev != nullptr) cudaEventDestroy(ev);
+    if (e != cudaSuccess) {
+        cudaStreamDestroy(cap);
+        return set_error(VAE_ERR_CUDA, "decode_graph_create: %s", cudaGetErrorString(e));
+    }
+    auto* g = new (std::nothrow) vae_decode_graph();
+    if (g == nullptr) {
+        cudaStreamDestroy(cap);
+        return set_error(VAE_ERR_NOMEM, "decode_graph_create: host allocation failed");
+    }
+    e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        rc = decode_impl(dec, z_dev, h0, w0, out_dev, opts, workspace_dev, workspace_bytes, cap, false);
+        const cudaError_t e2 = cudaStreamEndCapture(cap, &g->graph);
+        if (rc == VAE_OK && e2 != cudaSuccess) rc = set_error(VAE_ERR_CUDA, "decode_graph_create: %s",
+                                                              cudaGetErrorString(e2));
+    } else {
+        rc = set_error(VAE_ERR_CUDA, "decode_graph_create: %s", cudaGetErrorString(e));
+    }
+    if (rc == VAE_OK) {
+        e = cudaGraphInstantiate(&g->exec, g->graph, 0);
+        if (e != cudaSuccess) rc = set_error(VAE_ERR_CUDA, "decode_graph_create: instantiate: %s", cudaGetErrorString(e));
+    }
+    cudaStreamDestroy(cap);
+    if (rc != VAE_OK) {
+        if (g->exec != nullptr) cudaGraphExecDestroy(g->exec);
+        if (g->graph != nullptr) cudaGraphDestroy(g->graph);
+        delete g;
+        return rc;
+    }
+    *graph = g;
+    return VAE_OK;
+}
+
+int vae_decode_graph_launch(vae_decode_graph_t graph, vae_stream_t stream) {
+    clear_error();
+    if (graph == nullptr || graph->exec == nullptr) return set_error(VAE_ERR_ARG, "decode_graph_launch: NULL graph");
+    VAE_CUDA_CHECK(cudaGraphLaunch(graph->exec, reinterpret_cast<cudaStream_t>(stream)));
+    return VAE_OK;
+}
+
+int vae_decode_graph_destroy(vae_decode_graph_t graph) {
+    clear_error();
+    if (graph == nullptr) return VAE_OK;
+    if (graph->exec != nullptr) cudaGraphExecDestroy(graph->exec);
+    if (graph->graph != nullptr) cudaGraphDestroy(graph->graph);
+    delete graph;
+    return VAE_OK;
+}
+
 }  // extern "C"

@@ -477,6 +477,25 @@ int vae_decode_host(vae_decoder_t dec, const float* z_host, int h0, int w0, floa
                     const vae_decode_opts* opts, void* workspace_dev, size_t workspace_bytes,
                     vae_stream_t stream);
 
+/*
+ * A decode captured once as a CUDA graph and replayed: the buffers (z_dev,
+ * out_dev, workspace_dev), the sizes and the options are fixed at capture;
+ * every launch reads z_dev and writes out_dev as vae_decode would (same bits).
+ * Replays skip the host's per-kernel work and the launch gaps between the
+ * decode's ~70 kernels, which matters for small frames.
+ * vae_decode_graph_create runs one eager vae_decode on `stream` (validating
+ * every argument and doing the one-time kernel set-up), then captures the
+ * decode on a private stream; no profile flag. The graph may be launched on
+ * any stream of the same device; the caller orders it against other work on
+ * the buffers. Errors as vae_decode; on error *graph is NULL.
+ */
+typedef struct vae_decode_graph* vae_decode_graph_t;
+int vae_decode_graph_create(vae_decoder_t dec, const float* z_dev, int h0, int w0, float* out_dev,
+                            const vae_decode_opts* opts, void* workspace_dev, size_t workspace_bytes,
+                            vae_stream_t stream, vae_decode_graph_t* graph);
+int vae_decode_graph_launch(vae_decode_graph_t graph, vae_stream_t stream);
+int vae_decode_graph_destroy(vae_decode_graph_t graph);
+
 #ifdef __cplusplus
 }
 #endif

@@ -484,6 +484,22 @@ def main():
     t_e2e = reduce_max(t_e2e, dist)
     e2e_val = whole_job_tflops(step_flops, args.steps, world, t_e2e)
 
+    # The same decode replayed as a CUDA graph (no profile events in it).
+    dg = D.graph(z, out, ws2)
+    for _ in range(2):
+        dg.launch()
+    torch.cuda.synchronize()
+    e4 = torch.cuda.Event(enable_timing=True)
+    e5 = torch.cuda.Event(enable_timing=True)
+    e4.record(stream)
+    for _ in range(args.steps):
+        dg.launch()
+    e5.record(stream)
+    torch.cuda.synchronize()
+    vg.sync_status()
+    ms_graph = e4.elapsed_time(e5) / args.steps
+    del dg
+
     # The opt-in sub-pixel form of the up convs (it changes the rounding, so it is
     # reported beside the contract's number, not as it): device decodes, events.
     opts_sp = vg.Decoder.opts(subpixel=True)
@@ -521,6 +537,7 @@ def main():
                        "guard_log2": 8},
             "decode_ms_per_frame": ms_step, "mp_per_s": (h0 * 8) * (w0 * 8) * world / (ms_step / 1e3) / 1e6,
             "decode_ms_per_frame_subpixel_up": ms_sp,
+            "decode_ms_per_frame_graph": ms_graph,
             "frac_of_f16_peak": value / burst,
             "conv3x3_tflops": conv_all["flops"] / (conv_all["ms"] / 1e3) / 1e12,
             "step_tflop": step_flops / 1e12,

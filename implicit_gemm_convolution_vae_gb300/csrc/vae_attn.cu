@@ -39,7 +39,7 @@ namespace vae {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStageBytes = 64 * 1024;  // PV: 64 keys of P for two query tiles + the V^T box
+constexpr int kStageBytes = 64 * 1024;  // PV: a 64-key P half + V^T half
 constexpr int kStages = 3;
 // scores: one 64-channel chunk of Q (128 rows) and of K (256 keys) per stage
 constexpr int kScStageBytes = 48 * 1024;
@@ -48,8 +48,7 @@ static_assert(kScStages * kScStageBytes <= kStages * kStageBytes, "scores ring o
 constexpr int kRingBars = 4;  // barrier slots of each ring array
 static_assert(1024 + kStages * kStageBytes + 256 <= 232448, "attention shared memory over 227 KB");
 constexpr uint32_t kTmemCols = 512;
-constexpr int kMaxDv = 256;   // value channels per PV CTA (each of its two query tiles: 256 TMEM columns)
-constexpr int kPvTiles = 2;   // query tiles per PV CTA: each V^T box serves both
+constexpr int kMaxDv = 384;
 constexpr int kMaxFlagWords = 256;                   // key blocks <= 8192, i.e. m <= 2^20
 constexpr size_t kMaxPBytes = size_t(2) << 30;       // P of one group of query tiles
 constexpr int kPHalfBytes = 128 * 64 * 2;            // 128 query rows x 64 keys
@@ -70,7 +69,6 @@ struct ScoreParams {
 
 struct PvParams {
     int m, c, dv, ndv, nkb;
-    int ntiles;    // query tiles of this group
     int q_tile0, grows;
     int vbox_rows, vboxes;
     const float* alpha;
@@ -358,7 +356,7 @@ __device__ __forceinline__ bool flagged(const uint32_t* fl, int j) { return (fl[
 __device__ void pv_producer(const PvParams& p, const ASmem& s, const CUtensorMap* mp, const CUtensorMap* mv, int tl,
                             int d0) {
     const uint64_t pol = policy_evict_normal();
-    const uint32_t tx = static_cast<uint32_t>(kPvTiles * kPHalfBytes + p.vboxes * p.vbox_rows * 128);
+    const uint32_t tx = static_cast<uint32_t>(kPHalfBytes + p.vboxes * p.vbox_rows * 128);
     Ring r;
     for (int j = 0; j < p.nkb; ++j)
         for (int half = 0; half < 2; ++half) {
@@ -371,18 +369,15 @@ __device__ void pv_producer(const PvParams& p, const ASmem& s, const CUtensorMap
             r.arm();
             uint8_t* st = s.ring + r.stage * kStageBytes;
             const int key0 = j * 128 + half * 64;
-            // P of both query tiles (rows past the group's read as zeros)
-            for (int t = 0; t < kPvTiles; ++t)
-                tma_load_2d(smem_u32(st + t * kPHalfBytes), mp, fb, key0, (tl + t) * 128, pol);
+            tma_load_2d(smem_u32(st), mp, fb, key0, tl * 128, pol);
             for (int b = 0; b < p.vboxes; ++b)
-                tma_load_2d(smem_u32(st + kPvTiles * kPHalfBytes + b * p.vbox_rows * 128), mv, fb, key0,
-                            d0 + b * p.vbox_rows, pol);
+                tma_load_2d(smem_u32(st + kPHalfBytes + b * p.vbox_rows * 128), mv, fb, key0, d0 + b * p.vbox_rows,
+                            pol);
             r.next();
         }
     r.drain(s, p.status, p.timeout_ns);
 }
 
-// O_t (t = 0, 1: the CTA's two query tiles, TMEM columns t * 256 ..) += P_t V.
 __device__ void pv_mma(const PvParams& p, const ASmem& s, uint32_t tmem, const uint32_t* fl) {
     const int nsplit = p.dv > 256 ? 2 : 1;
     const int ns = p.dv / nsplit;
@@ -409,17 +404,13 @@ __device__ void pv_mma(const PvParams& p, const ASmem& s, uint32_t tmem, const u
             }
             tc_fence_after();
             uint8_t* st = s.ring + r.stage * kStageBytes;
+            const uint64_t ad = sw128_kmajor_desc(smem_u32(st));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-#pragma unroll
-                for (int t = 0; t < kPvTiles; ++t) {
-                    const uint64_t ad = sw128_kmajor_desc(smem_u32(st + t * kPHalfBytes));
-                    for (int sp = 0; sp < nsplit; ++sp) {
-                        const uint64_t bd =
-                            sw128_kmajor_desc(smem_u32(st + kPvTiles * kPHalfBytes + sp * ns * 128));
-                        umma_f16(tmem + static_cast<uint32_t>(t * 256 + sp * ns), ad + 2 * k, bd + 2 * k, id_o,
-                                 (j | half | k) != 0 ? 1u : 0u);
-                    }
+                for (int sp = 0; sp < nsplit; ++sp) {
+                    const uint64_t bd = sw128_kmajor_desc(smem_u32(st + kPHalfBytes + sp * ns * 128));
+                    umma_f16(tmem + static_cast<uint32_t>(sp * ns), ad + 2 * k, bd + 2 * k, id_o,
+                             (j | half | k) != 0 ? 1u : 0u);
                 }
             umma_commit(smem_u32(&s.empty[r.stage]));
             r.next();
@@ -429,30 +420,26 @@ __device__ void pv_mma(const PvParams& p, const ASmem& s, uint32_t tmem, const u
     mma_drain(s, p.status, p.timeout_ns);
 }
 
-// One thread per row r of both query tiles: the lazy rescales of O_t by alpha_j
-// (each tile's own factor; 1 where that tile did not rescale), then O_t / l + b_v.
 __device__ void pv_rows(const PvParams& p, const ASmem& s, uint32_t tmem, const uint32_t* fl, int warp, int lane,
                         int tl, int d0) {
     const int r = warp * 32 + lane;
+    const int row = tl * 128 + r;
     const uint32_t tO = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const int ntl = min(kPvTiles, p.ntiles - tl);  // query tiles of this CTA inside the group
     uint32_t ev = 0;
     for (int j = 1; j < p.nkb; ++j) {
         if (!flagged(fl, j)) continue;
         if (!wwait_(s.resc_ready, ev & 1u, s, p.status, p.timeout_ns)) return;
         ++ev;
         tc_fence_after();
-        for (int t = 0; t < ntl; ++t) {
-            const float alpha = p.alpha[static_cast<size_t>(j) * p.grows + (tl + t) * 128 + r];
-            for (int col = 0; col < p.dv; col += 16) {
-                uint32_t rr[16];
-                __syncwarp();
-                tmem_ld16(tO + static_cast<uint32_t>(t * 256 + col), rr);
-                tmem_ld_wait();
+        const float alpha = p.alpha[static_cast<size_t>(j) * p.grows + row];
+        for (int col = 0; col < p.dv; col += 16) {
+            uint32_t rr[16];
+            __syncwarp();
+            tmem_ld16(tO + col, rr);
+            tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-                tmem_st16(tO + static_cast<uint32_t>(t * 256 + col), rr);
-            }
+            for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st16(tO + col, rr);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -460,32 +447,29 @@ __device__ void pv_rows(const PvParams& p, const ASmem& s, uint32_t tmem, const 
     }
     if (!wwait_(s.final, 0u, s, p.status, p.timeout_ns)) return;
     tc_fence_after();
-    for (int t = 0; t < ntl; ++t) {
-        const int row = (tl + t) * 128 + r;
-        const float inv = 1.f / p.lsum[row];
-        const int q = (p.q_tile0 + tl + t) * 128 + r;
-        for (int col = 0; col < p.dv; col += 16) {
-            uint32_t rr[16];
-            __syncwarp();
-            tmem_ld16(tO + static_cast<uint32_t>(t * 256 + col), rr);
-            tmem_ld_wait();
-            const int d = d0 + col;
-            if (q >= p.m || d >= p.c) continue;
-            __half* dst = p.out + static_cast<long long>(q) * p.c + d;
-            if (d + 16 <= p.c) {
-                uint32_t h[8];
+    const float inv = 1.f / p.lsum[row];
+    const int q = (p.q_tile0 + tl) * 128 + r;
+    for (int col = 0; col < p.dv; col += 16) {
+        uint32_t rr[16];
+        __syncwarp();
+        tmem_ld16(tO + col, rr);
+        tmem_ld_wait();
+        const int d = d0 + col;
+        if (q >= p.m || d >= p.c) continue;
+        __half* dst = p.out + static_cast<long long>(q) * p.c + d;
+        if (d + 16 <= p.c) {
+            uint32_t h[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    __half2 tv = __floats2half2_rn(__uint_as_float(rr[2 * i]) * inv + __ldg(p.bv + d + 2 * i),
-                                                   __uint_as_float(rr[2 * i + 1]) * inv + __ldg(p.bv + d + 2 * i + 1));
-                    h[i] = *reinterpret_cast<uint32_t*>(&tv);
-                }
-                reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
-            } else {
-                for (int i = 0; i < 16 && d + i < p.c; ++i)
-                    dst[i] = __float2half_rn(__uint_as_float(rr[i]) * inv + __ldg(p.bv + d + i));
+            for (int i = 0; i < 8; ++i) {
+                __half2 t = __floats2half2_rn(__uint_as_float(rr[2 * i]) * inv + __ldg(p.bv + d + 2 * i),
+                                              __uint_as_float(rr[2 * i + 1]) * inv + __ldg(p.bv + d + 2 * i + 1));
+                h[i] = *reinterpret_cast<uint32_t*>(&t);
             }
+            reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        } else {
+            for (int i = 0; i < 16 && d + i < p.c; ++i)
+                dst[i] = __float2half_rn(__uint_as_float(rr[i]) * inv + __ldg(p.bv + d + i));
         }
     }
 }
@@ -496,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ uint32_t fl[kMaxFlagWords];
     const ASmem s = carve_attn(smem_raw);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int tl = (blockIdx.x / p.ndv) * kPvTiles;  // first query tile (within the group) of this CTA
+    const int tl = blockIdx.x / p.ndv;
     const int d0 = (blockIdx.x % p.ndv) * p.dv;
     const int nwords = (p.nkb + 31) / 32;
     for (int i = threadIdx.x; i < nwords; i += blockDim.x) fl[i] = 0u;
@@ -522,15 +506,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     pdl_wait();  // P, the flags and V come from kernels launched before
     __syncthreads();
-    // "Some row of either tile rescaled at block j" flags, one bit per key block.
-    const int ntl = min(kPvTiles, p.ntiles - tl);
+    // The tile's "some row rescaled at block j" flags, one bit per key block.
     for (int j = 1 + threadIdx.x; j < p.nkb; j += blockDim.x) {
-        uint32_t any = 0u;
-        for (int t = 0; t < ntl; ++t) {
-            const uint4 f = *reinterpret_cast<const uint4*>(p.flags + (static_cast<size_t>(tl + t) * p.nkb + j) * 4);
-            any |= f.x | f.y | f.z | f.w;
-        }
-        if (any != 0u) atomicOr(&fl[j >> 5], 1u << (j & 31));
+        const uint4 f = *reinterpret_cast<const uint4*>(p.flags + (static_cast<size_t>(tl) * p.nkb + j) * 4);
+        if ((f.x | f.y | f.z | f.w) != 0u) atomicOr(&fl[j >> 5], 1u << (j & 31));
     }
     tc_fence_before();
     __syncthreads();
@@ -573,7 +552,7 @@ int attn_layout(int m, int c, int groups, int norm_kind, AttnLayout* L) {
     }
     L->m_pad = (m + 7) / 8 * 8;
     const int nchunk = (c + kMaxDv - 1) / kMaxDv;
-    L->dv = ((c + nchunk - 1) / nchunk + 15) / 16 * 16;
+    L->dv = ((c + nchunk - 1) / nchunk + 31) / 32 * 32;
     L->ndv = (c + L->dv - 1) / L->dv;
     size_t off = 0;
     L->xn = off;
@@ -689,9 +668,7 @@ static int attn_core_run(const __half* q, const __half* k, const __half* vt, int
         pp.q_tile0 = t0;
         VAE_CUDA_CHECK(launch_kernel(attn_scores_kernel, dim3(static_cast<unsigned>(nt)), dim3(kThreads), smem,
                                      stream, mq, mk, sp));
-        pp.ntiles = nt;
-        VAE_CUDA_CHECK(launch_kernel(attn_pv_kernel,
-                                     dim3(static_cast<unsigned>((nt + kPvTiles - 1) / kPvTiles * L.ndv)), dim3(kThreads), smem,
+        VAE_CUDA_CHECK(launch_kernel(attn_pv_kernel, dim3(static_cast<unsigned>(nt * L.ndv)), dim3(kThreads), smem,
                                      stream, mp, mv, pp));
     }
     return VAE_OK;

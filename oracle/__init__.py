@@ -35,9 +35,11 @@ Pins (``tests/test_oracle_*.py``): the pages' printed worked examples
 (``tests/golden/``), independent brute-force loops on tiny inputs, delta
 kernels, linearity, closed forms of the norms and of SiLU, attention
 invariants, the DupUp index formula, and banded == whole-frame decoding.
-The whole decoders (``decode_gn``, ``decode_rms``) are pinned only by the
-composition of pinned parts: parity unpinned against any outside
-implementation (no trained weights or third-party decoder exist here).
+The whole decoders (``decode_gn``, ``decode_rms``) are pinned against an
+element-by-element brute-force restatement of both decoders on tiny random
+decoders (scalar loops over a pixel-major layout), with planted composition
+mistakes that the comparison must see; no trained weights or third-party
+decoder exist here to compare with.
 """
 from .ops import (conv2d, conv2d_at, conv2d_down, conv3d_causal, causal_source_frame, subpixel_up_weights, conv2d_up_subpixel,
                   upsample2x, silu, group_norm, rms_norm, dupup, attention, attention_rows, linear_tokens)

@@ -4,8 +4,9 @@ Composes the primitives of ``oracle.ops`` in the order the pages give.
 ``decode_gn`` / ``decode_rms`` are the plain whole-frame definitions;
 ``decode_rms_banded`` is the exact-halo banded decode, written separately
 so that banded == whole-frame pins the band planner.
-Whole-decoder parity is unpinned against any outside implementation: it is
-pinned only by the pinned parts it composes.
+The whole decoders are pinned against an element-by-element brute-force
+restatement on tiny decoders (scalar loops, a pixel-major layout), besides
+the pinned parts they compose.
 """
 from __future__ import annotations
 

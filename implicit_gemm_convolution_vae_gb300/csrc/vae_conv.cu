@@ -41,6 +41,7 @@
 //    TMA copies and MMAs, frees TMEM and returns with the status recorded.
 #include <algorithm>
 #include <cstdio>
+#include <cmath>
 #include <cstdlib>
 
 #include "vae_conv.h"
@@ -108,6 +109,7 @@ struct ConvParams {
     void* y;
     float oscale;
     int silu, out_f16, vec_ok;
+    float out_scale;      // f16 output: stored value x out_scale
     int res_prefetch;     // L2-prefetch each tile's residual span (one row, all channels)
     int dup_prefetch;     // L2-prefetch each tile's DupUp source span (one source row)
     int dup_step;         // DupUp: source channel = dup_base[2q+p] + dup_step * o (1 or 2), or 0
@@ -753,6 +755,8 @@ __device__ __forceinline__ void store_chunk(const ConvParams& p, long long pix, 
     }
     const bool full = p.vec_ok && (o0 + 16 <= p.cout);
     if (p.out_f16) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= p.out_scale;
         __half* y = static_cast<__half*>(p.y) + pix * p.cout + o0;
         if (full) {
             uint32_t h[8];
@@ -1923,6 +1927,8 @@ int conv_validate(const ConvArgs& a) {
         return set_error(VAE_ERR_ARG, "conv: the 3x3x3 conv has no fused norm, DupUp or NCHW output");
     if (a.subpix && (!a.up || a.taps != 9 || a.rms_out != nullptr))
         return set_error(VAE_ERR_ARG, "conv: the sub-pixel form is the 3x3 up conv's (no fused norm)");
+    if (a.out_scale != 1.0f && (!a.out_f16 || !(a.out_scale > 0.0f) || !std::isfinite(a.out_scale)))
+        return set_error(VAE_ERR_ARG, "conv: an output scale needs f16 output and a finite positive value");
     if (a.n < 1 || a.h_in < 1 || a.w_in < 1)
         return set_error(VAE_ERR_SHAPE, "conv: n=%d h=%d w=%d must be >= 1", a.n, a.h_in, a.w_in);
     if (a.cin < 16 || a.cin % 16 != 0 || a.cin > 8192)
@@ -2054,6 +2060,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     p.oscale = a.oscale;
     p.silu = a.silu ? 1 : 0;
     p.out_f16 = a.out_f16 ? 1 : 0;
+    p.out_scale = a.out_scale;
     p.vec_ok = (a.cout % 16 == 0) && (a.y == nullptr || aligned16(a.y)) && (a.residual == nullptr || aligned16(a.residual)) &&
                (a.bias == nullptr || aligned16(a.bias));
     p.v8_ok = p.vec_ok && (a.y == nullptr || (reinterpret_cast<uintptr_t>(a.y) & 31) == 0) &&

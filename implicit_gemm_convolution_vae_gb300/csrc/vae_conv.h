@@ -24,6 +24,9 @@ struct ConvArgs {
     void* y = nullptr;
     float oscale = 1.0f;
     bool up = false, rep = false, silu = false, out_f16 = false;
+    // f16 output only: the stored value is the epilogue's value times out_scale
+    // (the decoder's 2^-g range guard, exact), as the guarded cast would store it.
+    float out_scale = 1.0f;
     // Reflect padding (mirror about the edge, the edge not repeated).
     bool refl = false;
     // The encoder's downsample: x padded by one row and column on the far side

@@ -9,9 +9,10 @@
 //           conv2 (+bias +skip, in the epilogue) -> stream; the 1x1 shortcut
 //           reads the raw stream cast to f16 with the 2^-g guard and undoes
 //           it with oscale = 2^g.
-//   Up conv: raw stream cast with the guard, 3x3 conv with the nearest-2x
-//           fold, + bias (+ the DupUp shortcut of the block input) in the
-//           epilogue.
+//   Up conv: raw stream cast with the guard (written as f16 by the epilogue
+//           of the block's last conv2 unless fusion is off), 3x3 conv with the
+//           nearest-2x fold, + bias (+ the DupUp shortcut of the block input)
+//           in the epilogue.
 //   Output: norm_out+SiLU -> f16, conv_out writes NCHW f32 kept rows directly.
 // Banded decoding runs the head and blocks < band_from on the whole frame,
 // then each band from the saved stream rows its plan needs; every kernel is
@@ -201,6 +202,11 @@ struct Exec {
     vae_decoder* prof = nullptr;  // non-null: record events around stages
     int prof_only_w = 0;          // > 0: only the 3x3 convs with cin == cout on rows this wide
     bool fuse = false;            // VAE_DECODE_FUSE_NORM without VAE_DECODE_NO_FUSION
+    // Without VAE_DECODE_NO_FUSION the last ResNet of an up block writes its conv2
+    // output (the stream only the up conv still reads) straight as the guarded
+    // f16 input of the up conv: (acc * oscale + bias + residual) * 2^-g rounded to
+    // f16, the value and rounding of the separate cast of the f32 stream.
+    bool fuse_cast = true;
     bool subpix = false;          // VAE_DECODE_SUBPIXEL_UP
     // With VAE_DECODE_FUSE_NORM a ResNet's second RMS_norm rides in the epilogue
     // of its first conv (whose f32 output only feeds that norm) when the conv's
@@ -309,8 +315,9 @@ struct Exec {
     }
 
     // One ResNet on stream `x` (rows h x w, channels r.c1.cin) -> stream `y`
-    // (may equal x when the channel count does not change).
-    int resnet(const DRes& r, float* x, float* y, int h, int w) {
+    // (may equal x when the channel count does not change); with `y16` the
+    // result goes to y16 instead, as f16 times 2^-g (the guarded cast).
+    int resnet(const DRes& r, float* x, float* y, int h, int w, __half* y16 = nullptr) {
         const long long hw = static_cast<long long>(h) * w;
         const int cin = r.c1.cin, cout = r.c1.cout;
         int rc;
@@ -341,6 +348,11 @@ struct Exec {
         }
         ConvArgs a = c3(xmid, h, w, r.c2, y);
         a.residual = skip;
+        if (y16 != nullptr) {
+            a.y = y16;
+            a.out_f16 = true;
+            a.out_scale = 1.f / guard;
+        }
         return conv(a);
     }
 
@@ -361,13 +373,19 @@ struct Exec {
             const int in_b = *cur_buf;
             const int avoid = keep_input ? in_b : -1;
             int s_b = in_b;
+            bool cast_done = false;  // the last ResNet wrote the up conv's guarded f16 input
             for (size_t r = 0; r < u.res.size(); ++r) {
                 const DRes& rs = u.res[r];
                 const bool fresh = rs.c1.cin != rs.c1.cout || (r == 0 && keep_input);
                 const int out_b = fresh ? other(s_b, avoid) : s_b;
                 float* xin = f32(bufs[s_b], hw * rs.c1.cin);
                 float* xout = f32(bufs[out_b], hw * rs.c1.cout);
-                if ((rc = resnet(rs, xin, xout, h, w)) != VAE_OK) return rc;
+                __half* y16 = nullptr;
+                if (fuse_cast && u.up.present() && r + 1 == u.res.size()) {
+                    y16 = f16(kXN, hw * rs.c1.cout);
+                    cast_done = true;
+                }
+                if ((rc = resnet(rs, xin, xout, h, w, y16)) != VAE_OK) return rc;
                 s_b = out_b;
                 *ch = rs.c1.cout;
             }
@@ -384,7 +402,11 @@ struct Exec {
             const int out_b = other(s_b, avoid);
             float* xs = f32(bufs[s_b], hw * (*ch));
             __half* xn = f16(kXN, hw * (*ch));
-            if ((rc = cast(xs + (dry ? 0 : skip_px * (*ch)), fhw * (*ch), *ch, 1.f / guard, xn)) != VAE_OK) return rc;
+            if (cast_done) {
+                xn += dry ? 0 : skip_px * (*ch);  // the feed rows of the whole range's f16 stream
+            } else if ((rc = cast(xs + (dry ? 0 : skip_px * (*ch)), fhw * (*ch), *ch, 1.f / guard, xn)) != VAE_OK) {
+                return rc;
+            }
             float* y = f32(bufs[out_b], fhw * 4 * u.up.cout);
             ConvArgs a = c3(xn, f.n(), w, u.up, y);
             a.up = true;
@@ -478,6 +500,7 @@ int run_decode(Exec& X, int h0, int w0, const vae_decode_opts* opts, const float
     int rc;
     X.guard = std::ldexp(1.0f, opts ? (opts->guard_log2 < 0 ? 8 : std::min(opts->guard_log2, 14)) : 8);
     X.fuse = opts != nullptr && (opts->flags & VAE_DECODE_FUSE_NORM) != 0 && (opts->flags & VAE_DECODE_NO_FUSION) == 0;
+    X.fuse_cast = opts == nullptr || (opts->flags & VAE_DECODE_NO_FUSION) == 0;
     X.subpix = opts != nullptr && (opts->flags & VAE_DECODE_SUBPIXEL_UP) != 0;
     int nbands = 1;
     if (opts && opts->band_rows > 0) nbands = (hf + opts->band_rows - 1) / opts->band_rows;

@@ -404,7 +404,10 @@ typedef struct {
 enum {
     VAE_DECODE_PROFILE = 1,
     /* Run every RMS_norm as its own kernel (the default); overrides
-     * VAE_DECODE_FUSE_NORM. */
+     * VAE_DECODE_FUSE_NORM. Also cast the stream to the up convs' guarded f16
+     * input in a separate kernel; by default the last ResNet conv of an up block
+     * stores that f16 input itself ((conv + bias + skip) * 2^-g rounded to f16,
+     * the same bits) and the f32 stream it would replace is not written. */
     VAE_DECODE_NO_FUSION = 2,
     /* Compute a ResNet's second RMS_norm (+SiLU) in the epilogue of its first
      * conv where one CTA holds all <= 144 channels of a pixel (vae_conv3x3_nhwc_rms:

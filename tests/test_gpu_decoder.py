@@ -221,3 +221,23 @@ def test_graph_replay_matches_eager_decode(family):
     g.launch()
     vg.sync_status()
     assert torch.equal(out, D.decode(to_dev(z2)))
+
+
+@pytest.mark.parametrize("family,band_from,nbands", [("gn", 0, 1), ("rms", 0, 1), ("rms", 1, 3), ("rms", 2, 4)])
+def test_cast_fused_into_the_last_resnet_conv_is_bit_identical(family, band_from, nbands):
+    """By default the last ResNet conv of an up block stores the up conv's guarded
+    f16 input itself ((conv + bias + skip) * 2^-8 rounded to f16); with fusion off a
+    separate cast kernel reads the f32 stream. Same bits, whole frame and in bands
+    (where the up conv reads only the feed rows of the conv's whole row range)."""
+    torch = torch_mod()
+    if family == "gn":
+        dec = flux_decoder(seed=5, block_out=(32, 32, 64, 64), layers_per_block=1)
+        z = latent_normal(5, 16, 6, 10)
+    else:
+        dec = qwen_decoder(seed=6, widths=(64, 32, 32, 16), nres=2)
+        z = latent_channel_stats(6, 16, 12, 10)
+    kw = dict(band_from=band_from, nbands=nbands)
+    separate, D = gpu_decode(dec, z, opts=vg.Decoder.opts(fuse=False, **kw))
+    fused = D.decode(to_dev(z), opts=vg.Decoder.opts(**kw))
+    vg.sync_status()
+    assert torch.equal(fused, separate)

@@ -13,7 +13,9 @@
 //           of the block's last conv2 unless fusion is off), 3x3 conv with the
 //           nearest-2x fold, + bias (+ the DupUp shortcut of the block input)
 //           in the epilogue.
-//   Output: norm_out+SiLU -> f16, conv_out writes NCHW f32 kept rows directly.
+//   Output: norm_out+SiLU -> f16, conv_out (few channels) as one 1x1 GEMM with
+//           its nine taps folded into the output channels, then a tap-sum
+//           kernel writes NCHW f32 kept rows (+ bias).
 // Banded decoding runs the head and blocks < band_from on the whole frame,
 // then each band from the saved stream rows its plan needs; every kernel is
 // row-local with a per-pixel result independent of tiling, so kept rows are
@@ -67,6 +69,9 @@ struct vae_decoder {
     int family = 0, zc = 0, groups = 32, dupup = 0, device = 0;
     float scaling = 1.f, shift = 0.f, eps = 1e-6f;
     vae::DConv pq, conv_in, conv_out;
+    // conv_out with its nine taps folded into the output channels: a 1x1 conv
+    // [9 * cout rounded up to 16][cin], row t * cout + o = tap t of output o.
+    vae::DConv conv_out_t;
     vae::DRes mid1, mid2;
     vae::DAttn attn;
     std::vector<vae::DUp> ups;
@@ -81,6 +86,50 @@ struct vae_decoder {
 namespace vae {
 
 namespace {
+
+// ───────────────────────────── conv_out tap sum ─────────────────────────────
+// The second half of conv_out with its taps folded into N: z [rows][w][np]
+// holds, for every pixel and tap t = 3 * ky + kx, the channel contraction of
+// that tap (z[p][t * cout + o]). Output pixel (Y, X), channel o:
+// bias[o] + sum over (ky, kx) of z[(Y + ky - 1, X + kx - 1)][t * cout + o], taps
+// outside the rows' window or the width read zero (the conv's zero padding),
+// summed in (ky, kx) order. Kept rows [keep_lo, keep_hi) of the window land at
+// destination row (Y - keep_lo + dst_row0) of NCHW planes `plane` floats apart.
+__global__ void __launch_bounds__(256) tapsum_nchw_kernel(const float* __restrict__ z, int rows, int w, int cout,
+                                                          int np, const float* __restrict__ bias, int keep_lo,
+                                                          int keep_hi, float* __restrict__ out, int dst_row0,
+                                                          long long plane) {
+    pdl_wait();
+    const long long npx = static_cast<long long>(keep_hi - keep_lo) * w;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < npx;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int Y = keep_lo + static_cast<int>(i / w), X = static_cast<int>(i % w);
+        for (int o = 0; o < cout; ++o) {
+            float acc = 0.f;
+            for (int ky = 0; ky < 3; ++ky) {
+                const int yy = Y + ky - 1;
+                if (yy < 0 || yy >= rows) continue;
+                for (int kx = 0; kx < 3; ++kx) {
+                    const int xx = X + kx - 1;
+                    if (xx < 0 || xx >= w) continue;
+                    acc = __fadd_rn(acc, __ldg(z + (static_cast<long long>(yy) * w + xx) * np + (ky * 3 + kx) * cout + o));
+                }
+            }
+            out[o * plane + static_cast<long long>(Y - keep_lo + dst_row0) * w + X] = __fadd_rn(acc, __ldg(bias + o));
+        }
+    }
+}
+
+int tapsum_nchw_run(const float* z, int rows, int w, int cout, int np, const float* bias, int keep_lo, int keep_hi,
+                    float* out, int dst_row0, long long plane, cudaStream_t stream) {
+    const long long npx = static_cast<long long>(keep_hi - keep_lo) * w;
+    if (npx <= 0) return VAE_OK;
+    const int grid = static_cast<int>(std::min<long long>((npx + 255) / 256, 1LL << 20));
+    VAE_CUDA_CHECK(launch_kernel(tapsum_nchw_kernel, dim3(grid), dim3(256), 0, stream, z, rows, w, cout, np, bias,
+                                 keep_lo, keep_hi, out, dst_row0, plane));
+    VAE_CUDA_CHECK(cudaGetLastError());
+    return VAE_OK;
+}
 
 // ───────────────────────────── handle creation ─────────────────────────────
 
@@ -133,6 +182,26 @@ struct Uploader {
         return o;
     }
 
+    // The 3x3 conv `c` (few outputs) as a 1x1 conv whose output channel
+    // t * cout + o (t = 3 * ky + kx) is tap t of output o, zero rows up to a
+    // multiple of 16; no bias (the tap sum adds it).
+    DConv taps_folded(const vae_conv_desc& c) {
+        DConv o;
+        if (rc != VAE_OK || c.w == nullptr || c.k != 3) return o;
+        const int n = (9 * c.cout + 15) / 16 * 16;
+        std::vector<uint16_t> packed(static_cast<size_t>(n) * c.cin, 0);
+        for (int t = 0; t < 9; ++t)
+            for (int o_ = 0; o_ < c.cout; ++o_)
+                for (int ci = 0; ci < c.cin; ++ci)
+                    packed[static_cast<size_t>(t * c.cout + o_) * c.cin + ci] =
+                        c.w[(static_cast<size_t>(o_) * c.cin + ci) * 9 + t];
+        o.w = put<__half>(packed.data(), packed.size() * 2);
+        o.cout = n;
+        o.cin = c.cin;
+        o.k = 1;
+        return o;
+    }
+
     DNorm norm(const vae_norm_desc& n, int c, bool need_beta, const char* what) {
         DNorm o;
         if (rc != VAE_OK) return o;
@@ -176,7 +245,7 @@ struct Rows {
 Rows grow(Rows r, int k, int h) { return Rows{std::max(r.lo - k, 0), std::min(r.hi + k, h)}; }
 Rows half_rows(Rows r) { return Rows{r.lo / 2, (r.hi + 1) / 2}; }
 
-enum Buf { kS0, kS1, kS2, kB0, kB1, kB2, kH, kSC, kXN, kXN2, kZ, kATT, kGN, kZIN, kOUT, kNBuf };
+enum Buf { kS0, kS1, kS2, kB0, kB1, kB2, kH, kSC, kXN, kXN2, kZ, kATT, kGN, kZIN, kOUT, kTAP, kNBuf };
 
 struct Band {
     Rows input;
@@ -438,6 +507,22 @@ struct Exec {
         __half* xn = f16(kXN, hw * ch);
         int rc = norm(x, hw, ch, d->norm_out, true, xn);
         if (rc != VAE_OK) return rc;
+        if (d->conv_out_t.present()) {
+            // few output channels: one GEMM with the taps folded into N (9 MMAs per
+            // 128 pixels instead of 81 narrow ones), then the 3x3 tap sum + bias
+            const int np = d->conv_out_t.cout;
+            float* z = f32(kTAP, hw * np);
+            ConvArgs a = c3(xn, cur.n(), w, d->conv_out_t, z);
+            if (dry) return conv_validate(a);
+            const double flops = 2.0 * hw * d->conv_out.cout * 9.0 * ch;
+            const int i = begin(VAE_STAGE_CONV3X3, 2, cur.n(), w, ch, d->conv_out.cout, flops, 0.0);
+            rc = conv_run(a, st);
+            if (rc == VAE_OK)
+                rc = tapsum_nchw_run(z, cur.n(), w, d->conv_out.cout, np, d->conv_out.b, keep.lo - cur.lo,
+                                     keep.hi - cur.lo, out, keep.lo, static_cast<long long>(hf) * w, st);
+            end(i);
+            return rc;
+        }
         ConvArgs a = c3(xn, cur.n(), w, d->conv_out, out);
         a.out_nchw = true;
         a.keep_lo = keep.lo - cur.lo;
@@ -724,6 +809,7 @@ int vae_decoder_create(const vae_decoder_desc* desc, vae_decoder_t* out) {
     d->conv_out = U.conv(desc->conv_out, "conv_out");
     if (U.rc == VAE_OK && (d->conv_out.k != 3 || d->conv_out.cin != ch))
         U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: conv_out must be 3x3 from %d", ch);
+    if (U.rc == VAE_OK && 9 * d->conv_out.cout <= 256) d->conv_out_t = U.taps_folded(desc->conv_out);
     if (U.rc == VAE_OK && gn && ch % d->groups != 0)
         U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: %d channels not divisible by %d groups", ch, d->groups);
     if (U.rc != VAE_OK) {

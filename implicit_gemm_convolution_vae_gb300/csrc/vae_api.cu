@@ -25,7 +25,35 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+struct CtxFns {
+    CtxGetCurrentFn current = nullptr;
+    CtxGetIdFn id = nullptr;
+    CtxFns() {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            id = reinterpret_cast<CtxGetIdFn>(f);
+    }
+};
+CtxOnce g_status_once;
 }  // namespace
+
+unsigned long long context_id() {
+    static const CtxFns fns;  // resolved once (thread-safe static initialisation)
+    if (fns.current == nullptr || fns.id == nullptr) return 0;
+    CUcontext c = nullptr;
+    if (fns.current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    if (fns.id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 // The status word every kernel of this library writes on a timed-out wait.
 __device__ DevStatus g_dev_status[1];
@@ -50,8 +78,9 @@ static int current_device(int* dev) {
 DevStatus* device_status_ptr() {
     int dev;
     if (current_device(&dev) != VAE_OK) return nullptr;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_status_ptr[dev] == nullptr) {
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    if (g_status_ptr[dev] == nullptr || !g_status_once.done(dev)) {
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_dev_status);
         if (e != cudaSuccess) {
@@ -59,6 +88,7 @@ DevStatus* device_status_ptr() {
             return nullptr;
         }
         g_status_ptr[dev] = static_cast<DevStatus*>(p);
+        g_status_once.mark(dev);
     }
     return g_status_ptr[dev];
 }

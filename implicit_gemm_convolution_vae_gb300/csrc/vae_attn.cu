@@ -652,15 +652,15 @@ static int attn_core_run(const __half* q, const __half* k, const __half* vt, int
         if (rc != VAE_OK) return rc;
     }
     const size_t smem = 1024 + kStages * kStageBytes + 256;
-    static bool attr_set[64] = {false};
+    static CtxOnce attr_set;
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (!attr_set.done(dev)) {
         VAE_CUDA_CHECK(cudaFuncSetAttribute(attn_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(smem)));
         VAE_CUDA_CHECK(cudaFuncSetAttribute(attn_pv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(smem)));
-        attr_set[dev] = true;
+        attr_set.mark(dev);
     }
     for (int t0 = 0; t0 < L.qtiles; t0 += L.group) {
         const int nt = std::min(L.group, L.qtiles - t0);

@@ -475,6 +475,28 @@ void clear_error();
 // no allocation). nullptr on a CUDA error (then set_error was called).
 DevStatus* device_status_ptr();
 
+// Identity of the CUDA context current on the calling thread (cuCtxGetId,
+// unique for the life of the process), or 0 when none is current or the driver
+// calls fail.
+unsigned long long context_id();
+
+// One-time set-up of a device (function attributes, __device__ symbol
+// addresses) recorded against the context it was done in. After
+// cudaDeviceReset tears the context down and the runtime creates a new one, the
+// id changes and done() is false again, so the set-up is redone instead of
+// trusting state (or addresses) of the old context. An unknown id (0) is never
+// "done". Callers serialise access (a mutex) where threads may race.
+struct CtxOnce {
+    unsigned long long id[64] = {};
+    bool done(int dev) const {
+        const unsigned long long c = context_id();
+        return dev >= 0 && dev < 64 && c != 0 && id[dev] == c;
+    }
+    void mark(int dev) {
+        if (dev >= 0 && dev < 64) id[dev] = context_id();
+    }
+};
+
 // Timeout for device waits, in ns.
 unsigned long long wait_timeout_ns();
 

@@ -1863,13 +1863,13 @@ int choose_bn(int cout, bool halo3) {
 template <int kMode>
 int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my, size_t smem,
                 int grid, cudaStream_t stream) {
-    static bool attr_set[64] = {false};
+    static CtxOnce attr_set;
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (!attr_set.done(dev)) {
         VAE_CUDA_CHECK(
             cudaFuncSetAttribute(conv_pair_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
-        attr_set[dev] = true;
+        attr_set.mark(dev);
     }
     conv_pair_kernel<kMode><<<grid, 192, smem, stream>>>(ma, mb, my, p);
     VAE_CUDA_CHECK(cudaGetLastError());
@@ -1879,13 +1879,13 @@ int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& m
 template <int kMode, bool kRms, int kVar = 0>
 int launch(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma16,
            const CUtensorMap& mb16, const CUtensorMap& my, size_t smem, int grid, cudaStream_t stream) {
-    static bool attr_set[64] = {false};
+    static CtxOnce attr_set;
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (!attr_set.done(dev)) {
         VAE_CUDA_CHECK(
             cudaFuncSetAttribute(conv_kernel<kMode, kRms, kVar>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
-        attr_set[dev] = true;
+        attr_set.mark(dev);
     }
     const int threads = kMode == kModeGather ? 320 : (p.refl ? 224 : 192);
     VAE_CUDA_CHECK(launch_kernel(conv_kernel<kMode, kRms, kVar>, dim3(grid), dim3(threads), smem, stream, ma, mb, ma16,

@@ -556,13 +556,15 @@ int latent_run(const float* z, int c, long long hw, float mul, float add, void* 
 // Scratch of vae_groupnorm_silu_static: a fixed array in device memory that
 // every GPU loading this library holds until the process exits. Host code
 // must not pass the symbol itself to a kernel (on the host it only names a
-// stand-in); gn_static_scratch() looks its device address up once per device.
+// stand-in); gn_static_scratch() looks its device address up once per device
+// and context (again after a cudaDeviceReset).
 constexpr size_t kGnStaticFloats = 131072;  // 512 KB
 static __device__ __align__(256) float g_gn_static_scratch[kGnStaticFloats];
 
 static float* gn_static_scratch() {
     static std::mutex mu;
     static float* ptr[64] = {nullptr};
+    static CtxOnce once;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
@@ -574,7 +576,7 @@ static float* gn_static_scratch() {
         return nullptr;
     }
     std::lock_guard<std::mutex> lk(mu);
-    if (ptr[dev] == nullptr) {
+    if (ptr[dev] == nullptr || !once.done(dev)) {  // first call, or a new context since (cudaDeviceReset)
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_gn_static_scratch);
         if (e != cudaSuccess) {
@@ -582,6 +584,7 @@ static float* gn_static_scratch() {
             return nullptr;
         }
         ptr[dev] = static_cast<float*>(p);
+        once.mark(dev);
     }
     return ptr[dev];
 }

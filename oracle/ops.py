@@ -282,11 +282,12 @@ def group_norm(x, groups: int, gamma, beta, eps: float = 1e-6, bias_in=None):
     return out
 
 
-def rms_norm(x, gamma, bias_in=None, c_real=None):
+def rms_norm(x, gamma, bias_in=None):
     """Per-pixel RMS_norm over the channels (the Wan ``RMS_norm``).
 
     v = x + bias_in[c]; y = v * sqrt(C) / max(||v||_2, 1e-12) * gamma[c],
-    the norm taken over the C real channels of one pixel.
+    the norm taken over the C channels of one pixel (no padded channels: the
+    tensors carry exactly the model's channels).
 
     ``qi21_vae.rs``, the ``qv_rmsn`` kernel and its module doc.
     ``x``: [c][...spatial]; returns the same shape.
@@ -295,9 +296,8 @@ def rms_norm(x, gamma, bias_in=None, c_real=None):
     c = v.shape[0]
     if bias_in is not None:
         v = v + _f64(bias_in).reshape((c,) + (1,) * (v.ndim - 1))
-    C = c if c_real is None else c_real
     nrm = np.sqrt((v * v).sum(axis=0))
-    inv = np.sqrt(float(C)) / np.maximum(nrm, 1e-12)
+    inv = np.sqrt(float(c)) / np.maximum(nrm, 1e-12)
     return v * inv[None] * _f64(gamma).reshape((c,) + (1,) * (v.ndim - 1))
 
 

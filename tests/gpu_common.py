@@ -1,4 +1,8 @@
-"""Helpers of the GPU parity tests: device transfer, tolerances, sentinels."""
+"""Helpers of the GPU parity tests: device transfer, tolerances, sentinels,
+and the record of whole-decoder parity figures."""
+import json
+import os
+
 import numpy as np
 
 # Per conv, from the hot path's stated target: max|d| / max|ref| <= 2e-3,
@@ -49,3 +53,17 @@ def psnr_u8(got, ref):
 def saturated_fraction(ref):
     r = np.asarray(ref)
     return float(np.mean((r <= -1.0) | (r >= 1.0)))
+
+
+def report_parity(case, got, ref, **extra):
+    """Prints one JSON line with a decode's u8 PSNR, raw max|d|/max|ref| and
+    saturated fraction (and appends it to $VAE_PARITY_LOG when that is set);
+    returns the record."""
+    rec = {"case": case, "psnr_u8_db": round(psnr_u8(got, ref), 3), "max_rel_err_f32": rel_err(got, ref),
+           "saturated_fraction": saturated_fraction(ref), **extra}
+    print(json.dumps(rec))
+    log = os.environ.get("VAE_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write(json.dumps(rec) + "\n")
+    return rec

@@ -95,9 +95,9 @@ def test_conv_epilogue(silu, out_f16, with_res):
     res = stream_normal(2, "epi.res", (1, 12, 150, 96)) if with_res else None
     got = _run(case, silu=silu, out_f16=out_f16, residual=res, oscale=1.0)
     ref = _ref(case, silu=silu, residual=res)
-    tol = CONV_TOL + (1e-3 if out_f16 else 0.0)
     assert not np.isnan(got).any()
-    assert rel_err(got, ref) <= tol
+    # f16 output adds one rounding (at most 2^-11 of max|ref| ~ 4.9e-4), inside the per-conv bound
+    assert rel_err(got, ref) <= CONV_TOL
 
 
 def test_conv_in_place_residual_and_oscale():

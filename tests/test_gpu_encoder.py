@@ -97,8 +97,8 @@ def test_encoder_conv_epilogues(down, silu, out_f16, with_res):
     res = stream_normal(13, "enc.epi.res", (1, H, W, 96)) if with_res else None
     got = _run(case, pad="reflect", down=down, silu=silu, out_f16=out_f16, residual=res)
     ref = _ref(case, pad="reflect", down=down, silu=silu, residual=res)
-    tol = 2 * CONV_TOL if out_f16 else CONV_TOL  # one more f16 rounding of the output
-    assert rel_err(got, ref) <= tol
+    # f16 output adds one rounding (at most 2^-11 of max|ref| ~ 4.9e-4), inside the per-conv bound
+    assert rel_err(got, ref) <= CONV_TOL
 
 
 def test_reflect_conv_in_place_residual():

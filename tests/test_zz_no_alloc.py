@@ -1,13 +1,13 @@
 """The GroupNorm entry point that allocates nothing (its scratch is a fixed
 device array inside the library), for callers that cannot allocate device
 memory. Called through the C ABI; its output must match the workspace
-entry point's on two calls in a row (the second sees the first call's
-leftovers in the shared array). This file is collected last."""
-import ctypes
-
+entry point's, and the oracle's GroupNorm (+SiLU), on two calls in a row (the
+second sees the first call's leftovers in the shared array). This file is
+collected last."""
 import numpy as np
 import pytest
 
+import oracle
 import implicit_gemm_convolution_vae_gb300 as vg
 from gpu_common import NORM_TOL, rel_err, to_dev, torch_mod
 from vae_inputs import rng_for, stream_normal
@@ -38,6 +38,12 @@ def test_static_groupnorm_matches_workspace_groupnorm_twice():
         g, r = got.float().cpu().numpy(), ref.float().cpu().numpy()
         assert not np.isnan(g).any()
         assert rel_err(g, r) <= NORM_TOL
+        # the oracle: GroupNorm(32) of x + bias over each image's pixels, then SiLU
+        for i in range(n):
+            o = oracle.group_norm(x[i].T, 32, gam, bet, eps=1e-6, bias_in=bia)
+            if silu:
+                o = oracle.silu(o)
+            assert rel_err(g[i], o.T) <= NORM_TOL
 
 
 def test_static_groupnorm_rejects_calls_beyond_its_scratch():

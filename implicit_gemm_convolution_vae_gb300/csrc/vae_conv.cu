@@ -101,6 +101,7 @@ struct ConvParams {
                           // (ks == 3: box slot i belongs to stage i, one barrier pair)
     int ks;               // K chunks per pipeline stage (1 or 2; per-tap A path only)
     int pair;             // CTA-pair kernel: each CTA holds BN/2 rows of B (b_rows)
+    int stg_bytes;        // epilogue staging boxes in shared memory (0 without the TMA epilogue)
     int b_rows, typ_tiles, pair_tiles;
     uint32_t a_tx;        // bytes one A box delivers
     const __half* x;      // gather source
@@ -241,7 +242,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
     s.a = base;
     s.b = base + (p.halo ? p.a_stages * kHaloBytes : p.stages * p.ks * kABytes);
     s.stg = s.b + p.stages * p.ks * p.b_rows * 128;
-    s.bias = reinterpret_cast<float*>(s.stg + (p.epi_tma ? kEpiWarps * kStgBytes : 0));
+    s.bias = reinterpret_cast<float*>(s.stg + p.stg_bytes);
     uint8_t* tail = reinterpret_cast<uint8_t*>(s.bias) + (p.bias_smem ? (p.cout * 4 + 15) / 16 * 16 : 0);
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail);
     s.full = bars;
@@ -1205,26 +1206,33 @@ __device__ __forceinline__ void epilogue_tma_rms_row(const ConvParams& p, const 
 
 // Epilogue of one accumulator row (pixel) without a fused norm. kPipe: the
 // register-hungry pipelined residual path (off in the 320-thread gather kernel).
+// c0, cstep: this warp's 16-column chunks are c0, c0 + cstep, ... (the pair
+// kernel splits a tile's chunks between two warps per lane quadrant).
 template <bool kPipe, bool kGn = false>
 __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, bool valid,
                                                    int v, int u, int q, int pp, int Y, int X, long long pix,
-                                                   int ew = 0, int lane = 0, const float* sbias = nullptr) {
+                                                   int ew = 0, int lane = 0, const float* sbias = nullptr,
+                                                   int c0 = 0, int cstep = 1) {
     GnRun run{0.f, 0.f, 0.f};
     const float npx = kGn ? static_cast<float>(__popc(__ballot_sync(0xffffffffu, valid))) : 0.f;
     if (kPipe && p.residual != nullptr && p.v8_ok && !p.out_nchw) {
         // Residual loads run two chunks ahead of their use (a three-slot
-        // register ring), so three are in flight instead of one.
-        const int nch = p.BN / 16;
+        // register ring), so three are in flight instead of one. j counts this
+        // warp's chunks: chunk c0 + j * cstep.
+        const int nchunk = p.BN / 16;
+        const int nch = nchunk > c0 ? (nchunk - c0 + cstep - 1) / cstep : 0;
         float r0[16], r1[16], r2[16];
-        auto ld = [&](int c, float* rr) {
-            if (valid && c < nch && ti.n0 + c * 16 < p.cout) {
+        auto ld = [&](int j, float* rr) {
+            const int c = c0 + j * cstep;
+            if (valid && j < nch && ti.n0 + c * 16 < p.cout) {
                 const float* rs = p.residual + pix * p.cout + ti.n0 + c * 16;
                 ld_v8_f32(rs, rr);
                 ld_v8_f32(rs + 8, rr + 8);
             }
         };
-        auto step = [&](int c, const float* rr) {
-            if (c >= nch) return;  // warp-uniform
+        auto step = [&](int j, const float* rr) {
+            if (j >= nch) return;  // warp-uniform
+            const int c = c0 + j * cstep;
             uint32_t acc[16];
             __syncwarp();
             tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
@@ -1256,7 +1264,7 @@ __device__ __forceinline__ void epilogue_plain_row(const ConvParams& p, const Ti
         }
         return;
     }
-    for (int j = 0; j < p.BN; j += 16) {
+    for (int j = c0 * 16; j < p.BN; j += 16 * cstep) {
         uint32_t r[16];
         __syncwarp();
         tmem_ld16(tbase + static_cast<uint32_t>(j), r);
@@ -1459,16 +1467,36 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 224, 1)
 
 
 // ───────────────────────────── CTA-pair kernel ─────────────────────────────
-// A cluster of two CTAs computes a 256 x BN tile with tcgen05.mma.cta_group::2:
-// each CTA holds its own 128-row A tile and half (BN/2 rows) of B at the same
-// shared-memory offsets and its own 128 x BN accumulator in TMEM. Both CTAs'
-// TMA copies complete on the EVEN CTA's full barrier, whose single arrival
-// (by the even producer) expects the bytes of both. The even CTA's MMA thread
-// commits with multicast to the empty / accumulator barriers of both CTAs;
-// both epilogues arrive on the even CTA's accumulator-empty barrier. The odd
-// CTA learns its copies landed from its empty barriers (the MMAs that read
-// them completed). Halves the weight traffic and the shared-memory operand
-// reads per SM.
+// A cluster of two CTAs (the two SMs of a TPC) computes two 128-pixel row tiles
+// (rows 2j and 2j + 1 of one column block and parity class) with
+// tcgen05.mma.cta_group::2 (M = 256): each CTA holds its own A halo boxes and
+// HALF of every weight tile (BN/2 rows) at the same shared-memory offsets, and
+// receives its own 128 x BN accumulator in TMEM. Per SM this halves both the
+// weight bytes taken in from L2 and the B operand bytes the tensor core reads
+// from shared memory, which measured as the two limits of the single-CTA
+// kernel at 144 channels (its MMAs issue at ~86 cycles for 72 cycles of tensor
+// work; the pair's at 72).
+//
+// Stages are the three-tap halo stages of the single-CTA kernel (one 130-pixel
+// box per (ky, 64-channel chunk) and the three kx taps' weight halves, 12 pair
+// MMAs), with the exact 16-channel remainder stage when cin % 64 == 16.
+// Barriers: both CTAs' copies complete on the EVEN CTA's full barrier, armed
+// once by the even producer for the bytes of both; the even CTA's MMA thread
+// commits with multicast to the empty and accumulator-full barriers of both
+// CTAs; every epilogue warp of both CTAs arrives on the even CTA's
+// accumulator-empty barrier. The odd CTA learns its copies landed from its
+// empty barriers (the MMAs that read them completed).
+//
+// Eight epilogue warps per CTA: warp w drains TMEM lane quadrant w % 4 (its 32
+// pixels) and every other 16-column chunk starting at w / 4, through a
+// double-buffered 2 KB staging box (one TMA store in flight while the next
+// box is written), so the epilogue keeps up with the doubled MMA rate.
+constexpr int kPairEpiWarps = 8;
+constexpr int kPairProducerWarp = 8;
+constexpr int kPairMmaWarp = 9;
+constexpr int kPairThreads = 320;
+constexpr int kPairStgBytes = kPairEpiWarps * 2 * kStgBytes;  // two boxes per epilogue warp
+constexpr int kPairStages = 4;
 
 __device__ __forceinline__ TileInfo decode_pair_tile(const ConvParams& p, int t, int rank) {
     TileInfo ti;
@@ -1486,19 +1514,18 @@ __device__ __forceinline__ TileInfo decode_pair_tile(const ConvParams& p, int t,
     return ti;
 }
 
-template <int kMode>
-__device__ void pair_producer(const ConvParams& p, const Smem& s, const CUtensorMap* mapA,
-                              const CUtensorMap* mapB, int rank) {
+__device__ void pair_producer(const ConvParams& p, const Smem& s, const CUtensorMap* mapA, const CUtensorMap* mapB,
+                              const CUtensorMap* mapA16, const CUtensorMap* mapB16, int rank) {
     const uint64_t pol_w = policy_evict_last();
     const uint64_t pol_a = policy_evict_normal();
     const uint32_t b_bytes = static_cast<uint32_t>(p.b_rows) * 128u;
     const int boff = rank * p.b_rows;
-    int stage = 0, astage = 0;
-    uint32_t phase = 0, aphase = 0, armed = 0, arm_par = 0, aarmed = 0, aarm_par = 0;
+    int stage = 0;
+    uint32_t phase = 0, armed = 0, arm_par = 0;
     bool ok = true;
-    // Waits for a free B slot; the even CTA arms its (shared) full barrier for
+    // Waits for a free slot; the even CTA arms its (shared) full barrier for
     // the bytes of both CTAs. Returns the full barrier's cluster address.
-    auto next_b = [&](uint32_t tx, uint32_t* slot) -> uint32_t {
+    auto next_slot = [&](uint32_t tx, uint32_t* slot) -> uint32_t {
         if (!mbar_wait_cluster(smem_u32(&s.empty[stage]), phase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
                                kWhereProducerEmpty)) {
             ok = false;
@@ -1515,6 +1542,7 @@ __device__ void pair_producer(const ConvParams& p, const Smem& s, const CUtensor
         }
         return mapa_shared(fb, 0u);
     };
+    const int kc_end = p.rem16 ? p.kfull : p.kchunks;
     for (int t = blockIdx.x >> 1; t < p.pair_tiles && ok; t += gridDim.x >> 1) {
         const TileInfo ti = decode_pair_tile(p, t, rank);
         if (p.res_prefetch && ti.v0 < p.hv) {
@@ -1527,67 +1555,34 @@ __device__ void pair_producer(const ConvParams& p, const Smem& s, const CUtensor
             const long long pix0 = (static_cast<long long>(ti.img) * p.hv + ti.v0) * p.wv + ti.u0;
             prefetch_l2_bulk(p.dup_src + pix0 * p.dup_cin, static_cast<uint32_t>(npx * p.dup_cin * 4));
         }
-        if (kMode == kModeHalo && p.ks == 3) {
-            // one stage = this CTA's halo box of (ky, chunk) and its half of the
-            // three kx taps' weights
-            const int q = ti.par >> 1, pp = ti.par & 1;
-            const int dxmin = (p.up && pp == 1) ? 0 : -1;
-            for (int ky = 0; ky < 3 && ok; ++ky) {
-                const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
-                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
-                    uint32_t slot;
-                    const uint32_t fb = next_b(p.a_tx + 3u * b_bytes, &slot);
-                    if (!ok) break;
-                    tma_load_4d_pair(smem_u32(s.a + slot * kHaloBytes), mapA, fb, kc * kBK, ti.u0 + dxmin, ti.v0 + dy,
-                                     ti.img, pol_a);
-                    for (int kx = 0; kx < 3; ++kx)
-                        tma_load_3d_pair(smem_u32(s.b + (slot * 3 + kx) * p.b_rows * 128), mapB, fb, kc * kBK,
-                                         ky * 3 + kx, ti.n0 + boff, pol_w);
-                }
+        const int q = ti.par >> 1, pp = ti.par & 1;
+        const int dxmin = (p.up && pp == 1) ? 0 : -1;
+        for (int ky = 0; ky < 3 && ok; ++ky) {
+            const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+            for (int kc = 0; kc < kc_end && ok; ++kc) {
+                uint32_t slot;
+                const uint32_t fb = next_slot(p.a_tx + 3u * b_bytes, &slot);
+                if (!ok) break;
+                tma_load_4d_pair(smem_u32(s.a + slot * kHaloBytes), mapA, fb, kc * kBK, ti.u0 + dxmin, ti.v0 + dy,
+                                 ti.img, pol_a);
+                for (int kx = 0; kx < 3; ++kx)
+                    tma_load_3d_pair(smem_u32(s.b + (slot * 3 + kx) * p.b_rows * 128), mapB, fb, kc * kBK,
+                                     ky * 3 + kx, ti.n0 + boff, pol_w);
             }
-        } else if (kMode == kModeHalo) {
-            const int q = ti.par >> 1, pp = ti.par & 1;
-            const int dxmin = (p.up && pp == 1) ? 0 : -1;
-            for (int ky = 0; ky < 3 && ok; ++ky) {
-                const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
-                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
-                    if (!mbar_wait_cluster(smem_u32(&s.aempty[astage]), aphase ^ 1u, s.abort_flag, p.timeout_ns,
-                                           p.status, kWhereProducerEmpty)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t afb = smem_u32(&s.afull[astage]);
-                    if (rank == 0) mbar_arrive_expect_tx(afb, 2u * p.a_tx);
-                    aarmed |= 1u << astage;
-                    aarm_par = (aarm_par & ~(1u << astage)) | (aphase << astage);
-                    tma_load_4d_pair(smem_u32(s.a + astage * kHaloBytes), mapA, mapa_shared(afb, 0u), kc * kBK,
-                                     ti.u0 + dxmin, ti.v0 + dy, ti.img, pol_a);
-                    if (++astage == p.a_stages) {
-                        astage = 0;
-                        aphase ^= 1u;
-                    }
-                    for (int kx = 0; kx < 3; ++kx) {
-                        uint32_t slot;
-                        const uint32_t fb = next_b(b_bytes, &slot);
-                        if (!ok) break;
-                        tma_load_3d_pair(smem_u32(s.b + slot * p.b_rows * 128), mapB, fb, kc * kBK, ky * 3 + kx,
-                                         ti.n0 + boff, pol_w);
-                    }
+        }
+        if (p.rem16 && ok) {
+            // the last 16 channels of all three ky rows and all nine taps in one stage
+            uint32_t slot;
+            const uint32_t fb = next_slot(3u * kRemABytes + 9u * static_cast<uint32_t>(p.b_rows) * 32u, &slot);
+            if (ok) {
+                for (int ky = 0; ky < 3; ++ky) {
+                    const int dy = p.up ? (q + ky + 1) / 2 - 1 : ky - 1;
+                    tma_load_4d_pair(smem_u32(s.a + slot * kHaloBytes + ky * kRemAStride), mapA16, fb,
+                                     p.kfull * kBK, ti.u0 + dxmin, ti.v0 + dy, ti.img, pol_a);
                 }
-            }
-        } else {
-            for (int tap = 0; tap < p.taps && ok; ++tap) {
-                int dy, dx;
-                tap_offset(p, tap, ti.par, dy, dx);
-                for (int kc = 0; kc < p.kchunks; ++kc) {
-                    uint32_t slot;
-                    const uint32_t fb = next_b(b_bytes + p.a_tx, &slot);
-                    if (!ok) break;
-                    tma_load_4d_pair(smem_u32(s.a + slot * kABytes), mapA, fb, kc * kBK, ti.u0 + dx, ti.v0 + dy,
-                                     ti.img, pol_a);
-                    tma_load_3d_pair(smem_u32(s.b + slot * p.b_rows * 128), mapB, fb, kc * kBK, tap, ti.n0 + boff,
-                                     pol_w);
-                }
+                for (int tap = 0; tap < 9; ++tap)
+                    tma_load_3d_pair(smem_u32(s.b + slot * 3 * p.b_rows * 128 + tap * p.b_rows * 32), mapB16, fb,
+                                     p.kfull * kBK, tap, ti.n0 + boff, pol_w);
             }
         }
     }
@@ -1597,103 +1592,87 @@ __device__ void pair_producer(const ConvParams& p, const Smem& s, const CUtensor
     for (int st = 0; st < p.stages; ++st)
         if (armed & (1u << st))
             drain_wait(smem_u32(rank == 0 ? &s.full[st] : &s.empty[st]), (arm_par >> st) & 1u, p);
-    if (kMode == kModeHalo)
-        for (int st = 0; st < p.a_stages; ++st)
-            if (aarmed & (1u << st))
-                drain_wait(smem_u32(rank == 0 ? &s.afull[st] : &s.aempty[st]), (aarm_par >> st) & 1u, p);
 }
 
 // Even CTA: one thread issues the pair MMAs (M = 256).
 __device__ void pair_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base) {
     const uint32_t idesc = idesc_f16_f32(2 * kBM, p.BN);
-    int stage = 0, astage = 0;
-    uint32_t phase = 0, aphase = 0;
+    int stage = 0;
+    uint32_t phase = 0;
     int accbuf = 0;
     uint32_t accphase = 0;
     bool ok = true;
-    auto mma_slot = [&](uint32_t d, bool halo_a, uint32_t a_addr, int nk, int& kit) {
-        if (!mbar_wait_cluster(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
-                               kWhereMmaFull)) {
-            ok = false;
-            return;
-        }
-        tc_fence_after();
-        const uint64_t ad = sw128_kmajor_desc(halo_a ? a_addr : smem_u32(s.a + stage * kABytes));
-        const uint64_t bd = sw128_kmajor_desc(smem_u32(s.b + stage * p.b_rows * 128));
-        for (int k = 0; k < nk; ++k)
-            umma_f16_pair(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                          (kit | k) != 0 ? 1u : 0u);
-        umma_commit_pair(smem_u32(&s.empty[stage]));
-        ++kit;
-        if (++stage == p.stages) {
-            stage = 0;
-            phase ^= 1u;
-        }
-    };
+    const int kc_end = p.rem16 ? p.kfull : p.kchunks;
     for (int t = blockIdx.x >> 1; t < p.pair_tiles && ok; t += gridDim.x >> 1) {
         if (!mbar_wait_cluster(smem_u32(&s.acce[accbuf]), accphase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
                                kWhereMmaAccEmpty))
             break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
+        const int pp = decode_pair_tile(p, t, 0).par & 1;
+        const int dxmin = (p.up && pp == 1) ? 0 : -1;
         int kit = 0;
-        if (p.halo && p.ks == 3) {
-            const int pp = decode_pair_tile(p, t, 0).par & 1;
-            const int dxmin = (p.up && pp == 1) ? 0 : -1;
-            for (int ky = 0; ky < 3 && ok; ++ky)
-                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
-                    if (!mbar_wait_cluster(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
-                                           kWhereMmaFull)) {
-                        ok = false;
-                        break;
+        for (int ky = 0; ky < 3 && ok; ++ky)
+            for (int kc = 0; kc < kc_end && ok; ++kc) {
+                if (!mbar_wait_cluster(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                                       kWhereMmaFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int nk = min(4, (p.cin - kc * kBK) / 16);
+                const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
+                const uint32_t bbase = smem_u32(s.b + stage * 3 * p.b_rows * 128);
+#pragma unroll
+                for (int kx = 0; kx < 3; ++kx) {
+                    const int rel = (p.up ? (pp + kx + 1) / 2 - 1 : kx - 1) - dxmin;
+                    // a whole-row offset: the tensor core swizzles on absolute address bits
+                    const uint64_t ad = sw128_kmajor_desc(abase + static_cast<uint32_t>(rel * 128));
+                    const uint64_t bd = sw128_kmajor_desc(bbase + static_cast<uint32_t>(kx * p.b_rows * 128));
+                    if (nk == 4) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            umma_f16_pair(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k),
+                                          idesc, (kit | kx | k) != 0 ? 1u : 0u);
+                    } else {
+                        for (int k = 0; k < nk; ++k)
+                            umma_f16_pair(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k),
+                                          idesc, (kit | kx | k) != 0 ? 1u : 0u);
                     }
-                    tc_fence_after();
-                    const int nk = min(4, (p.cin - kc * kBK) / 16);
-                    const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
-                    const uint32_t bbase = smem_u32(s.b + stage * 3 * p.b_rows * 128);
+                }
+                umma_commit_pair(smem_u32(&s.empty[stage]));
+                ++kit;
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        if (p.rem16 && ok) {
+            if (!mbar_wait_cluster(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                                   kWhereMmaFull)) {
+                ok = false;
+            } else {
+                tc_fence_after();
+                // one K = 16 step per tap; the 64-channel chunks came first, so always accumulate
+                const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
+                const uint32_t bbase = smem_u32(s.b + stage * 3 * p.b_rows * 128);
+#pragma unroll
+                for (int ky = 0; ky < 3; ++ky)
 #pragma unroll
                     for (int kx = 0; kx < 3; ++kx) {
-                        const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
-                        const uint64_t ad = sw128_kmajor_desc(abase + static_cast<uint32_t>((dx - dxmin) * 128));
-                        const uint64_t bd = sw128_kmajor_desc(bbase + static_cast<uint32_t>(kx * p.b_rows * 128));
-                        for (int k = 0; k < nk; ++k)
-                            umma_f16_pair(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                                          (kit | kx | k) != 0 ? 1u : 0u);
+                        const int rel = (p.up ? (pp + kx + 1) / 2 - 1 : kx - 1) - dxmin;
+                        const uint64_t ad = sw32_kmajor_desc(abase + static_cast<uint32_t>(ky * kRemAStride) +
+                                                             static_cast<uint32_t>(rel * 32));
+                        const uint64_t bd =
+                            sw32_kmajor_desc(bbase + static_cast<uint32_t>((ky * 3 + kx) * p.b_rows * 32));
+                        umma_f16_pair(d, ad, bd, idesc, 1u);
                     }
-                    umma_commit_pair(smem_u32(&s.empty[stage]));
-                    ++kit;
-                    if (++stage == p.stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                umma_commit_pair(smem_u32(&s.empty[stage]));
+                if (++stage == p.stages) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
-        } else if (p.halo) {
-            const int pp = decode_pair_tile(p, t, 0).par & 1;
-            const int dxmin = (p.up && pp == 1) ? 0 : -1;
-            for (int ky = 0; ky < 3 && ok; ++ky)
-                for (int kc = 0; kc < p.kchunks && ok; ++kc) {
-                    if (!mbar_wait_cluster(smem_u32(&s.afull[astage]), aphase, s.abort_flag, p.timeout_ns, p.status,
-                                           kWhereMmaFull)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t abase = smem_u32(s.a + astage * kHaloBytes);
-                    const int nk = min(4, (p.cin - kc * kBK) / 16);
-                    for (int kx = 0; kx < 3 && ok; ++kx) {
-                        const int dx = p.up ? (pp + kx + 1) / 2 - 1 : kx - 1;
-                        mma_slot(d, true, abase + static_cast<uint32_t>((dx - dxmin) * 128), nk, kit);
-                    }
-                    if (!ok) break;
-                    umma_commit_pair(smem_u32(&s.aempty[astage]));
-                    if (++astage == p.a_stages) {
-                        astage = 0;
-                        aphase ^= 1u;
-                    }
-                }
-        } else {
-            for (int tap = 0; tap < p.taps && ok; ++tap)
-                for (int kc = 0; kc < p.kchunks && ok; ++kc)
-                    mma_slot(d, false, 0u, min(4, (p.cin - kc * kBK) / 16), kit);
+            }
         }
         if (!ok) break;
         umma_commit_pair(smem_u32(&s.accf[accbuf]));
@@ -1704,9 +1683,64 @@ __device__ void pair_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
     drain_wait(smem_u32(s.drain), 0u, p);
 }
 
-__device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int ew, int lane, int rank,
+// One accumulator row (pixel) of a pair tile through TMA: this warp's chunks
+// half, half + 2, ... each staged as a 32-pixel x 16-channel box (64-byte
+// swizzle) in one of the warp's two buffers and stored (or, when y is the
+// residual, added onto y in L2) by one bulk tensor operation; a buffer is
+// rewritten only after the store issued from it two boxes earlier has read it.
+__device__ __forceinline__ void pair_epi_tma_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, int v,
+                                                 int u, int q, int pp, long long pix, uint8_t* stg,
+                                                 const CUtensorMap* mapY, int quad, int half, int lane, bool valid,
+                                                 const float* sbias, uint32_t& nbox) {
+    const int seg = ti.u0 + quad * 32;  // first pixel of this warp's 32 (warp-uniform)
+    const bool store = seg < p.wv && ti.v0 < p.hv;
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 64u;
+    const uint32_t sw = static_cast<uint32_t>((lane >> 1) & 3);
+    const int nch = (min(p.BN, p.cout - ti.n0) + 15) / 16;  // 16-column chunks of this tile
+    for (int c = half; c < nch; c += 2) {
+        uint32_t acc[16];
+        __syncwarp();
+        tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
+        tmem_ld_wait_regs(acc);
+        const int o0 = ti.n0 + c * 16;
+        float val[16];
+        if (valid) {
+            compute_chunk(p, ti, acc, o0, v, u, q, pp, pix, val, nullptr, sbias);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) val[i] = 0.f;
+        }
+        const uint32_t sbase = smem_u32(stg + (nbox & 1u) * kStgBytes);
+        if (lane == 0) bulk_wait_read_1();  // the store issued from this buffer two boxes ago has read it
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + row_off +
+                                                                        ((static_cast<uint32_t>(k) ^ sw) << 4)),
+                         "f"(val[4 * k]), "f"(val[4 * k + 1]), "f"(val[4 * k + 2]), "f"(val[4 * k + 3])
+                         : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && store) {
+            if (p.epi_tma == 2)
+                tma_reduce_add_4d(mapY, sbase, o0, seg, ti.v0, ti.img);
+            else if (p.up)  // output pixels 2u + pp of row 2v + q: the (parity, W/2) view
+                tma_store_5d(mapY, sbase, o0, pp, seg, 2 * ti.v0 + q, ti.img);
+            else
+                tma_store_4d(mapY, sbase, o0, seg, ti.v0, ti.img);
+        }
+        if (lane == 0) bulk_commit_group();  // (an empty group when nothing was stored keeps the count)
+        ++nbox;
+    }
+}
+
+__device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int w, int lane, int rank,
                               const CUtensorMap* mapY) {
-    const int row = ew * 32 + lane;
+    const int quad = w & 3, half = w >> 2;
+    const int row = quad * 32 + lane;
+    uint8_t* stg = s.stg + w * 2 * kStgBytes;
+    const float* sbias = p.bias_smem ? s.bias : nullptr;
+    uint32_t nbox = 0;
     int accbuf = 0;
     uint32_t accphase = 0;
     for (int t = blockIdx.x >> 1; t < p.pair_tiles; t += gridDim.x >> 1) {
@@ -1715,22 +1749,18 @@ __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
                                         kWhereEpiAccFull)))
             break;
         tc_fence_after();
-        const int rr = row / p.Wt, cc = row % p.Wt;
-        const int v = ti.v0 + rr, u = ti.u0 + cc;
-        const bool valid = row < p.R * p.Wt && v < p.hv && u < p.wv && ti.img < p.n;
+        const int v = ti.v0, u = ti.u0 + row;
+        const bool valid = v < p.hv && u < p.wv && ti.img < p.n;
         const int q = ti.par >> 1, pp = ti.par & 1;
         const int Y = p.up ? 2 * v + q : v;
         const int X = p.up ? 2 * u + pp : u;
         const long long pix = (static_cast<long long>(ti.img) * p.H + Y) * p.W + X;
         const uint32_t tbase =
-            tmem_base + (static_cast<uint32_t>(ew * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
-        if (p.rms_out != nullptr) {
-            epilogue_rms_row(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
-        } else if (p.epi_tma) {
-            epilogue_tma_row<false>(p, ti, tbase, v, u, q, pp, pix, s.stg, mapY, ew, lane, valid);
-        } else {
-            epilogue_plain_row<true>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix);
-        }
+            tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
+        if (p.epi_tma)
+            pair_epi_tma_row(p, ti, tbase, v, u, q, pp, pix, stg, mapY, quad, half, lane, valid, sbias, nbox);
+        else
+            epilogue_plain_row<true>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix, 0, lane, sbias, half, 2);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&s.acce[accbuf]), 0u));
@@ -1740,9 +1770,9 @@ __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
     if (p.epi_tma && lane == 0) bulk_wait_all();  // boxes read and written before the CTA exits
 }
 
-template <int kMode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     conv_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                     const __grid_constant__ CUtensorMap mapA16, const __grid_constant__ CUtensorMap mapB16,
                      const __grid_constant__ CUtensorMap mapY, const ConvParams p) {
     extern __shared__ uint8_t smem_raw[];
     const Smem s = carve(smem_raw, p);
@@ -1751,19 +1781,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     const int rank = static_cast<int>(cluster_ctarank());
     if (threadIdx.x == 0) {
         *s.abort_flag = 0;
-        const uint32_t fullc = 1u;  // the even producer's arrive; both CTAs' bytes as transactions
         for (int i = 0; i < p.stages; ++i) {
-            mbar_init(smem_u32(&s.full[i]), fullc);
+            mbar_init(smem_u32(&s.full[i]), 1u);  // the even producer's arrive; both CTAs' bytes as transactions
             mbar_init(smem_u32(&s.empty[i]), 1u);
         }
-        if (kMode == kModeHalo && p.ks != 3)  // the separate halo-box ring
-            for (int i = 0; i < p.a_stages; ++i) {
-                mbar_init(smem_u32(&s.afull[i]), fullc);
-                mbar_init(smem_u32(&s.aempty[i]), 1u);
-            }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s.accf[i]), 1u);
-            mbar_init(smem_u32(&s.acce[i]), static_cast<uint32_t>(2 * kEpiWarps));
+            mbar_init(smem_u32(&s.acce[i]), static_cast<uint32_t>(2 * kPairEpiWarps));
         }
         mbar_init(smem_u32(s.drain), 1u);
         fence_mbar_init();
@@ -1773,42 +1797,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                                : p.acc_stride * 2 <= 128 ? 128u
                                : p.acc_stride * 2 <= 256 ? 256u
                                                           : 512u;
-    if (warp == kMmaWarp) {
+    if (warp == kPairMmaWarp) {
         tmem_alloc_pair(smem_u32(s.tmem_slot), tmem_cols);
         tmem_relinquish_pair();
     }
-    if (warp == kProducerWarp && lane == 0) {
+    if (warp == kPairProducerWarp && lane == 0) {
         tma_prefetch_desc(&mapA);
         tma_prefetch_desc(&mapB);
+        if (p.rem16) {
+            tma_prefetch_desc(&mapA16);
+            tma_prefetch_desc(&mapB16);
+        }
         if (p.epi_tma) tma_prefetch_desc(&mapY);
     }
+    // everything above touches only shared memory, TMEM and kernel parameters
+    pdl_wait();
+    if (p.bias_smem)  // visible to the epilogue after the barriers below
+        for (int i = threadIdx.x; i < p.cout; i += blockDim.x) s.bias[i] = __ldg(p.bias + i);
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // both CTAs' barriers and TMEM exist before any remote arrive or pair MMA
     tc_fence_after();
     const uint32_t tmem_base = *s.tmem_slot;
 
-    if (warp < kEpiWarps) {
+    if (warp < kPairEpiWarps) {
         pair_epilogue(p, s, tmem_base, warp, lane, rank, &mapY);
-    } else if (warp == kProducerWarp) {
-        if (lane == 0) pair_producer<kMode>(p, s, &mapA, &mapB, rank);
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kPairProducerWarp) {
+        if (lane == 0) pair_producer(p, s, &mapA, &mapB, &mapA16, &mapB16, rank);
+    } else if (warp == kPairMmaWarp) {
         if (lane == 0 && rank == 0) pair_mma(p, s, tmem_base);
     }
+    pdl_launch_dependents();
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // the even CTA's MMAs into both TMEMs are done; no remote arrives remain
-    if (warp == kMmaWarp) {
+    if (warp == kPairMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, tmem_cols);
     }
 }
 
+// The CTA-pair kernel takes the convs it covers unless VAE_CONV_CTA_PAIR=0 is
+// set in the environment (the single-CTA kernel then runs them; for tests and
+// measurements).
 bool cta_pair_enabled() {
     static const bool on = [] {
         const char* e = std::getenv("VAE_CONV_CTA_PAIR");
-        return e != nullptr && e[0] == '1';
+        return !(e != nullptr && e[0] == '0');
     }();
     return on;
 }
@@ -1860,18 +1896,17 @@ int choose_bn(int cout, bool halo3) {
     return best;
 }
 
-template <int kMode>
-int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& my, size_t smem,
-                int grid, cudaStream_t stream) {
+int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma16,
+                const CUtensorMap& mb16, const CUtensorMap& my, size_t smem, int grid, cudaStream_t stream) {
     static CtxOnce attr_set;
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
     if (!attr_set.done(dev)) {
-        VAE_CUDA_CHECK(
-            cudaFuncSetAttribute(conv_pair_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+        VAE_CUDA_CHECK(cudaFuncSetAttribute(conv_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set.mark(dev);
     }
-    conv_pair_kernel<kMode><<<grid, 192, smem, stream>>>(ma, mb, my, p);
+    VAE_CUDA_CHECK(launch_kernel(conv_pair_kernel, dim3(grid), dim3(kPairThreads), smem, stream, ma, mb, ma16, mb16, my,
+                                 p));
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -2249,52 +2284,89 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         }
         return true;
     };
-    // CTA pairs (cta_group::2) are correct and tested but measured 22-30 % slower
-    // than single CTAs on GB300 at every decoder shape, so they run only when
-    // requested (VAE_CONV_CTA_PAIR=1 in the environment).
-    if (cta_pair_enabled() && (mode == kModeTma || mode == kModeHalo) && !a.no_pair && p.tiles_y >= 2 && nsm >= 2 &&
-        a.taps != 27 && !a.subpix && !a.refl && !a.down && a.gn_part == nullptr) {
-        // CTA pairs: two row tiles share every weight tile (half each) through cta_group::2
-        p.pair = 1;
-        p.rem16 = 0;  // the pair kernel loads zero-filled 64-channel remainder boxes
-        p.epi_tma = 0;
-        p.bias_smem = 0;
-        const size_t stg = encode_epi() ? static_cast<size_t>(kEpiWarps) * kStgBytes : 0;
-        if (stg) p.epi_tma = res_self ? 2 : 1;
-        p.ks = 1;
-        p.b_rows = p.BN / 2;
-        p.typ_tiles = (p.tiles_y + 1) / 2;
-        const long long pt = static_cast<long long>(p.n) * p.typ_tiles * p.npar * p.tiles_x * p.n_tiles;
+    // CTA pairs (cta_group::2): two row tiles of one column block share every
+    // weight tile, half in each SM, on the three-tap halo stages. Plain 2-D 3x3
+    // convs with zero padding (with or without the nearest-2x fold) whose
+    // images have at least two tile rows; everything else runs on single CTAs.
+    if (cta_pair_enabled() && halo_geom && !a.no_pair && (mode == kModeTma || mode == kModeHalo) && a.taps == 9 &&
+        !a.subpix && !a.refl && !a.down && a.gn_part == nullptr && a.rms_out == nullptr && p.tiles_y >= 2 &&
+        nsm >= 2) {
+        ConvParams q = p;
+        q.pair = 1;
+        q.BN = choose_bn_small(a.cout);
+        q.b_rows = q.BN / 2;
+        q.n_tiles = (a.cout + q.BN - 1) / q.BN;
+        q.acc_stride = (q.BN + 31) / 32 * 32;
+        q.typ_tiles = (q.tiles_y + 1) / 2;
+        const long long pt = static_cast<long long>(q.n) * q.typ_tiles * q.npar * q.tiles_x * q.n_tiles;
         if (pt >= (1LL << 31)) return set_error(VAE_ERR_SHAPE, "conv: too many tiles");
-        p.pair_tiles = static_cast<int>(pt);
-        const uint64_t dims[3] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(wtaps),
-                                  static_cast<uint64_t>(a.cout)};
-        const uint64_t strides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(wtaps) * a.cin * 2};
-        const uint32_t box[3] = {static_cast<uint32_t>(kBK), 1u, static_cast<uint32_t>(p.b_rows)};
-        rc = encode_tiled(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, dims, strides, box,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
-        if (rc != VAE_OK) return rc;
-        size_t smem;
-        const int room = kMaxSmem - 1024 - kTail - static_cast<int>(stg);
-        const int pst3 = room / (kHaloBytes + 3 * p.b_rows * 128);
-        if (mode == kModeHalo && pst3 >= 3) {
-            p.ks = 3;  // three-tap stages, as in the single-CTA kernel
-            p.stages = std::min(kMaxStages, pst3);
-            p.a_stages = p.stages;
-            smem = 1024 + static_cast<size_t>(p.stages) * (kHaloBytes + 3 * p.b_rows * 128) + stg + kTail;
-        } else if (mode == kModeHalo) {
-            p.a_stages = 4;
-            p.stages = std::min(kMaxStages, (room - p.a_stages * kHaloBytes) / (p.b_rows * 128));
-            smem = 1024 + static_cast<size_t>(p.a_stages) * kHaloBytes + static_cast<size_t>(p.stages) * p.b_rows * 128 +
-                   stg + kTail;
-        } else {
-            const int sb = kABytes + p.b_rows * 128;
-            p.stages = std::min(kMaxStages, room / sb);
-            smem = 1024 + static_cast<size_t>(p.stages) * sb + stg + kTail;
+        q.pair_tiles = static_cast<int>(pt);
+        q.halo = 1;
+        q.ks = 3;
+        q.a_tx = static_cast<uint32_t>(kHaloRows * 128);
+        q.res_prefetch = (q.residual != nullptr && q.vec_ok && !q.up && q.n_tiles == 1 &&
+                          static_cast<long long>(q.Wt) * a.cout * 4 < (1LL << 31))
+                             ? 1
+                             : 0;
+        CUtensorMap pa{}, pb{}, pa16{}, pb16{};
+        bool ok = true;
+        {  // one 130-pixel halo box per (ky, chunk) of this CTA's row tile
+            const uint64_t dims[4] = {static_cast<uint64_t>(a.cin), static_cast<uint64_t>(q.wv),
+                                      static_cast<uint64_t>(q.hv), static_cast<uint64_t>(q.n_in)};
+            const uint64_t strides[3] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(q.wv) * a.cin * 2,
+                                         static_cast<uint64_t>(q.hv) * q.wv * a.cin * 2};
+            const uint32_t box[4] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kHaloRows), 1u, 1u};
+            ok = encode_tiled(&pa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.x, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B) == VAE_OK;
+            const uint64_t bdims[3] = {static_cast<uint64_t>(a.cin), 9u, static_cast<uint64_t>(a.cout)};
+            const uint64_t bstrides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(9) * a.cin * 2};
+            const uint32_t bbox[3] = {static_cast<uint32_t>(kBK), 1u, static_cast<uint32_t>(q.b_rows)};
+            ok = ok && encode_tiled(&pb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, bdims, bstrides, bbox,
+                                    CU_TENSOR_MAP_SWIZZLE_128B) == VAE_OK;
+            q.rem16 = 0;
+            q.kfull = 0;
+            if (ok && a.cin % kBK == 16 && a.cin > kBK) {
+                // exact 16-channel boxes for the remainder instead of zero-filled 64-channel ones
+                const uint32_t box16[4] = {16u, static_cast<uint32_t>(kHaloRows), 1u, 1u};
+                const uint32_t bbox16[3] = {16u, 1u, static_cast<uint32_t>(q.b_rows)};
+                if (encode_tiled(&pa16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.x, dims, strides, box16,
+                                 CU_TENSOR_MAP_SWIZZLE_32B) == VAE_OK &&
+                    encode_tiled(&pb16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, bdims, bstrides, bbox16,
+                                 CU_TENSOR_MAP_SWIZZLE_32B) == VAE_OK) {
+                    q.rem16 = 1;
+                    q.kfull = a.cin / kBK;
+                }
+            }
         }
-        const int pgrid = 2 * static_cast<int>(std::min<long long>(pt, nsm / 2));
-        return mode == kModeHalo ? launch_pair<kModeHalo>(p, ma, mb, my, smem, pgrid, stream)
-                                 : launch_pair<kModeTma>(p, ma, mb, my, smem, pgrid, stream);
+        if (ok) {
+            CUtensorMap pmy{};
+            q.epi_tma = 0;
+            q.stg_bytes = 0;
+            {
+                // encode_epi() reads p; the pair shares its output view
+                const ConvParams keep = p;
+                p = q;
+                if (encode_epi()) {
+                    q.epi_tma = res_self ? 2 : 1;
+                    q.stg_bytes = kPairStgBytes;
+                    pmy = my;
+                }
+                p = keep;
+            }
+            const size_t bias_bytes = static_cast<size_t>(a.cout * 4 + 15) / 16 * 16;
+            q.bias_smem = (bias_smem_enabled() && a.bias != nullptr && aligned16(a.bias)) ? 1 : 0;
+            const size_t stage_bytes = static_cast<size_t>(kHaloBytes) + 3u * static_cast<size_t>(q.b_rows) * 128u;
+            const size_t fixed = 1024 + static_cast<size_t>(q.stg_bytes) + (q.bias_smem ? bias_bytes : 0) + kTail;
+            const int st = static_cast<int>((kMaxSmem - fixed) / stage_bytes);
+            if (st >= 3) {
+                q.stages = std::min(kMaxStages, st);
+                q.a_stages = q.stages;
+                const size_t smem = fixed + static_cast<size_t>(q.stages) * stage_bytes;
+                const int pgrid = 2 * static_cast<int>(std::min<long long>(pt, nsm / 2));
+                return launch_pair(q, pa, pb, pa16, pb16, pmy, smem, pgrid, stream);
+            }
+        }
+        clear_error();
     }
     size_t ring = mode == kModeHalo
                       ? static_cast<size_t>(p.a_stages) * kHaloBytes + static_cast<size_t>(p.stages) * p.ks * p.BN * 128
@@ -2317,7 +2389,8 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         else
             clear_error();
     }
-    size_t smem = 1024 + ring + (p.epi_tma ? kEpiWarps * kStgBytes : 0) + kTail;
+    p.stg_bytes = p.epi_tma ? kEpiWarps * kStgBytes : 0;
+    size_t smem = 1024 + ring + p.stg_bytes + kTail;
     // A shared-memory copy of the bias where it fits: the epilogue's bias reads
     // otherwise miss the small L1 left beside the pipeline's shared memory.
     const size_t bias_bytes = static_cast<size_t>(a.cout * 4 + 15) / 16 * 16;

@@ -1485,7 +1485,10 @@ __global__ void __launch_bounds__(kMode == kModeGather ? 320 : 224, 1)
 // commits with multicast to the empty and accumulator-full barriers of both
 // CTAs; every epilogue warp of both CTAs arrives on the even CTA's
 // accumulator-empty barrier. The odd CTA learns its copies landed from its
-// empty barriers (the MMAs that read them completed).
+// empty barriers (the MMAs that read them completed). The ring's waits (full,
+// empty) order only async-proxy traffic (TMA writes, tensor-core reads) and
+// take CTA scope; the accumulator handshakes, which order generic TMEM reads
+// against MMAs across the pair, take cluster scope.
 //
 // Eight epilogue warps per CTA: warp w drains TMEM lane quadrant w % 4 (its 32
 // pixels) and every other 16-column chunk starting at w / 4, through a
@@ -1496,7 +1499,6 @@ constexpr int kPairProducerWarp = 8;
 constexpr int kPairMmaWarp = 9;
 constexpr int kPairThreads = 320;
 constexpr int kPairStgBytes = kPairEpiWarps * 2 * kStgBytes;  // two boxes per epilogue warp
-constexpr int kPairStages = 4;
 
 __device__ __forceinline__ TileInfo decode_pair_tile(const ConvParams& p, int t, int rank) {
     TileInfo ti;
@@ -1526,7 +1528,7 @@ __device__ void pair_producer(const ConvParams& p, const Smem& s, const CUtensor
     // Waits for a free slot; the even CTA arms its (shared) full barrier for
     // the bytes of both CTAs. Returns the full barrier's cluster address.
     auto next_slot = [&](uint32_t tx, uint32_t* slot) -> uint32_t {
-        if (!mbar_wait_cluster(smem_u32(&s.empty[stage]), phase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
+        if (!mbar_wait(smem_u32(&s.empty[stage]), phase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
                                kWhereProducerEmpty)) {
             ok = false;
             return 0u;
@@ -1594,84 +1596,101 @@ __device__ void pair_producer(const ConvParams& p, const Smem& s, const CUtensor
             drain_wait(smem_u32(rank == 0 ? &s.full[st] : &s.empty[st]), (arm_par >> st) & 1u, p);
 }
 
-// Even CTA: one thread issues the pair MMAs (M = 256).
+// Even CTA: one thread issues the pair MMAs (M = 256). This thread's own
+// work bounds the loop (measured: a tcgen05.mma takes ~78 cycles to issue
+// against 72 cycles of tensor work at N = 144, and every stage adds its
+// barrier wait and commit), so the loop carries the shared-memory descriptors
+// as running values (slot strides added, nothing recomputed per stage) and
+// keeps the work between MMAs to the descriptor adds.
 __device__ void pair_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base) {
     const uint32_t idesc = idesc_f16_f32(2 * kBM, p.BN);
+    // Descriptors of slot 0; the start-address field counts 16-byte units and
+    // every address here stays below 2^18 bytes, so offsets add without carry.
+    const uint64_t a128 = sw128_kmajor_desc(smem_u32(s.a));
+    const uint64_t b128 = sw128_kmajor_desc(smem_u32(s.b));
+    const uint64_t a32 = sw32_kmajor_desc(smem_u32(s.a));
+    const uint64_t b32 = sw32_kmajor_desc(smem_u32(s.b));
+    const uint32_t a_slot = kHaloBytes >> 4;
+    const uint32_t b_slot = static_cast<uint32_t>(3 * p.b_rows * 128) >> 4;
+    const uint32_t b_tap = static_cast<uint32_t>(p.b_rows * 128) >> 4;
+    const uint32_t b_tap16 = static_cast<uint32_t>(p.b_rows * 32) >> 4;
+    const int kc_end = p.rem16 ? p.kfull : p.kchunks;
+    const int nk_last = min(4, (p.cin - (kc_end - 1) * kBK) / 16);  // K steps of the last 64-channel chunk
     int stage = 0;
-    uint32_t phase = 0;
+    uint32_t phase = 0, soff_a = 0, soff_b = 0;  // this slot's offsets, in descriptor units
+    auto advance = [&]() {
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+            soff_a = 0;
+            soff_b = 0;
+        } else {
+            soff_a += a_slot;
+            soff_b += b_slot;
+        }
+    };
     int accbuf = 0;
     uint32_t accphase = 0;
     bool ok = true;
-    const int kc_end = p.rem16 ? p.kfull : p.kchunks;
     for (int t = blockIdx.x >> 1; t < p.pair_tiles && ok; t += gridDim.x >> 1) {
         if (!mbar_wait_cluster(smem_u32(&s.acce[accbuf]), accphase ^ 1u, s.abort_flag, p.timeout_ns, p.status,
                                kWhereMmaAccEmpty))
             break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
-        const int pp = decode_pair_tile(p, t, 0).par & 1;
+        const int pp = p.up ? decode_pair_tile(p, t, 0).par & 1 : 0;  // (the divisions only where parity matters)
         const int dxmin = (p.up && pp == 1) ? 0 : -1;
-        int kit = 0;
+        // row offset of tap kx inside the halo box, in 128-byte rows
+        uint32_t rel[3];
+#pragma unroll
+        for (int kx = 0; kx < 3; ++kx) rel[kx] = static_cast<uint32_t>((p.up ? (pp + kx + 1) / 2 - 1 : kx - 1) - dxmin);
+        uint32_t acc = 0u;  // the tile's first MMA overwrites the accumulator
         for (int ky = 0; ky < 3 && ok; ++ky)
-            for (int kc = 0; kc < kc_end && ok; ++kc) {
-                if (!mbar_wait_cluster(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
-                                       kWhereMmaFull)) {
+            for (int kc = 0; kc < kc_end; ++kc) {
+                if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                               kWhereMmaFull)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int nk = min(4, (p.cin - kc * kBK) / 16);
-                const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
-                const uint32_t bbase = smem_u32(s.b + stage * 3 * p.b_rows * 128);
+                const uint64_t ad = a128 + soff_a;
+                const uint64_t bd = b128 + soff_b;
+                if (kc + 1 < kc_end || nk_last == 4) {
 #pragma unroll
-                for (int kx = 0; kx < 3; ++kx) {
-                    const int rel = (p.up ? (pp + kx + 1) / 2 - 1 : kx - 1) - dxmin;
-                    // a whole-row offset: the tensor core swizzles on absolute address bits
-                    const uint64_t ad = sw128_kmajor_desc(abase + static_cast<uint32_t>(rel * 128));
-                    const uint64_t bd = sw128_kmajor_desc(bbase + static_cast<uint32_t>(kx * p.b_rows * 128));
-                    if (nk == 4) {
+                    for (int kx = 0; kx < 3; ++kx)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            umma_f16_pair(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k),
-                                          idesc, (kit | kx | k) != 0 ? 1u : 0u);
-                    } else {
-                        for (int k = 0; k < nk; ++k)
-                            umma_f16_pair(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k),
-                                          idesc, (kit | kx | k) != 0 ? 1u : 0u);
-                    }
+                        for (int k = 0; k < 4; ++k) {
+                            umma_f16_pair(d, ad + rel[kx] * 8u + 2u * k, bd + kx * b_tap + 2u * k, idesc, acc);
+                            acc = 1u;
+                        }
+                } else {
+                    for (int kx = 0; kx < 3; ++kx)
+                        for (int k = 0; k < nk_last; ++k) {
+                            umma_f16_pair(d, ad + rel[kx] * 8u + 2u * k, bd + kx * b_tap + 2u * k, idesc, acc);
+                            acc = 1u;
+                        }
                 }
                 umma_commit_pair(smem_u32(&s.empty[stage]));
-                ++kit;
-                if (++stage == p.stages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                advance();
             }
         if (p.rem16 && ok) {
-            if (!mbar_wait_cluster(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
-                                   kWhereMmaFull)) {
+            if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                           kWhereMmaFull)) {
                 ok = false;
             } else {
                 tc_fence_after();
-                // one K = 16 step per tap; the 64-channel chunks came first, so always accumulate
-                const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
-                const uint32_t bbase = smem_u32(s.b + stage * 3 * p.b_rows * 128);
+                // one K = 16 step per tap (the 64-channel chunks came first: always accumulate):
+                // box ky at ky * kRemAStride, 32-byte rows; tap (ky, kx) weights at (ky * 3 + kx) * b_rows * 32
+                const uint64_t ad = a32 + soff_a;
+                const uint64_t bd = b32 + soff_b;
 #pragma unroll
                 for (int ky = 0; ky < 3; ++ky)
 #pragma unroll
-                    for (int kx = 0; kx < 3; ++kx) {
-                        const int rel = (p.up ? (pp + kx + 1) / 2 - 1 : kx - 1) - dxmin;
-                        const uint64_t ad = sw32_kmajor_desc(abase + static_cast<uint32_t>(ky * kRemAStride) +
-                                                             static_cast<uint32_t>(rel * 32));
-                        const uint64_t bd =
-                            sw32_kmajor_desc(bbase + static_cast<uint32_t>((ky * 3 + kx) * p.b_rows * 32));
-                        umma_f16_pair(d, ad, bd, idesc, 1u);
-                    }
+                    for (int kx = 0; kx < 3; ++kx)
+                        umma_f16_pair(d, ad + static_cast<uint32_t>(ky * (kRemAStride >> 4)) + rel[kx] * 2u,
+                                      bd + static_cast<uint32_t>(ky * 3 + kx) * b_tap16, idesc, 1u);
                 umma_commit_pair(smem_u32(&s.empty[stage]));
-                if (++stage == p.stages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
+                advance();
             }
         }
         if (!ok) break;

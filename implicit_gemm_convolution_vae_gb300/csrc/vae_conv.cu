@@ -599,6 +599,29 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
     // slot, per-tap path) against the A tile at `a_addr` (halo) or in the slot.
     // reflect-padded downsample: stages come through the fixer warp
     const uint64_t* tap_ready = (is_2d(kVar) && p.refl && p.down_tma) ? s.fixed : s.full;
+    // Three-tap halo stages: descriptors of slot 0 and slot strides. The
+    // start-address field counts 16-byte units and every address here stays
+    // below 2^18 bytes, so offsets add without carry.
+    const uint64_t h_a128 = sw128_kmajor_desc(smem_u32(s.a));
+    const uint64_t h_b128 = sw128_kmajor_desc(smem_u32(s.b));
+    const uint64_t h_a32 = sw32_kmajor_desc(smem_u32(s.a));
+    const uint64_t h_b32 = sw32_kmajor_desc(smem_u32(s.b));
+    const uint32_t h_aslot = kHaloBytes >> 4;
+    const uint32_t h_bslot = static_cast<uint32_t>(3 * p.BN * 128) >> 4;
+    const uint32_t h_btap = static_cast<uint32_t>(p.BN * 128) >> 4;
+    const uint32_t h_btap16 = static_cast<uint32_t>(p.BN * 32) >> 4;
+    uint32_t h_soff_a = 0, h_soff_b = 0;  // the current slot's offsets, in descriptor units
+    auto h_advance = [&]() {
+        if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+            h_soff_a = 0;
+            h_soff_b = 0;
+        } else {
+            h_soff_a += h_aslot;
+            h_soff_b += h_bslot;
+        }
+    };
     auto mma_slot = [&](uint32_t d, bool halo_a, uint32_t a_addr, int kc0, int nck, int& kit) {
         if (!mbar_wait(smem_u32(&tap_ready[stage]), phase, s.abort_flag, p.timeout_ns, p.status, kWhereMmaFull)) {
             ok = false;
@@ -628,49 +651,48 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
         const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
         int kit = 0;
         if (p.halo && p.ks == 3) {
-            const TileInfo ti = decode_tile<kT3>(p, t);
-            const int pp = ti.par & 1;
+            // Three-tap stages with running descriptors (slot strides added, no
+            // per-stage recomputation): the issuing thread's own work between
+            // MMAs bounds this loop at N <= 144.
+            const int pp = (p.up || kVar == 2) ? decode_tile<kT3>(p, t).par & 1 : 0;
             const int dxmin = (p.up && pp == 1) ? 0 : -1;
             const int kc_end = p.rem16 ? p.kfull : p.kchunks;
+            const int nk_last = min(4, (p.cin - (kc_end - 1) * kBK) / 16);
             // reflect padding: the fixer warp has mirrored the edge columns; wait for it
             const uint64_t* ready = (is_2d(kVar) && p.refl) ? s.fixed : s.full;
+            uint32_t rel[NK];  // row offset of tap kx inside the halo box, in box rows
+#pragma unroll
+            for (int kx = 0; kx < NK; ++kx)
+                rel[kx] = static_cast<uint32_t>(kVar == 2 ? kx : (p.up ? (pp + kx + 1) / 2 - 1 : kx - 1) - dxmin);
+            uint32_t acc = 0u;  // the tile's first MMA overwrites the accumulator
             for (int kt = 0; kt < (kT3 ? p.nkt : 1) && ok; ++kt) {  // temporal taps (3-D); one pass for 2-D
                 for (int ky = 0; ky < NK && ok; ++ky) {
-                    for (int kc = 0; kc < kc_end && ok; ++kc) {
+                    for (int kc = 0; kc < kc_end; ++kc) {
                         if (!mbar_wait(smem_u32(&ready[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
                                        kWhereMmaFull)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        // All MMAs of the stage go out back to back: the tensor core's
-                        // issue queue then covers this thread's barrier work.
-                        const int nk = min(4, (p.cin - kc * kBK) / 16);
-                        const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
-                        const uint32_t bbase = smem_u32(s.b + stage * 3 * p.BN * 128);
-    #pragma unroll
-                        for (int kx = 0; kx < NK; ++kx) {
-                            const int rel = kVar == 2 ? kx : (p.up ? (pp + kx + 1) / 2 - 1 : kx - 1) - dxmin;
-                            // a whole-row offset: the tensor core swizzles on absolute address bits
-                            const uint64_t ad = sw128_kmajor_desc(abase + static_cast<uint32_t>(rel * 128));
-                            const uint64_t bd = sw128_kmajor_desc(bbase + static_cast<uint32_t>(kx * p.BN * 128));
-                            if (nk == 4) {
-    #pragma unroll
-                                for (int k = 0; k < 4; ++k)
-                                    umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                                             (kit | kx | k) != 0 ? 1u : 0u);
-                            } else {
-                                for (int k = 0; k < nk; ++k)
-                                    umma_f16(d, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(2 * k), idesc,
-                                             (kit | kx | k) != 0 ? 1u : 0u);
-                            }
+                        const uint64_t ad = h_a128 + h_soff_a;
+                        const uint64_t bd = h_b128 + h_soff_b;
+                        if (kc + 1 < kc_end || nk_last == 4) {
+#pragma unroll
+                            for (int kx = 0; kx < NK; ++kx)
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    umma_f16(d, ad + rel[kx] * 8u + 2u * k, bd + kx * h_btap + 2u * k, idesc, acc);
+                                    acc = 1u;
+                                }
+                        } else {
+                            for (int kx = 0; kx < NK; ++kx)
+                                for (int k = 0; k < nk_last; ++k) {
+                                    umma_f16(d, ad + rel[kx] * 8u + 2u * k, bd + kx * h_btap + 2u * k, idesc, acc);
+                                    acc = 1u;
+                                }
                         }
                         umma_commit(smem_u32(&s.empty[stage]));
-                        ++kit;
-                        if (++stage == p.stages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                        h_advance();
                     }
                 }
                 if (p.rem16 && ok) {
@@ -679,26 +701,18 @@ __device__ void role_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
                         ok = false;
                     } else {
                         tc_fence_after();
-                        // one K = 16 step per tap; the 64-channel chunks came first, so always accumulate
-                        const uint32_t abase = smem_u32(s.a + stage * kHaloBytes);
-                        const uint32_t bbase = smem_u32(s.b + stage * 3 * p.BN * 128);
-    #pragma unroll
+                        // one K = 16 step per tap; the 64-channel chunks came first, so always accumulate:
+                        // box ky at ky * kRemAStride, 32-byte rows; tap (ky, kx) weights at (ky * NK + kx) * BN * 32
+                        const uint64_t ad = h_a32 + h_soff_a;
+                        const uint64_t bd = h_b32 + h_soff_b;
+#pragma unroll
                         for (int ky = 0; ky < NK; ++ky)
-    #pragma unroll
-                            for (int kx = 0; kx < NK; ++kx) {
-                                const int rel = kVar == 2 ? kx : (p.up ? (pp + kx + 1) / 2 - 1 : kx - 1) - dxmin;
-                                const uint64_t ad = sw32_kmajor_desc(abase + static_cast<uint32_t>(ky * kRemAStride) +
-                                                                     static_cast<uint32_t>(rel * 32));
-                                const uint64_t bd =
-                                    sw32_kmajor_desc(bbase + static_cast<uint32_t>((ky * NK + kx) * p.BN * 32));
-                                umma_f16(d, ad, bd, idesc, 1u);
-                            }
+#pragma unroll
+                            for (int kx = 0; kx < NK; ++kx)
+                                umma_f16(d, ad + static_cast<uint32_t>(ky * (kRemAStride >> 4)) + rel[kx] * 2u,
+                                         bd + static_cast<uint32_t>(ky * NK + kx) * h_btap16, idesc, 1u);
                         umma_commit(smem_u32(&s.empty[stage]));
-                        ++kit;
-                        if (++stage == p.stages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                        h_advance();
                     }
                 }
             }

@@ -1767,6 +1767,78 @@ __device__ __forceinline__ void pair_epi_tma_row(const ConvParams& p, const Tile
     }
 }
 
+// The fused RMS_norm of a pair tile's pixel (one N tile holds all cout <= 144
+// channels; f16 rows only, no residual): each warp of the lane quadrant forms
+// the pixel's sum of squares over all its chunks in the standalone kernel's
+// order (channel quad i into partial sum i % 4, chunks in order, then the
+// butterfly) -- a split between the two warps would need another order, which
+// slows the standalone kernel -- then normalises its own chunks (half,
+// half + 2, ...) and stores them as 32-pixel x 16-channel f16 boxes (32-byte
+// rows, 32-byte swizzle) from two 1 KB staging buffers.
+__device__ __forceinline__ void pair_epi_tma_rms_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, int v,
+                                                     int u, int q, int pp, long long pix, uint8_t* stg,
+                                                     const CUtensorMap* mapY, int quad, int half, int lane,
+                                                     const float* sbias, uint32_t& nbox) {
+    const int nch = p.cout / 16;
+    float part[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int c = 0; c < nch; ++c) {
+        uint32_t acc[16];
+        __syncwarp();
+        tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
+        tmem_ld_wait_regs(acc);
+        float val[16];
+        compute_chunk(p, ti, acc, c * 16, v, u, q, pp, pix, val, nullptr, sbias);
+#pragma unroll
+        for (int l = 0; l < 4; ++l) part[l] = rms_acc4(part[l], val[4 * l], val[4 * l + 1], val[4 * l + 2], val[4 * l + 3]);
+    }
+    part[0] = __fadd_rn(part[0], part[2]);
+    part[1] = __fadd_rn(part[1], part[3]);
+    part[0] = __fadd_rn(part[0], part[1]);
+    const float inv = rms_inv(part[0], p.cout);
+    const int seg = ti.u0 + quad * 32;
+    const bool store = seg < p.wv && ti.v0 < p.hv;
+    const uint32_t row_off = static_cast<uint32_t>(lane) * 32u;
+    const uint32_t sw = static_cast<uint32_t>((lane >> 2) & 1);
+    for (int c = half; c < nch; c += 2) {
+        uint32_t acc[16];
+        __syncwarp();
+        tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
+        tmem_ld_wait_regs(acc);
+        float val[16];
+        compute_chunk(p, ti, acc, c * 16, v, u, q, pp, pix, val, nullptr, sbias);
+        uint32_t hv[8];
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+            const int o = c * 16 + 4 * i4;
+            const float4 g = __ldg(reinterpret_cast<const float4*>(p.rms_gamma + o));
+            float a[4] = {rms_apply(val[4 * i4], inv, g.x), rms_apply(val[4 * i4 + 1], inv, g.y),
+                          rms_apply(val[4 * i4 + 2], inv, g.z), rms_apply(val[4 * i4 + 3], inv, g.w)};
+            if (p.rms_silu) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) a[e] = silu_f(a[e]);
+            }
+            __half2 t0 = __floats2half2_rn(a[0], a[1]);
+            __half2 t1 = __floats2half2_rn(a[2], a[3]);
+            hv[2 * i4] = *reinterpret_cast<uint32_t*>(&t0);
+            hv[2 * i4 + 1] = *reinterpret_cast<uint32_t*>(&t1);
+        }
+        const uint32_t sbase = smem_u32(stg + (nbox & 1u) * (kStgBytes / 2));
+        if (lane == 0) bulk_wait_read_1();  // the store issued from this buffer two boxes ago has read it
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(sbase + row_off +
+                                                                        ((static_cast<uint32_t>(k) ^ sw) << 4)),
+                         "r"(hv[4 * k]), "r"(hv[4 * k + 1]), "r"(hv[4 * k + 2]), "r"(hv[4 * k + 3])
+                         : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && store) tma_store_4d(mapY, sbase, c * 16, seg, ti.v0, ti.img);
+        if (lane == 0) bulk_commit_group();
+        ++nbox;
+    }
+}
+
 __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int w, int lane, int rank,
                               const CUtensorMap* mapY) {
     const int quad = w & 3, half = w >> 2;
@@ -1790,7 +1862,9 @@ __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         const long long pix = (static_cast<long long>(ti.img) * p.H + Y) * p.W + X;
         const uint32_t tbase =
             tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
-        if (p.epi_tma)
+        if (p.epi_tma == 3)
+            pair_epi_tma_rms_row(p, ti, tbase, v, u, q, pp, pix, stg, mapY, quad, half, lane, sbias, nbox);
+        else if (p.epi_tma)
             pair_epi_tma_row(p, ti, tbase, v, u, q, pp, pix, stg, mapY, quad, half, lane, valid, sbias, nbox);
         else
             epilogue_plain_row<true>(p, ti, tbase, valid, v, u, q, pp, Y, X, pix, 0, lane, sbias, half, 2);
@@ -2321,9 +2395,14 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
     // weight tile, half in each SM, on the three-tap halo stages. Plain 2-D 3x3
     // convs with zero padding (with or without the nearest-2x fold) whose
     // images have at least two tile rows; everything else runs on single CTAs.
+    // The fused RMS_norm rides along when one N tile holds a pixel's channels and
+    // the conv writes only the normalised f16 rows.
+    const bool pair_rms = a.rms_out != nullptr && a.y == nullptr && a.residual == nullptr && a.dup_src == nullptr &&
+                          !a.up && a.cout <= 144 && a.cout % 16 == 0 && aligned16(a.rms_gamma) &&
+                          aligned16(a.rms_out);
     if (cta_pair_enabled() && halo_geom && !a.no_pair && (mode == kModeTma || mode == kModeHalo) && a.taps == 9 &&
-        !a.subpix && !a.refl && !a.down && a.gn_part == nullptr && a.rms_out == nullptr && p.tiles_y >= 2 &&
-        nsm >= 2) {
+        !a.subpix && !a.refl && !a.down && a.gn_part == nullptr && (a.rms_out == nullptr || pair_rms) &&
+        p.tiles_y >= 2 && nsm >= 2) {
         ConvParams q = p;
         q.pair = 1;
         q.BN = choose_bn_small(a.cout);
@@ -2379,7 +2458,21 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                 // encode_epi() reads p; the pair shares its output view
                 const ConvParams keep = p;
                 p = q;
-                if (encode_epi()) {
+                if (pair_rms) {
+                    const uint64_t dims[4] = {static_cast<uint64_t>(a.cout), static_cast<uint64_t>(q.W),
+                                              static_cast<uint64_t>(q.H), static_cast<uint64_t>(q.n)};
+                    const uint64_t strides[3] = {static_cast<uint64_t>(a.cout) * 2,
+                                                 static_cast<uint64_t>(q.W) * a.cout * 2,
+                                                 static_cast<uint64_t>(q.H) * q.W * a.cout * 2};
+                    const uint32_t box[4] = {16u, 32u, 1u, 1u};
+                    if (encode_tiled(&pmy, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, a.rms_out, dims, strides, box,
+                                     CU_TENSOR_MAP_SWIZZLE_32B) == VAE_OK) {
+                        q.epi_tma = 3;
+                        q.stg_bytes = kPairStgBytes;
+                    } else {
+                        ok = false;
+                    }
+                } else if (encode_epi()) {
                     q.epi_tma = res_self ? 2 : 1;
                     q.stg_bytes = kPairStgBytes;
                     pmy = my;
@@ -2391,7 +2484,7 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
             const size_t stage_bytes = static_cast<size_t>(kHaloBytes) + 3u * static_cast<size_t>(q.b_rows) * 128u;
             const size_t fixed = 1024 + static_cast<size_t>(q.stg_bytes) + (q.bias_smem ? bias_bytes : 0) + kTail;
             const int st = static_cast<int>((kMaxSmem - fixed) / stage_bytes);
-            if (st >= 3) {
+            if (ok && st >= 3) {
                 q.stages = std::min(kMaxStages, st);
                 q.a_stages = q.stages;
                 const size_t smem = fixed + static_cast<size_t>(q.stages) * stage_bytes;

@@ -204,6 +204,7 @@ def test_subpixel_up_conv_full_size_sampled():
 
 @pytest.mark.parametrize("n,h,w,cin,cout,kw", [
     (1, 6, 256, 144, 144, {}),                    # staged two-pass epilogue (rows of >= 128 pixels)
+    (2, 5, 130, 144, 144, {}),                    # CTA pairs over an odd tile-row count, two images
     (1, 5, 200, 64, 64, {}),                      # ragged last tile
     (2, 9, 40, 32, 48, {}),                       # rows shorter than a tile: the register form
     (1, 4, 130, 80, 16, {"reflect": True}),

@@ -193,6 +193,7 @@ __device__ void scores_producer(const ScoreParams& p, const ASmem& s, const CUte
 
 __device__ void scores_mma(const ScoreParams& p, const ASmem& s, uint32_t tmem) {
     const uint32_t id_s = idesc_f16_f32(128, 256);
+    const uint64_t q_desc0 = sw128_kmajor_desc(smem_u32(s.ring));  // every ring address stays below 2^18 bytes
     RingT<kScStages> r;
     bool ok = true;
     const int npair = (p.nkb + 1) / 2;
@@ -208,13 +209,13 @@ __device__ void scores_mma(const ScoreParams& p, const ASmem& s, uint32_t tmem) 
                 break;
             }
             tc_fence_after();
-            uint8_t* st = s.ring + r.stage * kScStageBytes;
-            const uint64_t ad = sw128_kmajor_desc(smem_u32(st));
-            const uint64_t bd = sw128_kmajor_desc(smem_u32(st + 16384));
+            // slot descriptors as running values (16-byte units: slot r.stage at r.stage * kScStageBytes)
+            const uint64_t ad = q_desc0 + static_cast<uint32_t>(r.stage) * (kScStageBytes >> 4);
+            const uint64_t bd = ad + (16384u >> 4);
+            const uint32_t dS = tmem + static_cast<uint32_t>(b * 256);
+            umma_f16(dS, ad, bd, id_s, cc != 0 ? 1u : 0u);  // S(128 x 256) += Q_c K_c^T, K = 16 per step
 #pragma unroll
-            for (int k = 0; k < 4; ++k)  // S(128 x 256) += Q_c K_c^T, K = 16 per step
-                umma_f16(tmem + static_cast<uint32_t>(b * 256), ad + static_cast<uint64_t>(2 * k),
-                         bd + static_cast<uint64_t>(2 * k), id_s, (cc | k) != 0 ? 1u : 0u);
+            for (int k = 1; k < 4; ++k) umma_f16(dS, ad + 2u * k, bd + 2u * k, id_s, 1u);
             umma_commit(smem_u32(&s.empty[r.stage]));
             r.next();
         }
@@ -382,6 +383,8 @@ __device__ void pv_mma(const PvParams& p, const ASmem& s, uint32_t tmem, const u
     const int nsplit = p.dv > 256 ? 2 : 1;
     const int ns = p.dv / nsplit;
     const uint32_t id_o = idesc_f16_f32(128, ns);
+    const uint64_t p_desc0 = sw128_kmajor_desc(smem_u32(s.ring));  // every ring address stays below 2^18 bytes
+    const uint32_t v_split = static_cast<uint32_t>(ns * 128) >> 4;   // second V^T half, in descriptor units
     Ring r;
     uint32_t ev = 0;
     bool ok = true;
@@ -403,15 +406,21 @@ __device__ void pv_mma(const PvParams& p, const ASmem& s, uint32_t tmem, const u
                 break;
             }
             tc_fence_after();
-            uint8_t* st = s.ring + r.stage * kStageBytes;
-            const uint64_t ad = sw128_kmajor_desc(smem_u32(st));
+            // slot descriptors as running values: P half at the slot, V^T halves after it
+            const uint64_t ad = p_desc0 + static_cast<uint32_t>(r.stage) * (kStageBytes >> 4);
+            const uint64_t bd0 = ad + (static_cast<uint32_t>(kPHalfBytes) >> 4);
+            const uint32_t acc0 = (j | half) != 0 ? 1u : 0u;
+            if (nsplit == 2) {
+                const uint64_t bd1 = bd0 + v_split;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                for (int sp = 0; sp < nsplit; ++sp) {
-                    const uint64_t bd = sw128_kmajor_desc(smem_u32(st + kPHalfBytes + sp * ns * 128));
-                    umma_f16(tmem + static_cast<uint32_t>(sp * ns), ad + 2 * k, bd + 2 * k, id_o,
-                             (j | half | k) != 0 ? 1u : 0u);
+                for (int k = 0; k < 4; ++k) {
+                    umma_f16(tmem, ad + 2u * k, bd0 + 2u * k, id_o, k != 0 ? 1u : acc0);
+                    umma_f16(tmem + static_cast<uint32_t>(ns), ad + 2u * k, bd1 + 2u * k, id_o, k != 0 ? 1u : acc0);
                 }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) umma_f16(tmem, ad + 2u * k, bd0 + 2u * k, id_o, k != 0 ? 1u : acc0);
+            }
             umma_commit(smem_u32(&s.empty[r.stage]));
             r.next();
         }

@@ -29,6 +29,7 @@
 // whose P fits a 2 GiB workspace. Every wait is bounded.
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 
 #include "vae_attn.h"
 #include "vae_conv.h"
@@ -45,7 +46,7 @@ constexpr int kStages = 3;
 constexpr int kScStageBytes = 48 * 1024;
 constexpr int kScStages = 4;
 static_assert(kScStages * kScStageBytes <= kStages * kStageBytes, "scores ring over the shared ring bytes");
-constexpr int kRingBars = 4;  // barrier slots of each ring array
+constexpr int kRingBars = 8;  // barrier slots of each ring array
 static_assert(1024 + kStages * kStageBytes + 256 <= 232448, "attention shared memory over 227 KB");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxDv = 384;
@@ -69,6 +70,7 @@ struct ScoreParams {
 
 struct PvParams {
     int m, c, dv, ndv, nkb;
+    int ntiles;    // query tiles of this group (the pair kernel's odd last tile may be missing)
     int q_tile0, grows;
     int vbox_rows, vboxes;
     const float* alpha;
@@ -107,11 +109,12 @@ struct ASmem {
     int* abort_flag;
 };
 
-__device__ __forceinline__ ASmem carve_attn(uint8_t* raw) {
+// ring_bytes: the ring's size; the barriers (<= 256 bytes) follow it.
+__device__ __forceinline__ ASmem carve_attn(uint8_t* raw, int ring_bytes = kStages * kStageBytes) {
     ASmem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     s.ring = base;
-    uint64_t* b = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes);
+    uint64_t* b = reinterpret_cast<uint64_t*>(base + ring_bytes);
     s.full = b;
     s.empty = b + kRingBars;
     s.s_full = b + 2 * kRingBars;
@@ -541,6 +544,248 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ───────────────────────── PV kernel on CTA pairs ─────────────────────────
+// A cluster of two CTAs computes O for two query tiles (2t, 2t + 1 of the
+// group) and one value chunk with tcgen05.mma.cta_group::2 (M = 256): each CTA
+// streams its own tile's 64-key P half and HALF of every V^T box (the rows of
+// N that the pair MMA takes from it), so per SM a stage carries 40 KB instead
+// of 64 KB (the single-CTA kernel is bound by the bytes each SM takes in from
+// L2). Both CTAs' copies complete on the even CTA's full barrier (armed once
+// for the bytes of both); the even CTA's MMA thread commits with multicast.
+// Rescaling follows the union of the two tiles' flags: on a flagged block j
+// the row warps of BOTH CTAs scale their O rows (by 1 where their rows did
+// not move) and arrive on the even CTA's `scaled` barrier. A missing odd tile
+// (an odd tile count) reads zero-filled P, scales by 1 and stores nothing.
+constexpr int kPvPairStageBytes = 40 * 1024;  // P half 16 KB + two V^T half boxes of <= 96 rows x 128 B
+constexpr int kPvPairStages = 5;
+static_assert(1024 + kPvPairStages * kPvPairStageBytes + 256 <= 232448, "PV pair shared memory over 227 KB");
+
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                 int c1, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ bool wait_c(uint64_t* bar, uint32_t parity, const ASmem& s, DevStatus* st,
+                                       unsigned long long timeout) {
+    return mbar_wait_cluster(smem_u32(bar), parity, s.abort_flag, timeout, st, kWhereAttn);
+}
+
+__device__ void pvp_producer(const PvParams& p, const ASmem& s, const CUtensorMap* mp, const CUtensorMap* mv, int tl,
+                             int d0, int rank) {
+    const uint64_t pol = policy_evict_normal();
+    const int nsplit = p.dv > 256 ? 2 : 1;
+    const int ns = p.dv / nsplit, hrows = ns / 2;
+    const uint32_t tx = static_cast<uint32_t>(kPHalfBytes + nsplit * hrows * 128);
+    RingT<kPvPairStages> r;
+    for (int j = 0; j < p.nkb; ++j)
+        for (int half = 0; half < 2; ++half) {
+            if (!wait_(&s.empty[r.stage], r.phase ^ 1u, s, p.status, p.timeout_ns)) {
+                j = p.nkb;
+                break;
+            }
+            const uint32_t fb = smem_u32(&s.full[r.stage]);
+            if (rank == 0) mbar_arrive_expect_tx(fb, 2u * tx);
+            r.arm();
+            const uint32_t fbc = mapa_shared(fb, 0u);
+            uint8_t* st = s.ring + r.stage * kPvPairStageBytes;
+            const int key0 = j * 128 + half * 64;
+            tma_load_2d_pair(smem_u32(st), mp, fbc, key0, tl * 128, pol);  // rows past the group read as zeros
+            for (int sp = 0; sp < nsplit; ++sp)
+                tma_load_2d_pair(smem_u32(st + kPHalfBytes + sp * hrows * 128), mv, fbc, key0,
+                                 d0 + sp * ns + rank * hrows, pol);
+            r.next();
+        }
+    // Let every copy land before the CTA can exit: the even CTA sees them on its
+    // full barriers, the odd CTA on its empty barriers (the MMAs that read them).
+    int never = 0;
+    for (int i = 0; i < kPvPairStages; ++i)
+        if (r.armed & (1u << i))
+            (void)mbar_wait(smem_u32(rank == 0 ? &s.full[i] : &s.empty[i]), (r.arm_par >> i) & 1u, &never,
+                            p.timeout_ns, p.status, kWhereDrain);
+}
+
+__device__ void pvp_mma(const PvParams& p, const ASmem& s, uint32_t tmem, const uint32_t* fl) {
+    const int nsplit = p.dv > 256 ? 2 : 1;
+    const int ns = p.dv / nsplit, hrows = ns / 2;
+    const uint32_t id_o = idesc_f16_f32(256, ns);
+    const uint64_t p_desc0 = sw128_kmajor_desc(smem_u32(s.ring));  // every ring address stays below 2^18 bytes
+    const uint32_t v_split = static_cast<uint32_t>(hrows * 128) >> 4;
+    RingT<kPvPairStages> r;
+    uint32_t ev = 0;
+    bool ok = true;
+    for (int j = 0; j < p.nkb && ok; ++j) {
+        if (j >= 1 && flagged(fl, j)) {
+            // both CTAs' row warps scale O once PV(j - 1) is done
+            umma_commit_pair(smem_u32(s.resc_ready));
+            if (!wait_c(s.scaled, ev & 1u, s, p.status, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            ++ev;
+            tc_fence_after();
+        }
+        for (int half = 0; half < 2; ++half) {
+            if (!wait_(&s.full[r.stage], r.phase, s, p.status, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t ad = p_desc0 + static_cast<uint32_t>(r.stage) * (kPvPairStageBytes >> 4);
+            const uint64_t bd0 = ad + (static_cast<uint32_t>(kPHalfBytes) >> 4);
+            const uint32_t acc0 = (j | half) != 0 ? 1u : 0u;
+            if (nsplit == 2) {
+                const uint64_t bd1 = bd0 + v_split;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    umma_f16_pair(tmem, ad + 2u * k, bd0 + 2u * k, id_o, k != 0 ? 1u : acc0);
+                    umma_f16_pair(tmem + static_cast<uint32_t>(ns), ad + 2u * k, bd1 + 2u * k, id_o,
+                                  k != 0 ? 1u : acc0);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) umma_f16_pair(tmem, ad + 2u * k, bd0 + 2u * k, id_o, k != 0 ? 1u : acc0);
+            }
+            umma_commit_pair(smem_u32(&s.empty[r.stage]));
+            r.next();
+        }
+    }
+    if (ok) umma_commit_pair(smem_u32(s.final));
+    umma_commit_pair(smem_u32(s.drain));
+    int never = 0;
+    (void)mbar_wait(smem_u32(s.drain), 0u, &never, p.timeout_ns, p.status, kWhereDrain);
+}
+
+__device__ void pvp_rows(const PvParams& p, const ASmem& s, uint32_t tmem, const uint32_t* fl, int warp, int lane,
+                         int tl, int d0, bool live) {
+    const int r = warp * 32 + lane;
+    const int row = tl * 128 + r;  // row of the group buffers (only read when the tile exists)
+    const uint32_t tO = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t scaled_c = mapa_shared(smem_u32(s.scaled), 0u);
+    uint32_t ev = 0;
+    for (int j = 1; j < p.nkb; ++j) {
+        if (!flagged(fl, j)) continue;
+        // (arrived by the even CTA's multicast commit: acquire at cluster scope)
+        if (!warp_all(wait_c(s.resc_ready, ev & 1u, s, p.status, p.timeout_ns))) return;
+        ++ev;
+        tc_fence_after();
+        const float alpha = live ? p.alpha[static_cast<size_t>(j) * p.grows + row] : 1.f;
+        for (int col = 0; col < p.dv; col += 16) {
+            uint32_t rr[16];
+            __syncwarp();
+            tmem_ld16(tO + col, rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st16(tO + col, rr);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive_cluster(scaled_c);
+    }
+    if (!warp_all(wait_c(s.final, 0u, s, p.status, p.timeout_ns))) return;
+    tc_fence_after();
+    if (!live) return;
+    const float inv = 1.f / p.lsum[row];
+    const int q = (p.q_tile0 + tl) * 128 + r;
+    for (int col = 0; col < p.dv; col += 16) {
+        uint32_t rr[16];
+        __syncwarp();
+        tmem_ld16(tO + col, rr);
+        tmem_ld_wait();
+        const int d = d0 + col;
+        if (q >= p.m || d >= p.c) continue;
+        __half* dst = p.out + static_cast<long long>(q) * p.c + d;
+        if (d + 16 <= p.c) {
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                __half2 t = __floats2half2_rn(__uint_as_float(rr[2 * i]) * inv + __ldg(p.bv + d + 2 * i),
+                                              __uint_as_float(rr[2 * i + 1]) * inv + __ldg(p.bv + d + 2 * i + 1));
+                h[i] = *reinterpret_cast<uint32_t*>(&t);
+            }
+            reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
+            reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
+        } else {
+            for (int i = 0; i < 16 && d + i < p.c; ++i)
+                dst[i] = __float2half_rn(__uint_as_float(rr[i]) * inv + __ldg(p.bv + d + i));
+        }
+    }
+}
+
+// grid: 2 x (tile pairs of the group) x ndv, clusters of 2; p.ntiles = tiles of the group.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_pv_pair_kernel(const __grid_constant__ CUtensorMap mp, const __grid_constant__ CUtensorMap mv,
+                        const PvParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint32_t fl[kMaxFlagWords];
+    const ASmem s = carve_attn(smem_raw, kPvPairStages * kPvPairStageBytes);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int cl = blockIdx.x >> 1;
+    const int tl = (cl / p.ndv) * 2 + rank;
+    const int d0 = (cl % p.ndv) * p.dv;
+    const bool live = tl < p.ntiles;
+    const int nwords = (p.nkb + 31) / 32;
+    for (int i = threadIdx.x; i < nwords; i += blockDim.x) fl[i] = 0u;
+    if (threadIdx.x == 0) {
+        *s.abort_flag = 0;
+        for (int i = 0; i < kPvPairStages; ++i) {
+            mbar_init(smem_u32(&s.full[i]), 1u);
+            mbar_init(smem_u32(&s.empty[i]), 1u);
+        }
+        mbar_init(smem_u32(s.resc_ready), 1u);
+        mbar_init(smem_u32(s.scaled), 256u);  // the row threads of both CTAs
+        mbar_init(smem_u32(s.final), 1u);
+        mbar_init(smem_u32(s.drain), 1u);
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc_pair(smem_u32(s.tmem_slot), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&mp);
+        tma_prefetch_desc(&mv);
+    }
+    pdl_wait();  // P, the flags and V come from kernels launched before
+    __syncthreads();
+    // The union of the two tiles' "some row rescaled at block j" flags.
+    const int t0 = (cl / p.ndv) * 2;
+    for (int j = 1 + threadIdx.x; j < p.nkb; j += blockDim.x) {
+        uint32_t any = 0u;
+        for (int t = t0; t < t0 + 2 && t < p.ntiles; ++t) {
+            const uint4 f = *reinterpret_cast<const uint4*>(p.flags + (static_cast<size_t>(t) * p.nkb + j) * 4);
+            any |= f.x | f.y | f.z | f.w;
+        }
+        if (any != 0u) atomicOr(&fl[j >> 5], 1u << (j & 31));
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers and TMEM exist before any remote arrive or pair MMA
+    tc_fence_after();
+    const uint32_t tmem = *s.tmem_slot;
+    if (warp < 4) {
+        pvp_rows(p, s, tmem, fl, warp, lane, tl, d0, live);
+    } else if (warp == 4) {
+        if (lane == 0) pvp_producer(p, s, &mp, &mv, tl, d0, rank);
+    } else {
+        if (lane == 0 && rank == 0) pvp_mma(p, s, tmem, fl);
+    }
+    pdl_launch_dependents();  // this CTA's work is done
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the even CTA's MMAs into both TMEMs are done; no remote arrives remain
+    if (warp == 5) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
 struct AttnLayout {
     int m_pad, ndv, dv;
     int qtiles, nkb, group;  // query tiles, key blocks, query tiles per scores/PV launch pair
@@ -592,6 +837,15 @@ int attn_layout(int m, int c, int groups, int norm_kind, AttnLayout* L) {
     off = align256(off + static_cast<size_t>(L->group) * L->nkb * 4 * 4);
     L->total = off;
     return VAE_OK;
+}
+
+// The CTA-pair PV kernel runs unless VAE_ATTN_PV_PAIR=0 is set (tests and measurements).
+bool attn_pv_pair_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("VAE_ATTN_PV_PAIR");
+        return !(e != nullptr && e[0] == '0');
+    }();
+    return on;
 }
 
 }  // namespace
@@ -660,7 +914,19 @@ static int attn_core_run(const __half* q, const __half* k, const __half* vt, int
         rc = encode_tiled(&mv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, vt, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != VAE_OK) return rc;
     }
+    // The PV kernel on CTA pairs: each CTA loads half of every V^T box (the
+    // N rows of the pair MMA it supplies).
+    CUtensorMap mv2{};
+    {
+        const int nsplit = L.dv > 256 ? 2 : 1;
+        const uint64_t dims[2] = {static_cast<uint64_t>(m_pad), static_cast<uint64_t>(c)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(m_pad) * 2};
+        const uint32_t box[2] = {64u, static_cast<uint32_t>(L.dv / nsplit / 2)};
+        rc = encode_tiled(&mv2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, vt, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != VAE_OK) return rc;
+    }
     const size_t smem = 1024 + kStages * kStageBytes + 256;
+    const size_t smem_pair = 1024 + kPvPairStages * kPvPairStageBytes + 256;
     static CtxOnce attr_set;
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
@@ -669,16 +935,23 @@ static int attn_core_run(const __half* q, const __half* k, const __half* vt, int
                                             static_cast<int>(smem)));
         VAE_CUDA_CHECK(cudaFuncSetAttribute(attn_pv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(smem)));
+        VAE_CUDA_CHECK(cudaFuncSetAttribute(attn_pv_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(smem_pair)));
         attr_set.mark(dev);
     }
     for (int t0 = 0; t0 < L.qtiles; t0 += L.group) {
         const int nt = std::min(L.group, L.qtiles - t0);
         sp.q_tile0 = t0;
         pp.q_tile0 = t0;
+        pp.ntiles = nt;
         VAE_CUDA_CHECK(launch_kernel(attn_scores_kernel, dim3(static_cast<unsigned>(nt)), dim3(kThreads), smem,
                                      stream, mq, mk, sp));
-        VAE_CUDA_CHECK(launch_kernel(attn_pv_kernel, dim3(static_cast<unsigned>(nt * L.ndv)), dim3(kThreads), smem,
-                                     stream, mp, mv, pp));
+        if (nt >= 2 && attn_pv_pair_enabled())
+            VAE_CUDA_CHECK(launch_kernel(attn_pv_pair_kernel, dim3(static_cast<unsigned>(2 * ((nt + 1) / 2) * L.ndv)),
+                                         dim3(kThreads), smem_pair, stream, mp, mv2, pp));
+        else
+            VAE_CUDA_CHECK(launch_kernel(attn_pv_kernel, dim3(static_cast<unsigned>(nt * L.ndv)), dim3(kThreads),
+                                         smem, stream, mp, mv, pp));
     }
     return VAE_OK;
 }

@@ -232,6 +232,7 @@ struct Smem {
     uint64_t* acce;      // [2]
     uint64_t* drain;     // [1]
     uint64_t* fixed;     // [stages] (reflect padding: the fixer warp hands each stage to the MMA thread)
+    uint64_t* xbar;      // [4] (pair kernel, fused RMS_norm: the two warps of a lane quadrant trade sums)
     uint32_t* tmem_slot;
     int* abort_flag;
 };
@@ -253,7 +254,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw, const ConvParams& p) {
     s.acce = s.accf + 2;
     s.drain = s.acce + 2;
     s.fixed = s.drain + 1;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.fixed + kMaxStages);
+    s.xbar = s.fixed + kMaxStages;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.xbar + 4);
     s.abort_flag = reinterpret_cast<int*>(s.tmem_slot + 1);
     return s;
 }
@@ -1768,28 +1770,50 @@ __device__ __forceinline__ void pair_epi_tma_row(const ConvParams& p, const Tile
 }
 
 // The fused RMS_norm of a pair tile's pixel (one N tile holds all cout <= 144
-// channels; f16 rows only, no residual): each warp of the lane quadrant forms
-// the pixel's sum of squares over all its chunks in the standalone kernel's
-// order (channel quad i into partial sum i % 4, chunks in order, then the
-// butterfly) -- a split between the two warps would need another order, which
-// slows the standalone kernel -- then normalises its own chunks (half,
-// half + 2, ...) and stores them as 32-pixel x 16-channel f16 boxes (32-byte
-// rows, 32-byte swizzle) from two 1 KB staging buffers.
-__device__ __forceinline__ void pair_epi_tma_rms_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase, int v,
-                                                     int u, int q, int pp, long long pix, uint8_t* stg,
-                                                     const CUtensorMap* mapY, int quad, int half, int lane,
-                                                     const float* sbias, uint32_t& nbox) {
+// channels; f16 rows only, no residual). The sum of squares follows the
+// standalone kernel's order (channel quad i into partial sum i % 4, chunks in
+// order, then the butterfly) while each warp of the lane quadrant reads only
+// its own chunks (half, half + 2, ...): it puts each chunk's four quad sums in
+// free TMEM columns of its lanes (two sets by tile parity), the two warps meet
+// on a bounded barrier, and each then adds all chunks' quad sums in order. Then
+// it reloads its chunks from TMEM (faster, measured, than holding them in
+// registers through the exchange), normalises them and stores them as 32-pixel
+// x 16-channel f16 boxes (32-byte rows, 32-byte swizzle) from two 1 KB staging
+// buffers.
+__device__ __forceinline__ void pair_epi_tma_rms_row(const ConvParams& p, const TileInfo& ti, uint32_t tbase,
+                                                     uint32_t xbase, int v, int u, int q, int pp, long long pix,
+                                                     uint8_t* stg, const CUtensorMap* mapY, int quad, int half,
+                                                     int lane, const float* sbias, uint32_t& nbox, uint64_t* xbar,
+                                                     volatile int* abort_flag, uint32_t& xphase) {
     const int nch = p.cout / 16;
-    float part[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c = 0; c < nch; ++c) {
+    for (int c = half; c < nch; c += 2) {
         uint32_t acc[16];
         __syncwarp();
         tmem_ld16(tbase + static_cast<uint32_t>(c * 16), acc);
         tmem_ld_wait_regs(acc);
         float val[16];
         compute_chunk(p, ti, acc, c * 16, v, u, q, pp, pix, val, nullptr, sbias);
+        float qs[4];
 #pragma unroll
-        for (int l = 0; l < 4; ++l) part[l] = rms_acc4(part[l], val[4 * l], val[4 * l + 1], val[4 * l + 2], val[4 * l + 3]);
+        for (int l = 0; l < 4; ++l) qs[l] = rms_acc4(0.f, val[4 * l], val[4 * l + 1], val[4 * l + 2], val[4 * l + 3]);
+        tmem_st4(xbase + static_cast<uint32_t>(c * 4), qs);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(smem_u32(xbar));
+    const bool met = warp_all(mbar_wait(smem_u32(xbar), xphase & 1u, abort_flag, p.timeout_ns, p.status,
+                                        kWhereEpiAccFull));
+    ++xphase;
+    tc_fence_after();
+    float part[4] = {0.f, 0.f, 0.f, 0.f};
+    if (met) {
+        for (int c = 0; c < nch; ++c) {
+            uint32_t r[4];
+            tmem_ld4(xbase + static_cast<uint32_t>(c * 4), r);
+            tmem_ld_wait_regs4(r);
+#pragma unroll
+            for (int l = 0; l < 4; ++l) part[l] = __fadd_rn(part[l], __uint_as_float(r[l]));
+        }
     }
     part[0] = __fadd_rn(part[0], part[2]);
     part[1] = __fadd_rn(part[1], part[3]);
@@ -1839,13 +1863,16 @@ __device__ __forceinline__ void pair_epi_tma_rms_row(const ConvParams& p, const 
     }
 }
 
+// kRms: the fused RMS_norm instantiation (its register-held chunks would
+// otherwise crowd the plain epilogues' registers).
+template <bool kRms>
 __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_base, int w, int lane, int rank,
                               const CUtensorMap* mapY) {
     const int quad = w & 3, half = w >> 2;
     const int row = quad * 32 + lane;
     uint8_t* stg = s.stg + w * 2 * kStgBytes;
     const float* sbias = p.bias_smem ? s.bias : nullptr;
-    uint32_t nbox = 0;
+    uint32_t nbox = 0, xphase = 0;
     int accbuf = 0;
     uint32_t accphase = 0;
     for (int t = blockIdx.x >> 1; t < p.pair_tiles; t += gridDim.x >> 1) {
@@ -1862,8 +1889,13 @@ __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
         const long long pix = (static_cast<long long>(ti.img) * p.H + Y) * p.W + X;
         const uint32_t tbase =
             tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(accbuf * p.acc_stride);
-        if (p.epi_tma == 3)
-            pair_epi_tma_rms_row(p, ti, tbase, v, u, q, pp, pix, stg, mapY, quad, half, lane, sbias, nbox);
+        if (kRms) {
+            // the quad-sum exchange columns follow the two accumulators, one set per tile parity
+            const uint32_t xbase = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                   static_cast<uint32_t>(2 * p.acc_stride + (xphase & 1u) * 4 * (p.BN / 16));
+            pair_epi_tma_rms_row(p, ti, tbase, xbase, v, u, q, pp, pix, stg, mapY, quad, half, lane, sbias, nbox,
+                                 &s.xbar[quad], s.abort_flag, xphase);
+        }
         else if (p.epi_tma)
             pair_epi_tma_row(p, ti, tbase, v, u, q, pp, pix, stg, mapY, quad, half, lane, valid, sbias, nbox);
         else
@@ -1877,6 +1909,7 @@ __device__ void pair_epilogue(const ConvParams& p, const Smem& s, uint32_t tmem_
     if (p.epi_tma && lane == 0) bulk_wait_all();  // boxes read and written before the CTA exits
 }
 
+template <bool kRms>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     conv_pair_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
                      const __grid_constant__ CUtensorMap mapA16, const __grid_constant__ CUtensorMap mapB16,
@@ -1897,13 +1930,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             mbar_init(smem_u32(&s.acce[i]), static_cast<uint32_t>(2 * kPairEpiWarps));
         }
         mbar_init(smem_u32(s.drain), 1u);
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&s.xbar[i]), 64u);  // both warps of a lane quadrant
         fence_mbar_init();
     }
-    const uint32_t tmem_cols = p.acc_stride * 2 <= 32 ? 32u
-                               : p.acc_stride * 2 <= 64 ? 64u
-                               : p.acc_stride * 2 <= 128 ? 128u
-                               : p.acc_stride * 2 <= 256 ? 256u
-                                                          : 512u;
+    // two accumulators, and with the fused RMS_norm two sets of quad-sum exchange columns
+    const int tcols = 2 * p.acc_stride + (p.epi_tma == 3 ? 8 * (p.BN / 16) : 0);
+    const uint32_t tmem_cols = tcols <= 32 ? 32u
+                               : tcols <= 64 ? 64u
+                               : tcols <= 128 ? 128u
+                               : tcols <= 256 ? 256u
+                                              : 512u;
     if (warp == kPairMmaWarp) {
         tmem_alloc_pair(smem_u32(s.tmem_slot), tmem_cols);
         tmem_relinquish_pair();
@@ -1928,7 +1964,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const uint32_t tmem_base = *s.tmem_slot;
 
     if (warp < kPairEpiWarps) {
-        pair_epilogue(p, s, tmem_base, warp, lane, rank, &mapY);
+        pair_epilogue<kRms>(p, s, tmem_base, warp, lane, rank, &mapY);
     } else if (warp == kPairProducerWarp) {
         if (lane == 0) pair_producer(p, s, &mapA, &mapB, &mapA16, &mapB16, rank);
     } else if (warp == kPairMmaWarp) {
@@ -2003,17 +2039,19 @@ int choose_bn(int cout, bool halo3) {
     return best;
 }
 
+template <bool kRms>
 int launch_pair(const ConvParams& p, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma16,
                 const CUtensorMap& mb16, const CUtensorMap& my, size_t smem, int grid, cudaStream_t stream) {
     static CtxOnce attr_set;
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
     if (!attr_set.done(dev)) {
-        VAE_CUDA_CHECK(cudaFuncSetAttribute(conv_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
+        VAE_CUDA_CHECK(
+            cudaFuncSetAttribute(conv_pair_kernel<kRms>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem));
         attr_set.mark(dev);
     }
-    VAE_CUDA_CHECK(launch_kernel(conv_pair_kernel, dim3(grid), dim3(kPairThreads), smem, stream, ma, mb, ma16, mb16, my,
-                                 p));
+    VAE_CUDA_CHECK(launch_kernel(conv_pair_kernel<kRms>, dim3(grid), dim3(kPairThreads), smem, stream, ma, mb, ma16,
+                                 mb16, my, p));
     VAE_CUDA_CHECK(cudaGetLastError());
     return VAE_OK;
 }
@@ -2489,7 +2527,8 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
                 q.a_stages = q.stages;
                 const size_t smem = fixed + static_cast<size_t>(q.stages) * stage_bytes;
                 const int pgrid = 2 * static_cast<int>(std::min<long long>(pt, nsm / 2));
-                return launch_pair(q, pa, pb, pa16, pb16, pmy, smem, pgrid, stream);
+                return q.epi_tma == 3 ? launch_pair<true>(q, pa, pb, pa16, pb16, pmy, smem, pgrid, stream)
+                                      : launch_pair<false>(q, pa, pb, pa16, pb16, pmy, smem, pgrid, stream);
             }
         }
         clear_error();

@@ -282,10 +282,10 @@ struct Exec {
     // CTA holds all of a pixel's channels (one N tile of <= 144): on rows of >= 128
     // pixels the staged two-pass epilogue (f16 rows only), else a register-held
     // row. Same bits as the separate norm. Off by default: on GB300 the 1024^2
-    // conv with the norm in its (CTA-pair) epilogue takes 0.42 ms against
-    // 0.29 + 0.136 ms for the conv and the separate norm, and whole 1024^2
-    // decodes measured the same with and without it (12.60-12.71 against
-    // 12.67-12.69 ms): the epilogue, which must read every chunk twice, becomes
+    // conv with the norm in its (CTA-pair) epilogue takes 0.40 ms against
+    // 0.295 + 0.136 ms for the conv and the separate norm, and whole 1024^2
+    // decodes measured the same with and without it (12.75-12.95 against
+    // 12.76-12.95 ms): the epilogue, which must read every chunk twice, becomes
     // the limit.
     bool fusable(int cout, int w) const {
         (void)w;

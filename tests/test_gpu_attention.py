@@ -58,11 +58,11 @@ def test_mid_attention_full_size_qwen_mid():
     assert rel_err(got - x, ref - x) <= ATTN_TOL
 
 
-@pytest.mark.parametrize("c", [128, 512, 1152])
-def test_peaked_softmax_rescales(c):
+@pytest.mark.parametrize("m,c", [(1024, 128), (1024, 512), (1024, 1152), (1100, 1152)])
+def test_peaked_softmax_rescales(m, c):
     """Scores that grow block after block force the lazy O rescale path (with
-    one, two and three value-channel chunks sharing the rescale flags)."""
-    m = 1024
+    one, two and three value-channel chunks sharing the rescale flags; 1100
+    tokens: nine query tiles, so the PV kernel's last CTA pair has one tile)."""
     x = stream_normal(22, f"attn.peak.x.{c}", (m, c))
     x = x + np.linspace(0, 40, m, dtype=np.float32)[:, None] * x[:, :1]
     a = _attn(22, c, "rms")
@@ -87,3 +87,19 @@ def test_mid_attention_two_query_groups():
     ref = oracle.attention_rows(x.T.reshape(c, m, 1), a, "rms", rows)
     assert np.isfinite(got).all()
     assert rel_err(got[rows] - x[rows], ref - x[rows]) <= ATTN_TOL
+
+
+def test_single_cta_pv_kernel_matches_oracle():
+    """The PV step on single CTAs (VAE_ATTN_PV_PAIR=0; by default query-tile
+    pairs share it through cta_group::2): the attention tests again in a child
+    process, which reads the switch once."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, VAE_ATTN_PV_PAIR="0")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
+                        os.path.join(root, "tests", "test_gpu_attention.py"), "-k",
+                        "not full_size and not two_query_groups and not single_cta"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]

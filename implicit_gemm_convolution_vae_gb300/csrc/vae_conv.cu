@@ -77,6 +77,14 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kGatherWarp0 = 6;
 constexpr int kMaxSmem = 232448;       // 227 KB opt-in per CTA
+#ifndef VAE_GEMM_PAIR_KS
+#define VAE_GEMM_PAIR_KS 2
+#endif
+constexpr int kGemmPairKs = VAE_GEMM_PAIR_KS;  // 64-channel chunks per stage of the pair GEMM
+#ifndef VAE_GEMM_PAIR_PREFETCH
+#define VAE_GEMM_PAIR_PREFETCH 1
+#endif
+constexpr bool kGemmPairPrefetch = VAE_GEMM_PAIR_PREFETCH != 0;  // L2 prefetch of the A rows one tile ahead
 
 struct ConvParams {
     int n, hv, wv;        // images, virtual grid rows/cols (= input grid)
@@ -101,6 +109,8 @@ struct ConvParams {
                           // (ks == 3: box slot i belongs to stage i, one barrier pair)
     int ks;               // K chunks per pipeline stage (1 or 2; per-tap A path only)
     int pair;             // CTA-pair kernel: each CTA holds BN/2 rows of B (b_rows)
+    int gemm;             // pair kernel on a 1x1 conv over one row of pixels (a plain GEMM): the two CTAs
+                          // take adjacent 128-pixel column tiles; a stage holds ks 64-channel chunks
     int stg_bytes;        // epilogue staging boxes in shared memory (0 without the TMA epilogue)
     int b_rows, typ_tiles, pair_tiles;
     uint32_t a_tx;        // bytes one A box delivers
@@ -1520,6 +1530,15 @@ __device__ __forceinline__ TileInfo decode_pair_tile(const ConvParams& p, int t,
     TileInfo ti;
     const int nt = t % p.n_tiles;
     int r = t / p.n_tiles;
+    if (p.gemm) {  // column tiles 2j and 2j + 1 of the one-row grid (typ_tiles = column pairs)
+        const int ptx = r % p.typ_tiles;
+        ti.img = r / p.typ_tiles;
+        ti.par = 0;
+        ti.v0 = 0;
+        ti.u0 = (2 * ptx + rank) * p.Wt;
+        ti.n0 = nt * p.BN;
+        return ti;
+    }
     const int tx = r % p.tiles_x;
     r /= p.tiles_x;
     ti.par = r % p.npar;
@@ -1572,6 +1591,37 @@ __device__ void pair_producer(const ConvParams& p, const Smem& s, const CUtensor
             const int npx = min(p.Wt, p.wv - ti.u0);
             const long long pix0 = (static_cast<long long>(ti.img) * p.hv + ti.v0) * p.wv + ti.u0;
             prefetch_l2_bulk(p.dup_src + pix0 * p.dup_cin, static_cast<uint32_t>(npx * p.dup_cin * 4));
+        }
+        if (p.gemm) {
+            // The N tiles of a column pair run side by side (N varies fastest), so their first
+            // touch of each A chunk waits on HBM. The pair whose next tile is the first N tile
+            // of its column pair asks L2 for that tile's A rows one tile ahead (and for its
+            // first tile at the start); the others then find them in L2.
+            if (kGemmPairPrefetch) {
+                const int step = static_cast<int>(gridDim.x >> 1);
+                for (int tn = (t == static_cast<int>(blockIdx.x >> 1) ? t : t + step); tn <= t + step; tn += step) {
+                    if (tn >= p.pair_tiles || tn % p.n_tiles != 0) continue;
+                    const TileInfo tj = decode_pair_tile(p, tn, rank);
+                    if (tj.u0 < p.wv)
+                        prefetch_l2_bulk(p.x + (static_cast<long long>(tj.img) * p.wv + tj.u0) * p.cin,
+                                         static_cast<uint32_t>(min(p.Wt, p.wv - tj.u0) * p.cin * 2));
+                }
+            }
+            // ks chunks per stage: chunk i of slot j at A slot (j * ks + i), B slot (j * ks + i)
+            for (int kc = 0; kc < p.kchunks && ok; kc += p.ks) {
+                const int nc = min(p.ks, p.kchunks - kc);
+                uint32_t slot;
+                const uint32_t fb = next_slot(static_cast<uint32_t>(nc) * (p.a_tx + b_bytes), &slot);
+                if (!ok) break;
+                for (int i = 0; i < nc; ++i) {
+                    const uint32_t j = slot * static_cast<uint32_t>(p.ks) + static_cast<uint32_t>(i);
+                    tma_load_4d_pair(smem_u32(s.a + j * kABytes), mapA, fb, (kc + i) * kBK, ti.u0, 0, ti.img,
+                                     pol_a);
+                    tma_load_3d_pair(smem_u32(s.b + j * b_bytes), mapB, fb, (kc + i) * kBK, 0, ti.n0 + boff,
+                                     pol_w);
+                }
+            }
+            continue;
         }
         const int q = ti.par >> 1, pp = ti.par & 1;
         const int dxmin = (p.up && pp == 1) ? 0 : -1;
@@ -1626,9 +1676,12 @@ __device__ void pair_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
     const uint64_t b128 = sw128_kmajor_desc(smem_u32(s.b));
     const uint64_t a32 = sw32_kmajor_desc(smem_u32(s.a));
     const uint64_t b32 = sw32_kmajor_desc(smem_u32(s.b));
-    const uint32_t a_slot = kHaloBytes >> 4;
-    const uint32_t b_slot = static_cast<uint32_t>(3 * p.b_rows * 128) >> 4;
+    // a slot: one halo box (three kx taps), or in GEMM mode ks A chunks; b slot: three taps or ks chunks
+    const uint32_t a_slot = p.gemm ? static_cast<uint32_t>(p.ks * kABytes) >> 4 : kHaloBytes >> 4;
+    const uint32_t b_slot = static_cast<uint32_t>((p.gemm ? p.ks : 3) * p.b_rows * 128) >> 4;
     const uint32_t b_tap = static_cast<uint32_t>(p.b_rows * 128) >> 4;
+    const uint32_t g_a_chunk = static_cast<uint32_t>(kABytes) >> 4;
+    const int g_nk_last = min(4, (p.cin - (p.kchunks - 1) * kBK + 15) / 16);  // GEMM mode: K steps of the last chunk
     const uint32_t b_tap16 = static_cast<uint32_t>(p.b_rows * 32) >> 4;
     const int kc_end = p.rem16 ? p.kfull : p.kchunks;
     const int nk_last = min(4, (p.cin - (kc_end - 1) * kBK) / 16);  // K steps of the last 64-channel chunk
@@ -1654,6 +1707,46 @@ __device__ void pair_mma(const ConvParams& p, const Smem& s, uint32_t tmem_base)
             break;
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(accbuf * p.acc_stride);
+        if (p.gemm) {
+            uint32_t acc = 0u;
+            for (int kc = 0; kc < p.kchunks; kc += p.ks) {
+                if (!mbar_wait(smem_u32(&s.full[stage]), phase, s.abort_flag, p.timeout_ns, p.status,
+                               kWhereMmaFull)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = a128 + soff_a;
+                const uint64_t bd = b128 + soff_b;
+                const int nc = min(p.ks, p.kchunks - kc);
+                if (nc == p.ks && (kc + nc < p.kchunks || g_nk_last == 4)) {
+#pragma unroll 3
+                    for (int i = 0; i < p.ks; ++i)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            umma_f16_pair(d, ad + static_cast<uint32_t>(i) * g_a_chunk + 2u * k,
+                                          bd + static_cast<uint32_t>(i) * b_tap + 2u * k, idesc, acc);
+                            acc = 1u;
+                        }
+                } else {
+                    for (int i = 0; i < nc; ++i) {
+                        const int nk = kc + i + 1 < p.kchunks ? 4 : g_nk_last;
+                        for (int k = 0; k < nk; ++k) {
+                            umma_f16_pair(d, ad + static_cast<uint32_t>(i) * g_a_chunk + 2u * k,
+                                          bd + static_cast<uint32_t>(i) * b_tap + 2u * k, idesc, acc);
+                            acc = 1u;
+                        }
+                    }
+                }
+                umma_commit_pair(smem_u32(&s.empty[stage]));
+                advance();
+            }
+            if (!ok) break;
+            umma_commit_pair(smem_u32(&s.accf[accbuf]));
+            accbuf ^= 1;
+            if (accbuf == 0) accphase ^= 1u;
+            continue;
+        }
         const int pp = p.up ? decode_pair_tile(p, t, 0).par & 1 : 0;  // (the divisions only where parity matters)
         const int dxmin = (p.up && pp == 1) ? 0 : -1;
         // row offset of tap kx inside the halo box, in 128-byte rows
@@ -2003,6 +2096,22 @@ int choose_bn_small(int cout) {
     if (c16 <= 144) return c16;
     int best = 144, best_cost = (c16 + 143) / 144 * 144;
     for (int bn = 144; bn >= 64; bn -= 16) {
+        const int cost = (c16 + bn - 1) / bn * bn;
+        if (cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+// N tile of the pair GEMM (M = 256, N <= 256): the least padding, ties to the
+// widest (1152 -> 192, 16384 -> 256, 576 -> 192).
+int choose_bn_pair_gemm(int cout) {
+    const int c16 = (cout + 15) / 16 * 16;
+    if (c16 <= 256) return c16;
+    int best = 256, best_cost = (c16 + 255) / 256 * 256;
+    for (int bn = 256; bn >= 128; bn -= 16) {
         const int cost = (c16 + bn - 1) / bn * bn;
         if (cost < best_cost) {
             best = bn;
@@ -2429,6 +2538,65 @@ int conv_run(const ConvArgs& a, cudaStream_t stream) {
         }
         return true;
     };
+    // CTA pairs for a 1x1 conv over one row of pixels (the plain GEMMs
+    // [pixels][cin] x [cout][cin]^T): adjacent 128-pixel column tiles share every
+    // weight tile, half in each SM; a stage holds kGemmPairKs 64-channel chunks.
+    if (cta_pair_enabled() && !a.no_pair && a.taps == 1 && mode == kModeTma && p.hv == 1 && p.R == 1 &&
+        p.Wt == kBM && p.tiles_x >= 2 && !p.up && !a.subpix && !a.refl && !a.down && !a.rep &&
+        a.gn_part == nullptr && a.rms_out == nullptr && !p.out_nchw && a.dup_src == nullptr && nsm >= 2) {
+        ConvParams q = p;
+        q.pair = 1;
+        q.gemm = 1;
+        q.BN = choose_bn_pair_gemm(a.cout);
+        q.b_rows = q.BN / 2;
+        q.n_tiles = (a.cout + q.BN - 1) / q.BN;
+        q.acc_stride = (q.BN + 31) / 32 * 32;
+        q.typ_tiles = (q.tiles_x + 1) / 2;  // column-tile pairs
+        const long long pt = static_cast<long long>(q.n) * q.typ_tiles * q.n_tiles;
+        if (pt >= (1LL << 31)) return set_error(VAE_ERR_SHAPE, "conv: too many tiles");
+        q.pair_tiles = static_cast<int>(pt);
+        q.halo = 0;
+        q.a_stages = 0;
+        q.rem16 = 0;
+        q.a_tx = static_cast<uint32_t>(kABytes);
+        q.res_prefetch = 0;
+        CUtensorMap pb{};
+        const uint64_t bdims[3] = {static_cast<uint64_t>(a.cin), 1u, static_cast<uint64_t>(a.cout)};
+        const uint64_t bstrides[2] = {static_cast<uint64_t>(a.cin) * 2, static_cast<uint64_t>(a.cin) * 2};
+        const uint32_t bbox[3] = {static_cast<uint32_t>(kBK), 1u, static_cast<uint32_t>(q.b_rows)};
+        bool ok = encode_tiled(&pb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, a.w, bdims, bstrides, bbox,
+                               CU_TENSOR_MAP_SWIZZLE_128B) == VAE_OK;
+        if (ok) {
+            CUtensorMap pmy{};
+            q.epi_tma = 0;
+            q.stg_bytes = 0;
+            {
+                const ConvParams keep = p;  // encode_epi() reads p; the pair shares its output view
+                p = q;
+                if (encode_epi()) {
+                    q.epi_tma = res_self ? 2 : 1;
+                    q.stg_bytes = kPairStgBytes;
+                    pmy = my;
+                }
+                p = keep;
+            }
+            const size_t bias_bytes = static_cast<size_t>(a.cout * 4 + 15) / 16 * 16;
+            q.bias_smem = (bias_smem_enabled() && a.bias != nullptr && aligned16(a.bias)) ? 1 : 0;
+            const size_t fixed = 1024 + static_cast<size_t>(q.stg_bytes) + (q.bias_smem ? bias_bytes : 0) + kTail;
+            for (q.ks = std::min(kGemmPairKs, q.kchunks); q.ks >= 1; --q.ks) {
+                const size_t stage_bytes =
+                    static_cast<size_t>(q.ks) * (static_cast<size_t>(kABytes) + static_cast<size_t>(q.b_rows) * 128u);
+                const int st = static_cast<int>((kMaxSmem - fixed) / stage_bytes);
+                if (st >= 3 || (q.ks == 1 && st >= 2)) {
+                    q.stages = std::min(kMaxStages, st);
+                    const size_t smem = fixed + static_cast<size_t>(q.stages) * stage_bytes;
+                    const int pgrid = 2 * static_cast<int>(std::min<long long>(pt, nsm / 2));
+                    return launch_pair<false>(q, ma, pb, ma, pb, pmy, smem, pgrid, stream);
+                }
+            }
+        }
+        clear_error();
+    }
     // CTA pairs (cta_group::2): two row tiles of one column block share every
     // weight tile, half in each SM, on the three-tap halo stages. Plain 2-D 3x3
     // convs with zero padding (with or without the nearest-2x fold) whose

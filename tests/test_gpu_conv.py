@@ -131,6 +131,38 @@ def test_conv1x1(m, cin, cout):
     assert rel_err(got, ref) <= CONV_TOL
 
 
+# The 1x1 convs over one row of pixels run on CTA pairs (adjacent 128-pixel
+# tiles share each weight tile): the attention projections' shapes (q / k: f16
+# rows, N tiles of 192; v^T: 9 pixel tiles, so one pair holds a single tile,
+# N tiles of 256; the output projection added in place onto the f32 stream), a
+# ragged N tile, a 16-channel tail chunk, and the single-CTA kernel on the same
+# inputs for comparison.
+@pytest.mark.parametrize("m,cin,cout,f16,inplace", [(16384, 1152, 1152, True, False),
+                                                    (1152, 1152, 16384, True, False),
+                                                    (16384, 1152, 1152, False, True),
+                                                    (333, 256, 200, False, True),
+                                                    (700, 80, 48, True, False),
+                                                    (5000, 144, 3, False, False)])
+def test_conv1x1_pair_gemm(m, cin, cout, f16, inplace):
+    torch = torch_mod()
+    x = f16_normal(5, f"pg.x.{m}.{cin}", (m, cin), 1.0)
+    w = f16_normal(5, f"pg.w.{cout}.{cin}", (cout, cin, 1, 1), (1.0 / cin) ** 0.5)
+    b = (stream_normal(5, f"pg.b.{cout}", (cout,)) * 0.1).astype(np.float32)
+    ref = x.astype(np.float64) @ w[:, :, 0, 0].astype(np.float64).T + b
+    if inplace:
+        s0 = stream_normal(5, f"pg.s.{m}.{cout}", (m, cout)).astype(np.float32)
+        out = to_dev(s0.copy())
+        vg.conv1x1(to_dev(x), to_dev(vg.pack_conv1x1(w)), to_dev(b), residual=out, out=out)
+        ref = ref + s0
+    else:
+        out = sentinel_like((m, cout), torch.float16 if f16 else torch.float32)
+        vg.conv1x1(to_dev(x), to_dev(vg.pack_conv1x1(w)), to_dev(b), out=out, out_f16=f16)
+    vg.sync_status()
+    got = out.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert rel_err(got, ref) <= CONV_TOL
+
+
 def _sample_points(H, W, n, seed):
     rng = np.random.default_rng(seed)
     ys = list(rng.integers(0, H, n))

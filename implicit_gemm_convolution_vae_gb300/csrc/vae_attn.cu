@@ -50,6 +50,9 @@ constexpr int kRingBars = 8;  // barrier slots of each ring array
 static_assert(1024 + kStages * kStageBytes + 256 <= 232448, "attention shared memory over 227 KB");
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxDv = 384;
+// The value bias, or 0 where the values carry none (the folded form adds it
+// through the output projection's bias).
+__device__ __forceinline__ float bias_at(const float* b, int i) { return b != nullptr ? __ldg(b + i) : 0.f; }
 constexpr int kMaxFlagWords = 256;                   // key blocks <= 8192, i.e. m <= 2^20
 constexpr size_t kMaxPBytes = size_t(2) << 30;       // P of one group of query tiles
 constexpr int kPHalfBytes = 128 * 64 * 2;            // 128 query rows x 64 keys
@@ -473,15 +476,15 @@ __device__ void pv_rows(const PvParams& p, const ASmem& s, uint32_t tmem, const 
             uint32_t h[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                __half2 t = __floats2half2_rn(__uint_as_float(rr[2 * i]) * inv + __ldg(p.bv + d + 2 * i),
-                                              __uint_as_float(rr[2 * i + 1]) * inv + __ldg(p.bv + d + 2 * i + 1));
+                __half2 t = __floats2half2_rn(__uint_as_float(rr[2 * i]) * inv + bias_at(p.bv, d + 2 * i),
+                                              __uint_as_float(rr[2 * i + 1]) * inv + bias_at(p.bv, d + 2 * i + 1));
                 h[i] = *reinterpret_cast<uint32_t*>(&t);
             }
             reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
             reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
         } else {
             for (int i = 0; i < 16 && d + i < p.c; ++i)
-                dst[i] = __float2half_rn(__uint_as_float(rr[i]) * inv + __ldg(p.bv + d + i));
+                dst[i] = __float2half_rn(__uint_as_float(rr[i]) * inv + bias_at(p.bv, d + i));
         }
     }
 }
@@ -703,15 +706,15 @@ __device__ void pvp_rows(const PvParams& p, const ASmem& s, uint32_t tmem, const
             uint32_t h[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                __half2 t = __floats2half2_rn(__uint_as_float(rr[2 * i]) * inv + __ldg(p.bv + d + 2 * i),
-                                              __uint_as_float(rr[2 * i + 1]) * inv + __ldg(p.bv + d + 2 * i + 1));
+                __half2 t = __floats2half2_rn(__uint_as_float(rr[2 * i]) * inv + bias_at(p.bv, d + 2 * i),
+                                              __uint_as_float(rr[2 * i + 1]) * inv + bias_at(p.bv, d + 2 * i + 1));
                 h[i] = *reinterpret_cast<uint32_t*>(&t);
             }
             reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
             reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
         } else {
             for (int i = 0; i < 16 && d + i < p.c; ++i)
-                dst[i] = __float2half_rn(__uint_as_float(rr[i]) * inv + __ldg(p.bv + d + i));
+                dst[i] = __float2half_rn(__uint_as_float(rr[i]) * inv + bias_at(p.bv, d + i));
         }
     }
 }
@@ -789,7 +792,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 struct AttnLayout {
     int m_pad, ndv, dv;
     int qtiles, nkb, group;  // query tiles, key blocks, query tiles per scores/PV launch pair
-    size_t xn, q, k, vt, o, gn, p, alpha, lsum, flags, total;
+    size_t xn, q, k, vt, o, gn, p, alpha, lsum, flags;
+    size_t wqk, wov, bqk, bov, wT;  // the folded weights and the transposes they are made from
+    size_t total;
 };
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
@@ -835,7 +840,90 @@ int attn_layout(int m, int c, int groups, int norm_kind, AttnLayout* L) {
     off = align256(off + grows * 4);
     L->flags = off;
     off = align256(off + static_cast<size_t>(L->group) * L->nkb * 4 * 4);
+    const size_t cc = static_cast<size_t>(c) * c * 2;
+    L->wqk = off;
+    off = align256(off + cc);
+    L->wov = off;
+    off = align256(off + cc);
+    L->bqk = off;
+    off = align256(off + static_cast<size_t>(c) * 4);
+    L->bov = off;
+    off = align256(off + static_cast<size_t>(c) * 4);
+    L->wT = off;  // the transposed Wq, Wk, Wv, one after another
+    off = align256(off + 3 * cc);
     L->total = off;
+    return VAE_OK;
+}
+
+
+// out[j][i] = in[i][j] for i < rows, j < cols (f16; rows, cols and both row
+// strides multiples of 8, bases 16-byte aligned): 64 x 64 tiles through shared
+// memory, 16-byte global accesses on both sides.
+__global__ void __launch_bounds__(256)
+    transpose_f16_kernel(const __half* __restrict__ in, int rows, int cols, long long ld_in, __half* __restrict__ out,
+                         long long ld_out) {
+    __shared__ __half2 tile[64][33];  // 64 rows of 64 halves (+1 word: the column reads spread over banks)
+    pdl_wait();
+    const int r0 = blockIdx.y * 64, c0 = blockIdx.x * 64;
+    const int t = threadIdx.x;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int r = (t >> 3) + 32 * pass, cc = (t & 7) * 8;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r0 + r < rows && c0 + cc < cols)
+            v = *reinterpret_cast<const uint4*>(in + static_cast<long long>(r0 + r) * ld_in + c0 + cc);
+        tile[r][cc / 2 + 0] = *reinterpret_cast<__half2*>(&v.x);
+        tile[r][cc / 2 + 1] = *reinterpret_cast<__half2*>(&v.y);
+        tile[r][cc / 2 + 2] = *reinterpret_cast<__half2*>(&v.z);
+        tile[r][cc / 2 + 3] = *reinterpret_cast<__half2*>(&v.w);
+    }
+    __syncthreads();
+    for (int pass = 0; pass < 2; ++pass) {
+        const int oc = (t >> 3) + 32 * pass, rr = (t & 7) * 8;  // input column, first of 8 input rows
+        if (c0 + oc >= cols || r0 + rr >= rows) continue;
+        __half h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const __half2 w = tile[rr + i][oc / 2];
+            h[i] = (oc & 1) ? __high2half(w) : __low2half(w);
+        }
+        *reinterpret_cast<uint4*>(out + static_cast<long long>(c0 + oc) * ld_out + r0 + rr) =
+            *reinterpret_cast<const uint4*>(h);
+    }
+    pdl_launch_dependents();
+}
+
+// The folded biases: bqk = Wk^T bq (rows of Wk^T) and bov = Wo bv + bo, one
+// warp per output; each lane sums a strided share of the c products, then the
+// lanes combine by a butterfly (a fixed order).
+__global__ void __launch_bounds__(256)
+    fold_bias_kernel(const __half* __restrict__ wkT, const float* __restrict__ bq, const __half* __restrict__ wo,
+                     const float* __restrict__ bv, const float* __restrict__ bo, int c, float* __restrict__ bqk,
+                     float* __restrict__ bov) {
+    pdl_wait();
+    const int w = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (w < 2 * c) {
+        const bool second = w >= c;
+        const int i = second ? w - c : w;
+        const __half* row = (second ? wo : wkT) + static_cast<long long>(i) * c;
+        const float* vec = second ? bv : bq;
+        float acc = 0.f;
+        for (int r = lane; r < c; r += 32) acc = fmaf(__half2float(row[r]), vec[r], acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            if (second)
+                bov[i] = acc + bo[i];
+            else
+                bqk[i] = acc;
+        }
+    }
+    pdl_launch_dependents();
+}
+
+int transpose_run(const __half* in, int rows, int cols, long long ld_in, __half* out, long long ld_out,
+                  cudaStream_t stream) {
+    const dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
+    VAE_CUDA_CHECK(launch_kernel(transpose_f16_kernel, grid, dim3(256), 0, stream, in, rows, cols, ld_in, out, ld_out));
     return VAE_OK;
 }
 
@@ -849,6 +937,15 @@ bool attn_pv_pair_enabled() {
 }
 
 }  // namespace
+
+// The folded form runs unless VAE_ATTN_FOLD=0 is set (tests and measurements).
+bool attn_fold_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("VAE_ATTN_FOLD");
+        return !(e != nullptr && e[0] == '0');
+    }();
+    return on;
+}
 
 // o = softmax(q k^T / sqrt(c)) v + b_v (f16 [m][c]) with the scratch of L in ws.
 static int attn_core_run(const __half* q, const __half* k, const __half* vt, int m, int m_pad, int c, const float* bv,
@@ -964,76 +1061,168 @@ int attn_workspace_bytes(int m, int c, int groups, int norm_kind, size_t* bytes)
     return VAE_OK;
 }
 
-int attn_run(float* x, int m, int c, int norm_kind, int groups, float eps, const float* gamma, const float* beta,
-             const void* wq, const float* bq, const void* wk, const float* bk, const void* wv, const float* bv,
-             const void* wo, const float* bo, void* ws, size_t ws_bytes, cudaStream_t stream) {
-    if (x == nullptr || gamma == nullptr || wq == nullptr || wk == nullptr || wv == nullptr || wo == nullptr ||
-        bq == nullptr || bk == nullptr || bv == nullptr || bo == nullptr || ws == nullptr)
+namespace {
+
+// Checks the common arguments, runs the norm into xn and zeroes its pad rows.
+struct AttnBufs {
+    AttnLayout L;
+    uint8_t* w8;
+    __half *xn, *q, *k, *vt, *o;
+};
+
+int attn_begin(float* x, int m, int c, int norm_kind, int groups, float eps, const float* gamma, const float* beta,
+               void* ws, size_t ws_bytes, cudaStream_t stream, AttnBufs* B) {
+    if (x == nullptr || gamma == nullptr || ws == nullptr)
         return set_error(VAE_ERR_ARG, "mid_attention: a required pointer is NULL");
     if (norm_kind != VAE_NORM_GROUP && norm_kind != VAE_NORM_RMS)
         return set_error(VAE_ERR_ARG, "mid_attention: norm_kind %d", norm_kind);
     if (norm_kind == VAE_NORM_GROUP && beta == nullptr)
         return set_error(VAE_ERR_ARG, "mid_attention: GroupNorm needs beta");
-    AttnLayout L;
+    AttnLayout& L = B->L;
     int rc = attn_layout(m, c, groups, norm_kind, &L);
     if (rc != VAE_OK) return rc;
     if (ws_bytes < L.total)
         return set_error(VAE_ERR_NOMEM, "mid_attention: workspace %zu < %zu bytes", ws_bytes, L.total);
     if (!aligned16(ws) || !aligned16(x)) return set_error(VAE_ERR_ALIGN, "mid_attention: x/workspace alignment");
     uint8_t* w8 = static_cast<uint8_t*>(ws);
-    __half* xn = reinterpret_cast<__half*>(w8 + L.xn);
-    __half* q = reinterpret_cast<__half*>(w8 + L.q);
-    __half* k = reinterpret_cast<__half*>(w8 + L.k);
-    __half* vt = reinterpret_cast<__half*>(w8 + L.vt);
-    __half* o = reinterpret_cast<__half*>(w8 + L.o);
+    B->w8 = w8;
+    B->xn = reinterpret_cast<__half*>(w8 + L.xn);
+    B->q = reinterpret_cast<__half*>(w8 + L.q);
+    B->k = reinterpret_cast<__half*>(w8 + L.k);
+    B->vt = reinterpret_cast<__half*>(w8 + L.vt);
+    B->o = reinterpret_cast<__half*>(w8 + L.o);
     if (norm_kind == VAE_NORM_GROUP)
-        rc = gn_run(x, 1, m, c, groups, eps, nullptr, gamma, beta, 0, 1.0f, xn, w8 + L.gn, L.total - L.gn, stream);
+        rc = gn_run(x, 1, m, c, groups, eps, nullptr, gamma, beta, 0, 1.0f, B->xn, w8 + L.gn, L.total - L.gn, stream);
     else
-        rc = rms_run(x, m, c, nullptr, gamma, 0, 1.0f, xn, stream);
+        rc = rms_run(x, m, c, nullptr, gamma, 0, 1.0f, B->xn, stream);
     if (rc != VAE_OK) return rc;
     if (L.m_pad > m)
-        VAE_CUDA_CHECK(cudaMemsetAsync(xn + static_cast<size_t>(m) * c, 0,
+        VAE_CUDA_CHECK(cudaMemsetAsync(B->xn + static_cast<size_t>(m) * c, 0,
                                        static_cast<size_t>(L.m_pad - m) * c * 2, stream));
+    return VAE_OK;
+}
+
+ConvArgs gemm_args(const void* x, int rows, int cin, const void* w, int cout, const float* bias, void* y, bool f16) {
     ConvArgs a{};
     a.taps = 1;
     a.n = 1;
     a.h_in = 1;
-    a.cin = c;
-    a.out_f16 = true;
-    // q, k = xn W^T + b (f16)
-    a.x = xn;
-    a.w_in = m;
-    a.cout = c;
-    a.w = wq;
-    a.bias = bq;
-    a.y = q;
-    if ((rc = conv_run(a, stream)) != VAE_OK) return rc;
-    a.w = wk;
-    a.bias = bk;
-    a.y = k;
-    if ((rc = conv_run(a, stream)) != VAE_OK) return rc;
-    // v^T [c][m_pad] = W_v xn^T (no bias: added after P.V)
-    a.x = wv;
-    a.w_in = c;
-    a.w = xn;
-    a.cout = L.m_pad;
-    a.bias = nullptr;
-    a.y = vt;
-    if ((rc = conv_run(a, stream)) != VAE_OK) return rc;
-    if ((rc = attn_core_run(q, k, vt, m, L.m_pad, c, bv, o, L, w8, stream)) != VAE_OK) return rc;
-    // x += o W_o^T + b_o
-    ConvArgs pr{};
-    pr.taps = 1;
-    pr.n = 1;
-    pr.h_in = 1;
-    pr.w_in = m;
-    pr.cin = c;
-    pr.cout = c;
-    pr.x = o;
-    pr.w = wo;
-    pr.bias = bo;
+    a.w_in = rows;
+    a.cin = cin;
+    a.x = x;
+    a.w = w;
+    a.cout = cout;
+    a.bias = bias;
+    a.y = y;
+    a.out_f16 = f16;
+    return a;
+}
+
+// The folded attention on the norm's rows in B (see attn_fold_run).
+int attn_folded_core(float* x, int m, int c, const __half* wqk, const float* bqk, const __half* wov, const float* bov,
+                     const AttnBufs& B, cudaStream_t stream) {
+    int rc;
+    // q' = xn M^T + Wk^T bq (f16)
+    if ((rc = conv_run(gemm_args(B.xn, m, c, wqk, c, bqk, B.q, true), stream)) != VAE_OK) return rc;
+    // xn^T [c][m_pad] (the zeroed pad rows included): the P.V operand
+    if ((rc = transpose_run(B.xn, B.L.m_pad, c, c, B.vt, B.L.m_pad, stream)) != VAE_OK) return rc;
+    if ((rc = attn_core_run(B.q, B.xn, B.vt, m, B.L.m_pad, c, nullptr, B.o, B.L, B.w8, stream)) != VAE_OK) return rc;
+    // x += xbar (Wo Wv)^T + (Wo bv + bo)
+    ConvArgs pr = gemm_args(B.o, m, c, wov, c, bov, x, false);
     pr.residual = x;
-    pr.y = x;
+    return conv_run(pr, stream);
+}
+
+}  // namespace
+
+// The folded weights. With q_i = Wq n_i + bq and k_j = Wk n_j + bk, the score
+// q_i . k_j = (Wk^T q_i) . n_j + q_i . bk, and the last term is the same for
+// every key j of row i, so the softmax drops it: the scores are q'_i . n_j with
+// q' = n M^T + Wk^T bq, M = Wk^T Wq. Each row of the softmax sums to one, so
+// o_i = Wv (sum_j p_ij n_j / l_i) + bv, and the block's output
+// Wo o_i + bo = (Wo Wv) nbar_i + (Wo bv + bo), nbar being the softmax average
+// of the normalised rows themselves. Two c x c weight products replace the key
+// and value projections of all m tokens; keys and values are the normalised
+// rows (xn, and xn^T for the P.V operand). wqk, wov f16 [c][c]; bqk, bov f32
+// [c]; scratch 3 c^2 f16 (the transposed Wq, Wk, Wv). All 16-byte aligned.
+int attn_fold_run(int c, const void* wq, const float* bq, const void* wk, const void* wv, const float* bv,
+                  const void* wo, const float* bo, __half* wqk, __half* wov, float* bqk, float* bov, __half* scratch,
+                  cudaStream_t stream) {
+    if (wq == nullptr || wk == nullptr || wv == nullptr || wo == nullptr || bq == nullptr || bv == nullptr ||
+        bo == nullptr || wqk == nullptr || wov == nullptr || bqk == nullptr || bov == nullptr || scratch == nullptr)
+        return set_error(VAE_ERR_ARG, "mid_attention: a required pointer is NULL");
+    if (c < 16 || c % 16 != 0 || c > 2048) return set_error(VAE_ERR_SHAPE, "mid_attention: c=%d", c);
+    if (!aligned16(wq) || !aligned16(wk) || !aligned16(wv) || !aligned16(wo) || !aligned16(wqk) || !aligned16(wov) ||
+        !aligned16(scratch))
+        return set_error(VAE_ERR_ALIGN, "mid_attention: the weights must be 16-byte aligned");
+    const size_t cc = static_cast<size_t>(c) * c;
+    __half* wqT = scratch;
+    __half* wkT = scratch + cc;
+    __half* wvT = scratch + 2 * cc;
+    int rc;
+    if ((rc = transpose_run(static_cast<const __half*>(wq), c, c, c, wqT, c, stream)) != VAE_OK) return rc;
+    if ((rc = transpose_run(static_cast<const __half*>(wk), c, c, c, wkT, c, stream)) != VAE_OK) return rc;
+    if ((rc = transpose_run(static_cast<const __half*>(wv), c, c, c, wvT, c, stream)) != VAE_OK) return rc;
+    // M[a][b] = sum_r Wk[r][a] Wq[r][b]: rows of Wk^T against rows of Wq^T
+    if ((rc = conv_run(gemm_args(wkT, c, c, wqT, c, nullptr, wqk, true), stream)) != VAE_OK) return rc;
+    // (Wo Wv)[a][b] = sum_r Wo[a][r] Wv[r][b]: rows of Wo against rows of Wv^T
+    if ((rc = conv_run(gemm_args(wo, c, c, wvT, c, nullptr, wov, true), stream)) != VAE_OK) return rc;
+    VAE_CUDA_CHECK(launch_kernel(fold_bias_kernel, dim3(static_cast<unsigned>((2 * c * 32 + 255) / 256)), dim3(256), 0,
+                                 stream, static_cast<const __half*>(wkT), bq, static_cast<const __half*>(wo), bv, bo, c,
+                                 bqk, bov));
+    return VAE_OK;
+}
+
+int attn_run_folded(float* x, int m, int c, int norm_kind, int groups, float eps, const float* gamma,
+                    const float* beta, const __half* wqk, const float* bqk, const __half* wov, const float* bov,
+                    void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (wqk == nullptr || bqk == nullptr || wov == nullptr || bov == nullptr)
+        return set_error(VAE_ERR_ARG, "mid_attention: a required pointer is NULL");
+    if (!aligned16(wqk) || !aligned16(wov))
+        return set_error(VAE_ERR_ALIGN, "mid_attention: the weights must be 16-byte aligned");
+    AttnBufs B;
+    int rc = attn_begin(x, m, c, norm_kind, groups, eps, gamma, beta, ws, ws_bytes, stream, &B);
+    if (rc != VAE_OK) return rc;
+    return attn_folded_core(x, m, c, wqk, bqk, wov, bov, B, stream);
+}
+
+int attn_run(float* x, int m, int c, int norm_kind, int groups, float eps, const float* gamma, const float* beta,
+             const void* wq, const float* bq, const void* wk, const float* bk, const void* wv, const float* bv,
+             const void* wo, const float* bo, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (wq == nullptr || wk == nullptr || wv == nullptr || wo == nullptr || bq == nullptr || bk == nullptr ||
+        bv == nullptr || bo == nullptr)
+        return set_error(VAE_ERR_ARG, "mid_attention: a required pointer is NULL");
+    if (!aligned16(wq) || !aligned16(wk) || !aligned16(wv) || !aligned16(wo))
+        return set_error(VAE_ERR_ALIGN, "mid_attention: the weights must be 16-byte aligned");
+    {
+        AttnLayout L;  // shape and workspace checks before anything is launched
+        int rc = attn_layout(m, c, groups, norm_kind, &L);
+        if (rc != VAE_OK) return rc;
+        if (ws != nullptr && ws_bytes < L.total)
+            return set_error(VAE_ERR_NOMEM, "mid_attention: workspace %zu < %zu bytes", ws_bytes, L.total);
+    }
+    AttnBufs B;
+    int rc = attn_begin(x, m, c, norm_kind, groups, eps, gamma, beta, ws, ws_bytes, stream, &B);
+    if (rc != VAE_OK) return rc;
+    const AttnLayout& L = B.L;
+    if (attn_fold_enabled()) {
+        __half* wqk = reinterpret_cast<__half*>(B.w8 + L.wqk);
+        __half* wov = reinterpret_cast<__half*>(B.w8 + L.wov);
+        float* bqk = reinterpret_cast<float*>(B.w8 + L.bqk);
+        float* bov = reinterpret_cast<float*>(B.w8 + L.bov);
+        if ((rc = attn_fold_run(c, wq, bq, wk, wv, bv, wo, bo, wqk, wov, bqk, bov,
+                                reinterpret_cast<__half*>(B.w8 + L.wT), stream)) != VAE_OK)
+            return rc;
+        return attn_folded_core(x, m, c, wqk, bqk, wov, bov, B, stream);
+    }
+    // The projections as written: q, k = xn W^T + b (f16); v^T [c][m_pad] = W_v xn^T
+    // (no bias: added after P.V); x += o W_o^T + b_o.
+    if ((rc = conv_run(gemm_args(B.xn, m, c, wq, c, bq, B.q, true), stream)) != VAE_OK) return rc;
+    if ((rc = conv_run(gemm_args(B.xn, m, c, wk, c, bk, B.k, true), stream)) != VAE_OK) return rc;
+    if ((rc = conv_run(gemm_args(wv, c, c, B.xn, L.m_pad, nullptr, B.vt, true), stream)) != VAE_OK) return rc;
+    if ((rc = attn_core_run(B.q, B.k, B.vt, m, L.m_pad, c, bv, B.o, L, B.w8, stream)) != VAE_OK) return rc;
+    ConvArgs pr = gemm_args(B.o, m, c, wo, c, bo, x, false);
+    pr.residual = x;
     return conv_run(pr, stream);
 }
 

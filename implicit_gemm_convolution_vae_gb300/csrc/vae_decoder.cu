@@ -55,6 +55,12 @@ struct DRes {
 struct DAttn {
     DNorm n;
     DConv q, k, v, o;
+    // the folded weights (Wk^T Wq, Wo Wv f16 [c][c]; Wk^T bq, Wo bv + bo f32 [c]),
+    // formed once at creation; NULL when the projections run as written
+    __half* wqk = nullptr;
+    __half* wov = nullptr;
+    float* bqk = nullptr;
+    float* bov = nullptr;
 };
 struct DUp {
     std::vector<DRes> res;
@@ -633,11 +639,19 @@ int run_decode(Exec& X, int h0, int w0, const vae_decode_opts* opts, const float
             float* xa = X.f32(s_bufs[cur_buf], hw0 * ch);
             if (!X.dry) {
                 const double m = static_cast<double>(hw0);
-                const int i = X.begin(VAE_STAGE_ATTENTION, (kind == VAE_NORM_GROUP ? 3 : 1) + 5 + (hw0 % 8 ? 1 : 0),
+                // norm (+ pad rows), q' GEMM, transpose, scores, P.V, output GEMM; as written:
+                // the q, k, v GEMMs instead of the q' GEMM and the transpose
+                const int i = X.begin(VAE_STAGE_ATTENTION,
+                                      (kind == VAE_NORM_GROUP ? 3 : 1) + (d->attn.wqk != nullptr ? 5 : 6) +
+                                          (hw0 % 8 ? 1 : 0),
                                       h0, w0, ch, ch, 4.0 * m * m * ch + 4.0 * 2.0 * m * ch * ch, 0.0);
-                rc = attn_run(xa, static_cast<int>(hw0), ch, kind, d->groups, d->eps, d->attn.n.gamma,
-                              d->attn.n.beta, d->attn.q.w, d->attn.q.b, d->attn.k.w, d->attn.k.b, d->attn.v.w,
-                              d->attn.v.b, d->attn.o.w, d->attn.o.b, aws, ab, X.st);
+                rc = d->attn.wqk != nullptr
+                         ? attn_run_folded(xa, static_cast<int>(hw0), ch, kind, d->groups, d->eps, d->attn.n.gamma,
+                                           d->attn.n.beta, d->attn.wqk, d->attn.bqk, d->attn.wov, d->attn.bov, aws,
+                                           ab, X.st)
+                         : attn_run(xa, static_cast<int>(hw0), ch, kind, d->groups, d->eps, d->attn.n.gamma,
+                                    d->attn.n.beta, d->attn.q.w, d->attn.q.b, d->attn.k.w, d->attn.k.b, d->attn.v.w,
+                                    d->attn.v.b, d->attn.o.w, d->attn.o.b, aws, ab, X.st);
                 X.end(i);
                 if (rc != VAE_OK) return rc;
             }
@@ -764,6 +778,34 @@ int vae_decoder_create(const vae_decoder_desc* desc, vae_decoder_t* out) {
         for (const DConv* c : {&d->attn.q, &d->attn.k, &d->attn.v, &d->attn.o})
             if (c->k != 1 || c->cin != ch || c->cout != ch)
                 U.rc = set_error(VAE_ERR_SHAPE, "decoder_create: attention projections must be 1x1 %d->%d", ch, ch);
+    }
+    if (U.rc == VAE_OK && attn_fold_enabled()) {
+        // the attention's folded weights, formed once on the device (the weights are fixed)
+        const size_t cc = static_cast<size_t>(ch) * ch * 2;
+        const size_t cb = (static_cast<size_t>(ch) * 4 + 255) / 256 * 256;
+        void* fw = nullptr;
+        void* scratch = nullptr;
+        if (cudaMalloc(&fw, 2 * cc + 2 * cb) != cudaSuccess) {
+            U.rc = set_error(VAE_ERR_NOMEM, "decoder_create: cudaMalloc(%zu) for the folded attention weights",
+                             2 * cc + 2 * cb);
+        } else {
+            d->allocs.push_back(fw);
+            uint8_t* f8 = static_cast<uint8_t*>(fw);
+            d->attn.wqk = reinterpret_cast<__half*>(f8);
+            d->attn.wov = reinterpret_cast<__half*>(f8 + cc);
+            d->attn.bqk = reinterpret_cast<float*>(f8 + 2 * cc);
+            d->attn.bov = reinterpret_cast<float*>(f8 + 2 * cc + cb);
+            if (cudaMalloc(&scratch, 3 * cc) != cudaSuccess) {
+                U.rc = set_error(VAE_ERR_NOMEM, "decoder_create: cudaMalloc(%zu) for the weight transposes", 3 * cc);
+            } else {
+                U.rc = attn_fold_run(ch, d->attn.q.w, d->attn.q.b, d->attn.k.w, d->attn.v.w, d->attn.v.b,
+                                     d->attn.o.w, d->attn.o.b, d->attn.wqk, d->attn.wov, d->attn.bqk, d->attn.bov,
+                                     static_cast<__half*>(scratch), nullptr);
+                if (U.rc == VAE_OK && cudaDeviceSynchronize() != cudaSuccess)
+                    U.rc = set_error(VAE_ERR_CUDA, "decoder_create: folding the attention weights failed");
+                cudaFree(scratch);
+            }
+        }
     }
     d->mid2 = U.res(desc->mid_res2, ch, gn, "mid_res2");
     if (U.rc == VAE_OK) ch = d->mid2.c1.cout;

@@ -308,16 +308,27 @@ enum { VAE_NORM_GROUP = 0, VAE_NORM_RMS = 1 };
 /*
  * Single-head spatial self-attention of the decoder's mid block, in place on
  * the f32 residual stream:
- *   n = GroupNorm(x) or RMS_norm(x)*gamma (no SiLU); q,k,v = n W^T + b (f16);
+ *   n = GroupNorm(x) or RMS_norm(x)*gamma (no SiLU); q,k,v = n W^T + b;
  *   o = softmax(q k^T / sqrt(c)) v; x += o W_o^T + b_o.
- * ("vae.rs" AttnBlock::apply / finish; "qi21_vae.rs" attention.) The
- * q k^T -> softmax -> P.V part is one fused tcgen05 kernel (no score matrix
- * in memory).
+ * ("vae.rs" AttnBlock::apply / finish; "qi21_vae.rs" attention.)
+ * Computed in a folded form that is exact in real arithmetic: the key bias
+ * adds the same amount to every score of a row, which the softmax removes,
+ * and the rows of the softmax sum to one, so with M = Wk^T Wq and
+ * Wov = Wo Wv (f16, formed on the device each call)
+ *   s_ij = (n_i M^T + Wk^T bq) . n_j,   x_i += (sum_j p_ij n_j) Wov^T + (Wo bv + bo).
+ * (VAE_ATTN_FOLD=0 in the environment runs the q, k, v projections as written.)
+ * Scores and the online softmax run in one tcgen05 kernel that writes P (f16)
+ * to the workspace; a second kernel forms P.V; the projections run on the
+ * implicit-GEMM kernel.
  *   x_dev f32 [m][c] (tokens = pixels of one image); w*_dev f16 [c][c]
- *   (row = output channel); b*_dev f32 [c]; norm_beta_dev ignored for RMS.
+ *   (row = output channel), 16-byte aligned; b*_dev f32 [c]; norm_beta_dev
+ *   ignored for RMS.
  *   workspace_dev >= vae_mid_attention_workspace_bytes(m, c, groups) (which
- *   sizes for GroupNorm when c % groups == 0, else for RMS_norm).
- * Requirements: c % 16 == 0, 16 <= c <= 2048, m >= 1.
+ *   sizes for GroupNorm when c % groups == 0, else for RMS_norm), 16-byte
+ *   aligned.
+ * Requirements: c % 16 == 0, 16 <= c <= 2048, m >= 1. Errors: VAE_ERR_ARG
+ * (NULL pointer, norm kind), VAE_ERR_SHAPE, VAE_ERR_ALIGN, VAE_ERR_NOMEM
+ * (workspace too small); argument checks fail before anything is launched.
  */
 size_t vae_mid_attention_workspace_bytes(int m, int c, int groups);
 int vae_mid_attention(float* x_dev, int m, int c, int norm_kind, int groups, float eps,

@@ -1,8 +1,10 @@
-"""GPU parity of the mid attention (norm, projections, fused QK^T-softmax-PV
-kernel, output projection) against the oracle, on the attention's
-contribution y - x. Tolerance 5e-3 of max|ref|: the GPU rounds xn, q, k, v,
-the unnormalised P and o to f16 (relative 2^-11 each) and accumulates in
-f32; those roundings stay near 1e-3 of the output scale."""
+"""GPU parity of the mid attention (norm, projections, the scores-softmax
+kernel and the P.V kernel, output projection) against the oracle, on the
+attention's contribution y - x. Tolerance 5e-3 of max|ref|: the GPU rounds to
+f16 (relative 2^-11 each) the normalised rows, the folded weights Wk^T Wq and
+Wo Wv, the folded queries, the unnormalised P and the softmax average (or,
+with VAE_ATTN_FOLD=0, q, k, v and o), and accumulates in f32; those roundings
+stay near 1e-3 of the output scale."""
 import numpy as np
 import pytest
 
@@ -69,8 +71,9 @@ def test_peaked_softmax_rescales(m, c):
     a.q = Conv(w=(a.q.w.astype(np.float32) * 4).astype(np.float16), b=a.q.b)
     got = run_gpu(x, a, "rms")
     ref = oracle.attention(x.T.reshape(c, m, 1), a, "rms").reshape(c, m).T
-    # Logits here reach the hundreds, so the f16 rounding of q and k moves them by
-    # up to |s| * 2^-10 and the sharply peaked softmax passes that on: 1e-2.
+    # Logits here reach the hundreds, so the f16 roundings of the query side
+    # (q and k, or the folded weights and queries) move them by up to about
+    # |s| * 2^-10 and the sharply peaked softmax passes that on: 1e-2.
     assert rel_err(got - x, ref - x) <= 1e-2
 
 
@@ -100,6 +103,21 @@ def test_single_cta_pv_kernel_matches_oracle():
     env = dict(os.environ, VAE_ATTN_PV_PAIR="0")
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
                         os.path.join(root, "tests", "test_gpu_attention.py"), "-k",
-                        "not full_size and not two_query_groups and not single_cta"],
+                        "not full_size and not two_query_groups and not single_cta and not literal"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+def test_literal_projections_match_oracle():
+    """The q, k, v projections as written (VAE_ATTN_FOLD=0) instead of the
+    folded weights: the attention tests again in a child process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, VAE_ATTN_FOLD="0")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
+                        os.path.join(root, "tests", "test_gpu_attention.py"), "-k",
+                        "not two_query_groups and not single_cta and not literal"],
                        cwd=root, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]

@@ -60,6 +60,7 @@ constexpr int kPHalfBytes = 128 * 64 * 2;            // 128 query rows x 64 keys
 struct ScoreParams {
     int m, nkb, nchunk_c;
     int q_tile0;   // first query tile of this group
+    int ntiles;    // query tiles of this group (the pair kernel's odd last tile may be missing)
     int kcols;     // P row length (nkb * 128)
     int grows;     // rows of the group buffers (tiles * 128)
     float scale_log2;
@@ -140,6 +141,20 @@ __device__ __forceinline__ bool wait_(uint64_t* bar, uint32_t parity, const ASme
 __device__ __forceinline__ bool wwait_(uint64_t* bar, uint32_t parity, const ASmem& s, DevStatus* st,
                                        unsigned long long timeout) {
     return warp_all(wait_(bar, parity, s, st, timeout));
+}
+
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                 int c1, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ bool wait_c(uint64_t* bar, uint32_t parity, const ASmem& s, DevStatus* st,
+                                       unsigned long long timeout) {
+    return mbar_wait_cluster(smem_u32(bar), parity, s.abort_flag, timeout, st, kWhereAttn);
 }
 
 // Ring bookkeeping shared by the producers and MMA threads (N slots).
@@ -236,29 +251,94 @@ __device__ void scores_mma(const ScoreParams& p, const ASmem& s, uint32_t tmem) 
 // then a second read of S for P (f16), the row sum and the per-block rescale
 // factors and flags the PV kernel replays (the pass's second block never
 // rescales).
-__device__ void scores_softmax(const ScoreParams& p, const ASmem& s, uint32_t tmem, int warp, int lane, int tl) {
-    const int r = warp * 32 + lane;
+// Eight softmax warps, one query row per thread: warp w reads TMEM lane
+// quadrant w % 4 (its 32 rows) and key half w / 4 (128 of the pass's 256 keys).
+// Per pass of 256 keys (two key blocks): the row max from a first read of S;
+// the two warps of a quadrant trade their half maxima through shared memory on
+// a bounded barrier, so both take the same max and the same rescale decision
+// (the running max moves only when the new one exceeds it by more than 2^8, so
+// P = 2^(s - m) <= 256 fits f16); then a second read of S for P (f16) and a
+// partial row sum. The first half writes the per-block rescale factors and
+// flags the PV kernel replays (the pass's second block never rescales); at the
+// end the second half's partial sum joins the first's (l = l0 + l1).
+// kPair: a CTA of a pair (S arrives by the even CTA's multicast commit; the
+// buffer is released on the even CTA's barrier, which counts both CTAs' rows);
+// live: this CTA's query tile exists (a missing odd tile of a pair writes
+// nothing but still takes part in every barrier).
+// 2^x by the PTX approximate base-2 exponential (relative error far below the
+// 2^-11 of the f16 P it feeds; results under 2^-126 flush to zero, where f16
+// holds nothing either).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+constexpr int kScWarps = 8;                       // softmax warps of the scores kernels
+constexpr int kScThreads = (kScWarps + 2) * 32;   // + producer + MMA warp
+constexpr int kScProducerWarp = kScWarps, kScMmaWarp = kScWarps + 1;
+
+struct ScExchange {
+    float* xmax;     // [2 pass parities][2 halves][128 rows]
+    float* xl;       // [128 rows]: the second half's partial row sum
+    uint64_t* xbar;  // [4]: the two warps (64 threads) of each lane quadrant
+};
+
+template <bool kPair>
+__device__ void scores_softmax(const ScoreParams& p, const ASmem& s, uint32_t tmem, int warp, int lane, int tl,
+                               bool live, const ScExchange& x) {
+    const int quad = warp & 3, half = warp >> 2;
+    const int r = quad * 32 + lane;
     const int row = tl * 128 + r;  // row of the group buffers
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     __half* prow = p.p + static_cast<size_t>(row) * p.kcols;
+    const uint32_t xb = smem_u32(&x.xbar[quad]);
+    uint32_t xph = 0;
+    auto exchange = [&]() -> bool {
+        mbar_arrive(xb);
+        const bool ok = mbar_wait(xb, xph, s.abort_flag, p.timeout_ns, p.status, kWhereAttn);
+        xph ^= 1u;
+        return warp_all(ok);
+    };
     float m_run = -INFINITY, l = 0.f;
     const int npair = (p.nkb + 1) / 2;
     for (int jj = 0; jj < npair; ++jj) {
         const int b = jj & 1;
-        if (!wwait_(&s.s_full[b], static_cast<uint32_t>((jj >> 1) & 1), s, p.status, p.timeout_ns)) return;
+        const uint32_t par = static_cast<uint32_t>((jj >> 1) & 1);
+        if (!(kPair ? warp_all(wait_c(&s.s_full[b], par, s, p.status, p.timeout_ns))
+                    : wwait_(&s.s_full[b], par, s, p.status, p.timeout_ns)))
+            return;
         tc_fence_after();
-        const int kbase = jj * 256;
-        const uint32_t sb = tmem + lane_off + static_cast<uint32_t>(b * 256);
+        const int kbase = jj * 256 + half * 128;  // this warp's first key
+        const uint32_t sb = tmem + lane_off + static_cast<uint32_t>(b * 256 + half * 128);
+        // S is read in batches of four 16-column loads under one wait.
+        const bool all_in = kbase + 128 <= p.m;  // no key of this half is past m
         float mx = -INFINITY;
-        for (int g = 0; g < 16; ++g) {
-            uint32_t rr[16];
+        for (int g = 0; g < 8; g += 4) {
+            uint32_t rr[4][16];
             __syncwarp();
-            tmem_ld16(sb + static_cast<uint32_t>(g * 16), rr);
-            tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (kbase + g * 16 + i < p.m) mx = fmaxf(mx, __uint_as_float(rr[i]) * p.scale_log2);
+            for (int u = 0; u < 4; ++u) tmem_ld16(sb + static_cast<uint32_t>((g + u) * 16), rr[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tmem_ld_wait_regs(rr[u]);
+            if (all_in) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) mx = fmaxf(mx, __uint_as_float(rr[u][i]));
+            } else {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (kbase + (g + u) * 16 + i < p.m) mx = fmaxf(mx, __uint_as_float(rr[u][i]));
+            }
         }
+        mx *= p.scale_log2;  // (the scale is positive: the max of the scaled scores)
+        float* xm = x.xmax + (jj & 1) * 256;
+        xm[half * 128 + r] = mx;
+        if (!exchange()) return;
+        mx = fmaxf(xm[r], xm[128 + r]);
         float alpha = 1.f;
         bool resc = false;
         if (jj == 0) {
@@ -270,45 +350,63 @@ __device__ void scores_softmax(const ScoreParams& p, const ASmem& s, uint32_t tm
         }
         const bool any = __any_sync(0xffffffffu, resc);
         const int j0 = 2 * jj, j1 = 2 * jj + 1;
-        if (j0 >= 1) {
-            p.alpha[static_cast<size_t>(j0) * p.grows + row] = alpha;
-            if (lane == 0) p.flags[(static_cast<size_t>(tl) * p.nkb + j0) * 4 + warp] = any ? 1u : 0u;
-        }
-        if (j1 < p.nkb) {
-            p.alpha[static_cast<size_t>(j1) * p.grows + row] = 1.f;
-            if (lane == 0) p.flags[(static_cast<size_t>(tl) * p.nkb + j1) * 4 + warp] = 0u;
+        if (live && half == 0) {
+            if (j0 >= 1) {
+                p.alpha[static_cast<size_t>(j0) * p.grows + row] = alpha;
+                if (lane == 0) p.flags[(static_cast<size_t>(tl) * p.nkb + j0) * 4 + quad] = any ? 1u : 0u;
+            }
+            if (j1 < p.nkb) {
+                p.alpha[static_cast<size_t>(j1) * p.grows + row] = 1.f;
+                if (lane == 0) p.flags[(static_cast<size_t>(tl) * p.nkb + j1) * 4 + quad] = 0u;
+            }
         }
         l *= alpha;
         float sum = 0.f;
-        const int ngr = min(16, (p.nkb * 128 - kbase) / 16);  // 16-key groups with P columns
-        for (int g = 0; g < ngr; ++g) {
-            uint32_t rr[16];
+        const int ngr = live && kbase < p.nkb * 128 ? 8 : 0;  // this half's 16-key groups with P columns
+        for (int g = 0; g < ngr; g += 4) {
+            uint32_t rr[4][16];
             __syncwarp();
-            tmem_ld16(sb + static_cast<uint32_t>(g * 16), rr);
-            tmem_ld_wait();
-            uint32_t h[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int key = kbase + g * 16 + 2 * i;
-                const float a = key < p.m ? exp2f(__uint_as_float(rr[2 * i]) * p.scale_log2 - m_run) : 0.f;
-                const float c = key + 1 < p.m ? exp2f(__uint_as_float(rr[2 * i + 1]) * p.scale_log2 - m_run) : 0.f;
-                sum += a + c;
-                __half2 t = __floats2half2_rn(a, c);
-                h[i] = *reinterpret_cast<uint32_t*>(&t);
+            for (int u = 0; u < 4; ++u) tmem_ld16(sb + static_cast<uint32_t>((g + u) * 16), rr[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tmem_ld_wait_regs(rr[u]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                uint32_t h[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int key = kbase + (g + u) * 16 + 2 * i;
+                    float a = ex2_approx(fmaf(__uint_as_float(rr[u][2 * i]), p.scale_log2, -m_run));
+                    float c = ex2_approx(fmaf(__uint_as_float(rr[u][2 * i + 1]), p.scale_log2, -m_run));
+                    if (!all_in) {
+                        a = key < p.m ? a : 0.f;
+                        c = key + 1 < p.m ? c : 0.f;
+                    }
+                    sum += a + c;
+                    __half2 t = __floats2half2_rn(a, c);
+                    h[i] = *reinterpret_cast<uint32_t*>(&t);
+                }
+                st_v8_b32(prow + kbase + (g + u) * 16, h);
             }
-            st_v8_b32(prow + kbase + g * 16, h);
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&s.s_free[b]));
+        if (kPair)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&s.s_free[b]), 0u));
+        else
+            mbar_arrive(smem_u32(&s.s_free[b]));
         l += sum;
     }
-    p.lsum[row] = l;
+    if (half == 1) x.xl[r] = l;
+    if (!exchange()) return;
+    if (live && half == 0) p.lsum[row] = l + x.xl[r];
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kScThreads, 1)
     attn_scores_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                        const ScoreParams p) {
     extern __shared__ uint8_t smem_raw[];
+    __shared__ float xmax[2 * 2 * 128], xl[128];
+    __shared__ uint64_t xbar[4];
     const ASmem s = carve_attn(smem_raw);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int tl = blockIdx.x;
@@ -321,16 +419,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s.s_full[i]), 1u);
-            mbar_init(smem_u32(&s.s_free[i]), 128u);
+            mbar_init(smem_u32(&s.s_free[i]), 32u * kScWarps);
         }
         mbar_init(smem_u32(s.drain), 1u);
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xbar[i]), 64u);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kScMmaWarp) {
         tmem_alloc(smem_u32(s.tmem_slot), kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kScProducerWarp && lane == 0) {
         tma_prefetch_desc(&mq);
         tma_prefetch_desc(&mk);
     }
@@ -339,9 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s.tmem_slot;
-    if (warp < 4) {
-        scores_softmax(p, s, tmem, warp, lane, tl);
-    } else if (warp == 4) {
+    if (warp < kScWarps) {
+        scores_softmax<false>(p, s, tmem, warp, lane, tl, true, ScExchange{xmax, xl, xbar});
+    } else if (warp == kScProducerWarp) {
         if (lane == 0) scores_producer(p, s, &mq, &mk, q0);
     } else {
         if (lane == 0) scores_mma(p, s, tmem);
@@ -349,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch_dependents();  // this CTA's work is done
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kScMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -563,20 +662,6 @@ constexpr int kPvPairStageBytes = 40 * 1024;  // P half 16 KB + two V^T half box
 constexpr int kPvPairStages = 5;
 static_assert(1024 + kPvPairStages * kPvPairStageBytes + 256 <= 232448, "PV pair shared memory over 227 KB");
 
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
-                                                 int c1, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ bool wait_c(uint64_t* bar, uint32_t parity, const ASmem& s, DevStatus* st,
-                                       unsigned long long timeout) {
-    return mbar_wait_cluster(smem_u32(bar), parity, s.abort_flag, timeout, st, kWhereAttn);
-}
-
 __device__ void pvp_producer(const PvParams& p, const ASmem& s, const CUtensorMap* mp, const CUtensorMap* mv, int tl,
                              int d0, int rank) {
     const uint64_t pol = policy_evict_normal();
@@ -789,6 +874,145 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
 }
 
+// ─────────────────────── scores kernel on CTA pairs ───────────────────────
+// A cluster of two CTAs computes S for two query tiles (2t, 2t + 1 of the
+// group) with tcgen05.mma.cta_group::2 (M = 256, N = 256 keys per pass): each
+// CTA streams its own tile's 64-channel Q chunk and HALF of the pass's 256 keys
+// (the 128 rows of N the pair MMA takes from it), 32 KB per stage per SM
+// instead of 48 KB. Both CTAs' copies complete on the even CTA's full barrier;
+// the even CTA's MMA thread commits with multicast (ring slots to both empty
+// barriers, each S buffer to both CTAs' s_full), and the softmax rows of both
+// CTAs release an S buffer on the even CTA's s_free (256 arrivals). The
+// softmax itself is the single-CTA kernel's, row for row, so P, the factors
+// and the flags are the same bits.
+constexpr int kScPairStageBytes = 32 * 1024;  // Q chunk 128 x 64 + K half 128 x 64 (f16)
+constexpr int kScPairStages = 6;
+static_assert(1024 + kScPairStages * kScPairStageBytes + 256 <= 232448, "scores pair shared memory over 227 KB");
+static_assert(kScPairStages <= kRingBars, "scores pair ring over the barrier slots");
+
+__device__ void scp_producer(const ScoreParams& p, const ASmem& s, const CUtensorMap* mq, const CUtensorMap* mk,
+                             int q0, int rank) {
+    const uint64_t pol = policy_evict_normal();
+    RingT<kScPairStages> r;
+    const int npair = (p.nkb + 1) / 2;
+    bool ok = true;
+    for (int jj = 0; jj < npair && ok; ++jj)
+        for (int cc = 0; cc < p.nchunk_c; ++cc) {
+            if (!wait_(&s.empty[r.stage], r.phase ^ 1u, s, p.status, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = smem_u32(&s.full[r.stage]);
+            if (rank == 0) mbar_arrive_expect_tx(fb, 2u * static_cast<uint32_t>(kScPairStageBytes));
+            r.arm();
+            const uint32_t fbc = mapa_shared(fb, 0u);
+            uint8_t* st = s.ring + r.stage * kScPairStageBytes;
+            tma_load_2d_pair(smem_u32(st), mq, fbc, cc * 64, q0, pol);  // rows past m read as zeros
+            tma_load_2d_pair(smem_u32(st + 16384), mk, fbc, cc * 64, jj * 256 + rank * 128, pol);
+            r.next();
+        }
+    // every copy lands before the CTA can exit: the even CTA sees them on its
+    // full barriers, the odd CTA on its empty barriers (the MMAs that read them)
+    int never = 0;
+    for (int i = 0; i < kScPairStages; ++i)
+        if (r.armed & (1u << i))
+            (void)mbar_wait(smem_u32(rank == 0 ? &s.full[i] : &s.empty[i]), (r.arm_par >> i) & 1u, &never,
+                            p.timeout_ns, p.status, kWhereDrain);
+}
+
+__device__ void scp_mma(const ScoreParams& p, const ASmem& s, uint32_t tmem) {
+    const uint32_t id_s = idesc_f16_f32(256, 256);
+    const uint64_t q_desc0 = sw128_kmajor_desc(smem_u32(s.ring));  // every ring address stays below 2^18 bytes
+    RingT<kScPairStages> r;
+    bool ok = true;
+    const int npair = (p.nkb + 1) / 2;
+    for (int jj = 0; jj < npair && ok; ++jj) {
+        const int b = jj & 1;
+        if (jj >= 2) {  // both CTAs' softmax rows have read S(jj - 2) out of this buffer
+            if (!wait_c(&s.s_free[b], static_cast<uint32_t>(((jj - 2) >> 1) & 1), s, p.status, p.timeout_ns)) break;
+            tc_fence_after();
+        }
+        for (int cc = 0; cc < p.nchunk_c; ++cc) {
+            if (!wait_(&s.full[r.stage], r.phase, s, p.status, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t ad = q_desc0 + static_cast<uint32_t>(r.stage) * (kScPairStageBytes >> 4);
+            const uint64_t bd = ad + (16384u >> 4);
+            const uint32_t dS = tmem + static_cast<uint32_t>(b * 256);
+            umma_f16_pair(dS, ad, bd, id_s, cc != 0 ? 1u : 0u);  // S(256 x 256) += Q_c K_c^T
+#pragma unroll
+            for (int k = 1; k < 4; ++k) umma_f16_pair(dS, ad + 2u * k, bd + 2u * k, id_s, 1u);
+            umma_commit_pair(smem_u32(&s.empty[r.stage]));
+            r.next();
+        }
+        if (ok) umma_commit_pair(smem_u32(&s.s_full[b]));
+    }
+    umma_commit_pair(smem_u32(s.drain));
+    int never = 0;
+    (void)mbar_wait(smem_u32(s.drain), 0u, &never, p.timeout_ns, p.status, kWhereDrain);
+}
+
+// grid: 2 x (tile pairs of the group), clusters of 2; p.ntiles = tiles of the group.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kScThreads, 1)
+    attn_scores_pair_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                            const ScoreParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ float xmax[2 * 2 * 128], xl[128];
+    __shared__ uint64_t xbar[4];
+    const ASmem s = carve_attn(smem_raw, kScPairStages * kScPairStageBytes);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int tl = (blockIdx.x >> 1) * 2 + rank;
+    const bool live = tl < p.ntiles;
+    const int q0 = (p.q_tile0 + tl) * 128;
+    if (threadIdx.x == 0) {
+        *s.abort_flag = 0;
+        for (int i = 0; i < kScPairStages; ++i) {
+            mbar_init(smem_u32(&s.full[i]), 1u);
+            mbar_init(smem_u32(&s.empty[i]), 1u);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&s.s_full[i]), 1u);
+            mbar_init(smem_u32(&s.s_free[i]), 2u * 32u * kScWarps);  // the softmax rows of both CTAs
+        }
+        mbar_init(smem_u32(s.drain), 1u);
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xbar[i]), 64u);
+        fence_mbar_init();
+    }
+    if (warp == kScMmaWarp) {
+        tmem_alloc_pair(smem_u32(s.tmem_slot), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    if (warp == kScProducerWarp && lane == 0) {
+        tma_prefetch_desc(&mq);
+        tma_prefetch_desc(&mk);
+    }
+    pdl_wait();  // q and the keys come from kernels launched before
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers and TMEM exist before any remote arrive or pair MMA
+    tc_fence_after();
+    const uint32_t tmem = *s.tmem_slot;
+    if (warp < kScWarps) {
+        scores_softmax<true>(p, s, tmem, warp, lane, tl, live, ScExchange{xmax, xl, xbar});
+    } else if (warp == kScProducerWarp) {
+        if (lane == 0) scp_producer(p, s, &mq, &mk, q0, rank);
+    } else {
+        if (lane == 0 && rank == 0) scp_mma(p, s, tmem);
+    }
+    pdl_launch_dependents();  // this CTA's work is done
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the even CTA's MMAs into both TMEMs are done; no remote arrives remain
+    if (warp == kScMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
 struct AttnLayout {
     int m_pad, ndv, dv;
     int qtiles, nkb, group;  // query tiles, key blocks, query tiles per scores/PV launch pair
@@ -927,6 +1151,15 @@ int transpose_run(const __half* in, int rows, int cols, long long ld_in, __half*
     return VAE_OK;
 }
 
+// The CTA-pair scores kernel runs unless VAE_ATTN_SCORES_PAIR=0 is set (tests and measurements).
+bool attn_scores_pair_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("VAE_ATTN_SCORES_PAIR");
+        return !(e != nullptr && e[0] == '0');
+    }();
+    return on;
+}
+
 // The CTA-pair PV kernel runs unless VAE_ATTN_PV_PAIR=0 is set (tests and measurements).
 bool attn_pv_pair_enabled() {
     static const bool on = [] {
@@ -985,7 +1218,7 @@ static int attn_core_run(const __half* q, const __half* k, const __half* vt, int
     pp.out = out;
     pp.status = st;
     pp.timeout_ns = sp.timeout_ns;
-    CUtensorMap mq{}, mk{}, mp{}, mv{};
+    CUtensorMap mq{}, mk{}, mk2{}, mp{}, mv{};
     {
         const uint64_t dims[2] = {static_cast<uint64_t>(c), static_cast<uint64_t>(m)};
         const uint64_t strides[1] = {static_cast<uint64_t>(c) * 2};
@@ -994,6 +1227,10 @@ static int attn_core_run(const __half* q, const __half* k, const __half* vt, int
         if (rc != VAE_OK) return rc;
         const uint32_t kbox[2] = {64u, 256u};  // two key blocks per box
         rc = encode_tiled(&mk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, k, dims, strides, kbox, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (rc != VAE_OK) return rc;
+        const uint32_t kbox2[2] = {64u, 128u};  // the pair kernel: each CTA loads one key block of the pass
+        rc = encode_tiled(&mk2, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, k, dims, strides, kbox2,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
         if (rc != VAE_OK) return rc;
     }
     {
@@ -1024,6 +1261,7 @@ static int attn_core_run(const __half* q, const __half* k, const __half* vt, int
     }
     const size_t smem = 1024 + kStages * kStageBytes + 256;
     const size_t smem_pair = 1024 + kPvPairStages * kPvPairStageBytes + 256;
+    const size_t smem_sc_pair = 1024 + kScPairStages * kScPairStageBytes + 256;
     static CtxOnce attr_set;
     int dev = 0;
     VAE_CUDA_CHECK(cudaGetDevice(&dev));
@@ -1034,15 +1272,22 @@ static int attn_core_run(const __half* q, const __half* k, const __half* vt, int
                                             static_cast<int>(smem)));
         VAE_CUDA_CHECK(cudaFuncSetAttribute(attn_pv_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             static_cast<int>(smem_pair)));
+        VAE_CUDA_CHECK(cudaFuncSetAttribute(attn_scores_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(smem_sc_pair)));
         attr_set.mark(dev);
     }
     for (int t0 = 0; t0 < L.qtiles; t0 += L.group) {
         const int nt = std::min(L.group, L.qtiles - t0);
         sp.q_tile0 = t0;
+        sp.ntiles = nt;
         pp.q_tile0 = t0;
         pp.ntiles = nt;
-        VAE_CUDA_CHECK(launch_kernel(attn_scores_kernel, dim3(static_cast<unsigned>(nt)), dim3(kThreads), smem,
-                                     stream, mq, mk, sp));
+        if (nt >= 2 && attn_scores_pair_enabled())
+            VAE_CUDA_CHECK(launch_kernel(attn_scores_pair_kernel, dim3(static_cast<unsigned>(2 * ((nt + 1) / 2))),
+                                         dim3(kScThreads), smem_sc_pair, stream, mq, mk2, sp));
+        else
+            VAE_CUDA_CHECK(launch_kernel(attn_scores_kernel, dim3(static_cast<unsigned>(nt)), dim3(kScThreads), smem,
+                                         stream, mq, mk, sp));
         if (nt >= 2 && attn_pv_pair_enabled())
             VAE_CUDA_CHECK(launch_kernel(attn_pv_pair_kernel, dim3(static_cast<unsigned>(2 * ((nt + 1) / 2) * L.ndv)),
                                          dim3(kThreads), smem_pair, stream, mp, mv2, pp));

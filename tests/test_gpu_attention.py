@@ -92,15 +92,16 @@ def test_mid_attention_two_query_groups():
     assert rel_err(got[rows] - x[rows], ref - x[rows]) <= ATTN_TOL
 
 
-def test_single_cta_pv_kernel_matches_oracle():
-    """The PV step on single CTAs (VAE_ATTN_PV_PAIR=0; by default query-tile
-    pairs share it through cta_group::2): the attention tests again in a child
-    process, which reads the switch once."""
+def test_single_cta_attention_kernels_match_oracle():
+    """The scores and PV steps on single CTAs (VAE_ATTN_SCORES_PAIR=0,
+    VAE_ATTN_PV_PAIR=0; by default query-tile pairs share them through
+    cta_group::2): the attention tests again in a child process, which reads
+    the switches once."""
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, VAE_ATTN_PV_PAIR="0")
+    env = dict(os.environ, VAE_ATTN_PV_PAIR="0", VAE_ATTN_SCORES_PAIR="0")
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p", "no:cacheprovider",
                         os.path.join(root, "tests", "test_gpu_attention.py"), "-k",
                         "not full_size and not two_query_groups and not single_cta and not literal"],

@@ -1,32 +1,40 @@
 // Mid-block single-head spatial self-attention ("vae.rs" AttnBlock::apply /
-// finish; "qi21_vae.rs" attention): norm -> q, k, v^T projections (the
-// implicit-GEMM kernel with one tap) -> o = softmax(q k^T / sqrt(c)) v + b_v
-// by two tcgen05 kernels -> output projection added onto the stream by the
-// conv epilogue's residual path.
+// finish; "qi21_vae.rs" attention): norm -> projections (the implicit-GEMM
+// kernel with one tap, on CTA pairs) -> o = softmax(q k^T / sqrt(c)) v by two
+// tcgen05 kernels -> output projection added onto the stream by the conv
+// epilogue's residual path.
 //
-// Scores kernel (one CTA per 128-query tile): S = Q K_j^T for key block j
-// (128 keys) accumulates in one of two TMEM buffers from 64-channel chunks of
-// Q and K streamed by TMA; four softmax warps (one query row per thread) read
-// S with tcgen05.ld, mask keys >= m and keep a running max m and sum l (online
-// softmax, rescaling only when the max grows by more than 2^8, so the
+// Folded form (the default; VAE_ATTN_FOLD=0 runs the projections as written):
+// the key bias adds the same amount to every score of a row, which the softmax
+// removes, and each softmax row sums to one, so with M = Wk^T Wq the scores are
+// q'_i . n_j, q' = n M^T + Wk^T bq, and the output is
+// (sum_j p_ij n_j / l_i) (Wo Wv)^T + (Wo bv + bo): keys and values are the
+// normalised rows themselves (n, and n^T for the P.V operand).
+//
+// Scores kernel (clusters of two query tiles, tcgen05.mma.cta_group::2, M = 256;
+// a single-CTA form for one tile): S = Q K^T for 256 keys accumulates in one of
+// two TMEM buffers from 64-channel chunks of Q and K streamed by TMA (each CTA
+// of a pair loads its Q chunk and half of the keys). Eight softmax warps (one
+// query row per thread; two warps per TMEM lane quadrant, one per key half)
+// read S with tcgen05.ld, mask keys >= m and keep a running max m and sum l
+// (online softmax, rescaling only when the max grows by more than 2^8, so the
 // unnormalised P = 2^(s - m) stays <= 256 in f16). They write P (f16) to a
 // row-major workspace, the factor alpha_j each row's O must be scaled by before
 // block j is added (1 when its max did not move), one "some row rescaled" flag
-// per warp and block, and the final l.
+// per lane quadrant and block, and the final l.
 //
-// PV kernel (one CTA per (query tile, value-channel chunk of <= 384)): O +=
-// P_j V_j^T in TMEM from TMA-streamed 64-key halves of P and V^T; on a flagged
-// block the four row warps scale O by alpha_j after PV(j-1) and before PV(j).
-// The epilogue writes O / l + b_v as f16 (the v bias is added after P.V, exact
-// because the rows of the softmax sum to one).
+// PV kernel (clusters of two query tiles per value-channel chunk of <= 384; a
+// single-CTA form): O += P_j V_j^T in TMEM from TMA-streamed 64-key halves of
+// P and V^T; on a flagged block the row warps scale O by alpha_j after PV(j-1)
+// and before PV(j). The epilogue writes O / l (+ b_v when the values carry a
+// bias: added after P.V, exact because the rows of the softmax sum to one) as
+// f16.
 //
 // S is computed once however many value chunks c needs (the O accumulator of
 // c = 1152 columns cannot live in one SM's 512 TMEM columns, so a fused kernel
 // had to recompute S per chunk, doubling the tensor work), at the price of
-// writing P (2 bytes per score) once and reading it once per chunk. The
-// arithmetic (S, the softmax, P, the rescale sequence, the P.V order) is the
-// same as the fused kernel's, so the output is too. Query tiles run in groups
-// whose P fits a 2 GiB workspace. Every wait is bounded.
+// writing P (2 bytes per score) once and reading it once per chunk. Query tiles
+// run in groups whose P fits a 2 GiB workspace. Every wait is bounded.
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>

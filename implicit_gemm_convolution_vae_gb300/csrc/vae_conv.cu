@@ -107,7 +107,7 @@ struct ConvParams {
                           // stage of 16-channel boxes (32-byte swizzle) for all three ky and nine taps
     int halo, a_stages;   // halo mode: a_stages halo boxes; B ring of `stages` x ks taps
                           // (ks == 3: box slot i belongs to stage i, one barrier pair)
-    int ks;               // K chunks per pipeline stage (1 or 2; per-tap A path only)
+    int ks;               // K chunks per pipeline stage (per-tap A path: 1 or 2; pair GEMM mode: up to kGemmPairKs)
     int pair;             // CTA-pair kernel: each CTA holds BN/2 rows of B (b_rows)
     int gemm;             // pair kernel on a 1x1 conv over one row of pixels (a plain GEMM): the two CTAs
                           // take adjacent 128-pixel column tiles; a stage holds ks 64-channel chunks
